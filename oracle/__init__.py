@@ -1,0 +1,164 @@
+"""CPU oracle for the W8A8 linear layer -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never touches it, and it never touches the product path:
+the two share no code.
+
+The arithmetic lives in ``i8_oracle.c`` (plain C, fp32 steps in the order the
+pages give them); this module only compiles it with gcc and marshals numpy
+arrays through ctypes.  bf16 tensors travel as ``uint16`` bit patterns.
+
+Source: "Realizing Native INT8 Compute for Diffusion Transformers on Consumer
+GPUs: A Fused INT8 GEMM Kernel for Ideogram 4.0" (arXiv 2606.14598), abstract:
+per-token activation and per-channel weight INT8 quantization, an int8 x int8
+-> int32 GEMM, and a per-token x per-channel dequantization plus bias epilogue
+that emits bf16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "i8_oracle.c")
+_HDR = os.path.join(_HERE, "i8_oracle.h")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+          "-shared", "-fopenmp", "-Wall", "-Wextra"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (gcc, no intrinsics)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= max(os.path.getmtime(_SRC),
+                                              os.path.getmtime(_HDR))):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            i64, vp = ctypes.c_int64, ctypes.c_void_p
+            lib.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.orc_bf16_to_f32.restype = ctypes.c_float
+            lib.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+            lib.orc_f32_to_bf16.restype = ctypes.c_uint16
+            lib.orc_quant_rows.argtypes = [vp, i64, i64, i64, vp, i64, vp]
+            lib.orc_quant_rows.restype = ctypes.c_int
+            lib.orc_gemm_s32.argtypes = [vp, i64, vp, i64, i64, i64, i64, vp, i64]
+            lib.orc_gemm_s32.restype = ctypes.c_int
+            lib.orc_dequant_bias.argtypes = [vp, i64, vp, vp, vp, i64, i64, vp, i64]
+            lib.orc_dequant_bias.restype = ctypes.c_int
+            lib.orc_num_threads.argtypes = []
+            lib.orc_num_threads.restype = ctypes.c_int
+            lib.orc_set_num_threads.argtypes = [ctypes.c_int]
+            lib.orc_set_num_threads.restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c2d(a, dtype) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    if a.ndim != 2:
+        raise ValueError("expected a 2-D array")
+    return np.ascontiguousarray(a)
+
+
+def num_threads() -> int:
+    return _load().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().orc_set_num_threads(int(n))
+
+
+def f32_to_bf16_bits(f: float) -> int:
+    return int(_load().orc_f32_to_bf16(float(f)))
+
+
+def bf16_bits_to_f32(b: int) -> float:
+    return float(_load().orc_bf16_to_f32(int(b)))
+
+
+def quant_rows(x_bits):
+    """Per-row symmetric INT8 quantization of a bf16 matrix (uint16 bits).
+
+    Returns ``(q int8 [rows,K], scale float32 [rows])``.
+    """
+    x = _c2d(x_bits, np.uint16)
+    rows, K = x.shape
+    q = np.zeros((rows, K), dtype=np.int8)
+    s = np.zeros((rows,), dtype=np.float32)
+    rc = _load().orc_quant_rows(_ptr(x), rows, K, K, _ptr(q), K, _ptr(s))
+    if rc != 0:
+        raise ValueError("orc_quant_rows rejected its arguments")
+    return q, s
+
+
+def gemm_s32(a, w) -> np.ndarray:
+    """int32 ``a @ w.T`` for int8 ``a [M,K]`` and ``w [N,K]``."""
+    a = _c2d(a, np.int8)
+    w = _c2d(w, np.int8)
+    M, K = a.shape
+    N, K2 = w.shape
+    if K != K2:
+        raise ValueError("K mismatch")
+    c = np.zeros((M, N), dtype=np.int32)
+    rc = _load().orc_gemm_s32(_ptr(a), K, _ptr(w), K, M, N, K, _ptr(c), N)
+    if rc != 0:
+        raise ValueError("orc_gemm_s32 rejected its arguments")
+    return c
+
+
+def dequant_bias(acc, s_a, s_w, bias_bits) -> np.ndarray:
+    """bf16 bits of ``acc * s_a[:,None] * s_w[None,:] + bias`` (see the C file)."""
+    c = _c2d(acc, np.int32)
+    M, N = c.shape
+    sa = np.ascontiguousarray(s_a, dtype=np.float32)
+    sw = np.ascontiguousarray(s_w, dtype=np.float32)
+    if sa.shape != (M,) or sw.shape != (N,):
+        raise ValueError("scale shapes")
+    b = None
+    if bias_bits is not None:
+        b = np.ascontiguousarray(bias_bits)
+        if b.dtype != np.uint16 or b.shape != (N,):
+            raise ValueError("bias must be uint16 bf16 bits of shape [N]")
+    y = np.zeros((M, N), dtype=np.uint16)
+    rc = _load().orc_dequant_bias(_ptr(c), N, _ptr(sa), _ptr(sw), _ptr(b), M, N,
+                                  _ptr(y), N)
+    if rc != 0:
+        raise ValueError("orc_dequant_bias rejected its arguments")
+    return y
+
+
+def linear(x_bits, w_bits, bias_bits):
+    """The whole path: quantize X per token and W per channel, GEMM, epilogue.
+
+    Returns a dict with ``aq, s_a, wq, s_w, acc, y`` (y as bf16 bits).
+    """
+    aq, s_a = quant_rows(x_bits)
+    wq, s_w = quant_rows(w_bits)
+    acc = gemm_s32(aq, wq)
+    y = dequant_bias(acc, s_a, s_w, bias_bits)
+    return dict(aq=aq, s_a=s_a, wq=wq, s_w=s_w, acc=acc, y=y)

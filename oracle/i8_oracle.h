@@ -1,0 +1,68 @@
+/*
+ * i8_oracle.h -- plain, slow, obviously-correct CPU definition of the W8A8
+ * linear layer.  TEST INFRASTRUCTURE ONLY: only the test-suite, the smoke
+ * check and the CPU-baseline leg of the benchmark may load this library.  It
+ * shares no code, header, table or helper with the CUDA library.
+ *
+ * Sources (cited by title and passage; there are no numbered sections):
+ *   [ABS]  "Realizing Native INT8 Compute for Diffusion Transformers on
+ *          Consumer GPUs: A Fused INT8 GEMM Kernel for Ideogram 4.0"
+ *          (arXiv 2606.14598), abstract -- the forward quantizes
+ *          activations per token and weights per output channel, multiplies
+ *          int8 by int8 into int32, and applies the per-token x per-channel
+ *          dequantization and the bias in the GEMM epilogue, emitting bf16.
+ *   [NEWS] aiexpert.news write-up of the same paper (Spanish), paragraph on
+ *          the mechanism -- operands stay INT8, accumulation is int32, the
+ *          epilogue dequantizes and adds the bias before writing bf16.
+ *
+ * Readings where the pages are silent (each one is listed in the design doc):
+ *   symmetric quantizer, no zero point; range +-127 (-128 never produced);
+ *   scale = absmax / 127 in IEEE fp32; q = round-half-even(x / scale) with a
+ *   true fp32 division; an all-zero row has scale 0 and codes 0; epilogue
+ *   order float(acc) * s_a[m] * s_w[n] + bias[n], each step rounded to fp32
+ *   (no FMA), then round-to-nearest-even to bf16; a missing bias adds +0.0f.
+ *
+ * bf16 values cross this interface as uint16_t bit patterns.
+ * Parity status of each function: see the header comment in i8_oracle.c.
+ */
+#ifndef I8_ORACLE_H
+#define I8_ORACLE_H
+#include <stdint.h>
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* bf16 bit pattern -> fp32 (exact widening). */
+float orc_bf16_to_f32(uint16_t b);
+/* fp32 -> bf16 bit pattern, round to nearest, ties to even; NaN stays NaN. */
+uint16_t orc_f32_to_bf16(float f);
+
+/* Symmetric per-row INT8 quantizer ([ABS] per-token activations and
+ * per-channel weights; both are "one scale per row of a K-contiguous
+ * matrix").  x: rows x K bf16, row stride ldx elements.  q: rows x K int8,
+ * row stride ldq.  scale: rows fp32.  Returns 0, or -1 on bad arguments. */
+int orc_quant_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
+                   int8_t* q, int64_t ldq, float* scale);
+
+/* acc[m][n] = sum_k a[m][k] * w[n][k] in int32 ([ABS] int8 x int8 -> int32).
+ * a: M x K row-major (lda), w: N x K row-major (ldw, the [out,in] layout),
+ * c: M x N row-major (ldc).  Requires K <= 131072 so that no int32 sum can
+ * overflow (127*127*131072 < 2^31).  Returns 0, or -1 on bad arguments. */
+int orc_gemm_s32(const int8_t* a, int64_t lda, const int8_t* w, int64_t ldw,
+                 int64_t M, int64_t N, int64_t K, int32_t* c, int64_t ldc);
+
+/* y[m][n] = bf16( ((float)acc[m][n] * s_a[m]) * s_w[n] + bias[n] )
+ * ([ABS], [NEWS]: per-token x per-channel dequantization plus bias, bf16
+ * out).  bias may be NULL (treated as +0.0f).  Returns 0, or -1. */
+int orc_dequant_bias(const int32_t* c, int64_t ldc, const float* s_a,
+                     const float* s_w, const uint16_t* bias, int64_t M,
+                     int64_t N, uint16_t* y, int64_t ldy);
+
+/* Threads the loops may use (OpenMP), or 1 when built without it. */
+int orc_num_threads(void);
+void orc_set_num_threads(int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
