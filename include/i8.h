@@ -1,0 +1,170 @@
+/*
+ * i8.h -- C ABI of libi8, a GB300 (sm_103a) W8A8 INT8 linear layer.
+ *
+ * The operation is the one described in "Realizing Native INT8 Compute for
+ * Diffusion Transformers on Consumer GPUs: A Fused INT8 GEMM Kernel for
+ * Ideogram 4.0" (arXiv 2606.14598), abstract, and in the aiexpert.news
+ * write-up of it (paragraph on the mechanism):
+ *
+ *   x  [M,K] bf16 activations  --per-token INT8 quant-->  aq [M,K] int8, s_a [M]
+ *   w  [N,K] bf16 weights      --per-channel INT8 quant->  wq [N,K] int8, s_w [N]
+ *   acc[m,n] = sum_k aq[m,k] * wq[n,k]                     (exact int32)
+ *   y[m,n]   = bf16( float(acc) * s_a[m] * s_w[n] + bias[n] )   (epilogue)
+ *
+ * Quantizer (per row r of a K-contiguous matrix): amax = max_k |x[r,k]|,
+ * scale = amax / 127 (IEEE fp32), q = clamp(round_half_even(x / scale),
+ * -127, 127); an all-zero row gets scale 0 and codes 0.  The pages do not
+ * print the quantizer; this symmetric form is the plain reading of their
+ * scale-only epilogue.
+ *
+ * Conventions for every call:
+ *   - All pointers are DEVICE pointers of the current CUDA device, except
+ *     where a call says otherwise.  The caller owns every buffer; the
+ *     library allocates no device memory.  Work is queued on `stream`
+ *     (NULL = legacy default stream) and the call returns without waiting.
+ *   - Matrices are row-major with the contiguous dimension last; weights use
+ *     the [out, in] = [N, K] layout, so both GEMM operands are K-contiguous.
+ *   - bf16 buffers hold IEEE bfloat16 bit patterns (2 bytes per element).
+ *   - Constraints: K % 16 == 0, 16 <= K <= 131072 (127*127*K must stay below
+ *     2^31); M, N >= 0 and below 2^31; matrix base pointers 16-byte aligned;
+ *     leading dimensions such that every row starts 16-byte aligned; scale
+ *     pointer s_a 4-byte aligned; s_w and bias 16-byte aligned.
+ *   - NaN or Inf inputs are outside the contract (results are unspecified,
+ *     but no call faults on them).
+ *   - Errors are returned, never thrown.  Argument, size and alignment errors
+ *     are detected on the host before anything is queued.  Launch failures
+ *     return I8_ERR_CUDA.  A kernel whose internal pipeline wait exceeds its
+ *     time limit stops, records I8_ERR_DEVICE_TIMEOUT in a per-device status
+ *     word and returns; i8_sync_check() reports (and clears) it.
+ */
+#ifndef I8_H
+#define I8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle type (cudaStream_t), declared without
+ * pulling in the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st* i8_stream_t;
+
+typedef enum {
+  I8_OK = 0,
+  I8_ERR_INVALID_ARG = 1,     /* NULL pointer, negative size, bad stride */
+  I8_ERR_ALIGNMENT = 2,       /* pointer or row not 16-byte aligned */
+  I8_ERR_UNSUPPORTED = 3,     /* K % 16 != 0, K > 131072, size out of range */
+  I8_ERR_WORKSPACE = 4,       /* workspace missing or smaller than required */
+  I8_ERR_CUDA = 5,            /* a CUDA runtime or launch error */
+  I8_ERR_DEVICE_TIMEOUT = 6   /* a kernel's pipeline wait ran out of time */
+} i8_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* i8_status_string(i8_status s);
+
+/* Library version string, e.g. "i8 0.1.0 sm_103a". */
+const char* i8_version(void);
+
+/* Per-channel weight quantization (arXiv 2606.14598, abstract: weights are
+ * quantized per output channel, offline, after training).
+ *   w   [N,K] bf16, row stride ldw elements (ldw >= K, ldw % 8 == 0)
+ *   wq  [N,K] int8, row stride ldq bytes (ldq >= K, ldq % 16 == 0)
+ *   s_w [N]   fp32 per-channel scales                                     */
+i8_status i8_quant_weight_perchannel(const void* w, int64_t N, int64_t K,
+                                     int64_t ldw, int8_t* wq, int64_t ldq,
+                                     float* s_w, i8_stream_t stream);
+
+/* Per-token activation quantization (arXiv 2606.14598, abstract: one scale
+ * per token; aiexpert.news mechanism paragraph: per-token activations).
+ *   x   [M,K] bf16, row stride ldx elements (ldx >= K, ldx % 8 == 0)
+ *   aq  [M,K] int8, row stride ldq bytes (ldq >= K, ldq % 16 == 0)
+ *   s_a [M]   fp32 per-token scales                                       */
+i8_status i8_quant_act_pertoken(const void* x, int64_t M, int64_t K,
+                                int64_t ldx, int8_t* aq, int64_t ldq,
+                                float* s_a, i8_stream_t stream);
+
+/* Workspace bytes that i8_gemm_int32 / i8_gemm_dequant_bias_bf16 need for
+ * this shape (0 when the shape runs without a K split).  Returns 0 for
+ * shapes the GEMM rejects. */
+size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Raw int32 accumulators, for checking (arXiv 2606.14598, abstract: the
+ * int8 x int8 -> int32 accumulation is verified bit-exact against a library
+ * integer GEMM).
+ *   aq [M,K] int8 contiguous (row stride K), wq [N,K] int8 contiguous
+ *   c  [M,N] int32, row stride ldc elements (ldc >= N, ldc % 4 == 0)
+ *   ws / ws_bytes: device workspace of at least i8_gemm_workspace_bytes()
+ *   (may be NULL when that is 0).  The result is exact for every input.   */
+i8_status i8_gemm_int32(const int8_t* aq, const int8_t* wq, int64_t M,
+                        int64_t N, int64_t K, int32_t* c, int64_t ldc,
+                        void* ws, size_t ws_bytes, i8_stream_t stream);
+
+/* The fused W8A8 GEMM (arXiv 2606.14598, abstract: int8 x int8 -> int32 with
+ * the per-token x per-channel dequantization and the bias folded into the
+ * epilogue; aiexpert.news mechanism paragraph: bf16 is emitted after the
+ * epilogue).
+ *   aq [M,K] int8 contiguous, s_a [M] fp32, wq [N,K] int8 contiguous,
+ *   s_w [N] fp32, bias [N] bf16 or NULL (treated as +0),
+ *   y  [M,N] bf16, row stride ldy elements (ldy >= N, ldy % 8 == 0)
+ *   y[m,n] = bf16_rne(((float(acc) * s_a[m]) * s_w[n]) + bias[n]), each
+ *   step an fp32 operation rounded to nearest even.                        */
+i8_status i8_gemm_dequant_bias_bf16(const int8_t* aq, const float* s_a,
+                                    const int8_t* wq, const float* s_w,
+                                    const void* bias, int64_t M, int64_t N,
+                                    int64_t K, void* y, int64_t ldy, void* ws,
+                                    size_t ws_bytes, i8_stream_t stream);
+
+/* Widens int8 weight codes to fp16 codes (the same integers, exactly), for
+ * i8_gemm_dequant_bias_bf16_w16.  This is part of the offline weight
+ * preparation, next to i8_quant_weight_perchannel: sm_103a has no INT8
+ * tensor-core MMA, the GEMM runs the integer codes through the fp16 tensor
+ * pipe, and a pre-widened weight copy saves the on-chip widening of the
+ * weight operand on every call (at 2 bytes per weight in HBM).
+ *   wq  [N,K] int8 contiguous;  w16 [N,K] fp16 bit patterns, contiguous.   */
+i8_status i8_widen_weight_codes(const int8_t* wq, int64_t N, int64_t K,
+                                void* w16, i8_stream_t stream);
+
+/* i8_gemm_dequant_bias_bf16 with the weight codes given pre-widened to fp16
+ * (from i8_widen_weight_codes).  Same arithmetic, bit-identical output.     */
+i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
+                                        const void* w16, const float* s_w,
+                                        const void* bias, int64_t M, int64_t N,
+                                        int64_t K, void* y, int64_t ldy,
+                                        void* ws, size_t ws_bytes,
+                                        i8_stream_t stream);
+
+/* Process-wide tuning knobs (not thread-safe; set them before launching).
+ *   I8_OPT_CHUNK_K      K-elements per exact fp32 accumulation chunk inside
+ *                       the GEMM: a multiple of 64 in [64, 1024]
+ *                       (default 512, so partial sums stay below 2^23).
+ *   I8_OPT_FORCE_SPLITS K-splits to use for every shape (0 = the table).
+ *   I8_OPT_MAX_CTAS     cap on the persistent grid (0 = one CTA per SM).
+ * Changing FORCE_SPLITS changes i8_gemm_workspace_bytes(). */
+typedef enum {
+  I8_OPT_CHUNK_K = 1,
+  I8_OPT_FORCE_SPLITS = 2,
+  I8_OPT_MAX_CTAS = 3
+} i8_option;
+i8_status i8_set_option(i8_option opt, int64_t value);
+
+/* Failure-detection self-test: queues a one-thread kernel that waits on a
+ * pipeline barrier nothing will ever complete, through the same bounded wait
+ * the GEMM uses, with a limit of limit_ms (1..5000).  The wait runs out, the
+ * kernel records I8_ERR_DEVICE_TIMEOUT in the device status word and returns
+ * normally; the next i8_sync_check() reports it.  The GPU context stays
+ * usable.  (No counterpart on the pages: this is the library's own check of
+ * its timeout path.) */
+i8_status i8_selftest_timeout(int limit_ms, i8_stream_t stream);
+
+/* Waits for `stream`, then reads and clears the current device's status
+ * word: I8_ERR_DEVICE_TIMEOUT if any kernel of this library timed out since
+ * the last check, I8_ERR_CUDA on a CUDA error, else I8_OK. */
+i8_status i8_sync_check(i8_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* I8_H */

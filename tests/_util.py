@@ -1,0 +1,43 @@
+"""Shared helpers for the parity tests: moving seeded inputs to the GPU and
+comparing results with the oracle.  No method arithmetic lives here."""
+import numpy as np
+import torch
+
+from w8a8_int8_quantized_i8_gb300 import inputs
+
+# bf16 parity bar: |gpu - oracle| <= 2^-7 * |oracle| + 1e-6 per element (one
+# bf16 ulp), cosine >= 0.99999, no NaN/Inf.
+REL_TOL = 2.0 ** -7
+ABS_TOL = 1e-6
+COS_MIN = 0.99999
+
+
+def bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def gpu_bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def assert_bf16_close(got_bits: np.ndarray, want_bits: np.ndarray, what: str = ""):
+    g = bits_to_f64(got_bits)
+    w = bits_to_f64(want_bits)
+    assert np.isfinite(g).all(), f"{what}: NaN/Inf in GPU output"
+    err = np.abs(g - w)
+    bad = err > REL_TOL * np.abs(w) + ABS_TOL
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements beyond 1 bf16 ulp; "
+                           f"worst {err.max():.3g}")
+    denom = np.linalg.norm(g) * np.linalg.norm(w)
+    if denom > 0:
+        cos = float((g * w).sum() / denom)
+        assert cos >= COS_MIN, f"{what}: cosine {cos}"
+    return float((got_bits == want_bits).mean())
+
+
+def to_dev(t: torch.Tensor) -> torch.Tensor:
+    return t.contiguous().to("cuda")
+
+
+def int8_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()

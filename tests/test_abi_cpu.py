@@ -1,0 +1,86 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for
+sm_103a, loads, exports every function include/i8.h declares, and rejects bad
+arguments on the host before touching a device."""
+import ctypes
+
+import pytest
+
+from w8a8_int8_quantized_i8_gb300 import binding, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_every_declared_function_is_exported(lib):
+    names = binding.header_functions()
+    assert len(names) >= 12
+    for n in ["i8_quant_weight_perchannel", "i8_quant_act_pertoken", "i8_gemm_int32",
+              "i8_gemm_dequant_bias_bf16", "i8_gemm_workspace_bytes", "i8_sync_check"]:
+        assert n in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    for code, name in binding.STATUS.items():
+        assert lib.i8_status_string(code).decode() == name
+    assert lib.i8_status_string(99).decode() == "I8_ERR_UNKNOWN"
+    assert b"sm_103a" in lib.i8_version()
+
+
+P = ctypes.c_void_p
+
+
+def test_quant_argument_errors(lib):
+    ok = P(0x10000)
+    for fn in (lib.i8_quant_act_pertoken, lib.i8_quant_weight_perchannel):
+        assert fn(ok, -1, 64, 64, ok, 64, ok, None) == 1            # negative rows
+        assert fn(ok, 4, 64, 32, ok, 64, ok, None) == 1             # ldx < K
+        assert fn(None, 4, 64, 64, ok, 64, ok, None) == 1           # NULL input
+        assert fn(ok, 4, 40, 40, ok, 48, ok, None) == 3             # K % 16
+        assert fn(ok, 4, 131072 + 16, 131072 + 16, ok, 131088, ok, None) == 3
+        assert fn(P(0x10008), 4, 64, 64, ok, 64, ok, None) == 2     # misaligned x
+        assert fn(ok, 4, 64, 68, ok, 64, ok, None) == 2             # row stride
+        assert fn(ok, 0, 64, 64, ok, 64, ok, None) == 0             # empty: no-op
+
+
+def test_gemm_argument_errors(lib):
+    ok = P(0x10000)
+    g = lib.i8_gemm_dequant_bias_bf16
+    assert g(ok, ok, ok, ok, None, -1, 8, 16, ok, 8, None, 0, None) == 1
+    assert g(ok, ok, ok, ok, None, 4, 8, 24, ok, 8, None, 0, None) == 3     # K % 16
+    assert g(ok, ok, ok, ok, None, 0, 8, 16, ok, 8, None, 0, None) == 0     # empty
+    assert g(None, ok, ok, ok, None, 4, 8, 16, ok, 8, None, 0, None) == 1
+    assert g(ok, None, ok, ok, None, 4, 8, 16, ok, 8, None, 0, None) == 1   # no scales
+    assert g(P(0x10001), ok, ok, ok, None, 4, 8, 16, ok, 8, None, 0, None) == 2
+    assert g(ok, ok, ok, P(0x10004), None, 4, 8, 16, ok, 8, None, 0, None) == 2  # s_w
+    assert g(ok, ok, ok, ok, P(0x10002), 4, 8, 16, ok, 8, None, 0, None) == 2    # bias
+    assert g(ok, ok, ok, ok, None, 4, 12, 16, ok, 12, None, 0, None) == 2        # ldy % 8
+    c = lib.i8_gemm_int32
+    assert c(ok, ok, 4, 8, 16, ok, 6, None, 0, None) == 1                   # ldc < N
+    assert c(ok, ok, 4, 8, 16, ok, 10, None, 0, None) == 2                  # ldc % 4
+    assert c(ok, ok, 4, 8, 200000, ok, 8, None, 0, None) == 3
+    assert lib.i8_widen_weight_codes(ok, 4, 24, ok, None) == 3
+
+
+def test_options_validation(lib):
+    assert lib.i8_set_option(1, 100) == 1
+    assert lib.i8_set_option(1, 2048) == 1
+    assert lib.i8_set_option(1, 512) == 0
+    assert lib.i8_set_option(2, -1) == 1
+    assert lib.i8_set_option(2, 0) == 0
+    assert lib.i8_set_option(77, 0) == 1
+    assert lib.i8_selftest_timeout(0, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(OSError):
+        binding.load(str(tmp_path / "missing_libi8.so"))
+
+
+def test_workspace_query_rejects_bad_shapes(lib):
+    assert lib.i8_gemm_workspace_bytes(4, 8, 24) == 0
+    assert lib.i8_gemm_workspace_bytes(-4, 8, 16) == 0

@@ -1,0 +1,217 @@
+"""Thin Python binding over libi8 (include/i8.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+checks tensor dtypes/devices/shapes, allocates outputs with torch (the
+library itself allocates nothing), passes raw device pointers and the
+current CUDA stream, and turns status codes into exceptions.  There is no
+fallback: if libi8.so is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {
+    0: "I8_OK", 1: "I8_ERR_INVALID_ARG", 2: "I8_ERR_ALIGNMENT", 3: "I8_ERR_UNSUPPORTED",
+    4: "I8_ERR_WORKSPACE", 5: "I8_ERR_CUDA", 6: "I8_ERR_DEVICE_TIMEOUT",
+}
+OPTIONS = {"chunk_k": 1, "force_splits": 2, "max_ctas": 3}
+
+
+class I8Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/i8.h."""
+    hdr = os.path.join(_build.ROOT, "include", "i8.h")
+    with open(hdr) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\**\s+\**(i8_[a-z0-9_]+)\s*\(",
+                      text, flags=re.M)
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libi8.so (building it first if it is stale).  Raises on failure."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        if path is None:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise OSError(f"libi8 not found at {path}")
+        lib = ctypes.CDLL(path)
+        i64, vp, sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+        st = ctypes.c_int
+        sigs = {
+            "i8_status_string": ([st], ctypes.c_char_p),
+            "i8_version": ([], ctypes.c_char_p),
+            "i8_quant_weight_perchannel": ([vp, i64, i64, i64, vp, i64, vp, vp], st),
+            "i8_quant_act_pertoken": ([vp, i64, i64, i64, vp, i64, vp, vp], st),
+            "i8_gemm_workspace_bytes": ([i64, i64, i64], sz),
+            "i8_gemm_int32": ([vp, vp, i64, i64, i64, vp, i64, vp, sz, vp], st),
+            "i8_gemm_dequant_bias_bf16": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, sz, vp], st),
+            "i8_widen_weight_codes": ([vp, i64, i64, vp, vp], st),
+            "i8_gemm_dequant_bias_bf16_w16": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, sz, vp], st),
+            "i8_set_option": ([ctypes.c_int, i64], st),
+            "i8_sync_check": ([vp], st),
+            "i8_selftest_timeout": ([ctypes.c_int, vp], st),
+        }
+        for name, (args, res) in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        if path == _build.LIB:
+            _lib = lib
+        return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise I8Error(status, what)
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, dtype, name: str, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _quant(fn_name: str, x: torch.Tensor):
+    _need(x, torch.bfloat16, "x", 2)
+    R, K = x.shape
+    q = torch.empty((R, K), dtype=torch.int8, device=x.device)
+    s = torch.empty((R,), dtype=torch.float32, device=x.device)
+    lib = load()
+    with torch.cuda.device(x.device):
+        _check(getattr(lib, fn_name)(_ptr(x), R, K, K, _ptr(q), K, _ptr(s), _stream(x)), fn_name)
+    return q, s
+
+
+def quant_act_pertoken(x: torch.Tensor):
+    """bf16 [M,K] -> (int8 codes [M,K], fp32 per-token scales [M])."""
+    return _quant("i8_quant_act_pertoken", x)
+
+
+def quant_weight_perchannel(w: torch.Tensor):
+    """bf16 [N,K] -> (int8 codes [N,K], fp32 per-channel scales [N])."""
+    return _quant("i8_quant_weight_perchannel", w)
+
+
+def widen_weight_codes(wq: torch.Tensor) -> torch.Tensor:
+    """int8 weight codes [N,K] -> the same integers as fp16 [N,K] (exact)."""
+    _need(wq, torch.int8, "wq", 2)
+    N, K = wq.shape
+    w16 = torch.empty((N, K), dtype=torch.float16, device=wq.device)
+    with torch.cuda.device(wq.device):
+        _check(load().i8_widen_weight_codes(_ptr(wq), N, K, _ptr(w16), _stream(wq)),
+               "i8_widen_weight_codes")
+    return w16
+
+
+def workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().i8_gemm_workspace_bytes(M, N, K))
+
+
+def _workspace(M, N, K, device, workspace):
+    need = workspace_bytes(M, N, K)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def gemm_int32(aq: torch.Tensor, wq: torch.Tensor, out: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Exact int32 accumulators aq @ wq.T (int8 [M,K] x int8 [N,K])."""
+    _need(aq, torch.int8, "aq", 2)
+    _need(wq, torch.int8, "wq", 2)
+    M, K = aq.shape
+    N = wq.shape[0]
+    if wq.shape[1] != K:
+        raise ValueError("K mismatch")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=aq.device)
+    _need(out, torch.int32, "out", 2)
+    ws, wsb = _workspace(M, N, K, aq.device, workspace)
+    with torch.cuda.device(aq.device):
+        _check(load().i8_gemm_int32(_ptr(aq), _ptr(wq), M, N, K, _ptr(out), out.stride(0),
+                                    _ptr(ws), wsb, _stream(aq)), "i8_gemm_int32")
+    return out
+
+
+def gemm_dequant_bias_bf16(aq, s_a, wq, s_w, bias=None, out=None, workspace=None):
+    """Fused W8A8 GEMM: bf16(acc * s_a[m] * s_w[n] + bias[n]).
+
+    ``wq`` is either the int8 codes [N,K] or their fp16-widened copy
+    (``widen_weight_codes``); the result is the same either way.
+    """
+    _need(aq, torch.int8, "aq", 2)
+    _need(s_a, torch.float32, "s_a", 1)
+    _need(s_w, torch.float32, "s_w", 1)
+    wide = isinstance(wq, torch.Tensor) and wq.dtype == torch.float16
+    _need(wq, torch.float16 if wide else torch.int8, "wq", 2)
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = aq.shape
+    N = wq.shape[0]
+    if wq.shape[1] != K or s_a.shape[0] != M or s_w.shape[0] != N:
+        raise ValueError("shape mismatch")
+    if bias is not None and bias.shape[0] != N:
+        raise ValueError("bias shape")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    _need(out, torch.bfloat16, "out", 2)
+    ws, wsb = _workspace(M, N, K, aq.device, workspace)
+    fn = "i8_gemm_dequant_bias_bf16_w16" if wide else "i8_gemm_dequant_bias_bf16"
+    with torch.cuda.device(aq.device):
+        _check(getattr(load(), fn)(_ptr(aq), _ptr(s_a), _ptr(wq), _ptr(s_w), _ptr(bias), M, N, K,
+                                   _ptr(out), out.stride(0), _ptr(ws), wsb, _stream(aq)), fn)
+    return out
+
+
+def linear(x, wq, s_w, bias=None, out=None, workspace=None):
+    """The whole W8A8 linear layer: per-token quant of x, then the fused GEMM."""
+    aq, s_a = quant_act_pertoken(x)
+    return gemm_dequant_bias_bf16(aq, s_a, wq, s_w, bias, out=out, workspace=workspace)
+
+
+def set_option(name: str, value: int) -> None:
+    _check(load().i8_set_option(OPTIONS[name], int(value)), f"i8_set_option({name})")
+
+
+def sync_check(device=None) -> None:
+    """Synchronize the current stream and raise if a kernel recorded an error."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        s = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+        _check(load().i8_sync_check(s), "i8_sync_check")

@@ -1,0 +1,412 @@
+// i8_api.cu -- the C ABI of libi8 (declared in include/i8.h): argument
+// validation, the shape -> kernel-configuration table, TMA descriptors and
+// the launches.  The whole library is this one translation unit.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/i8.h"
+#include "gemm.cuh"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+namespace i8 {
+
+// ----------------------------------------------------------------- widen
+// int8 codes -> fp16 codes (exact); 16 codes per thread per step.
+__global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restrict__ src,
+                                                          uint16_t* __restrict__ dst,
+                                                          int64_t n16) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + i * 16);
+    uint4 o0, o1;
+    s8x4_to_f16x4(v.x, o0.x, o0.y);
+    s8x4_to_f16x4(v.y, o0.z, o0.w);
+    s8x4_to_f16x4(v.z, o1.x, o1.y);
+    s8x4_to_f16x4(v.w, o1.z, o1.w);
+    reinterpret_cast<uint4*>(dst + i * 16)[0] = o0;
+    reinterpret_cast<uint4*>(dst + i * 16)[1] = o1;
+  }
+}
+
+// Failure-detection self-test: one thread waits on an mbarrier that nothing
+// ever arrives at, through the same bounded wait the GEMM pipeline uses.  The
+// wait gives up after limit_ns, records I8_ERR_DEVICE_TIMEOUT in the status
+// word and the kernel returns normally (no trap, no fault, no hang).
+__global__ void selftest_timeout_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  abort_flag = 0;
+  fence_mbarrier_init();
+  mbar_wait(b, 0u, &abort_flag, limit_ns);
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Process-wide tuning knobs (i8_set_option).
+struct Options {
+  int chunk_k = 512;       // K per exact fp32 chunk (multiple of 64, <= 1024)
+  int force_splits = 0;    // 0 = table
+  int max_ctas = 0;        // 0 = all SMs
+};
+Options g_opt;
+
+struct DeviceInfo {
+  bool init = false;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  bool smem_set[8] = {};
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+i8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? I8_OK : I8_ERR_CUDA; }
+
+i8_status device_info(DeviceInfo** out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return I8_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return I8_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+            cudaSuccess)
+      return I8_ERR_CUDA;
+    d.init = true;
+  }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return I8_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = &d;
+  if (dev_out) *dev_out = dev;
+  return I8_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// ----------------------------------------------------------------- quant
+template <int V>
+void launch_quant_v(const uint16_t* x, int64_t rows, int K, int64_t ldx, int8_t* q, int64_t ldq,
+                    float* s, int G, cudaStream_t st) {
+  const int rows_per_cta = 8 / G;
+  const int64_t grid = (rows + rows_per_cta - 1) / rows_per_cta;
+  quant_rows_kernel<V><<<static_cast<unsigned>(grid), 256, 0, st>>>(x, rows, K, ldx, q, ldq, s, G);
+}
+
+i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t* q, int64_t ldq,
+                     float* s, cudaStream_t st) {
+  if (rows < 0 || K <= 0 || ldx < K || ldq < K) return I8_ERR_INVALID_ARG;
+  if (rows > 0 && (!x || !q || !s)) return I8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || K > 131072 || rows > INT32_MAX) return I8_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(q) || !aligned4(s) || ldx % 8 != 0 || ldq % 16 != 0)
+    return I8_ERR_ALIGNMENT;
+  if (rows == 0) return I8_OK;
+  DeviceInfo* d;
+  if (i8_status e = device_info(&d, nullptr)) return e;
+  // Vectors of 8 elements per row; G warps per row, V vectors per lane.
+  const int vecs = static_cast<int>(K / 8);
+  int G = 1;
+  while (G < 8 && (vecs + 32 * G - 1) / (32 * G) > 12) G *= 2;
+  const int need = (vecs + 32 * G - 1) / (32 * G);
+  const auto* xb = static_cast<const uint16_t*>(x);
+  const int Ki = static_cast<int>(K);
+  if (need <= 1) launch_quant_v<1>(xb, rows, Ki, ldx, q, ldq, s, G, st);
+  else if (need <= 2) launch_quant_v<2>(xb, rows, Ki, ldx, q, ldq, s, G, st);
+  else if (need <= 4) launch_quant_v<4>(xb, rows, Ki, ldx, q, ldq, s, G, st);
+  else if (need <= 8) launch_quant_v<8>(xb, rows, Ki, ldx, q, ldq, s, G, st);
+  else if (need <= 12) launch_quant_v<12>(xb, rows, Ki, ldx, q, ldq, s, G, st);
+  else launch_quant_v<16>(xb, rows, Ki, ldx, q, ldq, s, G, st);
+  return cuda_status(cudaGetLastError());
+}
+
+// ----------------------------------------------------------------- GEMM plan
+struct Plan {
+  int bn = 128;
+  int splits = 1;
+  int kb_per_split = 1;
+  int total_kb = 1;
+  int num_m = 1, num_n = 1;
+  int num_tiles = 1;
+  int grid = 1;
+  int chunk_stages = 8;
+  int64_t ws_ld = 0;       // row stride of the split partials (elements)
+  size_t ws_bytes = 0;
+};
+
+// Shape -> configuration (replaces per-shape autotuning): 128 x 128 tiles;
+// when the output tiles cannot fill every SM, K is split so that tiles x
+// splits covers the SMs, with at least two 128-wide K-blocks per split.
+Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
+  Plan p;
+  p.bn = 128;
+  p.total_kb = static_cast<int>((K + 127) / 128);
+  p.num_m = static_cast<int>((M + 127) / 128);
+  p.num_n = static_cast<int>((N + p.bn - 1) / p.bn);
+  const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+  int splits = 1;
+  if (g_opt.force_splits > 0) {
+    splits = g_opt.force_splits;
+  } else if (tiles < sms) {
+    splits = static_cast<int>(sms / tiles);
+    splits = std::min(splits, std::max(1, p.total_kb / 2));
+    splits = std::min(splits, 16);
+  }
+  splits = std::max(1, std::min(splits, p.total_kb));
+  p.kb_per_split = (p.total_kb + splits - 1) / splits;
+  p.splits = (p.total_kb + p.kb_per_split - 1) / p.kb_per_split;
+  p.num_tiles = static_cast<int>(tiles * p.splits);
+  const int cap = g_opt.max_ctas > 0 ? std::min(g_opt.max_ctas, sms) : sms;
+  p.grid = std::max(1, std::min(p.num_tiles, cap));
+  p.chunk_stages = g_opt.chunk_k / 64;
+  if (p.splits > 1) {
+    p.ws_ld = (N + 3) / 4 * 4;
+    p.ws_bytes = static_cast<size_t>(p.splits) * static_cast<size_t>(M) *
+                 static_cast<size_t>(p.ws_ld) * sizeof(int32_t);
+  }
+  return p;
+}
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <class Cfg>
+i8_status launch_gemm_cfg(DeviceInfo* d, int slot, const CUtensorMap& ma, const CUtensorMap& mb,
+                          const GemmParams& gp, int grid, cudaStream_t st) {
+  auto kern = gemm_w8a8_kernel<Cfg>;
+  if (!d->smem_set[slot]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM_BYTES) != cudaSuccess)
+      return I8_ERR_CUDA;
+    d->smem_set[slot] = true;
+  }
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ma, mb, gp);
+  return cuda_status(cudaGetLastError());
+}
+
+using CfgConv = GemmCfg<128, 3, 3, true>;    // int8 weights, widened on chip
+using CfgWide = GemmCfg<128, 3, 3, false>;   // weights pre-widened to fp16 codes
+
+// Common GEMM driver.  b16 = weights given as fp16 codes instead of int8.
+i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int64_t N, int64_t K,
+                      int out_mode, void* out, int64_t ldo, const float* s_a, const float* s_w,
+                      const void* bias, void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (M < 0 || N < 0 || K <= 0) return I8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX) return I8_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return I8_OK;
+  if (!aq || !wb || !out || ldo < N) return I8_ERR_INVALID_ARG;
+  if (out_mode == kOutBf16 && (!s_a || !s_w)) return I8_ERR_INVALID_ARG;
+  if (!aligned16(aq) || !aligned16(wb) || !aligned16(out)) return I8_ERR_ALIGNMENT;
+  if (out_mode == kOutBf16 && (ldo % 8 != 0 || !aligned4(s_a) || !aligned16(s_w) ||
+                               (bias && !aligned16(bias))))
+    return I8_ERR_ALIGNMENT;
+  if (out_mode == kOutInt32 && ldo % 4 != 0) return I8_ERR_ALIGNMENT;
+  DeviceInfo* d;
+  if (i8_status e = device_info(&d, nullptr)) return e;
+  const Plan pl = make_plan(M, N, K, d->sms);
+  if (pl.ws_bytes > 0) {
+    if (!ws || ws_bytes < pl.ws_bytes) return I8_ERR_WORKSPACE;
+    if (!aligned16(ws)) return I8_ERR_ALIGNMENT;
+  }
+  CUtensorMap ma, mb;
+  if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M, K, 128, 128)) return I8_ERR_CUDA;
+  if (b16) {
+    if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wb, K, N, 2 * K, 64, 128))
+      return I8_ERR_CUDA;
+  } else {
+    if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, K, N, K, 128, 128)) return I8_ERR_CUDA;
+  }
+  GemmParams gp{};
+  gp.M = static_cast<int>(M);
+  gp.N = static_cast<int>(N);
+  gp.K = static_cast<int>(K);
+  gp.num_m_blk = pl.num_m;
+  gp.num_n_blk = pl.num_n;
+  gp.splits = pl.splits;
+  gp.kb_per_split = pl.kb_per_split;
+  gp.total_kb = pl.total_kb;
+  gp.num_tiles = pl.num_tiles;
+  gp.chunk_stages = pl.chunk_stages;
+  gp.s_a = s_a;
+  gp.s_w = s_w;
+  gp.bias = static_cast<const uint16_t*>(bias);
+  if (pl.splits > 1) {
+    gp.out_mode = kOutPartial;
+    gp.out = ws;
+    gp.ldo = pl.ws_ld;
+    gp.split_stride = static_cast<int64_t>(M) * pl.ws_ld;
+  } else {
+    gp.out_mode = out_mode;
+    gp.out = out;
+    gp.ldo = ldo;
+    gp.split_stride = 0;
+  }
+  i8_status e = b16 ? launch_gemm_cfg<CfgWide>(d, 1, ma, mb, gp, pl.grid, st)
+                    : launch_gemm_cfg<CfgConv>(d, 0, ma, mb, gp, pl.grid, st);
+  if (e != I8_OK) return e;
+  if (pl.splits > 1) {
+    GemmParams rp = gp;
+    rp.out_mode = out_mode;
+    rp.out = out;
+    rp.ldo = ldo;
+    const int64_t groups = M * ((N + 3) / 4);
+    const int64_t blocks = std::min<int64_t>((groups + 255) / 256, static_cast<int64_t>(d->sms) * 16);
+    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const int32_t*>(ws), gp.split_stride, pl.ws_ld, pl.splits, rp);
+    return cuda_status(cudaGetLastError());
+  }
+  return I8_OK;
+}
+
+}  // namespace
+}  // namespace i8
+
+using namespace i8;
+
+extern "C" {
+
+const char* i8_status_string(i8_status s) {
+  switch (s) {
+    case I8_OK: return "I8_OK";
+    case I8_ERR_INVALID_ARG: return "I8_ERR_INVALID_ARG";
+    case I8_ERR_ALIGNMENT: return "I8_ERR_ALIGNMENT";
+    case I8_ERR_UNSUPPORTED: return "I8_ERR_UNSUPPORTED";
+    case I8_ERR_WORKSPACE: return "I8_ERR_WORKSPACE";
+    case I8_ERR_CUDA: return "I8_ERR_CUDA";
+    case I8_ERR_DEVICE_TIMEOUT: return "I8_ERR_DEVICE_TIMEOUT";
+  }
+  return "I8_ERR_UNKNOWN";
+}
+
+const char* i8_version(void) { return "i8 0.1.0 sm_103a"; }
+
+i8_status i8_quant_weight_perchannel(const void* w, int64_t N, int64_t K, int64_t ldw, int8_t* wq,
+                                     int64_t ldq, float* s_w, i8_stream_t stream) {
+  return quant_rows(w, N, K, ldw, wq, ldq, s_w, reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_quant_act_pertoken(const void* x, int64_t M, int64_t K, int64_t ldx, int8_t* aq,
+                                int64_t ldq, float* s_a, i8_stream_t stream) {
+  return quant_rows(x, M, K, ldx, aq, ldq, s_a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX)
+    return 0;
+  DeviceInfo* d;
+  if (device_info(&d, nullptr) != I8_OK) return 0;
+  return make_plan(M, N, K, d->sms).ws_bytes;
+}
+
+i8_status i8_gemm_int32(const int8_t* aq, const int8_t* wq, int64_t M, int64_t N, int64_t K,
+                        int32_t* c, int64_t ldc, void* ws, size_t ws_bytes, i8_stream_t stream) {
+  return gemm_common(aq, wq, false, M, N, K, kOutInt32, c, ldc, nullptr, nullptr, nullptr, ws,
+                     ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_gemm_dequant_bias_bf16(const int8_t* aq, const float* s_a, const int8_t* wq,
+                                    const float* s_w, const void* bias, int64_t M, int64_t N,
+                                    int64_t K, void* y, int64_t ldy, void* ws, size_t ws_bytes,
+                                    i8_stream_t stream) {
+  return gemm_common(aq, wq, false, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_widen_weight_codes(const int8_t* wq, int64_t N, int64_t K, void* w16,
+                                i8_stream_t stream) {
+  if (N < 0 || K <= 0) return I8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || K > 131072) return I8_ERR_UNSUPPORTED;
+  if (N == 0) return I8_OK;
+  if (!wq || !w16) return I8_ERR_INVALID_ARG;
+  if (!aligned16(wq) || !aligned16(w16)) return I8_ERR_ALIGNMENT;
+  DeviceInfo* d;
+  if (i8_status e = device_info(&d, nullptr)) return e;
+  const int64_t n16 = N * K / 16;
+  const int64_t blocks = std::min<int64_t>((n16 + 255) / 256, static_cast<int64_t>(d->sms) * 8);
+  widen_codes_kernel<<<static_cast<unsigned>(blocks), 256, 0,
+                       reinterpret_cast<cudaStream_t>(stream)>>>(wq, static_cast<uint16_t*>(w16),
+                                                                 n16);
+  return cuda_status(cudaGetLastError());
+}
+
+i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a, const void* w16,
+                                        const float* s_w, const void* bias, int64_t M, int64_t N,
+                                        int64_t K, void* y, int64_t ldy, void* ws,
+                                        size_t ws_bytes, i8_stream_t stream) {
+  return gemm_common(aq, w16, true, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_set_option(i8_option opt, int64_t value) {
+  switch (opt) {
+    case I8_OPT_CHUNK_K:
+      if (value < 64 || value > 1024 || value % 64 != 0) return I8_ERR_INVALID_ARG;
+      g_opt.chunk_k = static_cast<int>(value);
+      return I8_OK;
+    case I8_OPT_FORCE_SPLITS:
+      if (value < 0 || value > 1024) return I8_ERR_INVALID_ARG;
+      g_opt.force_splits = static_cast<int>(value);
+      return I8_OK;
+    case I8_OPT_MAX_CTAS:
+      if (value < 0) return I8_ERR_INVALID_ARG;
+      g_opt.max_ctas = static_cast<int>(value);
+      return I8_OK;
+  }
+  return I8_ERR_INVALID_ARG;
+}
+
+i8_status i8_selftest_timeout(int limit_ms, i8_stream_t stream) {
+  if (limit_ms < 1 || limit_ms > 5000) return I8_ERR_INVALID_ARG;
+  selftest_timeout_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<unsigned long long>(limit_ms) * 1000000ull);
+  return cuda_status(cudaGetLastError());
+}
+
+i8_status i8_sync_check(i8_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return I8_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status, sizeof(word)) != cudaSuccess) return I8_ERR_CUDA;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return I8_ERR_CUDA;
+    if (word & (1u << I8_ERR_DEVICE_TIMEOUT)) return I8_ERR_DEVICE_TIMEOUT;
+    return I8_ERR_CUDA;
+  }
+  return I8_OK;
+}
+
+}  // extern "C"
