@@ -1,0 +1,400 @@
+"""Benchmark of the W8A8 INT8 linear layer on GB300.
+
+One step = the whole hot path over one batch of synthetic, device-resident
+input: per-token INT8 quantization of X (bf16 [M,K]) and the fused int8 GEMM
+with the per-token x per-channel dequantization + bias epilogue (bf16 [M,N]).
+Weights are quantized per channel once, before timing (post-training, offline).
+
+Default workload: the DiT QKV projection at 768px, batch 1:
+M = 2304 image + 256 text tokens = 2560, K = 3072, N = 9216.
+
+Prints ONE JSON line (rank 0).  `value` is INT8 TOPS (2*M*N*K per step over
+the device-timed step), `roofline` describes the GEMM kernel against the
+measured dense fp16/bf16 tensor peak (the pipe the int8 codes run through on
+sm_103a), `cpu_baseline` times the plain C oracle on a bounded row sample on
+the host cores, `e2e` repeats the metric through the public API with host
+buffers (H2D of X and D2H of Y inside the timed region).
+
+`--impl reference` times the oracle (the reference implementation of this
+build) on the host cores instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload qkv768|mlp_up1024|mlp_down1024|tiny] [--weights int8|w16]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from w8a8_int8_quantized_i8_gb300 import inputs  # noqa: E402
+
+METRIC = "fused W8A8 GEMM INT8 TOPS and % of GB300 dense INT8 peak at DiT shapes"
+WORKLOADS = {
+    "qkv768": inputs.QKV_768,
+    "mlp_up1024": inputs.MLP_UP_1024,
+    "mlp_down1024": inputs.MLP_DOWN_1024,
+    "tiny": inputs.TINY,
+}
+L2_BYTES = 129 * 1024 * 1024
+ROTATE_MIN_BYTES = 3 * L2_BYTES
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return dist, rank, ws, local
+    return None, 0, 1, 0
+
+
+def _max_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if sm:
+            out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                   "reasons": sorted(reasons), "samples": len(sm)}
+        return out
+
+
+# --------------------------------------------------------------------- oracle arm
+def _oracle_sample(shape, target_s: float):
+    """Time the oracle (quant of sampled rows + GEMM against all N weights +
+    epilogue) on the host cores; grow the row sample until it takes target_s."""
+    import oracle
+    oracle.build()
+    d = inputs.linear_inputs(shape)
+    xb = inputs.bits(d["x"])
+    wq, s_w = oracle.quant_rows(inputs.bits(d["w"]))   # offline, like the GPU arm
+    bb = inputs.bits(d["bias"])
+    rows = 4
+    while True:
+        t0 = time.perf_counter()
+        aq, s_a = oracle.quant_rows(xb[:rows])
+        acc = oracle.gemm_s32(aq, wq)
+        oracle.dequant_bias(acc, s_a, s_w, bb)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or rows >= shape.M:
+            break
+        rows = min(shape.M, max(rows * 2, int(rows * target_s / max(dt, 1e-3) * 0.8)))
+    ops = 2.0 * rows * shape.N * shape.K
+    return dict(rows=rows, seconds=dt, tops=ops / dt / 1e12, threads=oracle.num_threads(),
+                xb=xb, wq=wq, s_w=s_w, bb=bb)
+
+
+def run_reference(args, shape, dist, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    d = inputs.linear_inputs(shape)
+    xb = inputs.bits(d["x"])
+    wq, s_w = oracle.quant_rows(inputs.bits(d["w"]))
+    bb = inputs.bits(d["bias"])
+    # rows per step: about 0.25 s of oracle work per step on this host
+    rows = 4
+    while True:
+        t0 = time.perf_counter()
+        aq, s_a = oracle.quant_rows(xb[:rows])
+        oracle.dequant_bias(oracle.gemm_s32(aq, wq), s_a, s_w, bb)
+        dt = time.perf_counter() - t0
+        if dt >= 0.2 or rows >= shape.M:
+            break
+        rows = min(shape.M, rows * 2)
+    times = []
+    for i in range(args.warmup + args.steps):
+        r0 = (i * rows) % max(1, shape.M - rows + 1)
+        t0 = time.perf_counter()
+        aq, s_a = oracle.quant_rows(xb[r0:r0 + rows])
+        oracle.dequant_bias(oracle.gemm_s32(aq, wq), s_a, s_w, bb)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    t = sum(times) / len(times)
+    ops = 2.0 * rows * shape.N * shape.K
+    v = ops / t / 1e12
+    cores = oracle.num_threads()
+    sample = f"{rows} of {shape.M} token rows per step, all N={shape.N} channels, K={shape.K}"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": shape.name, "M": shape.M, "K": shape.K, "N": shape.N},
+        "cpu_baseline": {"value": v, "unit": "TOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
+# --------------------------------------------------------------------- GPU arm
+def run_ours(args, shape, dist, rank, world, local):
+    import w8a8_int8_quantized_i8_gb300 as i8
+    from w8a8_int8_quantized_i8_gb300 import binding
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = i8.load()
+    M, K, N = shape.M, shape.K, shape.N
+    hbm_peak, tc_peak, peak_kind = _peaks()
+
+    d = inputs.linear_inputs(shape)
+    x_host = d["x"]
+    set_bytes = M * K * 2 + M * K + M * 4 + M * N * 2 + N * K * (2 if args.weights == "w16" else 1)
+    R = max(2, min(8, -(-ROTATE_MIN_BYTES // set_bytes)))
+    sets = []
+    w_dev = d["w"].to(dev)
+    b_dev = d["bias"].to(dev)
+    wq0, s_w = i8.quant_weight_perchannel(w_dev)
+    if args.weights == "w16":
+        wq0 = i8.widen_weight_codes(wq0)
+    ws_bytes = i8.workspace_bytes(M, N, K)
+    for r in range(R):
+        sets.append(dict(
+            x=x_host.to(dev), aq=torch.empty(M, K, dtype=torch.int8, device=dev),
+            s_a=torch.empty(M, dtype=torch.float32, device=dev),
+            w=wq0.clone(), y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+            ws=torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)))
+    del wq0
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    gemm_fn = lib.i8_gemm_dequant_bias_bf16_w16 if args.weights == "w16" else lib.i8_gemm_dequant_bias_bf16
+    vp = ctypes.c_void_p
+    calls = []
+    for s in sets:
+        calls.append((
+            (vp(s["x"].data_ptr()), M, K, K, vp(s["aq"].data_ptr()), K, vp(s["s_a"].data_ptr()), sp),
+            (vp(s["aq"].data_ptr()), vp(s["s_a"].data_ptr()), vp(s["w"].data_ptr()),
+             vp(s_w.data_ptr()), vp(b_dev.data_ptr()), M, N, K, vp(s["y"].data_ptr()), N,
+             vp(s["ws"].data_ptr()), ws_bytes, sp)))
+    quant_fn = lib.i8_quant_act_pertoken
+
+    def step(i, evq=None, evg=None):
+        qa, ga = calls[i % R]
+        if evq is not None:
+            evq[0].record(stream)
+        st = quant_fn(*qa)
+        if evg is not None:
+            evg[0].record(stream)
+        st |= gemm_fn(*ga)
+        if evg is not None:
+            evg[1].record(stream)
+        if st:
+            raise RuntimeError(f"libi8 call failed with status {st}")
+
+    for i in range(args.warmup):
+        step(i)
+    binding.sync_check(dev)
+
+    ev_q = [(torch.cuda.Event(enable_timing=True),) for _ in range(args.steps)]
+    ev_g = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    _barrier(dist)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i, ev_q[i], ev_g[i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(dist)
+    clk = clocks.stop()
+    binding.sync_check(dev)
+    t_ms = e0.elapsed_time(e1) / args.steps
+    t_ms = _max_over_ranks(dist, t_ms)
+    gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_g)
+    quant_ms = statistics.mean(q[0].elapsed_time(g[0]) for q, g in zip(ev_q, ev_g))
+    ops = 2.0 * M * N * K
+    total_ops = _sum_over_ranks(dist, ops * args.steps)
+    value = total_ops / (t_ms * 1e-3 * args.steps) / 1e12
+    gemm_tops = ops / (gemm_ms * 1e-3) / 1e12
+    quant_bytes = 3.0 * M * K + 4.0 * M
+    splits = 1 if ws_bytes == 0 else "split-K"
+    launches_per_step = 2 + (1 if ws_bytes > 0 else 0)
+
+    # ---- e2e through the public API with host buffers
+    e2e_steps = max(3, min(args.steps, 50))
+    x_pin = x_host.pin_memory()
+    y_pin = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    s0 = sets[0]
+    for _ in range(2):
+        s0["x"].copy_(x_pin, non_blocking=True)
+        y = i8.linear(s0["x"], s0["w"], s_w, b_dev, out=s0["y"], workspace=s0["ws"] if ws_bytes else None)
+        y_pin.copy_(y, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    _barrier(dist)
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        s0["x"].copy_(x_pin, non_blocking=True)
+        y = i8.linear(s0["x"], s0["w"], s_w, b_dev, out=s0["y"], workspace=s0["ws"] if ws_bytes else None)
+        y_pin.copy_(y, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = _max_over_ranks(dist, f0.elapsed_time(f1) / e2e_steps)
+    e2e_val = _sum_over_ranks(dist, ops) / (e2e_ms * 1e-3) / 1e12
+
+    # ---- oracle on the host cores (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        o = _oracle_sample(shape, target_s=8.0)
+        cpu = {"value": o["tops"], "unit": "TOPS", "cores": o["threads"], "kind": "oracle",
+               "sample": (f"{o['rows']} of {M} token rows (all N={N} channels, K={K}): "
+                          f"quant + int32 GEMM + epilogue in {o['seconds']:.2f} s")}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8", "data": "synthetic",
+            "config": {"workload": shape.name, "M": M, "K": K, "N": N,
+                       "weights": "int8 codes" if args.weights == "int8" else
+                                  "fp16-widened int8 codes (offline)",
+                       "l2": f"rotating {R} buffer sets of {set_bytes / 1e6:.0f} MB "
+                             f"(inputs of a step last touched {R - 1} steps earlier)",
+                       "k_split": splits, "replicas": world},
+            "roofline": {"bound": "tensor", "achieved": gemm_tops, "peak": tc_peak,
+                         "unit": "TFLOP/s", "frac": gemm_tops / tc_peak, "traffic": None,
+                         "kernel": "gemm_w8a8_kernel (+split-K reduce when split)",
+                         "peak_note": f"{peak_kind} dense bf16 burst (same nominal rate as the "
+                                      "fp16 kind the int8 codes run through)"},
+            "quant_roofline": {"bound": "hbm", "achieved": quant_bytes / (quant_ms * 1e-3) / 1e9,
+                               "peak": hbm_peak, "unit": "GB/s",
+                               "frac": quant_bytes / (quant_ms * 1e-3) / 1e9 / hbm_peak,
+                               "kernel": "quant_rows_kernel", "us": quant_ms * 1e3},
+            "gemm_us": gemm_ms * 1e3,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "TOPS", "h2d_bytes_per_step": M * K * 2,
+                    "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+        }
+        print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qkv768")
+    ap.add_argument("--weights", choices=["int8", "w16"], default="int8")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    shape = WORKLOADS[args.workload]
+    dist, rank, world, local = _dist()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, shape, dist, rank, world)
+        return run_ours(args, shape, dist, rank, world, local)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,206 @@
+"""GPU parity of the fused W8A8 GEMM against the oracle.
+
+int32 accumulators must be bit-identical (also against torch._int_mm, the
+pages' own check); bf16 outputs must be within one bf16 ulp (|d| <= 2^-7|y| +
+1e-6), cosine >= 0.99999, no NaN/Inf.  Shapes span several tiles, ragged M/N/K
+tails, the split-K path, adversarial +-127 operands that would overflow fp32
+exactness without the chunked accumulation, and full-size DiT layers on
+sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+import w8a8_int8_quantized_i8_gb300 as i8
+from w8a8_int8_quantized_i8_gb300 import inputs
+from tests._util import assert_bf16_close, gpu_bf16_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+INT_SHAPES = [
+    (64, 128, 256),
+    (1, 8, 16),
+    (7, 24, 48),
+    (129, 136, 272),
+    (256, 384, 1024),
+    (300, 200, 1040),
+    (2, 9216, 3072),       # skinny: split-K
+    (16, 3072, 12288),     # skinny, deep: split-K
+    (1024, 1024, 4096),
+]
+
+
+@pytest.mark.parametrize("M,N,K", INT_SHAPES)
+def test_gemm_int32_matches_oracle(orc, M, N, K):
+    a = inputs.random_int8(M, K, seed=M + K)
+    w = inputs.random_int8(N, K, seed=N + 3 * K)
+    c = i8.gemm_int32(to_dev(a), to_dev(w))
+    i8.sync_check()
+    got = c.cpu().numpy()
+    want = orc.gemm_s32(a.numpy(), w.numpy())
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:4].tolist()}"
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 128, 256), (256, 384, 1024), (1024, 1024, 4096)])
+def test_gemm_int32_matches_torch_int_mm(M, N, K):
+    a = to_dev(inputs.random_int8(M, K, seed=5 + M))
+    w = to_dev(inputs.random_int8(N, K, seed=6 + N))
+    c = i8.gemm_int32(a, w)
+    ref = torch._int_mm(a, w.t())
+    assert torch.equal(c, ref)
+
+
+def _adversarial(M, N, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    a = torch.full((M, K), 127, dtype=torch.int8)
+    w = torch.full((N, K), 127, dtype=torch.int8)
+    # rows 1..: random signs at full magnitude; row 2: large then small terms
+    sa = torch.randint(0, 2, (M, K), generator=g, dtype=torch.int8) * 2 - 1
+    sw = torch.randint(0, 2, (N, K), generator=g, dtype=torch.int8) * 2 - 1
+    a[1:] *= sa[1:]
+    w[1:] *= sw[1:]
+    if M > 2:
+        a[2, K // 2:] = 1
+    if N > 2:
+        w[2, K // 2:] = -1
+    a[min(3, M - 1)] = -127
+    return a, w
+
+
+@pytest.mark.parametrize("chunk_k", [64, 256, 512, 1024])
+def test_gemm_int32_adversarial_exact(orc, chunk_k):
+    """+-127 operands: partial sums reach 127^2 * chunk_k; K = 8192 overflows
+    fp32 exactness (2^24) unless the accumulation is chunked correctly."""
+    M, N, K = 130, 136, 8192
+    a, w = _adversarial(M, N, K, seed=chunk_k)
+    i8.set_option("chunk_k", chunk_k)
+    try:
+        c = i8.gemm_int32(to_dev(a), to_dev(w))
+        i8.sync_check()
+    finally:
+        i8.set_option("chunk_k", 512)
+    got = c.cpu().numpy()
+    want = orc.gemm_s32(a.numpy(), w.numpy())
+    assert got[0, 0] == 127 * 127 * K
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"chunk {chunk_k}: {len(bad)} mismatches, first {bad[:4].tolist()}"
+
+
+def test_gemm_int32_extreme_k():
+    """K = 131072 (the int32 bound): +127 x +127 gives 2114060288 exactly."""
+    M, N, K = 2, 16, 131072
+    a = torch.full((M, K), 127, dtype=torch.int8, device="cuda")
+    w = torch.full((N, K), 127, dtype=torch.int8, device="cuda")
+    w[1] = -127
+    c = i8.gemm_int32(a, w)
+    i8.sync_check()
+    assert int(c[0, 0]) == 2114060288
+    assert int(c[1, 1]) == -2114060288
+
+
+def _oracle_linear_rows(orc, x, w, b, rows):
+    """Oracle y for the selected rows (per-token quant is row-local)."""
+    xs = inputs.bits(x[rows])
+    aq, s_a = orc.quant_rows(xs)
+    wq, s_w = orc.quant_rows(inputs.bits(w))
+    acc = orc.gemm_s32(aq, wq)
+    return orc.dequant_bias(acc, s_a, s_w, None if b is None else inputs.bits(b))
+
+
+def _gpu_linear(x, w, b, widened=False):
+    wq, s_w = i8.quant_weight_perchannel(to_dev(w))
+    if widened:
+        wq = i8.widen_weight_codes(wq)
+    y = i8.linear(to_dev(x), wq, s_w, None if b is None else to_dev(b))
+    i8.sync_check()
+    return y
+
+
+@pytest.mark.parametrize("M,N,K,bias", [
+    (64, 128, 256, True),        # tiny config
+    (1, 8, 16, True),
+    (7, 24, 48, False),
+    (129, 136, 272, True),
+    (300, 200, 1040, False),
+    (16, 3072, 12288, True),     # split-K path with the bf16 epilogue
+    (2, 9216, 3072, True),
+])
+def test_linear_bf16_matches_oracle(orc, M, N, K, bias):
+    shape = inputs.LinearShape("t", M, K, N, seed=M + N + K, outliers=K >= 256)
+    d = inputs.linear_inputs(shape, with_bias=bias)
+    y = _gpu_linear(d["x"], d["w"], d["bias"])
+    want = _oracle_linear_rows(orc, d["x"], d["w"], d["bias"], np.arange(M))
+    exact = assert_bf16_close(gpu_bf16_bits(y), want, f"{M}x{N}x{K}")
+    assert exact > 0.99
+
+
+def test_widened_weights_bit_identical(orc):
+    d = inputs.linear_inputs(inputs.LinearShape("w16", 300, 1040, 200, seed=9))
+    y8 = _gpu_linear(d["x"], d["w"], d["bias"], widened=False)
+    y16 = _gpu_linear(d["x"], d["w"], d["bias"], widened=True)
+    assert torch.equal(y8.view(torch.int16), y16.view(torch.int16))
+
+
+def test_zero_rows_give_bias(orc):
+    M, N, K = 5, 64, 128
+    x = torch.zeros(M, K, dtype=torch.bfloat16)
+    x[2] = 1.0
+    w = inputs.random_bf16(N, K, seed=3, std=0.02)
+    b = inputs.random_bf16(1, N, seed=4, std=0.5)[0]
+    y = _gpu_linear(x, w, b)
+    yb = gpu_bf16_bits(y)
+    bb = inputs.bits(b)
+    for r in (0, 1, 3, 4):
+        assert np.array_equal(yb[r], bb)
+
+
+SAMPLE_ROWS = lambda M: np.unique(np.concatenate([np.arange(0, 16), np.arange(M // 2, M // 2 + 16),
+                                                  np.arange(M - 24, M)]))
+
+
+@pytest.mark.parametrize("shape", [inputs.QKV_768, inputs.MLP_UP_1024, inputs.MLP_DOWN_1024],
+                         ids=lambda s: s.name)
+@pytest.mark.parametrize("widened", [False, True])
+def test_full_size_dit_layers_sampled_rows(orc, shape, widened):
+    d = inputs.linear_inputs(shape)
+    y = _gpu_linear(d["x"], d["w"], d["bias"], widened=widened)
+    rows = SAMPLE_ROWS(shape.M)
+    want = _oracle_linear_rows(orc, d["x"], d["w"], d["bias"], rows)
+    got = gpu_bf16_bits(y)[rows]
+    assert_bf16_close(got, want, shape.name)
+    assert torch.isfinite(y.float()).all()
+
+
+def test_error_paths():
+    a = torch.zeros(64, 128, dtype=torch.int8, device="cuda")
+    w = torch.zeros(64, 128, dtype=torch.int8, device="cuda")
+    raw = torch.zeros(64 * 128 + 16, dtype=torch.int8, device="cuda")
+    with pytest.raises(i8.I8Error) as e:
+        i8.gemm_int32(raw[1:1 + 64 * 128].view(64, 128), w)
+    assert e.value.status == 2
+    # a split-K shape with a too-small workspace
+    a2 = torch.zeros(2, 3072, dtype=torch.int8, device="cuda")
+    w2 = torch.zeros(9216, 3072, dtype=torch.int8, device="cuda")
+    need = i8.workspace_bytes(2, 9216, 3072)
+    assert need > 0
+    with pytest.raises(i8.I8Error) as e:
+        i8.gemm_int32(a2, w2, workspace=torch.empty(need - 16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 4
+    i8.sync_check()
+
+
+def test_timeout_is_reported_without_fault():
+    """A pipeline wait that nothing completes ends by its time limit; the
+    status word reports it and the context stays usable."""
+    lib = i8.load()
+    import ctypes
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.i8_selftest_timeout(50, s) == 0
+    with pytest.raises(i8.I8Error) as e:
+        i8.sync_check()
+    assert e.value.status == 6
+    i8.sync_check()  # cleared
+    a = torch.ones(64, 64, dtype=torch.int8, device="cuda")
+    c = i8.gemm_int32(a, a)
+    i8.sync_check()
+    assert int(c[0, 0]) == 64

@@ -105,25 +105,31 @@ def _need(t: torch.Tensor, dtype, name: str, ndim: int):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _quant(fn_name: str, x: torch.Tensor):
+def _quant(fn_name: str, x: torch.Tensor, q=None, s=None):
     _need(x, torch.bfloat16, "x", 2)
     R, K = x.shape
-    q = torch.empty((R, K), dtype=torch.int8, device=x.device)
-    s = torch.empty((R,), dtype=torch.float32, device=x.device)
+    if q is None:
+        q = torch.empty((R, K), dtype=torch.int8, device=x.device)
+    if s is None:
+        s = torch.empty((R,), dtype=torch.float32, device=x.device)
+    _need(q, torch.int8, "q", 2)
+    _need(s, torch.float32, "s", 1)
+    if tuple(q.shape) != (R, K) or s.shape[0] != R:
+        raise ValueError("output shape")
     lib = load()
     with torch.cuda.device(x.device):
         _check(getattr(lib, fn_name)(_ptr(x), R, K, K, _ptr(q), K, _ptr(s), _stream(x)), fn_name)
     return q, s
 
 
-def quant_act_pertoken(x: torch.Tensor):
+def quant_act_pertoken(x: torch.Tensor, q=None, s=None):
     """bf16 [M,K] -> (int8 codes [M,K], fp32 per-token scales [M])."""
-    return _quant("i8_quant_act_pertoken", x)
+    return _quant("i8_quant_act_pertoken", x, q, s)
 
 
-def quant_weight_perchannel(w: torch.Tensor):
+def quant_weight_perchannel(w: torch.Tensor, q=None, s=None):
     """bf16 [N,K] -> (int8 codes [N,K], fp32 per-channel scales [N])."""
-    return _quant("i8_quant_weight_perchannel", w)
+    return _quant("i8_quant_weight_perchannel", w, q, s)
 
 
 def widen_weight_codes(wq: torch.Tensor) -> torch.Tensor:
