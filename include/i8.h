@@ -117,6 +117,31 @@ i8_status i8_gemm_dequant_bias_bf16(const int8_t* aq, const float* s_a,
                                     int64_t K, void* y, int64_t ldy, void* ws,
                                     size_t ws_bytes, i8_stream_t stream);
 
+/* i8_gemm_dequant_bias_bf16 for callers that cannot allocate device memory
+ * at call time -- for example a plugin running inside another runtime that
+ * offers no workspace hook, an application whose device memory is all owned
+ * by a different allocator, or a latency-critical loop where cudaMalloc and
+ * cudaFree (which may synchronize the device) are not allowed.  The paper has
+ * no counterpart: this is a packaging variant of the fused GEMM.
+ *   Same arguments and result as i8_gemm_dequant_bias_bf16, without ws and
+ *   ws_bytes.  The split-K scratch lives in a fixed 16 MiB (16777216-byte)
+ *   array inside the library, held on every GPU
+ *   that loads the library until the process exits.  A shape whose split-K
+ *   scratch (i8_gemm_workspace_bytes) exceeds that size is rejected with
+ *   I8_ERR_WORKSPACE before anything is queued.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.  The call itself allocates nothing.
+ *   All calls share the one array and it keeps the last call's contents
+ *   (harmless: every partial is written before it is read).  Calls whose
+ *   kernels overlap on the GPU -- on different streams, or from different
+ *   host threads -- race on the array; serialize them.                      */
+i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a,
+                                            const int8_t* wq, const float* s_w,
+                                            const void* bias, int64_t M,
+                                            int64_t N, int64_t K, void* y,
+                                            int64_t ldy, i8_stream_t stream);
+
 /* Widens int8 weight codes to fp16 codes (the same integers, exactly), for
  * i8_gemm_dequant_bias_bf16_w16.  This is part of the offline weight
  * preparation, next to i8_quant_weight_perchannel: sm_103a has no INT8

@@ -67,6 +67,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "i8_widen_weight_codes": ([vp, i64, i64, vp, vp], st),
             "i8_gemm_dequant_bias_bf16_w16": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, sz, vp], st),
             "i8_set_option": ([ctypes.c_int, i64], st),
+            "i8_gemm_dequant_bias_bf16_noalloc": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp], st),
             "i8_sync_check": ([vp], st),
             "i8_selftest_timeout": ([ctypes.c_int, vp], st),
         }

@@ -291,6 +291,31 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   return I8_OK;
 }
 
+// ----------------------------------------------------------------- no-alloc variant
+// Split-K scratch for i8_gemm_dequant_bias_bf16_noalloc: a fixed array in the
+// library's own device memory, so that entry point never allocates.  Every
+// GPU that loads the library holds these bytes until the process exits.
+constexpr size_t kStaticWsBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+// Device address of g_static_ws per device.  In host code the symbol is only
+// a host-side stand-in, so the address is looked up once per device (with
+// that device current) and cached.
+void* g_static_ws_ptr[kMaxDevices] = {};
+
+i8_status static_ws_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return I8_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_static_ws_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return I8_ERR_CUDA;
+    g_static_ws_ptr[dev] = p;
+  }
+  *out = g_static_ws_ptr[dev];
+  return I8_OK;
+}
+
 }  // namespace
 }  // namespace i8
 
@@ -343,6 +368,26 @@ i8_status i8_gemm_dequant_bias_bf16(const int8_t* aq, const float* s_a, const in
                                     i8_stream_t stream) {
   return gemm_common(aq, wq, false, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a, const int8_t* wq,
+                                            const float* s_w, const void* bias, int64_t M,
+                                            int64_t N, int64_t K, void* y, int64_t ldy,
+                                            i8_stream_t stream) {
+  // Same checks and kernels as i8_gemm_dequant_bias_bf16; only the split-K
+  // scratch comes from the library's fixed device array.  The split partials
+  // are written in full before the reduction reads them, so nothing in the
+  // array has to start at zero.
+  void* ws = nullptr;
+  if (M > 0 && N > 0 && K > 0 && K % 16 == 0 && K <= 131072 && M <= INT32_MAX &&
+      N <= INT32_MAX) {
+    DeviceInfo* d;
+    if (i8_status e = device_info(&d, nullptr)) return e;
+    if (make_plan(M, N, K, d->sms).ws_bytes > kStaticWsBytes) return I8_ERR_WORKSPACE;
+    if (i8_status e = static_ws_address(&ws)) return e;
+  }
+  return gemm_common(aq, wq, false, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws,
+                     ws ? kStaticWsBytes : 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
 i8_status i8_widen_weight_codes(const int8_t* wq, int64_t N, int64_t K, void* w16,
