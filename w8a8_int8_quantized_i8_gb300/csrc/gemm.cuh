@@ -53,36 +53,64 @@ struct GemmParams {
   int64_t split_stride;                // elements between split partials (kOutPartial)
 };
 
-template <int BN_, int S8_, int S16_, bool CONV_B_>
+// Kernel configuration.  CONV_A / CONV_B: the operand arrives as int8 codes
+// and is widened to fp16 on chip; otherwise it arrives as fp16 codes through
+// TMA (weights pre-widened offline; fp16 A is used only for calibration).
+// Warp roles are warpgroup-aligned so that register budgets can be moved
+// between roles with setmaxnreg:
+//   warpgroup 0: warp 0 TMA producer, warp 1 MMA issuer, warps 2-3 converters
+//   warpgroup 1: converters
+//   warpgroups 2..: epilogue (BN / 128 warpgroups; one per 128 columns)
+template <int BN_, int S8_, int S16_, bool CONV_A_, bool CONV_B_>
 struct GemmCfg {
   static constexpr int BM = 128;
   static constexpr int BN = BN_;
   static constexpr int S8 = S8_;
   static constexpr int S16 = S16_;
+  static constexpr bool CONV_A = CONV_A_;
   static constexpr bool CONV_B = CONV_B_;
-  static constexpr int BK8 = 128;   // int8 K per stage (one 128-byte row)
+  static constexpr bool ANY_CONV = CONV_A || CONV_B;
+  static constexpr bool ANY_DIRECT = !CONV_A || !CONV_B;
+  static constexpr int BK8 = 128;   // int8 K per K-block (one 128-byte row)
   static constexpr int BK16 = 64;   // fp16 K per stage (one 128-byte row)
-  static constexpr int CONV_WARPS = 4;
-  static constexpr int EPI_WARPS = BN / 32;  // 4 lane quarters x (BN / 128) column groups
-  static constexpr int EPI_WARP0 = 2 + CONV_WARPS;
+  static constexpr int CONV_WARPS = 6;
+  static constexpr int CONV_THREADS = CONV_WARPS * 32;
+  static constexpr int EPI_WARPS = BN / 32;   // 4 lane quarters x (BN / 128)
+  static constexpr int EPI_WARP0 = 8;
   static constexpr int NUM_WARPS = EPI_WARP0 + EPI_WARPS;
   static constexpr int THREADS = NUM_WARPS * 32;
-  static constexpr int A8_BYTES = BM * BK8;
+  // registers per thread after setmaxnreg (launch: 65536 / THREADS)
+  static constexpr int REG_LO = BN == 256 ? 80 : 96;
+  static constexpr int REG_HI = BN == 256 ? 176 : 232;
+  static_assert(2 * 128 * REG_LO + (EPI_WARPS / 4) * 128 * REG_HI <=
+                    THREADS * ((65536 / THREADS) & ~7),
+                "register split exceeds the launch allocation");
+  // conversion work per fp16 stage: one item = one 16-byte int8 chunk
+  static constexpr int A_ITEMS = CONV_A ? BM * 4 : 0;
+  static constexpr int B_ITEMS = CONV_B ? BN * 4 : 0;
+  static constexpr int ITEMS = A_ITEMS + B_ITEMS;
+  static constexpr int IPT = (ITEMS + CONV_THREADS - 1) / CONV_THREADS;
+  // shared memory
+  static constexpr int A8_BYTES = CONV_A ? BM * BK8 : 0;
   static constexpr int B8_BYTES = CONV_B ? BN * BK8 : 0;
+  static constexpr int STAGE8 = A8_BYTES + B8_BYTES;
   static constexpr int A16_BYTES = BM * BK16 * 2;
   static constexpr int B16_BYTES = BN * BK16 * 2;
-  static constexpr int OFF_A8 = 0;
-  static constexpr int OFF_B8 = OFF_A8 + S8 * A8_BYTES;
-  static constexpr int OFF_A16 = OFF_B8 + S8 * B8_BYTES;
-  static constexpr int OFF_B16 = OFF_A16 + S16 * A16_BYTES;
-  static constexpr int OFF_BAR = OFF_B16 + S16 * B16_BYTES;
+  static constexpr int STAGE16 = A16_BYTES + B16_BYTES;
+  static constexpr int OFF_S8 = 0;
+  static constexpr int OFF_S16 = OFF_S8 + (ANY_CONV ? S8 : 0) * STAGE8;
+  static constexpr int OFF_BAR = OFF_S16 + S16 * STAGE16;
   // full8[S8] empty8[S8] full16[S16] empty16[S16] accfull[2] accempty[2] done
   static constexpr int NUM_BARS = 2 * S8 + 2 * S16 + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
   static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr uint32_t TX8 = STAGE8;
+  static constexpr uint32_t TX16 = (CONV_A ? 0 : A16_BYTES) + (CONV_B ? 0 : B16_BYTES);
+  static constexpr uint32_t FULL16_COUNT = (ANY_CONV ? CONV_WARPS : 0) + (ANY_DIRECT ? 1 : 0);
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(STAGE8 % 1024 == 0 && STAGE16 % 1024 == 0, "stage alignment");
 };
 
 struct Ring {
@@ -136,25 +164,38 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
 }
 
-// Convert the K-half `h` (int8 chunks 4h..4h+3) of row r of a swizzled int8
-// tile into the fp16 tile of that half (chunks 0..7), both 128-byte rows with
-// the 128-byte swizzle (16-byte chunk c of row r sits at c ^ (r & 7)).
-__device__ __forceinline__ void convert_row_half(uint32_t src_tile, uint32_t dst_tile, int r,
-                                                 int h) {
-  const uint32_t srow = src_tile + static_cast<uint32_t>(r) * 128u;
-  const uint32_t drow = dst_tile + static_cast<uint32_t>(r) * 128u;
-  const int x = r & 7;
-#pragma unroll
-  for (int cl = 0; cl < 4; ++cl) {
-    const uint4 v = lds128(srow + ((((h << 2) | cl) ^ x) << 4));
-    uint4 o0, o1;
-    s8x4_to_f16x4(v.x, o0.x, o0.y);
-    s8x4_to_f16x4(v.y, o0.z, o0.w);
-    s8x4_to_f16x4(v.z, o1.x, o1.y);
-    s8x4_to_f16x4(v.w, o1.z, o1.w);
-    sts128(drow + (((2 * cl) ^ x) << 4), o0);
-    sts128(drow + (((2 * cl + 1) ^ x) << 4), o1);
+// One conversion item = one 16-byte chunk (16 int8 codes) of one row of an
+// int8 stage, widened into two 16-byte chunks (16 fp16 codes) of the fp16
+// stage of the same K-half.  Both tiles use the 128-byte swizzle: 16-byte
+// chunk c of row r sits at position c ^ (r & 7) of the row's 128 bytes.
+// Offsets are relative to the stage bases; the K-half h (int8 chunks 4h..4h+3)
+// only flips bit 6 of the source offset, since (4h + c) ^ x == (c ^ x) ^ 4h.
+struct ConvItem {
+  uint32_t src;   // offset in the int8 stage, K-half 0
+  uint32_t dst;   // offset of the first fp16 chunk (the second is dst ^ 16)
+};
+
+template <class Cfg>
+__device__ __forceinline__ ConvItem conv_item(int i) {
+  ConvItem it;
+  int region8, region16, rows, idx;
+  if (i < Cfg::A_ITEMS) {
+    region8 = 0;
+    region16 = 0;
+    rows = Cfg::BM;
+    idx = i;
+  } else {
+    region8 = Cfg::A8_BYTES;
+    region16 = Cfg::A16_BYTES;
+    rows = Cfg::BN;
+    idx = i - Cfg::A_ITEMS;
   }
+  const int cl = idx / rows;
+  const int r = idx % rows;
+  const int x = r & 7;
+  it.src = static_cast<uint32_t>(region8 + r * 128 + ((cl ^ x) << 4));
+  it.dst = static_cast<uint32_t>(region16 + r * 128 + (((2 * cl) ^ x) << 4));
+  return it;
 }
 
 __device__ __forceinline__ int f32_exact_int_to_s32(uint32_t bits) {
@@ -232,6 +273,50 @@ __device__ __forceinline__ void store_row_segment(const GemmParams& p, int m, in
   }
 }
 
+// Epilogue role: drains chunk accumulators into int32 registers, then writes
+// the tile (bf16 with dequant + bias, int32, or a split-K partial).
+template <class Cfg>
+__device__ __forceinline__ void gemm_epilogue_role(const GemmParams& p, uint32_t tmem_base, int warp,
+                                                int lane, volatile int* abort_flag, uint32_t bar0) {
+  auto accfull = [&](int b) { return bar0 + 8u * (2 * Cfg::S8 + 2 * Cfg::S16 + b); };
+  auto accempty = [&](int b) { return bar0 + 8u * (2 * Cfg::S8 + 2 * Cfg::S16 + 2 + b); };
+  const int ew = warp - Cfg::EPI_WARP0;
+  const int quarter = warp & 3;       // TMEM lanes this warp may access
+  const int cg = ew >> 2;             // 128-column group
+  Ring racc;
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+    const TileCoord tc = decode_tile(p, tile);
+    const int nst = 2 * (tc.kb1 - tc.kb0);
+    int acc[128];
+#pragma unroll
+    for (int i = 0; i < 128; ++i) acc[i] = 0;
+    for (int st0 = 0; st0 < nst; st0 += p.chunk_stages) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(accfull(racc.s), racc.ph, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(racc.s * Cfg::BN + cg * 128);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + q4 * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[q4 * 32 + i] += f32_exact_int_to_s32(r[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accempty(racc.s));
+      racc.advance(2);
+    }
+    if (!ok) break;
+    const int m = tc.mb * Cfg::BM + quarter * 32 + lane;
+    const int n0 = tc.nb * Cfg::BN + cg * 128;
+    store_row_segment<128>(p, m, n0, acc, tc.ks);
+  }
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -252,6 +337,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   auto accfull = [&](int b) { return bar0 + 8u * (2 * Cfg::S8 + 2 * Cfg::S16 + b); };
   auto accempty = [&](int b) { return bar0 + 8u * (2 * Cfg::S8 + 2 * Cfg::S16 + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (2 * Cfg::S8 + 2 * Cfg::S16 + 4);
+  auto stage8 = [&](int s) { return sbase + Cfg::OFF_S8 + static_cast<uint32_t>(s * Cfg::STAGE8); };
+  auto stage16 = [&](int s) { return sbase + Cfg::OFF_S16 + static_cast<uint32_t>(s * Cfg::STAGE16); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
 
@@ -261,7 +348,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       mbar_init(empty8(s), Cfg::CONV_WARPS);
     }
     for (int s = 0; s < Cfg::S16; ++s) {
-      mbar_init(full16(s), Cfg::CONV_WARPS + (Cfg::CONV_B ? 0 : 1));
+      mbar_init(full16(s), Cfg::FULL16_COUNT);
       mbar_init(empty16(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -285,36 +372,46 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp >= Cfg::EPI_WARP0) {
+    regs_inc<Cfg::REG_HI>();
+    gemm_epilogue_role<Cfg>(p, tmem_base, warp, lane, abort_flag, bar0);
+  } else if (warp == 0) {
+    regs_dec<Cfg::REG_LO>();
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       Ring r8, r16;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !*abort_flag; tile += gridDim.x) {
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         const TileCoord tc = decode_tile(p, tile);
-        for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
-          if (!mbar_wait(empty8(r8.s), r8.ph ^ 1u, abort_flag)) break;
-          mbar_arrive_expect_tx(full8(r8.s), Cfg::A8_BYTES + Cfg::B8_BYTES);
-          tma_load_2d(sbase + Cfg::OFF_A8 + r8.s * Cfg::A8_BYTES, &tmA, full8(r8.s), kb * Cfg::BK8,
-                      tc.mb * Cfg::BM);
-          if constexpr (Cfg::CONV_B) {
-            tma_load_2d(sbase + Cfg::OFF_B8 + r8.s * Cfg::B8_BYTES, &tmB, full8(r8.s), kb * Cfg::BK8,
-                        tc.nb * Cfg::BN);
+        for (int kb = tc.kb0; ok && kb < tc.kb1; ++kb) {
+          if constexpr (Cfg::ANY_CONV) {
+            if (!(ok = mbar_wait(empty8(r8.s), r8.ph ^ 1u, abort_flag))) break;
+            mbar_arrive_expect_tx(full8(r8.s), Cfg::TX8);
+            if constexpr (Cfg::CONV_A)
+              tma_load_2d(stage8(r8.s), &tmA, full8(r8.s), kb * Cfg::BK8, tc.mb * Cfg::BM);
+            if constexpr (Cfg::CONV_B)
+              tma_load_2d(stage8(r8.s) + Cfg::A8_BYTES, &tmB, full8(r8.s), kb * Cfg::BK8,
+                          tc.nb * Cfg::BN);
+            r8.advance(Cfg::S8);
           }
-          r8.advance(Cfg::S8);
-          if constexpr (!Cfg::CONV_B) {
+          if constexpr (Cfg::ANY_DIRECT) {
             for (int h = 0; h < 2; ++h) {
-              if (!mbar_wait(empty16(r16.s), r16.ph ^ 1u, abort_flag)) break;
-              mbar_arrive_expect_tx(full16(r16.s), Cfg::B16_BYTES);
-              tma_load_2d(sbase + Cfg::OFF_B16 + r16.s * Cfg::B16_BYTES, &tmB, full16(r16.s),
-                          kb * Cfg::BK8 + h * Cfg::BK16, tc.nb * Cfg::BN);
+              if (!(ok = mbar_wait(empty16(r16.s), r16.ph ^ 1u, abort_flag))) break;
+              mbar_arrive_expect_tx(full16(r16.s), Cfg::TX16);
+              const int k16 = kb * Cfg::BK8 + h * Cfg::BK16;
+              if constexpr (!Cfg::CONV_A)
+                tma_load_2d(stage16(r16.s), &tmA, full16(r16.s), k16, tc.mb * Cfg::BM);
+              if constexpr (!Cfg::CONV_B)
+                tma_load_2d(stage16(r16.s) + Cfg::A16_BYTES, &tmB, full16(r16.s), k16,
+                            tc.nb * Cfg::BN);
               r16.advance(Cfg::S16);
             }
           }
-          if (*abort_flag) break;
         }
       }
     }
   } else if (warp == 1) {
+    regs_dec<Cfg::REG_LO>();
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(Cfg::BM, Cfg::BN);
@@ -331,8 +428,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           for (int st = st0; st < st1; ++st) {
             if (!(ok = mbar_wait(full16(r16.s), r16.ph, abort_flag))) break;
             tc_fence_after();
-            const uint64_t ad = smem_desc_sw128(sbase + Cfg::OFF_A16 + r16.s * Cfg::A16_BYTES);
-            const uint64_t bd = smem_desc_sw128(sbase + Cfg::OFF_B16 + r16.s * Cfg::B16_BYTES);
+            const uint64_t ad = smem_desc_sw128(stage16(r16.s));
+            const uint64_t bd = smem_desc_sw128(stage16(r16.s) + Cfg::A16_BYTES);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               mma_f16_ss(d, ad + 2u * j, bd + 2u * j, idesc, (st > st0 || j > 0) ? 1u : 0u);
@@ -350,79 +447,59 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       mma_commit(done_bar);
       mbar_wait_bounded(done_bar, 0u, 100000000ull);
     }
-  } else if (warp < Cfg::EPI_WARP0) {
-    // ------------------------------------------------------------ converters
-    const int ct = threadIdx.x - 64;  // 0..127: the row this thread converts
-    Ring r8, r16;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      const TileCoord tc = decode_tile(p, tile);
-      for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(full8(r8.s), r8.ph, abort_flag));
-        if (!ok) break;
-        const uint32_t a8 = sbase + Cfg::OFF_A8 + r8.s * Cfg::A8_BYTES;
-        const uint32_t b8 = sbase + Cfg::OFF_B8 + r8.s * Cfg::B8_BYTES;
-        for (int h = 0; h < 2; ++h) {
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty16(r16.s), r16.ph ^ 1u, abort_flag));
-          if (!ok) break;
-          const uint32_t a16 = sbase + Cfg::OFF_A16 + r16.s * Cfg::A16_BYTES;
-          convert_row_half(a8, a16, ct, h);
-          if constexpr (Cfg::CONV_B) {
-            const uint32_t b16 = sbase + Cfg::OFF_B16 + r16.s * Cfg::B16_BYTES;
-#pragma unroll
-            for (int r = ct; r < Cfg::BN; r += 128) convert_row_half(b8, b16, r, h);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(full16(r16.s));
-          r16.advance(Cfg::S16);
-        }
-        if (!ok) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty8(r8.s));
-        r8.advance(Cfg::S8);
-      }
-    }
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int ew = warp - Cfg::EPI_WARP0;
-    const int quarter = warp & 3;       // TMEM lanes this warp may access
-    const int cg = ew >> 2;             // 128-column group
-    Ring racc;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      const TileCoord tc = decode_tile(p, tile);
-      const int nst = 2 * (tc.kb1 - tc.kb0);
-      int acc[128];
+    regs_dec<Cfg::REG_LO>();
+    // ------------------------------------------------------------ converters
+    if constexpr (Cfg::ANY_CONV) {
+      const int ct = threadIdx.x - 64;  // 0 .. CONV_THREADS-1
+      ConvItem items[Cfg::IPT];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0;
-      for (int st0 = 0; st0 < nst; st0 += p.chunk_stages) {
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(accfull(racc.s), racc.ph, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                               static_cast<uint32_t>(racc.s * Cfg::BN + cg * 128);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(taddr + half * 64, r0);
-          tmem_ld_32x32b_x32(taddr + half * 64 + 32, r1);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            acc[half * 64 + i] += f32_exact_int_to_s32(r0[i]);
-            acc[half * 64 + 32 + i] += f32_exact_int_to_s32(r1[i]);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(accempty(racc.s));
-        racc.advance(2);
+      for (int j = 0; j < Cfg::IPT; ++j) {
+        const int i = ct + j * Cfg::CONV_THREADS;
+        items[j] = conv_item<Cfg>(i < Cfg::ITEMS ? i : 0);
       }
-      if (!ok) break;
-      const int m = tc.mb * Cfg::BM + quarter * 32 + lane;
-      const int n0 = tc.nb * Cfg::BN + cg * 128;
-      store_row_segment<128>(p, m, n0, acc, tc.ks);
+      Ring r8, r16;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const TileCoord tc = decode_tile(p, tile);
+        for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(full8(r8.s), r8.ph, abort_flag));
+          if (!ok) break;
+          const uint32_t s8 = stage8(r8.s);
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty16(r16.s), r16.ph ^ 1u, abort_flag));
+            if (!ok) break;
+            const uint32_t s16 = stage16(r16.s);
+            const uint32_t hx = static_cast<uint32_t>(h) << 6;
+            uint4 v[Cfg::IPT];
+#pragma unroll
+            for (int j = 0; j < Cfg::IPT; ++j) {
+              if (ct + j * Cfg::CONV_THREADS < Cfg::ITEMS) v[j] = lds128(s8 + (items[j].src ^ hx));
+            }
+#pragma unroll
+            for (int j = 0; j < Cfg::IPT; ++j) {
+              if (ct + j * Cfg::CONV_THREADS < Cfg::ITEMS) {
+                uint4 o0, o1;
+                s8x4_to_f16x4(v[j].x, o0.x, o0.y);
+                s8x4_to_f16x4(v[j].y, o0.z, o0.w);
+                s8x4_to_f16x4(v[j].z, o1.x, o1.y);
+                s8x4_to_f16x4(v[j].w, o1.z, o1.w);
+                sts128(s16 + items[j].dst, o0);
+                sts128(s16 + (items[j].dst ^ 16u), o1);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full16(r16.s));
+            r16.advance(Cfg::S16);
+          }
+          if (!ok) break;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty8(r8.s));
+          r8.advance(Cfg::S8);
+        }
+      }
     }
   }
 

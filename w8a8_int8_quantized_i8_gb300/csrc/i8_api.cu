@@ -57,6 +57,7 @@ struct Options {
   int chunk_k = 512;       // K per exact fp32 chunk (multiple of 64, <= 1024)
   int force_splits = 0;    // 0 = table
   int max_ctas = 0;        // 0 = all SMs
+  int force_bn = 0;        // 0 = table, else 128 or 256
 };
 Options g_opt;
 
@@ -163,7 +164,10 @@ struct Plan {
 // splits covers the SMs, with at least two 128-wide K-blocks per split.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
   Plan p;
-  p.bn = 128;
+  // 256-wide tiles halve the on-chip widening of A per MAC; keep 128 when
+  // N is small or the wider tiles would leave SMs idle.
+  p.bn = (N >= 256 && ((M + 127) / 128) * ((N + 255) / 256) >= sms) ? 256 : 128;
+  if (g_opt.force_bn == 128 || g_opt.force_bn == 256) p.bn = g_opt.force_bn;
   p.total_kb = static_cast<int>((K + 127) / 128);
   p.num_m = static_cast<int>((M + 127) / 128);
   p.num_n = static_cast<int>((N + p.bn - 1) / p.bn);
@@ -217,8 +221,11 @@ i8_status launch_gemm_cfg(DeviceInfo* d, int slot, const CUtensorMap& ma, const 
   return cuda_status(cudaGetLastError());
 }
 
-using CfgConv = GemmCfg<128, 3, 3, true>;    // int8 weights, widened on chip
-using CfgWide = GemmCfg<128, 3, 3, false>;   // weights pre-widened to fp16 codes
+// <BN, int8 stages, fp16 stages, widen A on chip, widen B on chip>
+using CfgConv128 = GemmCfg<128, 3, 3, true, true>;   // int8 weights
+using CfgWide128 = GemmCfg<128, 4, 4, true, false>;  // weights pre-widened to fp16 codes
+using CfgConv256 = GemmCfg<256, 2, 2, true, true>;
+using CfgWide256 = GemmCfg<256, 4, 3, true, false>;
 
 // Common GEMM driver.  b16 = weights given as fp16 codes instead of int8.
 i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int64_t N, int64_t K,
@@ -242,12 +249,13 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
     if (!aligned16(ws)) return I8_ERR_ALIGNMENT;
   }
   CUtensorMap ma, mb;
+  const uint32_t bn = static_cast<uint32_t>(pl.bn);
   if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M, K, 128, 128)) return I8_ERR_CUDA;
   if (b16) {
-    if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wb, K, N, 2 * K, 64, 128))
+    if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wb, K, N, 2 * K, 64, bn))
       return I8_ERR_CUDA;
   } else {
-    if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, K, N, K, 128, 128)) return I8_ERR_CUDA;
+    if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, K, N, K, 128, bn)) return I8_ERR_CUDA;
   }
   GemmParams gp{};
   gp.M = static_cast<int>(M);
@@ -274,8 +282,14 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
     gp.ldo = ldo;
     gp.split_stride = 0;
   }
-  i8_status e = b16 ? launch_gemm_cfg<CfgWide>(d, 1, ma, mb, gp, pl.grid, st)
-                    : launch_gemm_cfg<CfgConv>(d, 0, ma, mb, gp, pl.grid, st);
+  i8_status e;
+  if (pl.bn == 256) {
+    e = b16 ? launch_gemm_cfg<CfgWide256>(d, 3, ma, mb, gp, pl.grid, st)
+            : launch_gemm_cfg<CfgConv256>(d, 2, ma, mb, gp, pl.grid, st);
+  } else {
+    e = b16 ? launch_gemm_cfg<CfgWide128>(d, 1, ma, mb, gp, pl.grid, st)
+            : launch_gemm_cfg<CfgConv128>(d, 0, ma, mb, gp, pl.grid, st);
+  }
   if (e != I8_OK) return e;
   if (pl.splits > 1) {
     GemmParams rp = gp;
@@ -428,6 +442,10 @@ i8_status i8_set_option(i8_option opt, int64_t value) {
     case I8_OPT_MAX_CTAS:
       if (value < 0) return I8_ERR_INVALID_ARG;
       g_opt.max_ctas = static_cast<int>(value);
+      return I8_OK;
+    case I8_OPT_TILE_N:
+      if (value != 0 && value != 128 && value != 256) return I8_ERR_INVALID_ARG;
+      g_opt.force_bn = static_cast<int>(value);
       return I8_OK;
   }
   return I8_ERR_INVALID_ARG;
