@@ -1,0 +1,205 @@
+"""Comparison measurements on the same GB300: engine rates and the DiT shapes.
+
+Prints one JSON object per line:
+
+* ``engine``: peak rates of the legacy warp MMA on this chip (register-only
+  loops of mma.sync m16n8k32 s8->s32 and m16n8k16 f16->f32), compiled here
+  from the CUDA source below with nvcc;
+* ``shape``: for each DiT linear shape, the device time of
+  - this library's full step (per-token quant + fused GEMM) and GEMM alone,
+    with int8 weights and with pre-widened (fp16-code) weights,
+  - torch bf16 ``X @ W.T + b`` (cuBLAS),
+  - ``torch._int_mm`` (int32 only, the pages' exactness reference),
+  - the "fake INT8" forward the pages replace: dequantize A_q and W_q to bf16,
+    then a bf16 matmul + bias (all torch ops);
+  inputs rotate over enough buffer sets to exceed 3x the 129 MB L2.
+
+Usage: python bench_engines.py [--sweep] [--iters N]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import w8a8_int8_quantized_i8_gb300 as i8  # noqa: E402
+from w8a8_int8_quantized_i8_gb300 import inputs  # noqa: E402
+
+MMA_SYNC_SRC = r"""
+#include <cstdio>
+#include <cuda_runtime.h>
+__global__ void mma_s8(int iters, int* out) {
+  int a0 = threadIdx.x, a1 = a0 * 3, a2 = a0 ^ 5, a3 = a0 + 7, b0 = a0 * 11, b1 = a0 - 1;
+  int c[4][4] = {};
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      asm volatile("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                   : "+r"(c[j][0]), "+r"(c[j][1]), "+r"(c[j][2]), "+r"(c[j][3])
+                   : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+  int s = 0;
+  for (int j = 0; j < 4; ++j) s += c[j][0] + c[j][1] + c[j][2] + c[j][3];
+  if (s == 123456789) out[0] = s;
+}
+__global__ void mma_f16(int iters, int* out) {
+  unsigned a0 = threadIdx.x, a1 = a0 * 3, a2 = a0 ^ 5, a3 = a0 + 7, b0 = a0 * 11, b1 = a0 - 1;
+  float c[4][4] = {};
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                   : "+f"(c[j][0]), "+f"(c[j][1]), "+f"(c[j][2]), "+f"(c[j][3])
+                   : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+  float s = 0;
+  for (int j = 0; j < 4; ++j) s += c[j][0] + c[j][1] + c[j][2] + c[j][3];
+  if (s == 123456789.f) out[0] = 1;
+}
+int main() {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
+  int* out;
+  cudaMalloc(&out, 4);
+  const int iters = 4096, blocks = sms * 4, threads = 256;
+  double best_s8 = 0, best_f16 = 0;
+  for (int rep = 0; rep < 3; ++rep) {
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    float ms;
+    const double warps = blocks * threads / 32.0;
+    cudaEventRecord(e0);
+    mma_s8<<<blocks, threads>>>(iters, out);
+    cudaEventRecord(e1);
+    cudaEventSynchronize(e1);
+    cudaEventElapsedTime(&ms, e0, e1);
+    double v = 2.0 * 16 * 8 * 32 * 4.0 * iters * warps / ms / 1e9;
+    if (v > best_s8) best_s8 = v;
+    cudaEventRecord(e0);
+    mma_f16<<<blocks, threads>>>(iters, out);
+    cudaEventRecord(e1);
+    cudaEventSynchronize(e1);
+    cudaEventElapsedTime(&ms, e0, e1);
+    v = 2.0 * 16 * 8 * 16 * 4.0 * iters * warps / ms / 1e9;
+    if (v > best_f16) best_f16 = v;
+  }
+  printf("{\"engine\": \"mma.sync m16n8k32 s8->s32\", \"tops\": %.1f}\n", best_s8);
+  printf("{\"engine\": \"mma.sync m16n8k16 f16->f32\", \"tflops\": %.1f}\n", best_f16);
+  return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+"""
+
+
+def engine_rates():
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "mma_sync_rates.cu")
+        exe = os.path.join(d, "mma_sync_rates")
+        with open(src, "w") as fh:
+            fh.write(MMA_SYNC_SRC)
+        subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe, src],
+                       check=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    for line in out.splitlines():
+        print(line, flush=True)
+
+
+def _time(fn, iters):
+    for _ in range(3):
+        fn(0)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(iters):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters * 1e-3
+
+
+def shape_row(shape, iters, full=True):
+    M, K, N = shape.M, shape.K, shape.N
+    d = inputs.linear_inputs(shape)
+    dev = "cuda"
+    w = d["w"].to(dev)
+    b = d["bias"].to(dev)
+    wq, s_w = i8.quant_weight_perchannel(w)
+    w16 = i8.widen_weight_codes(wq)
+    per_set = M * K * 2 + M * K + M * N * 2
+    R = max(2, min(16, -(-3 * 129 * 2**20 // max(per_set, 1))))
+    xs = [d["x"].to(dev) for _ in range(R)]
+    aqs = [torch.empty(M, K, dtype=torch.int8, device=dev) for _ in range(R)]
+    sas = [torch.empty(M, dtype=torch.float32, device=dev) for _ in range(R)]
+    ys = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    ws = torch.empty(max(i8.workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=dev)
+    for r in range(R):
+        i8.quant_act_pertoken(xs[r], aqs[r], sas[r])
+    ops = 2.0 * M * N * K
+    res = {"shape": shape.name, "M": M, "K": K, "N": N, "l2_sets": R,
+           "k_splits": "yes" if i8.workspace_bytes(M, N, K) else "no"}
+
+    def step(wmat):
+        def f(i):
+            r = i % R
+            i8.quant_act_pertoken(xs[r], aqs[r], sas[r])
+            i8.gemm_dequant_bias_bf16(aqs[r], sas[r], wmat, s_w, b, out=ys[r], workspace=ws)
+        return f
+
+    def gemm(wmat):
+        def f(i):
+            r = i % R
+            i8.gemm_dequant_bias_bf16(aqs[r], sas[r], wmat, s_w, b, out=ys[r], workspace=ws)
+        return f
+
+    for key, fn in (("step_int8_us", step(wq)), ("gemm_int8_us", gemm(wq)),
+                    ("step_w16_us", step(w16)), ("gemm_w16_us", gemm(w16))):
+        res[key] = _time(fn, iters) * 1e6
+    i8.sync_check()
+    res["gemm_int8_tops"] = ops / (res["gemm_int8_us"] * 1e-6) / 1e12
+    res["gemm_w16_tops"] = ops / (res["gemm_w16_us"] * 1e-6) / 1e12
+    res["step_int8_tops"] = ops / (res["step_int8_us"] * 1e-6) / 1e12
+    if full:
+        wt = w.t()
+        res["torch_bf16_us"] = _time(lambda i: torch.addmm(b, xs[i % R], wt, out=ys[i % R]), iters) * 1e6
+        if M > 16:
+            wqt = wq.t()
+            res["torch_int_mm_us"] = _time(lambda i: torch._int_mm(aqs[i % R], wqt), iters) * 1e6
+        def fake(i):
+            r = i % R
+            a_deq = aqs[r].to(torch.bfloat16) * sas[r].to(torch.bfloat16)[:, None]
+            w_deq = wq.to(torch.bfloat16) * s_w.to(torch.bfloat16)[:, None]
+            torch.addmm(b, a_deq, w_deq.t(), out=ys[r])
+        res["fake_int8_us"] = _time(fake, iters) * 1e6
+        res["torch_bf16_tflops"] = ops / (res["torch_bf16_us"] * 1e-6) / 1e12
+    print(json.dumps(res), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--sweep", action="store_true", help="also run the 35-shape sweep")
+    ap.add_argument("--iters", type=int, default=30)
+    ap.add_argument("--no-engines", action="store_true")
+    args = ap.parse_args(argv)
+    i8.load()
+    if not args.no_engines:
+        engine_rates()
+    for shape in (inputs.QKV_768, inputs.MLP_UP_1024, inputs.MLP_DOWN_1024):
+        shape_row(shape, args.iters)
+    if args.sweep:
+        for shape in inputs.sweep_shapes():
+            shape_row(shape, args.iters, full=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

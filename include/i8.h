@@ -168,12 +168,15 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *   I8_OPT_FORCE_SPLITS K-splits to use for every shape (0 = the table).
  *   I8_OPT_MAX_CTAS     cap on the persistent grid (0 = one CTA per SM).
  *   I8_OPT_TILE_N       GEMM tile width, 128 or 256 (0 = the table).
+ *   I8_OPT_QUANT_VPL    quantizer: most 16-byte vectors one lane holds
+ *                       (1..16, default 6); more warps share a row above.
  * Changing FORCE_SPLITS changes i8_gemm_workspace_bytes(). */
 typedef enum {
   I8_OPT_CHUNK_K = 1,
   I8_OPT_FORCE_SPLITS = 2,
   I8_OPT_MAX_CTAS = 3,
-  I8_OPT_TILE_N = 4
+  I8_OPT_TILE_N = 4,
+  I8_OPT_QUANT_VPL = 5
 } i8_option;
 i8_status i8_set_option(i8_option opt, int64_t value);
 

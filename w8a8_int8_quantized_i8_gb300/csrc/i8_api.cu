@@ -58,6 +58,7 @@ struct Options {
   int force_splits = 0;    // 0 = table
   int max_ctas = 0;        // 0 = all SMs
   int force_bn = 0;        // 0 = table, else 128 or 256
+  int quant_vpl = 6;       // max 16-byte vectors per lane in the quantizer
 };
 Options g_opt;
 
@@ -132,7 +133,7 @@ i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t
   // Vectors of 8 elements per row; G warps per row, V vectors per lane.
   const int vecs = static_cast<int>(K / 8);
   int G = 1;
-  while (G < 8 && (vecs + 32 * G - 1) / (32 * G) > 12) G *= 2;
+  while (G < 8 && (vecs + 32 * G - 1) / (32 * G) > g_opt.quant_vpl) G *= 2;
   const int need = (vecs + 32 * G - 1) / (32 * G);
   const auto* xb = static_cast<const uint16_t*>(x);
   const int Ki = static_cast<int>(K);
@@ -442,6 +443,10 @@ i8_status i8_set_option(i8_option opt, int64_t value) {
     case I8_OPT_MAX_CTAS:
       if (value < 0) return I8_ERR_INVALID_ARG;
       g_opt.max_ctas = static_cast<int>(value);
+      return I8_OK;
+    case I8_OPT_QUANT_VPL:
+      if (value < 1 || value > 16) return I8_ERR_INVALID_ARG;
+      g_opt.quant_vpl = static_cast<int>(value);
       return I8_OK;
     case I8_OPT_TILE_N:
       if (value != 0 && value != 128 && value != 256) return I8_ERR_INVALID_ARG;

@@ -10,13 +10,17 @@
 // Design (HBM-bound: 2 bytes read + 1 byte written per element):
 //   * a group of G warps owns one row; every lane holds V 16-byte vectors
 //     (8 bf16 each) of the row in registers, so X is read from HBM once;
-//   * absmax on the raw bit patterns (|x| ordered like its bits), one
-//     redux.sync per warp, shared memory across the G warps of a row;
+//   * absmax per lane with the packed bf16x2 |max| (exact: it returns one of
+//     its inputs), one redux.sync per warp, shared memory across the G warps
+//     of a row;
 //   * the quotient: t = x * fl(1/s) is within 2^-15 of the correctly rounded
 //     fl(x / s) for every |x| <= amax when s is a normal float, so whenever t
 //     is at least 2^-14 away from a half-integer both round to the same
-//     integer; the rare near-tie elements (and rows with a subnormal scale)
-//     take an IEEE division.  The result equals round_half_even(fl(x / s)).
+//     integer; a vector of 8 with any near-tie element (and every row with a
+//     subnormal scale) takes an IEEE division instead.  The result equals
+//     round_half_even(fl(x / s)); the clamp to +-127 can only bind on that
+//     slow path (|t| <= 127 * (1 + 2^-22) when s is normal).
+//   * fp32 pairs run through the packed f32x2 instructions.
 //   * rounding to an integer uses the fp32 add of 1.5 * 2^23 (exact for
 //     |t| <= 127.x, ties to even); the low byte of that sum's bit pattern is
 //     the two's-complement int8 code.
@@ -37,33 +41,82 @@ __device__ __forceinline__ void st_v2(void* p, uint32_t a, uint32_t b) {
   asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
-// One element: returns the fp32 bit pattern whose low byte is the code.
-__device__ __forceinline__ uint32_t quant_one(float x, float s, float r, bool fast) {
-  constexpr float kMagic = 12582912.0f;          // 1.5 * 2^23
-  constexpr float kNearTie = 0.5f - 0x1p-14f;
-  float t = fminf(fmaxf(__fmul_rn(x, r), -127.0f), 127.0f);
-  float y = __fadd_rn(t, kMagic);                // y - kMagic = round_half_even(t)
-  float d = fabsf(__fadd_rn(t, -__fadd_rn(y, -kMagic)));
-  if (!fast || d > kNearTie) {
-    t = fminf(fmaxf(__fdiv_rn(x, s), -127.0f), 127.0f);
-    y = __fadd_rn(t, kMagic);
-  }
-  return __float_as_uint(y);
+// Packed fp32 pairs (f32x2 arithmetic, IEEE round-to-nearest per lane).
+__device__ __forceinline__ unsigned long long f2(float lo, float hi) {
+  unsigned long long d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f2_split(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Low bytes of four fp32 bit patterns -> one word (first pattern in byte 0).
+__device__ __forceinline__ uint32_t low_bytes4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
+constexpr float kRoundMagic = 12582912.0f;     // 1.5 * 2^23: adding it rounds to an integer
+constexpr float kNearTie = 0.5f - 0x1p-14f;
+
+// Exact path for one element: clamp(x / s) rounded half-to-even, as the
+// bit pattern of (q + 1.5 * 2^23) whose low byte is the code.
+__device__ __forceinline__ uint32_t quant_exact(float x, float s) {
+  const float t = fminf(fmaxf(__fdiv_rn(x, s), -127.0f), 127.0f);
+  return __float_as_uint(__fadd_rn(t, kRoundMagic));
 }
 
 // 8 bf16 (one 16-byte vector) -> 8 int8 codes packed in two words.
-__device__ __forceinline__ uint2 quant_vec8(uint4 v, float s, float r, bool fast) {
+__device__ __forceinline__ uint2 quant_vec8(uint4 v, float s, unsigned long long rr, bool fast) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const unsigned long long mm = f2(kRoundMagic, kRoundMagic);
   uint32_t b[8];
+  float dmax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    b[2 * i] = quant_one(__uint_as_float(w[i] << 16), s, r, fast);
-    b[2 * i + 1] = quant_one(__uint_as_float(w[i] & 0xFFFF0000u), s, r, fast);
+    const unsigned long long x = f2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+    const unsigned long long t = f2_mul(x, rr);         // x * fl(1/s)
+    const unsigned long long y = f2_add(t, mm);         // rounds t to an integer (+ magic)
+    const unsigned long long d = f2_sub(t, f2_sub(y, mm));  // t - rint(t), exact
+    float y0, y1, d0, d1;
+    f2_split(y, y0, y1);
+    f2_split(d, d0, d1);
+    b[2 * i] = __float_as_uint(y0);
+    b[2 * i + 1] = __float_as_uint(y1);
+    dmax = fmaxf(dmax, fmaxf(fabsf(d0), fabsf(d1)));
   }
-  // gather the low byte of each pattern: bytes {b0.0, b1.0, b2.0, b3.0}
-  uint32_t lo = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
-  uint32_t hi = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
-  return make_uint2(lo, hi);
+  if (!fast || dmax > kNearTie) {
+    // a near-tie somewhere in the vector (or a subnormal scale): IEEE division
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      b[2 * i] = quant_exact(__uint_as_float(w[i] << 16), s);
+      b[2 * i + 1] = quant_exact(__uint_as_float(w[i] & 0xFFFF0000u), s);
+    }
+  }
+  return make_uint2(low_bytes4(b[0], b[1], b[2], b[3]), low_bytes4(b[4], b[5], b[6], b[7]));
+}
+
+// Lane-wise max of |a| and |b| over bf16 pairs; the result's sign bits are
+// the xor of the inputs' signs and are masked off by the caller.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // Grid: ceil(rows / (8 / G)) CTAs of 256 threads; warp w of a CTA serves row
@@ -84,7 +137,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 
   const uint16_t* xr = x + (valid_row ? row : 0) * ldx;
   uint4 v[V];
-  uint32_t amax2 = 0;  // two 15-bit |bf16| patterns, max taken lane-wise
+  uint32_t amax2 = 0;  // bf16x2 running max of |x| (sign bits meaningless)
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int e = slice0 + (i * 32 + lane) * 8;
@@ -96,11 +149,12 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   }
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    amax2 = __vmaxu2(amax2, v[i].x & 0x7FFF7FFFu);
-    amax2 = __vmaxu2(amax2, v[i].y & 0x7FFF7FFFu);
-    amax2 = __vmaxu2(amax2, v[i].z & 0x7FFF7FFFu);
-    amax2 = __vmaxu2(amax2, v[i].w & 0x7FFF7FFFu);
+    amax2 = absmax_bf16x2(amax2, v[i].x);
+    amax2 = absmax_bf16x2(amax2, v[i].y);
+    amax2 = absmax_bf16x2(amax2, v[i].z);
+    amax2 = absmax_bf16x2(amax2, v[i].w);
   }
+  amax2 &= 0x7FFF7FFFu;
   uint32_t abits = max(amax2 & 0xFFFFu, amax2 >> 16);
   abits = __reduce_max_sync(0xFFFFFFFFu, abits);
   if (G > 1) {
@@ -126,11 +180,12 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   }
   const bool fast = s >= 0x1p-126f;  // s normal: 1/s is finite and normal
   const float r = __frcp_rn(s);
+  const unsigned long long rr = f2(r, r);
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int e = slice0 + (i * 32 + lane) * 8;
     if (e < K) {
-      const uint2 c = quant_vec8(v[i], s, r, fast);
+      const uint2 c = quant_vec8(v[i], s, rr, fast);
       st_v2(qr + e, c.x, c.y);
     }
   }
