@@ -163,11 +163,15 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
 
 /* Process-wide tuning knobs (not thread-safe; set them before launching).
  *   I8_OPT_CHUNK_K      K-elements per exact fp32 accumulation chunk inside
- *                       the GEMM: a multiple of 64 in [64, 1024]
- *                       (default 512, so partial sums stay below 2^23).
+ *                       the GEMM: a multiple of 64 in [64, 1024] (default
+ *                       1024: partial sums stay below 127*127*1024 < 2^24).
  *   I8_OPT_FORCE_SPLITS K-splits to use for every shape (0 = the table).
  *   I8_OPT_MAX_CTAS     cap on the persistent grid (0 = one CTA per SM).
  *   I8_OPT_TILE_N       GEMM tile width, 128 or 256 (0 = the table).
+ *   I8_OPT_CTA_PAIR     GEMM on CTA pairs (256 x 256 tiles per cluster of 2):
+ *                       0 = the table (default: pairs for int8 weights when
+ *                       the 256 x 256 tiles fill every pair of SMs), 1 = never,
+ *                       2 = whenever M, N >= 256.
  *   I8_OPT_QUANT_VPL    quantizer: most 16-byte vectors one lane holds
  *                       (1..16, default 6); more warps share a row above.
  * Changing FORCE_SPLITS changes i8_gemm_workspace_bytes(). */
@@ -176,7 +180,8 @@ typedef enum {
   I8_OPT_FORCE_SPLITS = 2,
   I8_OPT_MAX_CTAS = 3,
   I8_OPT_TILE_N = 4,
-  I8_OPT_QUANT_VPL = 5
+  I8_OPT_QUANT_VPL = 5,
+  I8_OPT_CTA_PAIR = 6
 } i8_option;
 i8_status i8_set_option(i8_option opt, int64_t value);
 

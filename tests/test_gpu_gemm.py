@@ -78,7 +78,7 @@ def test_gemm_int32_adversarial_exact(orc, chunk_k):
         c = i8.gemm_int32(to_dev(a), to_dev(w))
         i8.sync_check()
     finally:
-        i8.set_option("chunk_k", 512)
+        i8.set_option("chunk_k", 1024)
     got = c.cpu().numpy()
     want = orc.gemm_s32(a.numpy(), w.numpy())
     assert got[0, 0] == 127 * 127 * K
@@ -204,3 +204,38 @@ def test_timeout_is_reported_without_fault():
     c = i8.gemm_int32(a, a)
     i8.sync_check()
     assert int(c[0, 0]) == 64
+
+
+@pytest.fixture
+def cta_pair_option():
+    yield
+    i8.set_option("cta_pair", 0)
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["single_cta", "cta_pair"])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 264, 1040), (520, 776, 4096)])
+def test_gemm_int32_both_kernels(orc, cta_pair_option, mode, M, N, K):
+    """Both GEMM kernels (one CTA per tile, and CTA pairs with 256 x 256
+    tiles) on ragged shapes, random and adversarial operands."""
+    i8.set_option("cta_pair", mode)
+    a = inputs.random_int8(M, K, seed=M + 7 * K)
+    w = inputs.random_int8(N, K, seed=N + 11 * K)
+    a[:3], w[:3] = _adversarial(3, 3, K, seed=M)[0], _adversarial(3, 3, K, seed=N)[1]
+    c = i8.gemm_int32(to_dev(a), to_dev(w))
+    i8.sync_check()
+    got = c.cpu().numpy()
+    want = orc.gemm_s32(a.numpy(), w.numpy())
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"mode {mode}: {len(bad)} mismatches, first {bad[:4].tolist()}"
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["single_cta", "cta_pair"])
+@pytest.mark.parametrize("widened", [False, True])
+def test_linear_both_kernels_qkv_sampled(orc, cta_pair_option, mode, widened):
+    i8.set_option("cta_pair", mode)
+    shape = inputs.QKV_768
+    d = inputs.linear_inputs(shape)
+    y = _gpu_linear(d["x"], d["w"], d["bias"], widened=widened)
+    rows = SAMPLE_ROWS(shape.M)
+    want = _oracle_linear_rows(orc, d["x"], d["w"], d["bias"], rows)
+    assert_bf16_close(gpu_bf16_bits(y)[rows], want, f"mode {mode} widened {widened}")

@@ -43,7 +43,7 @@ def _noalloc(lib, aq, s_a, wq, s_w, b, y):
 
 def test_noalloc_matches_regular_entry_point_on_two_calls():
     lib = binding.load()
-    i8.set_option("chunk_k", 512)
+    i8.set_option("chunk_k", 1024)
     i8.set_option("force_splits", 0)
     # Two calls in a row, both on shapes that split K (so the fixed scratch is
     # used), the second one after the first has left its partials behind.

@@ -9,8 +9,10 @@
 // pipe, exactly:
 //   * every int8 code is exactly representable in fp16, every product
 //     (|p| <= 127^2) is exact, and the fp32 accumulator is restarted every
-//     `chunk` K-elements so that no partial sum reaches 2^24 (chunk <= 1024;
-//     the default keeps partial sums below 2^23);
+//     `chunk` K-elements so that no partial sum reaches 2^24 (chunk <= 1024,
+//     the default: |partial| <= 127^2 * 1024 = 16516096 < 2^24; the GPU
+//     tests confirm bit-exact int32 at every chunk length on adversarial
+//     +-127 operands, so the tensor pipe keeps 24-bit integers exact);
 //   * each chunk's fp32 accumulator (integer-valued, hence exact) is read
 //     from tensor memory, converted to int32 and summed in registers, so the
 //     int32 result is exact for any K <= 131072.
@@ -21,11 +23,12 @@
 //                 arrives as fp16 codes straight into the fp16 ring.
 //   warp 1        TMEM allocator and single-thread tcgen05.mma issuer
 //                 (M=128, N=BN, K=16 per instruction, fp32 accumulators).
-//   warps 2-5     converters: int8 codes -> fp16 codes in the 128-byte-swizzled
+//   warps 2-7     converters: int8 codes -> fp16 codes in the 128-byte-swizzled
 //                 K-major layout the MMA descriptors expect.
-//   warps 6-..    epilogue: drain chunk accumulators (two TMEM buffers, so the
+//   warps 8-..    epilogue: drain chunk accumulators (two TMEM buffers, so the
 //                 drain overlaps the next chunk's MMAs) into int32 registers,
-//                 then dequantize + bias -> bf16, or store int32.
+//                 then dequantize + bias -> bf16 (or int32) into a swizzled
+//                 shared-memory staging buffer and a bulk tensor store.
 // Every pipeline wait is bounded (ptx.cuh); a timeout aborts the CTA cleanly.
 #pragma once
 #include <cuda.h>
@@ -33,6 +36,7 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace i8 {
 
@@ -99,7 +103,8 @@ struct GemmCfg {
   static constexpr int STAGE16 = A16_BYTES + B16_BYTES;
   static constexpr int OFF_S8 = 0;
   static constexpr int OFF_S16 = OFF_S8 + (ANY_CONV ? S8 : 0) * STAGE8;
-  static constexpr int OFF_BAR = OFF_S16 + S16 * STAGE16;
+  static constexpr int OFF_EPI = OFF_S16 + S16 * STAGE16;   // 4 KB store staging per epilogue warp
+  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 4096;
   // full8[S8] empty8[S8] full16[S16] empty16[S16] accfull[2] accempty[2] done
   static constexpr int NUM_BARS = 2 * S8 + 2 * S16 + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -216,58 +221,91 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Epilogue store of one thread's row segment (row m, 128 columns from n0).
+// Epilogue store of one warp's 32 rows x 128 columns through a 4 KB
+// shared-memory staging buffer (32 rows x 128 bytes, 128-byte swizzle) and a
+// bulk tensor store per 128-byte-wide column group: bf16 groups are 64
+// columns, int32 groups 32.  Lane i holds row (m_base + i) in acc[0..127].
+// The tensor store clips rows >= M and columns >= N, so ragged tiles need no
+// masking.  tmY is 3-D {N, M, splits}; z selects the split-K partial.
 template <int COLS>
-__device__ __forceinline__ void store_row_segment(const GemmParams& p, int m, int n0,
-                                                  const int (&acc)[COLS], int ks) {
-  if (m >= p.M) return;
+__device__ __forceinline__ void store_warp_tile(const GemmParams& p, const CUtensorMap* tmY,
+                                                uint32_t stage, int lane, int m_base, int n0,
+                                                const int (&acc)[COLS], int z) {
+  const uint32_t row = stage + static_cast<uint32_t>(lane) * 128u;
+  const uint32_t x = static_cast<uint32_t>(lane & 7);
+  const int m = m_base + lane;
   if (p.out_mode == kOutBf16) {
-    const float sa = p.s_a[m];
-    uint16_t* yrow = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(m) * p.ldo;
+    const float sa = m < p.M ? p.s_a[m] : 0.0f;
+    const unsigned long long sa2 = f2(sa, sa);
 #pragma unroll
-    for (int j = 0; j < COLS; j += 8) {
-      const int n = n0 + j;
-      if (n >= p.N) break;
-      if (n + 8 <= p.N) {
-        const float4 w0 = *reinterpret_cast<const float4*>(p.s_w + n);
-        const float4 w1 = *reinterpret_cast<const float4*>(p.s_w + n + 4);
+    for (int g = 0; g < COLS / 64; ++g) {
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      const int nb = n0 + g * 64;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int n = nb + 8 * c;
+        float sw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         uint4 bb = make_uint4(0u, 0u, 0u, 0u);
-        if (p.bias) bb = *reinterpret_cast<const uint4*>(p.bias + n);
-        const float sw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        if (n + 8 <= p.N) {
+          const float4 w0 = *reinterpret_cast<const float4*>(p.s_w + n);
+          const float4 w1 = *reinterpret_cast<const float4*>(p.s_w + n + 4);
+          sw[0] = w0.x; sw[1] = w0.y; sw[2] = w0.z; sw[3] = w0.w;
+          sw[4] = w1.x; sw[5] = w1.y; sw[6] = w1.z; sw[7] = w1.w;
+          if (p.bias) bb = *reinterpret_cast<const uint4*>(p.bias + n);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (n + i < p.N) {
+              sw[i] = p.s_w[n + i];
+              if (p.bias) {
+                const uint32_t hb = p.bias[n + i];
+                if (i & 1) reinterpret_cast<uint32_t*>(&bb)[i >> 1] |= hb << 16;
+                else reinterpret_cast<uint32_t*>(&bb)[i >> 1] |= hb;
+              }
+            }
+          }
+        }
         const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float b0 = __uint_as_float(bw[i] << 16);
-          const float b1 = __uint_as_float(bw[i] & 0xFFFF0000u);
-          o[i] = pack_bf16x2(dequant_one(acc[j + 2 * i], sa, sw[2 * i], b0),
-                             dequant_one(acc[j + 2 * i + 1], sa, sw[2 * i + 1], b1));
+          const int j = g * 64 + 8 * c + 2 * i;
+          // ((float(acc) * s_a) * s_w) + bias, each step rounded to fp32
+          unsigned long long t = f2(__int2float_rn(acc[j]), __int2float_rn(acc[j + 1]));
+          t = f2_mul(t, sa2);
+          t = f2_mul(t, f2(sw[2 * i], sw[2 * i + 1]));
+          t = f2_add(t, f2(__uint_as_float(bw[i] << 16), __uint_as_float(bw[i] & 0xFFFF0000u)));
+          float lo, hi;
+          f2_split(t, lo, hi);
+          o[i] = pack_bf16x2(lo, hi);
         }
-        *reinterpret_cast<uint4*>(yrow + n) = make_uint4(o[0], o[1], o[2], o[3]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (n + i < p.N) {
-            const float b = p.bias ? __uint_as_float(static_cast<uint32_t>(p.bias[n + i]) << 16) : 0.0f;
-            const __nv_bfloat16 v = __float2bfloat16_rn(dequant_one(acc[j + i], sa, p.s_w[n + i], b));
-            yrow[n + i] = *reinterpret_cast<const uint16_t*>(&v);
-          }
-        }
+        sts128(row + ((static_cast<uint32_t>(c) ^ x) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(tmY, stage, nb, m_base, 0);
+        bulk_commit_group();
       }
     }
   } else {
-    int32_t* crow = static_cast<int32_t*>(p.out) + static_cast<int64_t>(m) * p.ldo;
-    if (p.out_mode == kOutPartial) crow += static_cast<int64_t>(ks) * p.split_stride;
 #pragma unroll
-    for (int j = 0; j < COLS; j += 4) {
-      const int n = n0 + j;
-      if (n >= p.N) break;
-      if (n + 4 <= p.N) {
-        *reinterpret_cast<int4*>(crow + n) = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-      } else {
+    for (int g = 0; g < COLS / 32; ++g) {
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (n + i < p.N) crow[n + i] = acc[j + i];
+      for (int c = 0; c < 8; ++c) {
+        const int j = g * 32 + 4 * c;
+        sts128(row + ((static_cast<uint32_t>(c) ^ x) << 4),
+               make_uint4(static_cast<uint32_t>(acc[j]), static_cast<uint32_t>(acc[j + 1]),
+                          static_cast<uint32_t>(acc[j + 2]), static_cast<uint32_t>(acc[j + 3])));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(tmY, stage, n0 + g * 32, m_base, z);
+        bulk_commit_group();
       }
     }
   }
@@ -276,8 +314,9 @@ __device__ __forceinline__ void store_row_segment(const GemmParams& p, int m, in
 // Epilogue role: drains chunk accumulators into int32 registers, then writes
 // the tile (bf16 with dequant + bias, int32, or a split-K partial).
 template <class Cfg>
-__device__ __forceinline__ void gemm_epilogue_role(const GemmParams& p, uint32_t tmem_base, int warp,
-                                                int lane, volatile int* abort_flag, uint32_t bar0) {
+__device__ __forceinline__ void gemm_epilogue_role(const GemmParams& p, const CUtensorMap* tmY,
+                                                   uint32_t sbase, uint32_t tmem_base, int warp,
+                                                   int lane, volatile int* abort_flag, uint32_t bar0) {
   auto accfull = [&](int b) { return bar0 + 8u * (2 * Cfg::S8 + 2 * Cfg::S16 + b); };
   auto accempty = [&](int b) { return bar0 + 8u * (2 * Cfg::S8 + 2 * Cfg::S16 + 2 + b); };
   const int ew = warp - Cfg::EPI_WARP0;
@@ -311,16 +350,18 @@ __device__ __forceinline__ void gemm_epilogue_role(const GemmParams& p, uint32_t
       racc.advance(2);
     }
     if (!ok) break;
-    const int m = tc.mb * Cfg::BM + quarter * 32 + lane;
-    const int n0 = tc.nb * Cfg::BN + cg * 128;
-    store_row_segment<128>(p, m, n0, acc, tc.ks);
+    const uint32_t stage = sbase + Cfg::OFF_EPI + static_cast<uint32_t>(ew) * 4096u;
+    store_warp_tile<128>(p, tmY, stage, lane, tc.mb * Cfg::BM + quarter * 32,
+                         tc.nb * Cfg::BN + cg * 128, acc, tc.ks);
   }
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
 }
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -366,6 +407,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmY);
   }
   tc_fence_before();
   __syncthreads();
@@ -374,7 +416,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   if (warp >= Cfg::EPI_WARP0) {
     regs_inc<Cfg::REG_HI>();
-    gemm_epilogue_role<Cfg>(p, tmem_base, warp, lane, abort_flag, bar0);
+    gemm_epilogue_role<Cfg>(p, &tmY, sbase, tmem_base, warp, lane, abort_flag, bar0);
   } else if (warp == 0) {
     regs_dec<Cfg::REG_LO>();
     // ------------------------------------------------------------ producer

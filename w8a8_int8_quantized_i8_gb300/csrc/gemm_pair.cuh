@@ -1,0 +1,411 @@
+// gemm_pair.cuh -- the fused W8A8 GEMM on a CTA pair (cta_group::2).
+//
+// Same arithmetic as gemm.cuh (int8 codes through the fp16 tensor pipe with
+// exact chunked accumulation, fused per-token x per-channel dequant + bias).
+// Two CTAs of a cluster compute one 256 x 256 output tile together:
+//   CTA r (r = 0, 1) stages and widens A rows [m0 + 128 r, +128) and B rows
+//   [n0 + 128 r, +128) of every K-block; one thread of CTA 0 issues
+//   tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), which reads both
+//   CTAs' shared memory and writes each CTA's 128 rows x 256 columns of D
+//   into that CTA's tensor memory.  Each SM therefore stages (and widens) half
+//   of the B tile it multiplies, which halves the shared-memory traffic per
+//   MAC spent on B compared with a 128 x 256 tile on one SM.
+// Cross-CTA protocol (all waits bounded):
+//   * converters arrive on their own CTA's full16[s] and epilogue warps on
+//     their own accempty[b] (CTA-scope release: cheap);
+//   * in CTA 1 one relay thread forwards each completed phase of those two
+//     barriers to CTA 0's pfull16[s] / paccempty[b] (one cluster-scope
+//     release per phase instead of one per warp);
+//   * the MMA thread of CTA 0 waits on its own barrier and the forwarded one,
+//     and commits to empty16[s] / accfull[b] of both CTAs (multicast).
+#pragma once
+#include "gemm.cuh"
+
+namespace i8 {
+
+// SYNC selects the memory-model scope of the cross-CTA hand-off:
+//   0: relay arrives with release.cluster, the MMA thread waits with acquire.cluster
+//   1: relay release.cluster, MMA thread acquire.cta
+//   2: relay release.cta (remote arrive), MMA thread acquire.cta
+// Measured on GB300 at DiT shapes: 0 and 1 run at ~725 TOPS, 2 at ~920-990
+// (the cluster-scope release drains the relay's memory pipeline every stage);
+// all three gave bit-exact results on repeated runs.  2 is the default.  The
+// data a stage hands over is written to the issuing CTA's own shared memory
+// and made visible to the async proxy (fence.proxy.async) before the local
+// arrive that the relay observes.
+template <int S8_, int S16_, bool CONV_A_, bool CONV_B_, int SYNC_ = 2>
+struct PairCfg {
+  static constexpr int SYNC = SYNC_;
+  static constexpr int BM = 128;        // A rows staged per CTA
+  static constexpr int BN = 128;        // B rows staged per CTA
+  static constexpr int PAIR_M = 256;
+  static constexpr int PAIR_N = 256;
+  static constexpr int S8 = S8_;
+  static constexpr int S16 = S16_;
+  static constexpr bool CONV_A = CONV_A_;
+  static constexpr bool CONV_B = CONV_B_;
+  static constexpr bool ANY_CONV = CONV_A || CONV_B;
+  static constexpr bool ANY_DIRECT = !CONV_A || !CONV_B;
+  static constexpr int BK8 = 128;
+  static constexpr int BK16 = 64;
+  static constexpr int CONV_WARPS = 6;
+  static constexpr int CONV_THREADS = CONV_WARPS * 32;
+  static constexpr int EPI_WARPS = 8;   // 4 lane quarters x 2 column groups of 128
+  static constexpr int EPI_WARP0 = 8;
+  static constexpr int NUM_WARPS = 16;
+  static constexpr int THREADS = 512;
+  static constexpr int REG_LO = 88;
+  static constexpr int REG_HI = 168;
+  static_assert(2 * 128 * REG_LO + 2 * 128 * REG_HI <= THREADS * (65536 / THREADS),
+                "register split exceeds the launch allocation");
+  static constexpr int A_ITEMS = CONV_A ? BM * 4 : 0;
+  static constexpr int B_ITEMS = CONV_B ? BN * 4 : 0;
+  static constexpr int ITEMS = A_ITEMS + B_ITEMS;
+  static constexpr int IPT = ITEMS > 0 ? (ITEMS + CONV_THREADS - 1) / CONV_THREADS : 1;
+  static constexpr int A8_BYTES = CONV_A ? BM * BK8 : 0;
+  static constexpr int B8_BYTES = CONV_B ? BN * BK8 : 0;
+  static constexpr int STAGE8 = A8_BYTES + B8_BYTES;
+  static constexpr int A16_BYTES = BM * BK16 * 2;
+  static constexpr int B16_BYTES = BN * BK16 * 2;
+  static constexpr int STAGE16 = A16_BYTES + B16_BYTES;
+  static constexpr int OFF_S8 = 0;
+  static constexpr int OFF_S16 = OFF_S8 + (ANY_CONV ? S8 : 0) * STAGE8;
+  static constexpr int OFF_EPI = OFF_S16 + S16 * STAGE16;   // 4 KB store staging per epilogue warp
+  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 4096;
+  // full8[S8] empty8[S8] full16[S16] tma16[S16] empty16[S16] pfull16[S16]
+  // accfull[2] accempty[2] paccempty[2] done
+  static constexpr int NUM_BARS = 2 * S8 + 4 * S16 + 7;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int TMEM_COLS = 2 * PAIR_N;
+  static constexpr uint32_t TX8 = STAGE8;
+  static constexpr uint32_t TX16 = (CONV_A ? 0 : A16_BYTES) + (CONV_B ? 0 : B16_BYTES);
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(STAGE8 % 1024 == 0 && STAGE16 % 1024 == 0, "stage alignment");
+};
+
+struct PairBars {
+  uint32_t base;
+  int S8, S16;
+  __device__ uint32_t full8(int s) const { return base + 8u * s; }
+  __device__ uint32_t empty8(int s) const { return base + 8u * (S8 + s); }
+  __device__ uint32_t full16(int s) const { return base + 8u * (2 * S8 + s); }
+  __device__ uint32_t tma16(int s) const { return base + 8u * (2 * S8 + S16 + s); }
+  __device__ uint32_t empty16(int s) const { return base + 8u * (2 * S8 + 2 * S16 + s); }
+  __device__ uint32_t pfull16(int s) const { return base + 8u * (2 * S8 + 3 * S16 + s); }
+  __device__ uint32_t accfull(int b) const { return base + 8u * (2 * S8 + 4 * S16 + b); }
+  __device__ uint32_t accempty(int b) const { return base + 8u * (2 * S8 + 4 * S16 + 2 + b); }
+  __device__ uint32_t paccempty(int b) const { return base + 8u * (2 * S8 + 4 * S16 + 4 + b); }
+  __device__ uint32_t done() const { return base + 8u * (2 * S8 + 4 * S16 + 6); }
+};
+
+struct PairTile {
+  int mp, nb, ks, kb0, kb1;
+};
+
+// Pair tiles: num_m_blk counts 256-row pair blocks, num_n_blk 256-column blocks.
+__device__ __forceinline__ PairTile decode_pair_tile(const GemmParams& p, int tile) {
+  PairTile t;
+  t.ks = tile % p.splits;
+  const int rest = tile / p.splits;
+  t.mp = rest % p.num_m_blk;
+  t.nb = rest / p.num_m_blk;
+  t.kb0 = t.ks * p.kb_per_split;
+  t.kb1 = min(t.kb0 + p.kb_per_split, p.total_kb);
+  return t;
+}
+
+template <class Cfg>
+__device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CUtensorMap* tmY,
+                                                   uint32_t sbase, uint32_t tmem_base,
+                                                   int warp, int lane, uint32_t rank,
+                                                   volatile int* abort_flag, const PairBars& bars) {
+  const int ew = warp - Cfg::EPI_WARP0;
+  const int quarter = warp & 3;
+  const int cg = ew >> 2;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  Ring racc;
+  bool ok = true;
+  for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+    const PairTile tc = decode_pair_tile(p, tile);
+    const int nst = 2 * (tc.kb1 - tc.kb0);
+    int acc[128];
+#pragma unroll
+    for (int i = 0; i < 128; ++i) acc[i] = 0;
+    for (int st0 = 0; st0 < nst; st0 += p.chunk_stages) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.accfull(racc.s), racc.ph, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(racc.s * Cfg::PAIR_N + cg * 128);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + q4 * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[q4 * 32 + i] += f32_exact_int_to_s32(r[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.accempty(racc.s));
+      racc.advance(2);
+    }
+    if (!ok) break;
+    const uint32_t stage = sbase + Cfg::OFF_EPI + static_cast<uint32_t>(ew) * 4096u;
+    store_warp_tile<128>(p, tmY, stage, lane,
+                         tc.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM + quarter * 32,
+                         tc.nb * Cfg::PAIR_N + cg * 128, acc, tc.ks);
+  }
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
+}
+
+template <class Cfg>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
+    gemm_w8a8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw_base);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  const PairBars bars{sbase + Cfg::OFF_BAR, Cfg::S8, Cfg::S16};
+  auto stage8 = [&](int s) { return sbase + Cfg::OFF_S8 + static_cast<uint32_t>(s * Cfg::STAGE8); };
+  auto stage16 = [&](int s) { return sbase + Cfg::OFF_S16 + static_cast<uint32_t>(s * Cfg::STAGE16); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::S8; ++s) {
+      mbar_init(bars.full8(s), 1);
+      mbar_init(bars.empty8(s), Cfg::CONV_WARPS);
+    }
+    for (int s = 0; s < Cfg::S16; ++s) {
+      mbar_init(bars.full16(s), Cfg::CONV_WARPS);
+      mbar_init(bars.tma16(s), 1);
+      mbar_init(bars.empty16(s), 1);
+      mbar_init(bars.pfull16(s), 1);     // CTA 0: forwarded by CTA 1's relay
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars.accfull(b), 1);
+      mbar_init(bars.accempty(b), Cfg::EPI_WARPS);
+      mbar_init(bars.paccempty(b), 1);   // CTA 0: forwarded by CTA 1's relay
+    }
+    mbar_init(bars.done(), 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmY);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp >= Cfg::EPI_WARP0) {
+    regs_inc<Cfg::REG_HI>();
+    pair_epilogue_role<Cfg>(p, &tmY, sbase, tmem_base, warp, lane, rank, abort_flag, bars);
+  } else if (warp == 0) {
+    regs_dec<Cfg::REG_LO>();
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      Ring r8, r16;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+        const PairTile tc = decode_pair_tile(p, tile);
+        const int m0 = tc.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM;
+        const int n0 = tc.nb * Cfg::PAIR_N + static_cast<int>(rank) * Cfg::BN;
+        for (int kb = tc.kb0; ok && kb < tc.kb1; ++kb) {
+          if constexpr (Cfg::ANY_CONV) {
+            if (!(ok = mbar_wait(bars.empty8(r8.s), r8.ph ^ 1u, abort_flag))) break;
+            mbar_arrive_expect_tx(bars.full8(r8.s), Cfg::TX8);
+            if constexpr (Cfg::CONV_A)
+              tma_load_2d(stage8(r8.s), &tmA, bars.full8(r8.s), kb * Cfg::BK8, m0);
+            if constexpr (Cfg::CONV_B)
+              tma_load_2d(stage8(r8.s) + Cfg::A8_BYTES, &tmB, bars.full8(r8.s), kb * Cfg::BK8, n0);
+            r8.advance(Cfg::S8);
+          }
+          if constexpr (Cfg::ANY_DIRECT) {
+            for (int h = 0; h < 2; ++h) {
+              if (!(ok = mbar_wait(bars.empty16(r16.s), r16.ph ^ 1u, abort_flag))) break;
+              mbar_arrive_expect_tx(bars.tma16(r16.s), Cfg::TX16);
+              const int k16 = kb * Cfg::BK8 + h * Cfg::BK16;
+              if constexpr (!Cfg::CONV_A)
+                tma_load_2d(stage16(r16.s), &tmA, bars.tma16(r16.s), k16, m0);
+              if constexpr (!Cfg::CONV_B)
+                tma_load_2d(stage16(r16.s) + Cfg::A16_BYTES, &tmB, bars.tma16(r16.s), k16, n0);
+              r16.advance(Cfg::S16);
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    regs_dec<Cfg::REG_LO>();
+    // ------------------------------------------------------------ MMA issuer (CTA 0)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(Cfg::PAIR_M, Cfg::PAIR_N);
+      Ring r16, racc;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+        const PairTile tc = decode_pair_tile(p, tile);
+        const int nst = 2 * (tc.kb1 - tc.kb0);
+        for (int st0 = 0; ok && st0 < nst; st0 += p.chunk_stages) {
+          const int st1 = min(nst, st0 + p.chunk_stages);
+          if (!(ok = mbar_wait(bars.accempty(racc.s), racc.ph ^ 1u, abort_flag))) break;
+          if (!(ok = Cfg::SYNC == 0
+                         ? mbar_wait_cluster(bars.paccempty(racc.s), racc.ph ^ 1u, abort_flag)
+                         : mbar_wait(bars.paccempty(racc.s), racc.ph ^ 1u, abort_flag)))
+            break;
+          tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(racc.s * Cfg::PAIR_N);
+          for (int st = st0; st < st1; ++st) {
+            if (!(ok = mbar_wait(bars.full16(r16.s), r16.ph, abort_flag))) break;
+            if (!(ok = Cfg::SYNC == 0 ? mbar_wait_cluster(bars.pfull16(r16.s), r16.ph, abort_flag)
+                                      : mbar_wait(bars.pfull16(r16.s), r16.ph, abort_flag)))
+              break;
+            tc_fence_after();
+            const uint64_t ad = smem_desc_sw128(stage16(r16.s));
+            const uint64_t bd = smem_desc_sw128(stage16(r16.s) + Cfg::A16_BYTES);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              mma_f16_ss_pair(d, ad + 2u * j, bd + 2u * j, idesc, (st > st0 || j > 0) ? 1u : 0u);
+            }
+            mma_commit_pair(bars.empty16(r16.s), 0x3);
+            r16.advance(Cfg::S16);
+          }
+          if (!ok) break;
+          mma_commit_pair(bars.accfull(racc.s), 0x3);
+          racc.advance(2);
+        }
+      }
+      mma_commit_pair(bars.done(), 0x1);
+      mbar_wait_bounded(bars.done(), 0u, 100000000ull);
+    } else if (lane == 0) {
+      // ---------------------------------------------------------- relay (CTA 1)
+      // Walks the MMA thread's schedule and forwards each completed phase of
+      // this CTA's full16 / accempty barriers to CTA 0.  The first use of
+      // each accumulator buffer needs no drain, so nothing is forwarded then.
+      const uint32_t pfull0 = mapa_shared(bars.pfull16(0), 0);
+      const uint32_t pacc0 = mapa_shared(bars.paccempty(0), 0);
+      Ring r16, racc;
+      int chunk = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+        const PairTile tc = decode_pair_tile(p, tile);
+        const int nst = 2 * (tc.kb1 - tc.kb0);
+        for (int st0 = 0; ok && st0 < nst; st0 += p.chunk_stages, ++chunk) {
+          const int st1 = min(nst, st0 + p.chunk_stages);
+          if (chunk >= 2) {
+            if (!(ok = mbar_wait(bars.accempty(racc.s), racc.ph ^ 1u, abort_flag))) break;
+            if constexpr (Cfg::SYNC == 2) mbar_arrive_remote_cta(pacc0 + 8u * racc.s);
+            else mbar_arrive_cluster(pacc0 + 8u * racc.s);
+          }
+          racc.advance(2);
+          for (int st = st0; st < st1; ++st) {
+            if (!(ok = mbar_wait(bars.full16(r16.s), r16.ph, abort_flag))) break;
+            if constexpr (Cfg::SYNC == 2) mbar_arrive_remote_cta(pfull0 + 8u * r16.s);
+            else mbar_arrive_cluster(pfull0 + 8u * r16.s);
+            r16.advance(Cfg::S16);
+          }
+        }
+      }
+    }
+  } else {
+    regs_dec<Cfg::REG_LO>();
+    // ------------------------------------------------------------ converters
+    const int ct = threadIdx.x - 64;
+    ConvItem items[Cfg::IPT];
+#pragma unroll
+    for (int j = 0; j < Cfg::IPT; ++j) {
+      const int i = ct + j * Cfg::CONV_THREADS;
+      items[j] = conv_item<Cfg>(i < Cfg::ITEMS ? i : 0);
+    }
+    Ring r8, r16;
+    bool ok = true;
+    for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+      const PairTile tc = decode_pair_tile(p, tile);
+      for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
+        // Both K-halves of the int8 block are read from shared memory in one
+        // batch, so the load latency is exposed once per block.
+        uint4 v[2][Cfg::IPT];
+        if constexpr (Cfg::ANY_CONV) {
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.full8(r8.s), r8.ph, abort_flag));
+          if (!ok) break;
+          const uint32_t s8 = stage8(r8.s);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int j = 0; j < Cfg::IPT; ++j) {
+              if (ct + j * Cfg::CONV_THREADS < Cfg::ITEMS)
+                v[h][j] = lds128(s8 + (items[j].src ^ (static_cast<uint32_t>(h) << 6)));
+            }
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.empty16(r16.s), r16.ph ^ 1u, abort_flag));
+          if (!ok) break;
+          if constexpr (Cfg::ANY_CONV) {
+            const uint32_t s16 = stage16(r16.s);
+#pragma unroll
+            for (int j = 0; j < Cfg::IPT; ++j) {
+              if (ct + j * Cfg::CONV_THREADS < Cfg::ITEMS) {
+                uint4 o0, o1;
+                s8x4_to_f16x4(v[h][j].x, o0.x, o0.y);
+                s8x4_to_f16x4(v[h][j].y, o0.z, o0.w);
+                s8x4_to_f16x4(v[h][j].z, o1.x, o1.y);
+                s8x4_to_f16x4(v[h][j].w, o1.z, o1.w);
+                sts128(s16 + items[j].dst, o0);
+                sts128(s16 + (items[j].dst ^ 16u), o1);
+              }
+            }
+            fence_proxy_async_smem();
+          }
+          if constexpr (Cfg::ANY_DIRECT) {
+            // this CTA's directly loaded half of the stage must have landed
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.tma16(r16.s), r16.ph, abort_flag));
+            if (!ok) break;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.full16(r16.s));
+          r16.advance(Cfg::S16);
+        }
+        if (!ok) break;
+        if constexpr (Cfg::ANY_CONV) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.empty8(r8.s));
+          r8.advance(Cfg::S8);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer's MMAs and remote arrivals are finished
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace i8

@@ -11,6 +11,7 @@
 
 #include "../../include/i8.h"
 #include "gemm.cuh"
+#include "gemm_pair.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
 
@@ -54,17 +55,19 @@ constexpr int kMaxDevices = 64;
 
 // Process-wide tuning knobs (i8_set_option).
 struct Options {
-  int chunk_k = 512;       // K per exact fp32 chunk (multiple of 64, <= 1024)
+  int chunk_k = 1024;      // K per exact fp32 chunk (multiple of 64, <= 1024)
   int force_splits = 0;    // 0 = table
   int max_ctas = 0;        // 0 = all SMs
   int force_bn = 0;        // 0 = table, else 128 or 256
   int quant_vpl = 6;       // max 16-byte vectors per lane in the quantizer
+  int cta_pair = 0;        // 0 = table, 1 = never, 2 = whenever the shape allows
 };
 Options g_opt;
 
 struct DeviceInfo {
   bool init = false;
   int sms = 0;
+  int pair_clusters[4] = {};  // co-resident clusters per pair-kernel config
   int cc_major = 0, cc_minor = 0;
   bool smem_set[8] = {};
 };
@@ -148,6 +151,7 @@ i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t
 
 // ----------------------------------------------------------------- GEMM plan
 struct Plan {
+  bool pair = false;       // CTA-pair kernel (256 x 256 tiles per cluster of 2)
   int bn = 128;
   int splits = 1;
   int kb_per_split = 1;
@@ -163,8 +167,40 @@ struct Plan {
 // Shape -> configuration (replaces per-shape autotuning): 128 x 128 tiles;
 // when the output tiles cannot fill every SM, K is split so that tiles x
 // splits covers the SMs, with at least two 128-wide K-blocks per split.
-Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
+Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
+               bool b16 = false) {
   Plan p;
+  // CTA pairs: one 256 x 256 tile per cluster of two SMs, each SM staging
+  // (and, for int8 weights, widening) half of B.  Used for int8 weights when
+  // the pair tiles alone fill every cluster slot; with pre-widened weights
+  // the single-CTA 128 x 256 kernel measured slightly faster.
+  if (pair_clusters <= 0) pair_clusters = sms / 2;
+  const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+  const bool pair_ok = M >= 256 && N >= 256;
+  p.pair = g_opt.cta_pair == 2
+               ? pair_ok
+               : (g_opt.cta_pair == 0 && !b16 && pair_ok && pair_tiles >= pair_clusters);
+  if (p.pair) {
+    p.bn = 256;
+    p.total_kb = static_cast<int>((K + 127) / 128);
+    p.num_m = static_cast<int>((M + 255) / 256);
+    p.num_n = static_cast<int>((N + 255) / 256);
+    int splits = g_opt.force_splits > 0 ? g_opt.force_splits : 1;
+    splits = std::max(1, std::min(splits, p.total_kb));
+    p.kb_per_split = (p.total_kb + splits - 1) / splits;
+    p.splits = (p.total_kb + p.kb_per_split - 1) / p.kb_per_split;
+    p.num_tiles = static_cast<int>(pair_tiles * p.splits);
+    int cap = pair_clusters;
+    if (g_opt.max_ctas > 0) cap = std::max(1, std::min(cap, g_opt.max_ctas / 2));
+    p.grid = 2 * std::max(1, std::min(p.num_tiles, cap));
+    p.chunk_stages = g_opt.chunk_k / 64;
+    if (p.splits > 1) {
+      p.ws_ld = (N + 3) / 4 * 4;
+      p.ws_bytes = static_cast<size_t>(p.splits) * static_cast<size_t>(M) *
+                   static_cast<size_t>(p.ws_ld) * sizeof(int32_t);
+    }
+    return p;
+  }
   // 256-wide tiles halve the on-chip widening of A per MAC; keep 128 when
   // N is small or the wider tiles would leave SMs idle.
   p.bn = (N >= 256 && ((M + 127) / 128) * ((N + 255) / 256) >= sms) ? 256 : 128;
@@ -208,9 +244,24 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output map for the epilogue's bulk tensor stores: {N, M, planes} with the
+// split-K partial index as the third coordinate; 128-byte-wide boxes of 32 rows.
+bool encode_out(CUtensorMap* map, bool bf16, const void* base, uint64_t N, uint64_t M,
+                uint64_t ld_elems, uint64_t planes) {
+  const uint64_t esz = bf16 ? 2 : 4;
+  const cuuint64_t dims[3] = {N, M, planes};
+  const cuuint64_t strides[2] = {ld_elems * esz, ld_elems * esz * M};
+  const cuuint32_t box[3] = {bf16 ? 64u : 32u, 32u, 1u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_INT32, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <class Cfg>
 i8_status launch_gemm_cfg(DeviceInfo* d, int slot, const CUtensorMap& ma, const CUtensorMap& mb,
-                          const GemmParams& gp, int grid, cudaStream_t st) {
+                          const CUtensorMap& my, const GemmParams& gp, int grid, cudaStream_t st) {
   auto kern = gemm_w8a8_kernel<Cfg>;
   if (!d->smem_set[slot]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -218,15 +269,51 @@ i8_status launch_gemm_cfg(DeviceInfo* d, int slot, const CUtensorMap& ma, const 
       return I8_ERR_CUDA;
     d->smem_set[slot] = true;
   }
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ma, mb, gp);
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ma, mb, my, gp);
   return cuda_status(cudaGetLastError());
 }
 
 // <BN, int8 stages, fp16 stages, widen A on chip, widen B on chip>
+template <class Cfg>
+int pair_cluster_capacity(DeviceInfo* d, int slot) {
+  if (d->pair_clusters[slot] > 0) return d->pair_clusters[slot];
+  auto kern = gemm_w8a8_pair_kernel<Cfg>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (d->sms / 2), 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  if (n <= 0) n = d->sms / 2;
+  d->pair_clusters[slot] = n;
+  return n;
+}
+
+template <class Cfg>
+i8_status launch_pair_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my,
+                          const GemmParams& gp, int grid, cudaStream_t st) {
+  auto kern = gemm_w8a8_pair_kernel<Cfg>;
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ma, mb, my, gp);
+  return cuda_status(cudaGetLastError());
+}
+
+using PairConv = PairCfg<3, 3, true, true>;    // int8 weights, CTA pair
+using PairWide = PairCfg<4, 4, true, false>;   // pre-widened weights, CTA pair
 using CfgConv128 = GemmCfg<128, 3, 3, true, true>;   // int8 weights
 using CfgWide128 = GemmCfg<128, 4, 4, true, false>;  // weights pre-widened to fp16 codes
 using CfgConv256 = GemmCfg<256, 2, 2, true, true>;
-using CfgWide256 = GemmCfg<256, 4, 3, true, false>;
+using CfgWide256 = GemmCfg<256, 3, 3, true, false>;
 
 // Common GEMM driver.  b16 = weights given as fp16 codes instead of int8.
 i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int64_t N, int64_t K,
@@ -244,13 +331,15 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   if (out_mode == kOutInt32 && ldo % 4 != 0) return I8_ERR_ALIGNMENT;
   DeviceInfo* d;
   if (i8_status e = device_info(&d, nullptr)) return e;
-  const Plan pl = make_plan(M, N, K, d->sms);
+  const int clusters = b16 ? pair_cluster_capacity<PairWide>(d, 1)
+                           : pair_cluster_capacity<PairConv>(d, 0);
+  const Plan pl = make_plan(M, N, K, d->sms, clusters, b16);
   if (pl.ws_bytes > 0) {
     if (!ws || ws_bytes < pl.ws_bytes) return I8_ERR_WORKSPACE;
     if (!aligned16(ws)) return I8_ERR_ALIGNMENT;
   }
   CUtensorMap ma, mb;
-  const uint32_t bn = static_cast<uint32_t>(pl.bn);
+  const uint32_t bn = pl.pair ? 128u : static_cast<uint32_t>(pl.bn);
   if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M, K, 128, 128)) return I8_ERR_CUDA;
   if (b16) {
     if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wb, K, N, 2 * K, 64, bn))
@@ -283,13 +372,21 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
     gp.ldo = ldo;
     gp.split_stride = 0;
   }
+  CUtensorMap my;
+  if (!encode_out(&my, gp.out_mode == kOutBf16, gp.out, static_cast<uint64_t>(N),
+                  static_cast<uint64_t>(M), static_cast<uint64_t>(gp.ldo),
+                  static_cast<uint64_t>(pl.splits)))
+    return I8_ERR_CUDA;
   i8_status e;
-  if (pl.bn == 256) {
-    e = b16 ? launch_gemm_cfg<CfgWide256>(d, 3, ma, mb, gp, pl.grid, st)
-            : launch_gemm_cfg<CfgConv256>(d, 2, ma, mb, gp, pl.grid, st);
+  if (pl.pair) {
+    e = b16 ? launch_pair_cfg<PairWide>(ma, mb, my, gp, pl.grid, st)
+            : launch_pair_cfg<PairConv>(ma, mb, my, gp, pl.grid, st);
+  } else if (pl.bn == 256) {
+    e = b16 ? launch_gemm_cfg<CfgWide256>(d, 3, ma, mb, my, gp, pl.grid, st)
+            : launch_gemm_cfg<CfgConv256>(d, 2, ma, mb, my, gp, pl.grid, st);
   } else {
-    e = b16 ? launch_gemm_cfg<CfgWide128>(d, 1, ma, mb, gp, pl.grid, st)
-            : launch_gemm_cfg<CfgConv128>(d, 0, ma, mb, gp, pl.grid, st);
+    e = b16 ? launch_gemm_cfg<CfgWide128>(d, 1, ma, mb, my, gp, pl.grid, st)
+            : launch_gemm_cfg<CfgConv128>(d, 0, ma, mb, my, gp, pl.grid, st);
   }
   if (e != I8_OK) return e;
   if (pl.splits > 1) {
@@ -368,7 +465,7 @@ size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return 0;
   DeviceInfo* d;
   if (device_info(&d, nullptr) != I8_OK) return 0;
-  return make_plan(M, N, K, d->sms).ws_bytes;
+  return make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0)).ws_bytes;
 }
 
 i8_status i8_gemm_int32(const int8_t* aq, const int8_t* wq, int64_t M, int64_t N, int64_t K,
@@ -398,7 +495,9 @@ i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a, 
       N <= INT32_MAX) {
     DeviceInfo* d;
     if (i8_status e = device_info(&d, nullptr)) return e;
-    if (make_plan(M, N, K, d->sms).ws_bytes > kStaticWsBytes) return I8_ERR_WORKSPACE;
+    if (make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0)).ws_bytes >
+        kStaticWsBytes)
+      return I8_ERR_WORKSPACE;
     if (i8_status e = static_ws_address(&ws)) return e;
   }
   return gemm_common(aq, wq, false, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws,
@@ -447,6 +546,10 @@ i8_status i8_set_option(i8_option opt, int64_t value) {
     case I8_OPT_QUANT_VPL:
       if (value < 1 || value > 16) return I8_ERR_INVALID_ARG;
       g_opt.quant_vpl = static_cast<int>(value);
+      return I8_OK;
+    case I8_OPT_CTA_PAIR:
+      if (value < 0 || value > 2) return I8_ERR_INVALID_ARG;
+      g_opt.cta_pair = static_cast<int>(value);
       return I8_OK;
     case I8_OPT_TILE_N:
       if (value != 0 && value != 128 && value != 256) return I8_ERR_INVALID_ARG;
