@@ -62,6 +62,46 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+PROFILE_SUMMARIES = {
+    "dit_qkv_768px_M2560_K3072_N9216": "gemm_w8a8_qkv768_M2560_K3072_N9216.md",
+}
+KERNEL_SOURCES = ("w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
+                  "w8a8_int8_quantized_i8_gb300/csrc/gemm_pair.cuh",
+                  "w8a8_int8_quantized_i8_gb300/csrc/ptx.cuh",
+                  "w8a8_int8_quantized_i8_gb300/csrc/quant.cuh")
+
+
+def _profiled_traffic(workload: str, weights: str):
+    """DRAM bytes per launch of the GEMM from the committed ncu summary, or
+    None when no summary covers this workload or the kernel sources changed
+    since the capture."""
+    import hashlib
+    name = PROFILE_SUMMARIES.get(workload)
+    if weights != "int8" or name is None:
+        return None
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as fh:
+        for line in fh:
+            if ":" in line and not line.startswith(("|", "#", " ")):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("workload") != workload:
+        return None
+    h = hashlib.sha256()
+    for src in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, src), "rb") as fh:
+            h.update(fh.read())
+    if fields.get("kernel_sources_sha256") != h.hexdigest():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -354,8 +394,10 @@ def run_ours(args, shape, dist, rank, world, local):
                              f"(inputs of a step last touched {R - 1} steps earlier)",
                        "k_split": splits, "replicas": world},
             "roofline": {"bound": "tensor", "achieved": gemm_tops, "peak": tc_peak,
-                         "unit": "TFLOP/s", "frac": gemm_tops / tc_peak, "traffic": None,
-                         "kernel": "gemm_w8a8_kernel (+split-K reduce when split)",
+                         "unit": "TFLOP/s", "frac": gemm_tops / tc_peak,
+                         "traffic": _profiled_traffic(shape.name, args.weights),
+                         "traffic_unit": "bytes per launch (ncu dram read + write)",
+                         "kernel": "gemm_w8a8 (CTA-pair or single-CTA per the shape table)",
                          "peak_note": f"{peak_kind} dense bf16 burst (same nominal rate as the "
                                       "fp16 kind the int8 codes run through)"},
             "quant_roofline": {"bound": "hbm", "achieved": quant_bytes / (quant_ms * 1e-3) / 1e9,

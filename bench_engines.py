@@ -12,9 +12,11 @@ Prints one JSON object per line:
   - ``torch._int_mm`` (int32 only, the pages' exactness reference),
   - the "fake INT8" forward the pages replace: dequantize A_q and W_q to bf16,
     then a bf16 matmul + bias (all torch ops);
-  inputs rotate over enough buffer sets to exceed 3x the 129 MB L2.
+  inputs rotate over enough buffer sets to exceed 3x the 129 MB L2;
+* ``stack`` (with --stack): the linear-layer time per denoising step of the
+  synthetic 28-block DiT stack at 1024px batch 2 (M = 8704), glue excluded.
 
-Usage: python bench_engines.py [--sweep] [--iters N]
+Usage: python bench_engines.py [--sweep] [--stack] [--no-engines] [--iters N]
 """
 from __future__ import annotations
 
@@ -184,11 +186,48 @@ def shape_row(shape, iters, full=True):
     print(json.dumps(res), flush=True)
 
 
+def stack_time(blocks=28, M=8704, iters=5):
+    """Linear-layer time per denoising step of the synthetic 28-block DiT
+    stack at 1024px batch 2 (M = 8704): the sum over 112 layers of per-token
+    quant + fused GEMM, timed with CUDA events around each layer; the glue
+    (LayerNorm, GELU, V slice) is excluded."""
+    from w8a8_int8_quantized_i8_gb300 import dit_stack
+    stack = dit_stack.build(blocks=blocks, seed=5)
+    h = inputs.activations(M, dit_stack.WIDTH, torch.Generator().manual_seed(5)).to("cuda")
+    events = []
+
+    def timer(begin):
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record()
+        events.append(ev)
+
+    dit_stack.forward(stack, h)  # warm-up
+    torch.cuda.synchronize()
+    lin, tot = [], []
+    for _ in range(iters):
+        events.clear()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dit_stack.forward(stack, h, timer=timer)
+        e1.record()
+        torch.cuda.synchronize()
+        lin.append(sum(events[i].elapsed_time(events[i + 1]) for i in range(0, len(events), 2)))
+        tot.append(e0.elapsed_time(e1))
+    i8.sync_check()
+    ops = 2.0 * M * blocks * sum(K * N for _, K, N in dit_stack.LAYERS)
+    lin_ms = sorted(lin)[len(lin) // 2]
+    print(json.dumps({"stack": f"dit_1024px_b2_{blocks}blocks_M{M}", "linear_ms_per_step": lin_ms,
+                      "step_ms_with_glue": sorted(tot)[len(tot) // 2], "layers": 4 * blocks,
+                      "linear_tops": ops / (lin_ms * 1e-3) / 1e12}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--sweep", action="store_true", help="also run the 35-shape sweep")
     ap.add_argument("--iters", type=int, default=30)
     ap.add_argument("--no-engines", action="store_true")
+    ap.add_argument("--stack", action="store_true", help="time the 28-block DiT linear stack")
     args = ap.parse_args(argv)
     i8.load()
     if not args.no_engines:
@@ -198,6 +237,8 @@ def main(argv=None):
     if args.sweep:
         for shape in inputs.sweep_shapes():
             shape_row(shape, args.iters, full=True)
+    if args.stack:
+        stack_time()
     return 0
 
 

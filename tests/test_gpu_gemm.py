@@ -68,17 +68,20 @@ def _adversarial(M, N, K, seed):
 
 
 @pytest.mark.parametrize("chunk_k", [64, 256, 512, 1024])
-def test_gemm_int32_adversarial_exact(orc, chunk_k):
+@pytest.mark.parametrize("M,N,pair", [(130, 136, 1), (260, 264, 2)], ids=["single_cta", "cta_pair"])
+def test_gemm_int32_adversarial_exact(orc, chunk_k, M, N, pair):
     """+-127 operands: partial sums reach 127^2 * chunk_k; K = 8192 overflows
     fp32 exactness (2^24) unless the accumulation is chunked correctly."""
-    M, N, K = 130, 136, 8192
+    K = 8192
     a, w = _adversarial(M, N, K, seed=chunk_k)
     i8.set_option("chunk_k", chunk_k)
+    i8.set_option("cta_pair", pair)
     try:
         c = i8.gemm_int32(to_dev(a), to_dev(w))
         i8.sync_check()
     finally:
         i8.set_option("chunk_k", 1024)
+        i8.set_option("cta_pair", 0)
     got = c.cpu().numpy()
     want = orc.gemm_s32(a.numpy(), w.numpy())
     assert got[0, 0] == 127 * 127 * K

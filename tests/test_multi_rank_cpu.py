@@ -1,0 +1,78 @@
+"""The bench's multi-rank host logic on CPU: two gloo ranks on 127.0.0.1.
+
+The path shards without any exchange (replicas), so the only multi-rank
+logic is the barrier around the timed region, the max-over-ranks step time,
+the sum-over-ranks work, and the rule that the reference arm runs on rank 0
+only.  No GPU is involved.
+"""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import bench
+    dist, r, w, local = bench._dist()
+    assert (r, w, local) == (rank, world, rank)
+    bench._barrier(dist)
+    t_max = bench._max_over_ranks(dist, 1.0 + rank)        # rank 1 is the slow one
+    work = bench._sum_over_ranks(dist, 100.0 * (rank + 1))
+    # value = all ranks' work / the slowest rank's time
+    q.put((rank, t_max, work, work / t_max))
+    dist.destroy_process_group()
+
+
+def test_max_and_sum_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, t_max, work, value in out:
+        assert t_max == 2.0          # max over ranks, not the local time
+        assert work == 300.0         # sum over ranks
+        assert value == 150.0
+
+
+def _ref_worker(rank, world, port, q):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import contextlib
+    import io
+    import bench
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3"])
+    q.put((rank, rc, buf.getvalue()))
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_ref_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=300) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (r0, rc0, s0), (r1, rc1, s1) = out
+    assert rc0 == 0 and rc1 == 0
+    assert '"impl": "reference"' in s0 and s0.count("\n") == 1
+    assert s1 == ""
