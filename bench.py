@@ -50,6 +50,9 @@ WORKLOADS = {
     "tiny": inputs.TINY,
 }
 L2_BYTES = 129 * 1024 * 1024
+# Dense INT8 rate of this GB300's legacy warp MMA (mma.sync s8 -> s32), the
+# chip's INT8 engine, measured by bench_engines.py (profiles/engine_rates.md).
+INT8_ENGINE_TOPS = 158.4
 ROTATE_MIN_BYTES = 3 * L2_BYTES
 
 
@@ -405,6 +408,8 @@ def run_ours(args, shape, dist, rank, world, local):
                                "frac": quant_bytes / (quant_ms * 1e-3) / 1e9 / hbm_peak,
                                "kernel": "quant_rows_kernel", "us": quant_ms * 1e3},
             "gemm_us": gemm_ms * 1e3,
+            "vs_int8_engine": {"int8_tops_measured": INT8_ENGINE_TOPS, "gemm_ratio": gemm_tops / INT8_ENGINE_TOPS,
+                               "source": "mma.sync m16n8k32 s8 rate on this GB300 (bench_engines.py)"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TOPS", "h2d_bytes_per_step": M * K * 2,
                     "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms},
