@@ -86,9 +86,10 @@ i8_status i8_quant_act_pertoken(const void* x, int64_t M, int64_t K,
                                 int64_t ldx, int8_t* aq, int64_t ldq,
                                 float* s_a, i8_stream_t stream);
 
-/* Workspace bytes that i8_gemm_int32 / i8_gemm_dequant_bias_bf16 need for
- * this shape (0 when the shape runs without a K split).  Returns 0 for
- * shapes the GEMM rejects. */
+/* Workspace bytes that i8_gemm_int32 / i8_gemm_dequant_bias_bf16 /
+ * i8_gemm_dequant_bias_bf16_w16 need for this shape on the current device
+ * (0 when the shape runs without a K split; the larger figure of the two
+ * weight formats).  Returns 0 for shapes the GEMM rejects. */
 size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* Raw int32 accumulators, for checking (arXiv 2606.14598, abstract: the

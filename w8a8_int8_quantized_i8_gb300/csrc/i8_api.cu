@@ -164,65 +164,66 @@ struct Plan {
   size_t ws_bytes = 0;
 };
 
-// Shape -> configuration (replaces per-shape autotuning): 128 x 128 tiles;
-// when the output tiles cannot fill every SM, K is split so that tiles x
-// splits covers the SMs, with at least two 128-wide K-blocks per split.
+// K-splits for `tiles` output tiles on `slots` concurrent workers: the
+// smallest split count that maximises the filled fraction of the last wave,
+// with at least 4 K-blocks (512 K) per split; 1 when the tiles already fill
+// every worker.
+int best_splits(int64_t tiles, int slots, int total_kb) {
+  if (tiles >= slots) return 1;
+  int best = 1;
+  double best_eff = static_cast<double>(tiles) / slots;
+  const int max_s = std::max(1, std::min(16, total_kb / 4));
+  for (int s = 2; s <= max_s; ++s) {
+    const int64_t items = tiles * s;
+    const int64_t rounds = (items + slots - 1) / slots;
+    const double eff = static_cast<double>(items) / static_cast<double>(rounds * slots);
+    if (eff > best_eff + 1e-9) {
+      best = s;
+      best_eff = eff;
+    }
+  }
+  return best;
+}
+
+// Shape -> configuration (replaces per-shape autotuning).
+//   * CTA pairs (one 256 x 256 tile per cluster of two SMs, each SM staging
+//     and widening half of B) for int8 weights whenever M, N >= 256; with
+//     pre-widened weights the single-CTA kernel measured slightly faster.
+//   * otherwise one CTA per 128 x 256 tile (128 x 128 when the wider tiles
+//     would leave SMs idle);
+//   * split-K (exact int32 partials + a reduction) when the tiles cannot fill
+//     every worker.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
                bool b16 = false) {
   Plan p;
-  // CTA pairs: one 256 x 256 tile per cluster of two SMs, each SM staging
-  // (and, for int8 weights, widening) half of B.  Used for int8 weights when
-  // the pair tiles alone fill every cluster slot; with pre-widened weights
-  // the single-CTA 128 x 256 kernel measured slightly faster.
   if (pair_clusters <= 0) pair_clusters = sms / 2;
-  const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+  p.total_kb = static_cast<int>((K + 127) / 128);
   const bool pair_ok = M >= 256 && N >= 256;
-  p.pair = g_opt.cta_pair == 2
-               ? pair_ok
-               : (g_opt.cta_pair == 0 && !b16 && pair_ok && pair_tiles >= pair_clusters);
+  p.pair = g_opt.cta_pair == 2 ? pair_ok : (g_opt.cta_pair == 0 && !b16 && pair_ok);
+  int64_t tiles;
+  int slots;
   if (p.pair) {
     p.bn = 256;
-    p.total_kb = static_cast<int>((K + 127) / 128);
     p.num_m = static_cast<int>((M + 255) / 256);
     p.num_n = static_cast<int>((N + 255) / 256);
-    int splits = g_opt.force_splits > 0 ? g_opt.force_splits : 1;
-    splits = std::max(1, std::min(splits, p.total_kb));
-    p.kb_per_split = (p.total_kb + splits - 1) / splits;
-    p.splits = (p.total_kb + p.kb_per_split - 1) / p.kb_per_split;
-    p.num_tiles = static_cast<int>(pair_tiles * p.splits);
-    int cap = pair_clusters;
-    if (g_opt.max_ctas > 0) cap = std::max(1, std::min(cap, g_opt.max_ctas / 2));
-    p.grid = 2 * std::max(1, std::min(p.num_tiles, cap));
-    p.chunk_stages = g_opt.chunk_k / 64;
-    if (p.splits > 1) {
-      p.ws_ld = (N + 3) / 4 * 4;
-      p.ws_bytes = static_cast<size_t>(p.splits) * static_cast<size_t>(M) *
-                   static_cast<size_t>(p.ws_ld) * sizeof(int32_t);
-    }
-    return p;
+    tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+    slots = pair_clusters;
+    if (g_opt.max_ctas > 0) slots = std::max(1, std::min(slots, g_opt.max_ctas / 2));
+  } else {
+    p.bn = (N >= 256 && ((M + 127) / 128) * ((N + 255) / 256) >= sms) ? 256 : 128;
+    if (g_opt.force_bn == 128 || g_opt.force_bn == 256) p.bn = g_opt.force_bn;
+    p.num_m = static_cast<int>((M + 127) / 128);
+    p.num_n = static_cast<int>((N + p.bn - 1) / p.bn);
+    tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+    slots = g_opt.max_ctas > 0 ? std::min(g_opt.max_ctas, sms) : sms;
   }
-  // 256-wide tiles halve the on-chip widening of A per MAC; keep 128 when
-  // N is small or the wider tiles would leave SMs idle.
-  p.bn = (N >= 256 && ((M + 127) / 128) * ((N + 255) / 256) >= sms) ? 256 : 128;
-  if (g_opt.force_bn == 128 || g_opt.force_bn == 256) p.bn = g_opt.force_bn;
-  p.total_kb = static_cast<int>((K + 127) / 128);
-  p.num_m = static_cast<int>((M + 127) / 128);
-  p.num_n = static_cast<int>((N + p.bn - 1) / p.bn);
-  const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
-  int splits = 1;
-  if (g_opt.force_splits > 0) {
-    splits = g_opt.force_splits;
-  } else if (tiles < sms) {
-    splits = static_cast<int>(sms / tiles);
-    splits = std::min(splits, std::max(1, p.total_kb / 2));
-    splits = std::min(splits, 16);
-  }
+  int splits = g_opt.force_splits > 0 ? g_opt.force_splits : best_splits(tiles, slots, p.total_kb);
   splits = std::max(1, std::min(splits, p.total_kb));
   p.kb_per_split = (p.total_kb + splits - 1) / splits;
   p.splits = (p.total_kb + p.kb_per_split - 1) / p.kb_per_split;
   p.num_tiles = static_cast<int>(tiles * p.splits);
-  const int cap = g_opt.max_ctas > 0 ? std::min(g_opt.max_ctas, sms) : sms;
-  p.grid = std::max(1, std::min(p.num_tiles, cap));
+  p.grid = std::max(1, static_cast<int>(std::min<int64_t>(p.num_tiles, slots)));
+  if (p.pair) p.grid *= 2;
   p.chunk_stages = g_opt.chunk_k / 64;
   if (p.splits > 1) {
     p.ws_ld = (N + 3) / 4 * 4;
@@ -465,7 +466,10 @@ size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return 0;
   DeviceInfo* d;
   if (device_info(&d, nullptr) != I8_OK) return 0;
-  return make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0)).ws_bytes;
+  // the larger of the two weight formats' plans, so one query serves both
+  const size_t a = make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0), false).ws_bytes;
+  const size_t b = make_plan(M, N, K, d->sms, pair_cluster_capacity<PairWide>(d, 1), true).ws_bytes;
+  return a > b ? a : b;
 }
 
 i8_status i8_gemm_int32(const int8_t* aq, const int8_t* wq, int64_t M, int64_t N, int64_t K,
