@@ -5,7 +5,8 @@ Prints one JSON object per line:
 * ``engine``: peak rates of the legacy warp MMA on this chip (register-only
   loops of mma.sync m16n8k32 s8->s32 and m16n8k16 f16->f32), compiled here
   from the CUDA source below with nvcc;
-* ``shape``: for each DiT linear shape, the device time of
+* ``shape``: for each DiT linear shape, the device time (calls captured in a
+  CUDA graph and replayed) of
   - this library's full step (per-token quant + fused GEMM) and GEMM alone,
     with int8 weights and with pre-widened (fp16-code) weights,
   - torch bf16 ``X @ W.T + b`` (cuBLAS),
@@ -116,17 +117,31 @@ def engine_rates():
 
 
 def _time(fn, iters):
+    """Device time per call: `iters` calls captured into one CUDA graph and
+    replayed, so host-side launch cost (the Python binding's marshalling)
+    does not starve the GPU on small shapes."""
     for _ in range(3):
         fn(0)
     torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(iters):
+                fn(i)
+    torch.cuda.current_stream().wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    reps = 3
     e0.record()
-    for i in range(iters):
-        fn(i)
+    for _ in range(reps):
+        graph.replay()
     e1.record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / iters * 1e-3
+    return e0.elapsed_time(e1) / (reps * iters) * 1e-3
 
 
 def shape_row(shape, iters, full=True):

@@ -133,8 +133,8 @@ i8_status i8_gemm_dequant_bias_bf16(const int8_t* aq, const float* s_a,
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any
  *   stream capture.  The call itself allocates nothing.
- *   All calls share the one array and it keeps the last call's contents
- *   (harmless: every partial is written before it is read).  Calls whose
+ *   All calls share the one array and it keeps the last call's contents;
+ *   the call clears (on its stream) the part that must start at zero.  Calls whose
  *   kernels overlap on the GPU -- on different streams, or from different
  *   host threads -- race on the array; serialize them.                      */
 i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a,
@@ -173,6 +173,8 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *                       0 = the table (default: pairs for int8 weights when
  *                       the 256 x 256 tiles fill every pair of SMs), 1 = never,
  *                       2 = whenever M, N >= 256.
+ *   I8_OPT_SKINNY_MAX_M token counts M up to this value (0..16, default 16)
+ *                       use the weight-streaming kernel for few tokens.
  *   I8_OPT_QUANT_VPL    quantizer: most 16-byte vectors one lane holds
  *                       (1..16, default 6); more warps share a row above.
  * Changing FORCE_SPLITS changes i8_gemm_workspace_bytes(). */
@@ -182,7 +184,8 @@ typedef enum {
   I8_OPT_MAX_CTAS = 3,
   I8_OPT_TILE_N = 4,
   I8_OPT_QUANT_VPL = 5,
-  I8_OPT_CTA_PAIR = 6
+  I8_OPT_CTA_PAIR = 6,
+  I8_OPT_SKINNY_MAX_M = 7
 } i8_option;
 i8_status i8_set_option(i8_option opt, int64_t value);
 

@@ -242,3 +242,33 @@ def test_linear_both_kernels_qkv_sampled(orc, cta_pair_option, mode, widened):
     rows = SAMPLE_ROWS(shape.M)
     want = _oracle_linear_rows(orc, d["x"], d["w"], d["bias"], rows)
     assert_bf16_close(gpu_bf16_bits(y)[rows], want, f"mode {mode} widened {widened}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 200, 8192), (16, 520, 8192), (9, 64, 131072)])
+def test_skinny_kernel_adversarial_exact(orc, M, N, K):
+    """Few tokens (M <= 16) take the weight-streaming kernel: per-CTA partial
+    sums over 512 K in fp32 (< 2^24 for +-127 operands) plus int32 atomics."""
+    a, w = _adversarial(max(M, 4), N, K, seed=M + N)
+    a = a[:M].contiguous()
+    c = i8.gemm_int32(to_dev(a), to_dev(w))
+    i8.sync_check()
+    got = c.cpu().numpy()
+    want = orc.gemm_s32(a.numpy(), w.numpy())
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:4].tolist()}"
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_skinny_kernel_widened_weights_and_off_switch(orc, M):
+    shape = inputs.LinearShape("sk", M, 3072, 9216, seed=40 + M)
+    d = inputs.linear_inputs(shape)
+    rows = np.arange(M)
+    want = _oracle_linear_rows(orc, d["x"], d["w"], d["bias"], rows)
+    y16 = _gpu_linear(d["x"], d["w"], d["bias"], widened=True)
+    assert_bf16_close(gpu_bf16_bits(y16), want, "skinny w16")
+    i8.set_option("skinny_max_m", 0)   # the tiled kernels for the same shape
+    try:
+        y8 = _gpu_linear(d["x"], d["w"], d["bias"], widened=False)
+    finally:
+        i8.set_option("skinny_max_m", 16)
+    assert_bf16_close(gpu_bf16_bits(y8), want, "tiled")

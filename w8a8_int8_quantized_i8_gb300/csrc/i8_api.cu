@@ -12,6 +12,7 @@
 #include "../../include/i8.h"
 #include "gemm.cuh"
 #include "gemm_pair.cuh"
+#include "skinny.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
 
@@ -61,6 +62,7 @@ struct Options {
   int force_bn = 0;        // 0 = table, else 128 or 256
   int quant_vpl = 6;       // max 16-byte vectors per lane in the quantizer
   int cta_pair = 0;        // 0 = table, 1 = never, 2 = whenever the shape allows
+  int skinny_max_m = 16;   // token counts up to this use the weight-streaming kernel (0 = off)
 };
 Options g_opt;
 
@@ -151,6 +153,7 @@ i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t
 
 // ----------------------------------------------------------------- GEMM plan
 struct Plan {
+  bool skinny = false;     // few tokens: weight-streaming kernel
   bool pair = false;       // CTA-pair kernel (256 x 256 tiles per cluster of 2)
   int bn = 128;
   int splits = 1;
@@ -198,6 +201,26 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
   Plan p;
   if (pair_clusters <= 0) pair_clusters = sms / 2;
   p.total_kb = static_cast<int>((K + 127) / 128);
+  if (M <= g_opt.skinny_max_m) {
+    // int32 [M, N] accumulator + one completion counter per 64-row N-block
+    // K split for about two CTAs per SM; each split owns whole 512-K chunks.
+    p.skinny = true;
+    p.num_n = static_cast<int>((N + kSkinnyRows - 1) / kSkinnyRows);
+    p.num_m = 1;
+    const int chunks = static_cast<int>((K + kSkinnyK - 1) / kSkinnyK);
+    int splits = g_opt.force_splits > 0 ? g_opt.force_splits
+                                        : static_cast<int>((2 * sms + p.num_n - 1) / p.num_n);
+    splits = std::max(1, std::min(splits, chunks));
+    p.kb_per_split = (chunks + splits - 1) / splits;          // chunks per split
+    p.splits = (chunks + p.kb_per_split - 1) / p.kb_per_split;
+    p.total_kb = chunks;
+    p.ws_ld = N;
+    if (p.splits > 1) {
+      const size_t acc_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 15) / 16 * 16;
+      p.ws_bytes = acc_bytes + (static_cast<size_t>(p.num_n) * 4 + 15) / 16 * 16;
+    }
+    return p;
+  }
   const bool pair_ok = M >= 256 && N >= 256;
   p.pair = g_opt.cta_pair == 2 ? pair_ok : (g_opt.cta_pair == 0 && !b16 && pair_ok);
   int64_t tiles;
@@ -338,6 +361,54 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   if (pl.ws_bytes > 0) {
     if (!ws || ws_bytes < pl.ws_bytes) return I8_ERR_WORKSPACE;
     if (!aligned16(ws)) return I8_ERR_ALIGNMENT;
+  }
+  if (pl.skinny) {
+    const size_t acc_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 15) / 16 * 16;
+    if (pl.splits > 1 && cudaMemsetAsync(ws, 0, pl.ws_bytes, st) != cudaSuccess) return I8_ERR_CUDA;
+    CUtensorMap mw;
+    if (b16) {
+      if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wb, K, N, 2 * K, 64, kSkinnyRows))
+        return I8_ERR_CUDA;
+    } else {
+      if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, K, N, K, 128, kSkinnyRows))
+        return I8_ERR_CUDA;
+    }
+    SkinnyParams sp{};
+    sp.M = static_cast<int>(M);
+    sp.N = static_cast<int>(N);
+    sp.K = static_cast<int>(K);
+    sp.num_kc = pl.total_kb;
+    sp.kc_per_cta = pl.kb_per_split;
+    sp.out_mode = out_mode;
+    sp.aq = aq;
+    sp.s_a = s_a;
+    sp.s_w = s_w;
+    sp.bias = static_cast<const uint16_t*>(bias);
+    sp.out = out;
+    sp.ldo = ldo;
+    sp.acc = static_cast<int32_t*>(ws);
+    sp.counters = ws ? reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + acc_bytes) : nullptr;
+    const dim3 grid(static_cast<unsigned>(pl.num_n), static_cast<unsigned>(pl.splits));
+    if (b16) {
+      auto kern = gemm_skinny_kernel<true>;
+      if (!d->smem_set[5]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SkinnyCfg<true>::SMEM_BYTES) != cudaSuccess)
+          return I8_ERR_CUDA;
+        d->smem_set[5] = true;
+      }
+      kern<<<grid, 128, SkinnyCfg<true>::SMEM_BYTES, st>>>(mw, sp);
+    } else {
+      auto kern = gemm_skinny_kernel<false>;
+      if (!d->smem_set[4]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SkinnyCfg<false>::SMEM_BYTES) != cudaSuccess)
+          return I8_ERR_CUDA;
+        d->smem_set[4] = true;
+      }
+      kern<<<grid, 128, SkinnyCfg<false>::SMEM_BYTES, st>>>(mw, sp);
+    }
+    return cuda_status(cudaGetLastError());
   }
   CUtensorMap ma, mb;
   const uint32_t bn = pl.pair ? 128u : static_cast<uint32_t>(pl.bn);
@@ -554,6 +625,10 @@ i8_status i8_set_option(i8_option opt, int64_t value) {
     case I8_OPT_CTA_PAIR:
       if (value < 0 || value > 2) return I8_ERR_INVALID_ARG;
       g_opt.cta_pair = static_cast<int>(value);
+      return I8_OK;
+    case I8_OPT_SKINNY_MAX_M:
+      if (value < 0 || value > 16) return I8_ERR_INVALID_ARG;
+      g_opt.skinny_max_m = static_cast<int>(value);
       return I8_OK;
     case I8_OPT_TILE_N:
       if (value != 0 && value != 128 && value != 256) return I8_ERR_INVALID_ARG;
