@@ -172,9 +172,7 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *   I8_OPT_CTA_PAIR     GEMM on CTA pairs (256 x 256 tiles per cluster of 2):
  *                       0 = the table (default: pairs for int8 weights when
  *                       the 256 x 256 tiles fill every pair of SMs), 1 = never,
- *                       2 = whenever M, N >= 256, 3 = the pair kernel that
- *                       keeps A in tensor memory (256 x 192 tiles) whenever
- *                       M >= 256 and N >= 192.
+ *                       2 = whenever M, N >= 256.
  *   I8_OPT_SKINNY_MAX_M token counts M up to this value (0..16, default 16)
  *                       use the weight-streaming kernel for few tokens.
  *   I8_OPT_QUANT_VPL    quantizer: most 16-byte vectors one lane holds

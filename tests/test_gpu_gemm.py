@@ -68,8 +68,7 @@ def _adversarial(M, N, K, seed):
 
 
 @pytest.mark.parametrize("chunk_k", [64, 256, 512, 1024])
-@pytest.mark.parametrize("M,N,pair", [(130, 136, 1), (260, 264, 2), (260, 200, 3)],
-                         ids=["single_cta", "cta_pair", "cta_pair_tmem_a"])
+@pytest.mark.parametrize("M,N,pair", [(130, 136, 1), (260, 264, 2)], ids=["single_cta", "cta_pair"])
 def test_gemm_int32_adversarial_exact(orc, chunk_k, M, N, pair):
     """+-127 operands: partial sums reach 127^2 * chunk_k; K = 8192 overflows
     fp32 exactness (2^24) unless the accumulation is chunked correctly."""
@@ -216,7 +215,7 @@ def cta_pair_option():
     i8.set_option("cta_pair", 0)
 
 
-@pytest.mark.parametrize("mode", [1, 2, 3], ids=["single_cta", "cta_pair", "cta_pair_tmem_a"])
+@pytest.mark.parametrize("mode", [1, 2], ids=["single_cta", "cta_pair"])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 264, 1040), (520, 776, 4096)])
 def test_gemm_int32_both_kernels(orc, cta_pair_option, mode, M, N, K):
     """Both GEMM kernels (one CTA per tile, and CTA pairs with 256 x 256
@@ -233,7 +232,7 @@ def test_gemm_int32_both_kernels(orc, cta_pair_option, mode, M, N, K):
     assert bad.size == 0, f"mode {mode}: {len(bad)} mismatches, first {bad[:4].tolist()}"
 
 
-@pytest.mark.parametrize("mode", [1, 2, 3], ids=["single_cta", "cta_pair", "cta_pair_tmem_a"])
+@pytest.mark.parametrize("mode", [1, 2], ids=["single_cta", "cta_pair"])
 @pytest.mark.parametrize("widened", [False, True])
 def test_linear_both_kernels_qkv_sampled(orc, cta_pair_option, mode, widened):
     i8.set_option("cta_pair", mode)

@@ -12,7 +12,6 @@
 #include "../../include/i8.h"
 #include "gemm.cuh"
 #include "gemm_pair.cuh"
-#include "gemm_pair_t.cuh"
 #include "skinny.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
@@ -72,7 +71,7 @@ struct DeviceInfo {
   int sms = 0;
   int pair_clusters[4] = {};  // co-resident clusters per pair-kernel config
   int cc_major = 0, cc_minor = 0;
-  bool smem_set[12] = {};
+  bool smem_set[8] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -155,7 +154,6 @@ i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t
 // ----------------------------------------------------------------- GEMM plan
 struct Plan {
   bool skinny = false;     // few tokens: weight-streaming kernel
-  bool pair_t = false;     // CTA pair with A in TMEM (256 x 192 tiles)
   bool pair = false;       // CTA-pair kernel (256 x 256 tiles per cluster of 2)
   int bn = 128;
   int splits = 1;
@@ -224,15 +222,13 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
     return p;
   }
   const bool pair_ok = M >= 256 && N >= 256;
-  p.pair_t = g_opt.cta_pair == 3 && M >= 256 && N >= 192;
-  p.pair = p.pair_t || (g_opt.cta_pair == 2 ? pair_ok : (g_opt.cta_pair == 0 && !b16 && pair_ok));
+  p.pair = g_opt.cta_pair == 2 ? pair_ok : (g_opt.cta_pair == 0 && !b16 && pair_ok);
   int64_t tiles;
   int slots;
   if (p.pair) {
-    const int pn = p.pair_t ? 192 : 256;
-    p.bn = pn;
+    p.bn = 256;
     p.num_m = static_cast<int>((M + 255) / 256);
-    p.num_n = static_cast<int>((N + pn - 1) / pn);
+    p.num_n = static_cast<int>((N + 255) / 256);
     tiles = static_cast<int64_t>(p.num_m) * p.num_n;
     slots = pair_clusters;
     if (g_opt.max_ctas > 0) slots = std::max(1, std::min(slots, g_opt.max_ctas / 2));
@@ -274,20 +270,16 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
 
 // Output map for the epilogue's bulk tensor stores: {N, M, planes} with the
 // split-K partial index as the third coordinate; 128-byte-wide boxes of 32 rows.
-// cols32: 32-column boxes (bf16 rows of 64 bytes with the 64-byte swizzle),
-// used by the 192-wide pair tiles; otherwise 128-byte-wide boxes.
 bool encode_out(CUtensorMap* map, bool bf16, const void* base, uint64_t N, uint64_t M,
-                uint64_t ld_elems, uint64_t planes, bool cols32 = false) {
+                uint64_t ld_elems, uint64_t planes) {
   const uint64_t esz = bf16 ? 2 : 4;
   const cuuint64_t dims[3] = {N, M, planes};
   const cuuint64_t strides[2] = {ld_elems * esz, ld_elems * esz * M};
-  const cuuint32_t box[3] = {(bf16 && !cols32) ? 64u : 32u, 32u, 1u};
+  const cuuint32_t box[3] = {bf16 ? 64u : 32u, 32u, 1u};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapSwizzle sw =
-      (bf16 && cols32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   return g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_INT32, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -340,22 +332,6 @@ i8_status launch_pair_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const CU
   return cuda_status(cudaGetLastError());
 }
 
-template <class Cfg>
-i8_status launch_pair_t_cfg(DeviceInfo* d, int slot, const CUtensorMap& ma, const CUtensorMap& mb,
-                            const CUtensorMap& my, const GemmParams& gp, int grid, cudaStream_t st) {
-  auto kern = gemm_w8a8_pair_t_kernel<Cfg>;
-  if (!d->smem_set[slot]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::SMEM_BYTES) != cudaSuccess)
-      return I8_ERR_CUDA;
-    d->smem_set[slot] = true;
-  }
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ma, mb, my, gp);
-  return cuda_status(cudaGetLastError());
-}
-
-using PairTConv = PairTCfg<4, 4, true>;   // int8 weights, CTA pair, A in TMEM
-using PairTWide = PairTCfg<6, 4, false>;  // pre-widened weights, CTA pair, A in TMEM
 using PairConv = PairCfg<3, 3, true, true>;    // int8 weights, CTA pair
 using PairWide = PairCfg<4, 4, true, false>;   // pre-widened weights, CTA pair
 using CfgConv128 = GemmCfg<128, 3, 3, true, true>;   // int8 weights
@@ -435,7 +411,7 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
     return cuda_status(cudaGetLastError());
   }
   CUtensorMap ma, mb;
-  const uint32_t bn = pl.pair_t ? 96u : pl.pair ? 128u : static_cast<uint32_t>(pl.bn);
+  const uint32_t bn = pl.pair ? 128u : static_cast<uint32_t>(pl.bn);
   if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M, K, 128, 128)) return I8_ERR_CUDA;
   if (b16) {
     if (!encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wb, K, N, 2 * K, 64, bn))
@@ -471,13 +447,10 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   CUtensorMap my;
   if (!encode_out(&my, gp.out_mode == kOutBf16, gp.out, static_cast<uint64_t>(N),
                   static_cast<uint64_t>(M), static_cast<uint64_t>(gp.ldo),
-                  static_cast<uint64_t>(pl.splits), pl.pair_t))
+                  static_cast<uint64_t>(pl.splits)))
     return I8_ERR_CUDA;
   i8_status e;
-  if (pl.pair_t) {
-    e = b16 ? launch_pair_t_cfg<PairTWide>(d, 7, ma, mb, my, gp, pl.grid, st)
-            : launch_pair_t_cfg<PairTConv>(d, 6, ma, mb, my, gp, pl.grid, st);
-  } else if (pl.pair) {
+  if (pl.pair) {
     e = b16 ? launch_pair_cfg<PairWide>(ma, mb, my, gp, pl.grid, st)
             : launch_pair_cfg<PairConv>(ma, mb, my, gp, pl.grid, st);
   } else if (pl.bn == 256) {
@@ -650,7 +623,7 @@ i8_status i8_set_option(i8_option opt, int64_t value) {
       g_opt.quant_vpl = static_cast<int>(value);
       return I8_OK;
     case I8_OPT_CTA_PAIR:
-      if (value < 0 || value > 3) return I8_ERR_INVALID_ARG;
+      if (value < 0 || value > 2) return I8_ERR_INVALID_ARG;
       g_opt.cta_pair = static_cast<int>(value);
       return I8_OK;
     case I8_OPT_SKINNY_MAX_M:
