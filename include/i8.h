@@ -177,6 +177,12 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *                       use the weight-streaming kernel for few tokens.
  *   I8_OPT_QUANT_VPL    quantizer: most 16-byte vectors one lane holds
  *                       (1..16, default 6); more warps share a row above.
+ *   I8_OPT_PDL          1 (default): launch the kernels with programmatic
+ *                       stream serialization, so a kernel is scheduled while
+ *                       the previous one drains (each waits for the previous
+ *                       kernel's memory before touching global memory);
+ *                       0: plain stream-ordered launches.
+ *   I8_OPT_QUANT_ROWS   quantizer rows per CTA, 1..8 (0 = chosen by shape).
  * Changing FORCE_SPLITS changes i8_gemm_workspace_bytes(). */
 typedef enum {
   I8_OPT_CHUNK_K = 1,
@@ -185,7 +191,9 @@ typedef enum {
   I8_OPT_TILE_N = 4,
   I8_OPT_QUANT_VPL = 5,
   I8_OPT_CTA_PAIR = 6,
-  I8_OPT_SKINNY_MAX_M = 7
+  I8_OPT_SKINNY_MAX_M = 7,
+  I8_OPT_PDL = 8,
+  I8_OPT_QUANT_ROWS = 9
 } i8_option;
 i8_status i8_set_option(i8_option opt, int64_t value);
 

@@ -73,6 +73,13 @@ def test_options_validation(lib):
     assert lib.i8_set_option(2, -1) == 1
     assert lib.i8_set_option(2, 0) == 0
     assert lib.i8_set_option(77, 0) == 1
+    assert lib.i8_set_option(8, 2) == 1           # PDL: 0 or 1
+    assert lib.i8_set_option(8, 0) == 0
+    assert lib.i8_set_option(8, 1) == 0
+    assert lib.i8_set_option(9, 9) == 1           # quantizer rows per CTA: 0..8
+    assert lib.i8_set_option(9, -1) == 1
+    assert lib.i8_set_option(9, 0) == 0
+    assert lib.i8_set_option(1, 1024) == 0        # restore the default chunk
     assert lib.i8_selftest_timeout(0, None) == 1
 
 

@@ -272,3 +272,57 @@ def test_skinny_kernel_widened_weights_and_off_switch(orc, M):
     finally:
         i8.set_option("skinny_max_m", 16)
     assert_bf16_close(gpu_bf16_bits(y8), want, "tiled")
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 512, 1024), (130, 144, 272), (2, 9216, 3072), (5, 256, 512)],
+                         ids=["cta_pair", "single_cta", "skinny_split", "skinny"])
+def test_dependent_launches_keep_stream_order(M, N, K):
+    """Kernels are scheduled while the previous kernel drains; each one waits
+    for the previous kernel's memory before touching global memory.  A chain
+    that reuses every buffer at once (codes, scales, workspace overwritten by
+    the next call; a GEMM output quantized as the next layer's input) run
+    back to back without host syncs must give the results of the same chain
+    run one call at a time with plain launches."""
+    g = torch.Generator().manual_seed(M + N + K)
+    xs = [inputs.activations(M, K, g, "normal", True).cuda() for _ in range(3)]
+    w1 = inputs.random_bf16(N, K, seed=5, std=0.02).cuda()
+    w2 = inputs.random_bf16(K, N, seed=6, std=0.02).cuda()
+    b1 = inputs.random_bf16(1, N, seed=7, std=0.1)[0].cuda()
+    w1q, s1 = i8.quant_weight_perchannel(w1)
+    w2q, s2 = i8.quant_weight_perchannel(w2)
+    codes = torch.empty(M * max(K, N), dtype=torch.int8, device="cuda")   # shared by both layers
+    sa = torch.empty(M, dtype=torch.float32, device="cuda")
+    ws_bytes = max(i8.workspace_bytes(M, N, K), i8.workspace_bytes(M, K, N), 16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+
+    def chain(sync):
+        outs = []
+        for x in xs:
+            a = codes[:M * K].view(M, K)
+            i8.quant_act_pertoken(x, a, sa)
+            if sync:
+                torch.cuda.synchronize()
+            y = i8.gemm_dequant_bias_bf16(a, sa, w1q, s1, b1, workspace=ws)
+            if sync:
+                torch.cuda.synchronize()
+            a2 = codes[:M * N].view(M, N)
+            i8.quant_act_pertoken(y, a2, sa)       # the GEMM output is the next input
+            if sync:
+                torch.cuda.synchronize()
+            z = i8.gemm_dequant_bias_bf16(a2, sa, w2q, s2, None, workspace=ws)
+            if sync:
+                torch.cuda.synchronize()
+            outs += [y, z]
+        torch.cuda.synchronize()
+        return [o.clone() for o in outs]
+
+    try:
+        i8.set_option("pdl", 0)
+        want = chain(sync=True)
+        i8.set_option("pdl", 1)
+        for _ in range(5):
+            got = chain(sync=False)
+            for a, b in zip(got, want):
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    finally:
+        i8.set_option("pdl", 1)

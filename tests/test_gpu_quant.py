@@ -73,3 +73,18 @@ def test_quant_act_full_qkv(orc):
 def test_quant_act_full_mlp_down(orc):
     d = inputs.linear_inputs(inputs.MLP_DOWN_1024)
     _compare(orc, d["x"], what="X 8704x12288")
+
+
+@pytest.mark.parametrize("rows", [1, 2, 4, 8])
+@pytest.mark.parametrize("vpl", [1, 3, 6, 16])
+def test_quant_launch_shapes_identical(orc, rows, vpl):
+    """Every rows-per-CTA / vectors-per-lane launch shape gives the oracle's
+    codes and scales (ragged M, ragged K tail, several warps per row)."""
+    x = inputs.activations(45, 3072 + 48, torch.Generator().manual_seed(rows * 31 + vpl), "gelu", True)
+    try:
+        i8.set_option("quant_rows", rows)
+        i8.set_option("quant_vpl", vpl)
+        _compare(orc, x, what=f"rows{rows} vpl{vpl}")
+    finally:
+        i8.set_option("quant_rows", 0)
+        i8.set_option("quant_vpl", 6)

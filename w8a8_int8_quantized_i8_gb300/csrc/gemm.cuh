@@ -413,6 +413,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // operands and outputs may belong to the previous kernel
 
   if (warp >= Cfg::EPI_WARP0) {
     regs_inc<Cfg::REG_HI>();
@@ -546,6 +547,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   }
 
   __syncwarp();
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -559,6 +561,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const int32_t* __restrict__ ws,
                                                            int64_t split_stride, int64_t ldw,
                                                            int splits, GemmParams p) {
+  pdl_wait();  // the partials come from the GEMM kernel just before
+  pdl_trigger();
   const int groups_per_row = (p.N + 3) / 4;
   const int64_t total = static_cast<int64_t>(p.M) * groups_per_row;
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;

@@ -218,6 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
   cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // operands and outputs may belong to the previous kernel
 
   if (warp >= Cfg::EPI_WARP0) {
     regs_inc<Cfg::REG_HI>();
@@ -399,6 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
   }
 
   __syncwarp();
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // the peer's MMAs and remote arrivals are finished

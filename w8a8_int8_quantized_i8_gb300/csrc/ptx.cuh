@@ -26,6 +26,18 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// ----------------------------------------------------------------- dependent launch
+// Kernels launched with programmatic stream serialization may start while the
+// previous kernel of the stream is still running.  pdl_wait() blocks until
+// that kernel has completed and its memory is visible, so every such kernel
+// calls it before its first global-memory access; pdl_trigger() lets the next
+// kernel of the stream be scheduled once every CTA of this grid has called it
+// (or exited).  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

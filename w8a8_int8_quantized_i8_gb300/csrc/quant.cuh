@@ -27,6 +27,8 @@
 #pragma once
 #include <cstdint>
 
+#include "ptx.cuh"
+
 namespace i8 {
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
@@ -119,8 +121,8 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Grid: ceil(rows / (8 / G)) CTAs of 256 threads; warp w of a CTA serves row
-// (blockIdx.x * (8 / G) + w / G), slice (w % G) of that row.
+// Grid: ceil(rows / R) CTAs of 32 * G * R threads (G * R <= 8); warp w of a
+// CTA serves row (blockIdx.x * R + w / G), slice (w % G) of that row.
 template <int V>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ x,
                                                          int64_t rows, int K, int64_t ldx,
@@ -129,12 +131,13 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   __shared__ uint32_t red[8];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rows_per_cta = 8 / G;
+  const int rows_per_cta = static_cast<int>(blockDim.x >> 5) / G;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * rows_per_cta + warp / G;
   const int wig = warp % G;
   const bool valid_row = (warp / G) < rows_per_cta && row < rows;
   const int slice0 = wig * (32 * 8 * V);  // first element of this warp's slice
 
+  pdl_wait();  // X may be the previous kernel's output
   const uint16_t* xr = x + (valid_row ? row : 0) * ldx;
   uint4 v[V];
   uint32_t amax2 = 0;  // bf16x2 running max of |x| (sign bits meaningless)
@@ -147,6 +150,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
       v[i] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
+  pdl_trigger();
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     amax2 = absmax_bf16x2(amax2, v[i].x);

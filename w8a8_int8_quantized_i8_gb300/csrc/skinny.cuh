@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(128) gemm_skinny_kernel(const __grid_constant_
     fence_mbarrier_init();
   }
   __syncthreads();
+  pdl_wait();  // weights, codes and the zeroed workspace may come from earlier work
   auto load_chunk = [&](int kc, int stage) {
     const uint32_t bar = bar0 + 8u * stage;
     mbar_arrive_expect_tx(bar, Cfg::TILE_BYTES);
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(128) gemm_skinny_kernel(const __grid_constant_
       for (int i = 0; i < 4; ++i) acc[grp][i] += f32_exact_int_to_s32(__float_as_uint(d[grp][i]));
   }
 
+  pdl_trigger();
   // D fragment: acc[grp][0..1] -> token g, weight rows 2q, 2q+1 of the n8
   // group; acc[grp][2..3] -> token g + 8.
   if (!split) {
