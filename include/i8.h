@@ -183,6 +183,13 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *                       kernel's memory before touching global memory);
  *                       0: plain stream-ordered launches.
  *   I8_OPT_QUANT_ROWS   quantizer rows per CTA, 1..8 (0 = chosen by shape).
+ *   I8_OPT_STREAM_K     stream-K schedule for the CTA-pair kernel (equal
+ *                       (tile, K-block) shares per pair, tiles cut between
+ *                       pairs finished from exact int32 partials; it needs
+ *                       workspace): 1 (default) where the table predicts a
+ *                       gain (K >= 8192 and whole tiles leave many pairs
+ *                       idle), 2 whenever whole tiles leave pairs idle,
+ *                       0 never.
  * Changing FORCE_SPLITS changes i8_gemm_workspace_bytes(). */
 typedef enum {
   I8_OPT_CHUNK_K = 1,
@@ -193,7 +200,8 @@ typedef enum {
   I8_OPT_CTA_PAIR = 6,
   I8_OPT_SKINNY_MAX_M = 7,
   I8_OPT_PDL = 8,
-  I8_OPT_QUANT_ROWS = 9
+  I8_OPT_QUANT_ROWS = 9,
+  I8_OPT_STREAM_K = 10
 } i8_option;
 i8_status i8_set_option(i8_option opt, int64_t value);
 

@@ -35,6 +35,16 @@ def assert_bf16_close(got_bits: np.ndarray, want_bits: np.ndarray, what: str = "
     return float((got_bits == want_bits).mean())
 
 
+def assert_bf16_exact(got_bits: np.ndarray, want_bits: np.ndarray, what: str = ""):
+    """Bit-identical bf16: the GPU epilogue takes the oracle's fp32 steps in
+    the same order with the same rounding.  The 1-ulp check runs first so a
+    failure says whether the difference is a rounding step or a real error."""
+    assert_bf16_close(got_bits, want_bits, what)
+    bad = np.argwhere(got_bits != want_bits)
+    assert bad.size == 0, (f"{what}: {len(bad)} of {got_bits.size} elements differ by one "
+                           f"rounding step, first {bad[:4].tolist()}")
+
+
 def to_dev(t: torch.Tensor) -> torch.Tensor:
     return t.contiguous().to("cuda")
 

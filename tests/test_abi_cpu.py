@@ -79,6 +79,10 @@ def test_options_validation(lib):
     assert lib.i8_set_option(9, 9) == 1           # quantizer rows per CTA: 0..8
     assert lib.i8_set_option(9, -1) == 1
     assert lib.i8_set_option(9, 0) == 0
+    assert lib.i8_set_option(10, 3) == 1          # stream-K: 0, 1 or 2
+    assert lib.i8_set_option(10, 2) == 0
+    assert lib.i8_set_option(10, 0) == 0
+    assert lib.i8_set_option(10, 1) == 0
     assert lib.i8_set_option(1, 1024) == 0        # restore the default chunk
     assert lib.i8_selftest_timeout(0, None) == 1
 

@@ -12,7 +12,7 @@ import torch
 
 import w8a8_int8_quantized_i8_gb300 as i8
 from w8a8_int8_quantized_i8_gb300 import inputs
-from tests._util import assert_bf16_close, gpu_bf16_bits, to_dev
+from tests._util import assert_bf16_exact, gpu_bf16_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -133,8 +133,7 @@ def test_linear_bf16_matches_oracle(orc, M, N, K, bias):
     d = inputs.linear_inputs(shape, with_bias=bias)
     y = _gpu_linear(d["x"], d["w"], d["bias"])
     want = _oracle_linear_rows(orc, d["x"], d["w"], d["bias"], np.arange(M))
-    exact = assert_bf16_close(gpu_bf16_bits(y), want, f"{M}x{N}x{K}")
-    assert exact > 0.99
+    assert_bf16_exact(gpu_bf16_bits(y), want, f"{M}x{N}x{K}")
 
 
 def test_widened_weights_bit_identical(orc):
@@ -170,7 +169,7 @@ def test_full_size_dit_layers_sampled_rows(orc, shape, widened):
     rows = SAMPLE_ROWS(shape.M)
     want = _oracle_linear_rows(orc, d["x"], d["w"], d["bias"], rows)
     got = gpu_bf16_bits(y)[rows]
-    assert_bf16_close(got, want, shape.name)
+    assert_bf16_exact(got, want, shape.name)
     assert torch.isfinite(y.float()).all()
 
 
@@ -241,7 +240,7 @@ def test_linear_both_kernels_qkv_sampled(orc, cta_pair_option, mode, widened):
     y = _gpu_linear(d["x"], d["w"], d["bias"], widened=widened)
     rows = SAMPLE_ROWS(shape.M)
     want = _oracle_linear_rows(orc, d["x"], d["w"], d["bias"], rows)
-    assert_bf16_close(gpu_bf16_bits(y)[rows], want, f"mode {mode} widened {widened}")
+    assert_bf16_exact(gpu_bf16_bits(y)[rows], want, f"mode {mode} widened {widened}")
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 200, 8192), (16, 520, 8192), (9, 64, 131072)])
@@ -265,13 +264,13 @@ def test_skinny_kernel_widened_weights_and_off_switch(orc, M):
     rows = np.arange(M)
     want = _oracle_linear_rows(orc, d["x"], d["w"], d["bias"], rows)
     y16 = _gpu_linear(d["x"], d["w"], d["bias"], widened=True)
-    assert_bf16_close(gpu_bf16_bits(y16), want, "skinny w16")
+    assert_bf16_exact(gpu_bf16_bits(y16), want, "skinny w16")
     i8.set_option("skinny_max_m", 0)   # the tiled kernels for the same shape
     try:
         y8 = _gpu_linear(d["x"], d["w"], d["bias"], widened=False)
     finally:
         i8.set_option("skinny_max_m", 16)
-    assert_bf16_close(gpu_bf16_bits(y8), want, "tiled")
+    assert_bf16_exact(gpu_bf16_bits(y8), want, "tiled")
 
 
 @pytest.mark.parametrize("M,N,K", [(512, 512, 1024), (130, 144, 272), (2, 9216, 3072), (5, 256, 512)],
@@ -326,3 +325,93 @@ def test_dependent_launches_keep_stream_order(M, N, K):
                 assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     finally:
         i8.set_option("pdl", 1)
+
+
+@pytest.fixture
+def stream_k_option():
+    yield
+    i8.set_option("stream_k", 1)
+    i8.set_option("cta_pair", 0)
+
+
+# Shapes on CTA pairs whose whole tiles leave pairs idle, so the stream-K
+# schedule splits tiles between pairs: 2 x 3 tiles spread over many pairs
+# (each tile shared by several), a ragged one, and a multi-wave one with a
+# partial last wave.
+STREAM_K_SHAPES = [(512, 768, 4096), (300, 520, 1040), (1280, 2816, 2048)]
+
+
+@pytest.mark.parametrize("M,N,K", STREAM_K_SHAPES)
+def test_stream_k_int32_exact(orc, stream_k_option, M, N, K):
+    """Tiles finished from int32 partials of several pairs are bit-exact,
+    adversarial rows included (partials near the int32 range)."""
+    i8.set_option("cta_pair", 2)
+    i8.set_option("stream_k", 2)
+    a = inputs.random_int8(M, K, seed=M + 3 * K)
+    w = inputs.random_int8(N, K, seed=N + 5 * K)
+    a[:3], w[:3] = _adversarial(3, 3, K, seed=M)[0], _adversarial(3, 3, K, seed=N)[1]
+    c = i8.gemm_int32(to_dev(a), to_dev(w))
+    i8.sync_check()
+    got = c.cpu().numpy()
+    want = orc.gemm_s32(a.numpy(), w.numpy())
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:4].tolist()}"
+
+
+@pytest.mark.parametrize("M,N,K", STREAM_K_SHAPES + [(2560, 9216, 3072), (8704, 3072, 12288)])
+def test_stream_k_matches_whole_tiles(stream_k_option, M, N, K):
+    """The bf16 output with the stream-K schedule equals the whole-tile
+    schedule's bit for bit (both exact in int32, same epilogue)."""
+    i8.set_option("cta_pair", 2)
+    g = torch.Generator().manual_seed(M + N)
+    x = inputs.activations(M, K, g, "normal", True).cuda()
+    w = inputs.random_bf16(N, K, seed=N + K, std=0.02).cuda()
+    b = inputs.random_bf16(1, N, seed=K, std=0.1)[0].cuda()
+    wq, s_w = i8.quant_weight_perchannel(w)
+    i8.set_option("stream_k", 0)
+    want = i8.linear(x, wq, s_w, b)
+    i8.set_option("stream_k", 2)
+    got = i8.linear(x, wq, s_w, b)
+    i8.sync_check()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+def test_stream_k_workspace_garbage_and_graph_replay(stream_k_option):
+    """Arrival words are tagged per launch: a workspace full of random bytes,
+    or of another shape's leftovers, and CUDA-graph replays of one captured
+    launch (which reuse its tag) all give the exact result."""
+    i8.set_option("cta_pair", 2)
+    i8.set_option("stream_k", 2)
+    M, N, K = 512, 768, 4096
+    a = inputs.random_int8(M, K, seed=1).cuda()
+    w = inputs.random_int8(N, K, seed=2).cuda()
+    want = torch._int_mm(a, w.t())
+    nbytes = max(i8.workspace_bytes(M, N, K), i8.workspace_bytes(1280, 2816, 2048))
+    assert i8.workspace_bytes(M, N, K) > 0
+    ws = torch.randint(-128, 128, (nbytes,), dtype=torch.int8, device="cuda").view(torch.uint8)
+    out = torch.empty(M, N, dtype=torch.int32, device="cuda")
+    i8.gemm_int32(a, w, out=out, workspace=ws)
+    i8.sync_check()
+    assert torch.equal(out, want)
+    # another shape through the same workspace, then this one again
+    a2 = inputs.random_int8(1280, 2048, seed=3).cuda()
+    w2 = inputs.random_int8(2816, 2048, seed=4).cuda()
+    assert torch.equal(i8.gemm_int32(a2, w2, workspace=ws), torch._int_mm(a2, w2.t()))
+    out.zero_()
+    i8.gemm_int32(a, w, out=out, workspace=ws)
+    i8.sync_check()
+    assert torch.equal(out, want)
+    # one launch captured in a graph and replayed
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            i8.gemm_int32(a, w, out=out, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, want)
+    i8.sync_check()

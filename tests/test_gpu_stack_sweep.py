@@ -9,7 +9,7 @@ import torch
 
 import w8a8_int8_quantized_i8_gb300 as i8
 from w8a8_int8_quantized_i8_gb300 import dit_stack, inputs
-from tests._util import assert_bf16_close, gpu_bf16_bits
+from tests._util import assert_bf16_exact, gpu_bf16_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +34,7 @@ def test_sweep_shape_sampled_rows(orc, shape):
     i8.sync_check()
     rows = _rows(shape.M)
     want = _oracle_rows(orc, inputs.bits(d["x"][rows]), inputs.bits(d["w"]), inputs.bits(d["bias"]))
-    assert_bf16_close(gpu_bf16_bits(y)[rows], want, shape.name)
+    assert_bf16_exact(gpu_bf16_bits(y)[rows], want, shape.name)
     # codes of the weights are bit-exact too
     assert np.array_equal(wq.cpu().numpy(), orc.quant_rows(inputs.bits(d["w"]))[0])
 
@@ -60,4 +60,4 @@ def test_dit_linear_stack_1024px_layers_sampled(orc):
         K, N = lin.wq.shape[1], lin.wq.shape[0]
         w, b = dit_stack.layer_weight(lin.seed, N, K, "cuda")
         want = _oracle_rows(orc, inputs.bits(x), inputs.bits(w.cpu()), inputs.bits(b.cpu()))
-        assert_bf16_close(gpu_bf16_bits(y), want, f"block {blk} {name}")
+        assert_bf16_exact(gpu_bf16_bits(y), want, f"block {blk} {name}")

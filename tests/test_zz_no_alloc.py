@@ -17,7 +17,7 @@ import torch
 
 import w8a8_int8_quantized_i8_gb300 as i8
 from w8a8_int8_quantized_i8_gb300 import binding, inputs
-from tests._util import assert_bf16_close, gpu_bf16_bits
+from tests._util import assert_bf16_exact, gpu_bf16_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +54,7 @@ def test_noalloc_matches_regular_entry_point_on_two_calls():
         y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
         assert _noalloc(lib, aq, s_a, wq, s_w, b, y) == 0
         i8.sync_check()
-        assert_bf16_close(gpu_bf16_bits(y), gpu_bf16_bits(y_ref), f"noalloc {M}x{N}x{K}")
+        assert_bf16_exact(gpu_bf16_bits(y), gpu_bf16_bits(y_ref), f"noalloc {M}x{N}x{K}")
         assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
 
 

@@ -55,6 +55,15 @@ struct GemmParams {
   void* out;                           // y (bf16), c (int32) or workspace (int32)
   int64_t ldo;                         // elements
   int64_t split_stride;                // elements between split partials (kOutPartial)
+  // Stream-K schedule (CTA-pair kernel only): pair p of P takes the units
+  // [p*U/P, (p+1)*U/P) of the U = num_tiles * total_kb (tile, K-block) units,
+  // so every pair does the same work whatever the tile count.  A tile cut
+  // between pairs is finished from exact int32 partials by the last pair to
+  // arrive at it.
+  int stream_k;                        // 0: tile-strided schedule
+  unsigned long long* sk_arrive;       // [num_tiles][2] arrival words: epoch << 16 | count
+  const int32_t* sk_part;              // [2 P][256][256] int32 partial slots
+  unsigned long long sk_epoch;         // this launch's tag, in [1, 2^48)
 };
 
 // Kernel configuration.  CONV_A / CONV_B: the operand arrives as int8 codes
@@ -228,15 +237,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // The tensor store clips rows >= M and columns >= N, so ragged tiles need no
 // masking.  tmY is 3-D {N, M, splits}; z selects the split-K partial.
 template <int COLS>
-__device__ __forceinline__ void store_warp_tile(const GemmParams& p, const CUtensorMap* tmY,
-                                                uint32_t stage, int lane, int m_base, int n0,
-                                                const int (&acc)[COLS], int z) {
+__device__ __forceinline__ void store_warp_tile_bf16(const GemmParams& p, const CUtensorMap* tmY,
+                                                     uint32_t stage, int lane, int m_base, int n0,
+                                                     const int (&acc)[COLS]) {
   const uint32_t row = stage + static_cast<uint32_t>(lane) * 128u;
   const uint32_t x = static_cast<uint32_t>(lane & 7);
   const int m = m_base + lane;
-  if (p.out_mode == kOutBf16) {
+  {
     const float sa = m < p.M ? p.s_a[m] : 0.0f;
-    const unsigned long long sa2 = f2(sa, sa);
 #pragma unroll
     for (int g = 0; g < COLS / 64; ++g) {
       if (lane == 0) bulk_wait_read_all();
@@ -271,13 +279,13 @@ __device__ __forceinline__ void store_warp_tile(const GemmParams& p, const CUten
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int j = g * 64 + 8 * c + 2 * i;
-          // ((float(acc) * s_a) * s_w) + bias, each step rounded to fp32
-          unsigned long long t = f2(__int2float_rn(acc[j]), __int2float_rn(acc[j + 1]));
-          t = f2_mul(t, sa2);
-          t = f2_mul(t, f2(sw[2 * i], sw[2 * i + 1]));
-          t = f2_add(t, f2(__uint_as_float(bw[i] << 16), __uint_as_float(bw[i] & 0xFFFF0000u)));
-          float lo, hi;
-          f2_split(t, lo, hi);
+          // ((float(acc) * s_a) * s_w) + bias, each step rounded to fp32.
+          // Scalar __fmul_rn / __fadd_rn are never contracted into an FMA;
+          // packed f32x2 mul + add were (one bf16 ulp off where the product
+          // and the bias nearly cancel).
+          const float lo = dequant_one(acc[j], sa, sw[2 * i], __uint_as_float(bw[i] << 16));
+          const float hi =
+              dequant_one(acc[j + 1], sa, sw[2 * i + 1], __uint_as_float(bw[i] & 0xFFFF0000u));
           o[i] = pack_bf16x2(lo, hi);
         }
         sts128(row + ((static_cast<uint32_t>(c) ^ x) << 4), make_uint4(o[0], o[1], o[2], o[3]));
@@ -289,7 +297,18 @@ __device__ __forceinline__ void store_warp_tile(const GemmParams& p, const CUten
         bulk_commit_group();
       }
     }
-  } else {
+  }
+}
+
+// int32 values (results or partials) through the same staging buffer in
+// 32-column groups; z selects the plane of the 3-D map tm.
+template <int COLS>
+__device__ __forceinline__ void store_warp_tile_s32(const CUtensorMap* tm, uint32_t stage, int lane,
+                                                    int m_base, int n0, const int (&acc)[COLS],
+                                                    int z) {
+  const uint32_t row = stage + static_cast<uint32_t>(lane) * 128u;
+  const uint32_t x = static_cast<uint32_t>(lane & 7);
+  {
 #pragma unroll
     for (int g = 0; g < COLS / 32; ++g) {
       if (lane == 0) bulk_wait_read_all();
@@ -304,11 +323,19 @@ __device__ __forceinline__ void store_warp_tile(const GemmParams& p, const CUten
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_3d(tmY, stage, n0 + g * 32, m_base, z);
+        tma_store_3d(tm, stage, n0 + g * 32, m_base, z);
         bulk_commit_group();
       }
     }
   }
+}
+
+template <int COLS>
+__device__ __forceinline__ void store_warp_tile(const GemmParams& p, const CUtensorMap* tmY,
+                                                uint32_t stage, int lane, int m_base, int n0,
+                                                const int (&acc)[COLS], int z) {
+  if (p.out_mode == kOutBf16) store_warp_tile_bf16<COLS>(p, tmY, stage, lane, m_base, n0, acc);
+  else store_warp_tile_s32<COLS>(tmY, stage, lane, m_base, n0, acc, z);
 }
 
 // Epilogue role: drains chunk accumulators into int32 registers, then writes

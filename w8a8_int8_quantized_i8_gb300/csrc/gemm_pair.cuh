@@ -73,8 +73,8 @@ struct PairCfg {
   static constexpr int OFF_EPI = OFF_S16 + S16 * STAGE16;   // 4 KB store staging per epilogue warp
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 4096;
   // full8[S8] empty8[S8] full16[S16] tma16[S16] empty16[S16] pfull16[S16]
-  // accfull[2] accempty[2] paccempty[2] done
-  static constexpr int NUM_BARS = 2 * S8 + 4 * S16 + 7;
+  // accfull[2] accempty[2] paccempty[2] done skstored skdecided
+  static constexpr int NUM_BARS = 2 * S8 + 4 * S16 + 9;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int TMEM_COLS = 2 * PAIR_N;
@@ -97,10 +97,16 @@ struct PairBars {
   __device__ uint32_t accempty(int b) const { return base + 8u * (2 * S8 + 4 * S16 + 2 + b); }
   __device__ uint32_t paccempty(int b) const { return base + 8u * (2 * S8 + 4 * S16 + 4 + b); }
   __device__ uint32_t done() const { return base + 8u * (2 * S8 + 4 * S16 + 6); }
+  // stream-K fix-up: every epilogue warp's partial is stored / the decision
+  // whether this CTA finishes the tile is made
+  __device__ uint32_t skstored() const { return base + 8u * (2 * S8 + 4 * S16 + 7); }
+  __device__ uint32_t skdecided() const { return base + 8u * (2 * S8 + 4 * S16 + 8); }
 };
 
 struct PairTile {
   int mp, nb, ks, kb0, kb1;
+  int tile;
+  bool partial;      // stream-K: only part of the tile's K range
 };
 
 // Pair tiles: num_m_blk counts 256-row pair blocks, num_n_blk 256-column blocks.
@@ -115,11 +121,74 @@ __device__ __forceinline__ PairTile decode_pair_tile(const GemmParams& p, int ti
   return t;
 }
 
+// Stream-K units are (tile, K-block) pairs in tile-major order; pair q of P
+// owns units [sk_first(q), sk_first(q + 1)).  The host plans stream-K only
+// when units * P < 2^31, so 32-bit arithmetic is exact here.
+__device__ __forceinline__ uint32_t sk_units(const GemmParams& p) {
+  return static_cast<uint32_t>(p.num_tiles) * static_cast<uint32_t>(p.total_kb);
+}
+__device__ __forceinline__ uint32_t sk_first(const GemmParams& p, int q, int npairs) {
+  return sk_units(p) * static_cast<uint32_t>(q) / static_cast<uint32_t>(npairs);
+}
+// The pair whose range holds unit u: the largest q with sk_first(q) <= u.
+__device__ __forceinline__ int sk_holder(const GemmParams& p, uint32_t u, int npairs) {
+  return static_cast<int>(((u + 1) * static_cast<uint32_t>(npairs) - 1) / sk_units(p));
+}
+
+// Item `it` of this pair's schedule; false once the pair has no more work.
+// Without stream-K the items are the tiles pair, pair + P, ...; with it they
+// are the pieces of the pair's unit range cut at tile boundaries (only the
+// first and the last piece can be part of a tile).
+__device__ __forceinline__ bool pair_item(const GemmParams& p, int pair, int npairs, int it,
+                                          PairTile& t) {
+  if (!p.stream_k) {
+    const int tile = pair + it * npairs;
+    if (tile >= p.num_tiles) return false;
+    t = decode_pair_tile(p, tile);
+    t.tile = tile;
+    t.partial = false;
+    return true;
+  }
+  const uint32_t kb = static_cast<uint32_t>(p.total_kb);
+  const uint32_t u0 = sk_first(p, pair, npairs);
+  const uint32_t u1 = sk_first(p, pair + 1, npairs);
+  const uint32_t tile = u0 / kb + static_cast<uint32_t>(it);
+  const uint32_t t0 = tile * kb;
+  if (u0 >= u1 || t0 >= u1) return false;
+  t.tile = static_cast<int>(tile);
+  t.ks = 0;
+  t.mp = t.tile % p.num_m_blk;
+  t.nb = t.tile / p.num_m_blk;
+  t.kb0 = static_cast<int>((u0 > t0 ? u0 : t0) - t0);
+  t.kb1 = static_cast<int>((u1 < t0 + kb ? u1 : t0 + kb) - t0);
+  t.partial = t.kb0 > 0 || t.kb1 < p.total_kb;
+  return true;
+}
+
+// Counts one arrival at a split tile's word and returns true for the n-th
+// (last) arrival of this launch.  A word left by an earlier launch carries
+// another epoch and counts as zero, so the array never needs clearing.  Each
+// failed exchange means another participant arrived, so the loop ends within
+// n rounds; the bound only guards against a corrupted word.
+__device__ __forceinline__ bool sk_arrive(unsigned long long* word, unsigned long long epoch,
+                                          int n, bool& ok) {
+  unsigned long long cur = atomicAdd(word, 0ull);
+  for (int i = 0; i < 4096; ++i) {
+    const unsigned long long cnt = (cur >> 16) == epoch ? (cur & 0xFFFFull) : 0ull;
+    const unsigned long long prev = atomicCAS(word, cur, (epoch << 16) | (cnt + 1));
+    if (prev == cur) return static_cast<int>(cnt + 1) == n;
+    cur = prev;
+  }
+  ok = false;
+  return false;
+}
+
 template <class Cfg>
 __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CUtensorMap* tmY,
-                                                   uint32_t sbase, uint32_t tmem_base,
-                                                   int warp, int lane, uint32_t rank,
-                                                   volatile int* abort_flag, const PairBars& bars) {
+                                                   const CUtensorMap* tmP, uint32_t sbase,
+                                                   uint32_t tmem_base, int warp, int lane,
+                                                   uint32_t rank, volatile int* abort_flag,
+                                                   volatile int* sk_flag, const PairBars& bars) {
   const int ew = warp - Cfg::EPI_WARP0;
   const int quarter = warp & 3;
   const int cg = ew >> 2;
@@ -127,8 +196,8 @@ __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CU
   const int npairs = gridDim.x >> 1;
   Ring racc;
   bool ok = true;
-  for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
-    const PairTile tc = decode_pair_tile(p, tile);
+  PairTile tc;
+  for (int it = 0; ok && pair_item(p, pair, npairs, it, tc); ++it) {
     const int nst = 2 * (tc.kb1 - tc.kb0);
     int acc[128];
 #pragma unroll
@@ -154,9 +223,97 @@ __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CU
     }
     if (!ok) break;
     const uint32_t stage = sbase + Cfg::OFF_EPI + static_cast<uint32_t>(ew) * 4096u;
-    store_warp_tile<128>(p, tmY, stage, lane,
-                         tc.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM + quarter * 32,
-                         tc.nb * Cfg::PAIR_N + cg * 128, acc, tc.ks);
+    const int m_loc = static_cast<int>(rank) * Cfg::BM + quarter * 32;  // rows within the tile
+    const int n_loc = cg * 128;
+    if (tc.partial) {
+      // Stream-K fix-up.  Publish this pair's int32 partial in its slot,
+      // count the arrival, and let the last of the tile's pairs add the
+      // others' partials and write the tile.  Nobody waits for another pair.
+      store_warp_tile_s32<128>(tmP, stage, lane, m_loc, n_loc, acc, 2 * pair + (it == 0 ? 0 : 1));
+      if (lane == 0) {
+        bulk_wait_all();             // the partial is in global memory
+        fence_proxy_async_global();
+        mbar_arrive(bars.skstored());
+      }
+      __syncwarp();
+      // A pair has at most two split items, its first and its last: the
+      // fix-up barriers' phase is 1 only for a last item after a split first.
+      const uint32_t sk_phase =
+          (it > 0 && sk_first(p, pair, npairs) % static_cast<uint32_t>(p.total_kb) != 0) ? 1u : 0u;
+      // the tile's pairs: [holder of its first unit, holder of its last unit]
+      auto first_pair = [&] {
+        return sk_holder(p, static_cast<uint32_t>(tc.tile) * static_cast<uint32_t>(p.total_kb),
+                         npairs);
+      };
+      auto last_pair = [&] {
+        return sk_holder(p, static_cast<uint32_t>(tc.tile + 1) * static_cast<uint32_t>(p.total_kb) - 1,
+                         npairs);
+      };
+      if (ew == 0 && lane == 0) {
+        // (a timed-out wait has raised the abort flag and the status word)
+        bool last = false;
+        if (mbar_wait(bars.skstored(), sk_phase, abort_flag)) {
+          bool aok = true;
+          __threadfence();
+          unsigned long long* word = p.sk_arrive + 2 * tc.tile + rank;
+          last = sk_arrive(word, p.sk_epoch, last_pair() - first_pair() + 1, aok);
+          // every participant has arrived: clear the word, so that a replay
+          // of this launch (same epoch, e.g. from a CUDA graph) starts at zero
+          if (last) atomicExch(word, 0ull);
+          __threadfence();
+          if (!aok) {
+            *abort_flag = 1;
+            atomicOr(&g_status, 1u << 5);  // I8_ERR_CUDA: corrupted arrival word
+          }
+        }
+        *sk_flag = last ? 1 : 0;
+        mbar_arrive(bars.skdecided());     // always, so no epilogue warp waits in vain
+      }
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.skdecided(), sk_phase, abort_flag));
+      if (!ok) break;
+      if (*sk_flag == 0) continue;
+      // Last to arrive: rebuild the tile from all the pairs' slots (this
+      // pair's own included, so acc is no longer needed), 64 columns at a
+      // time, and write it.
+      __threadfence();
+      const int q0 = first_pair();
+      const int q1 = last_pair();
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        int sum[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) sum[i] = 0;
+#pragma unroll 1
+        for (int q = q0; q <= q1; ++q) {
+          const int slot =
+              2 * q + (sk_first(p, q, npairs) / static_cast<uint32_t>(p.total_kb) ==
+                               static_cast<uint32_t>(tc.tile) ? 0 : 1);
+          const int4* src = reinterpret_cast<const int4*>(
+              p.sk_part + (static_cast<int64_t>(slot) * 256 + m_loc + lane) * 256 + n_loc + 64 * h);
+          // 8 loads in flight at a time (the compiler barrier keeps the next
+          // group's loads behind this group's adds)
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            int4 v[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) v[c] = __ldcg(src + 8 * g + c);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              sum[32 * g + 4 * c] += v[c].x;
+              sum[32 * g + 4 * c + 1] += v[c].y;
+              sum[32 * g + 4 * c + 2] += v[c].z;
+              sum[32 * g + 4 * c + 3] += v[c].w;
+            }
+            asm volatile("" ::: "memory");
+          }
+        }
+        store_warp_tile<64>(p, tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
+                            tc.nb * Cfg::PAIR_N + n_loc + 64 * h, sum, tc.ks);
+      }
+      continue;
+    }
+    store_warp_tile<128>(p, tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
+                         tc.nb * Cfg::PAIR_N + n_loc, acc, tc.ks);
   }
   if (lane == 0) bulk_wait_all();
   __syncwarp();
@@ -166,7 +323,8 @@ template <class Cfg>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     gemm_w8a8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+                          const __grid_constant__ CUtensorMap tmY,
+                          const __grid_constant__ CUtensorMap tmP, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -183,6 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
   auto stage16 = [&](int s) { return sbase + Cfg::OFF_S16 + static_cast<uint32_t>(s * Cfg::STAGE16); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
+  volatile int* sk_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 8);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::S8; ++s) {
@@ -201,6 +360,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
       mbar_init(bars.paccempty(b), 1);   // CTA 0: forwarded by CTA 1's relay
     }
     mbar_init(bars.done(), 1);
+    mbar_init(bars.skstored(), Cfg::EPI_WARPS);
+    mbar_init(bars.skdecided(), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -212,6 +373,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmY);
+    if (p.stream_k) tma_prefetch_desc(&tmP);
   }
   tc_fence_before();
   __syncthreads();
@@ -222,15 +384,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
 
   if (warp >= Cfg::EPI_WARP0) {
     regs_inc<Cfg::REG_HI>();
-    pair_epilogue_role<Cfg>(p, &tmY, sbase, tmem_base, warp, lane, rank, abort_flag, bars);
+    pair_epilogue_role<Cfg>(p, &tmY, &tmP, sbase, tmem_base, warp, lane, rank, abort_flag,
+                            sk_flag, bars);
   } else if (warp == 0) {
     regs_dec<Cfg::REG_LO>();
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       Ring r8, r16;
       bool ok = true;
-      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
-        const PairTile tc = decode_pair_tile(p, tile);
+      PairTile tc;
+      for (int it = 0; ok && pair_item(p, pair, npairs, it, tc); ++it) {
         const int m0 = tc.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM;
         const int n0 = tc.nb * Cfg::PAIR_N + static_cast<int>(rank) * Cfg::BN;
         for (int kb = tc.kb0; ok && kb < tc.kb1; ++kb) {
@@ -265,8 +428,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
       constexpr uint32_t idesc = idesc_f16_f32(Cfg::PAIR_M, Cfg::PAIR_N);
       Ring r16, racc;
       bool ok = true;
-      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
-        const PairTile tc = decode_pair_tile(p, tile);
+      PairTile tc;
+      for (int it = 0; ok && pair_item(p, pair, npairs, it, tc); ++it) {
         const int nst = 2 * (tc.kb1 - tc.kb0);
         for (int st0 = 0; ok && st0 < nst; st0 += p.chunk_stages) {
           const int st1 = min(nst, st0 + p.chunk_stages);
@@ -309,8 +472,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
       Ring r16, racc;
       int chunk = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
-        const PairTile tc = decode_pair_tile(p, tile);
+      PairTile tc;
+      for (int it = 0; ok && pair_item(p, pair, npairs, it, tc); ++it) {
         const int nst = 2 * (tc.kb1 - tc.kb0);
         for (int st0 = 0; ok && st0 < nst; st0 += p.chunk_stages, ++chunk) {
           const int st1 = min(nst, st0 + p.chunk_stages);
@@ -341,8 +504,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     }
     Ring r8, r16;
     bool ok = true;
-    for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
-      const PairTile tc = decode_pair_tile(p, tile);
+    PairTile tc;
+    for (int it = 0; ok && pair_item(p, pair, npairs, it, tc); ++it) {
       for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
         // Both K-halves of the int8 block are read from shared memory in one
         // batch, so the load latency is exposed once per block.

@@ -6,8 +6,11 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <atomic>
+#include <chrono>
 #include <cstring>
 #include <mutex>
+#include <random>
 
 #include "../../include/i8.h"
 #include "gemm.cuh"
@@ -65,6 +68,7 @@ struct Options {
   int skinny_max_m = 16;   // token counts up to this use the weight-streaming kernel (0 = off)
   int pdl = 1;             // launch with programmatic stream serialization
   int quant_rows = 0;      // quantizer rows per CTA (0 = by shape)
+  int stream_k = 1;        // CTA-pair stream-K: 0 never, 1 by the table, 2 whenever pairs idle
 };
 Options g_opt;
 
@@ -180,10 +184,30 @@ i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t
   return cuda_status(e);
 }
 
+// Stream-K launch tags: a process-wide counter started at a random 48-bit
+// value, so a launch's tag differs from every earlier launch's (whose words
+// may still sit in a reused workspace) and, with overwhelming probability,
+// from whatever a fresh workspace holds.
+unsigned long long next_sk_epoch() {
+  static std::atomic<unsigned long long> counter{[] {
+    std::random_device rd;
+    const unsigned long long t = static_cast<unsigned long long>(
+        std::chrono::steady_clock::now().time_since_epoch().count());
+    return ((static_cast<unsigned long long>(rd()) << 32) ^ rd() ^ t) & ((1ull << 48) - 1);
+  }()};
+  unsigned long long e;
+  do {
+    e = counter.fetch_add(1) & ((1ull << 48) - 1);
+  } while (e == 0);
+  return e;
+}
+
 // ----------------------------------------------------------------- GEMM plan
 struct Plan {
   bool skinny = false;     // few tokens: weight-streaming kernel
   bool pair = false;       // CTA-pair kernel (256 x 256 tiles per cluster of 2)
+  bool stream_k = false;   // pair kernel with the stream-K schedule
+  size_t sk_arrive_bytes = 0;  // stream-K: arrival words at the start of ws
   int bn = 128;
   int splits = 1;
   int kb_per_split = 1;
@@ -226,7 +250,7 @@ int best_splits(int64_t tiles, int slots, int total_kb) {
 //   * split-K (exact int32 partials + a reduction) when the tiles cannot fill
 //     every worker.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
-               bool b16 = false) {
+               bool b16 = false, size_t ws_cap = SIZE_MAX) {
   Plan p;
   if (pair_clusters <= 0) pair_clusters = sms / 2;
   p.total_kb = static_cast<int>((K + 127) / 128);
@@ -261,6 +285,36 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
     tiles = static_cast<int64_t>(p.num_m) * p.num_n;
     slots = pair_clusters;
     if (g_opt.max_ctas > 0) slots = std::max(1, std::min(slots, g_opt.max_ctas / 2));
+    // Stream-K: every pair gets an equal share of the (tile, K-block)
+    // units, at least 4 K-blocks each.  Workspace: one arrival word per
+    // (tile, CTA) and two 256 x 256 int32 partial slots per pair.  Each tile
+    // cut between pairs costs its pairs a fix-up of roughly 5-10 us (int32
+    // partial out, partials back in), so the table takes it only where a
+    // tile carries far more MMA time than that and whole tiles leave many
+    // pairs idle: K >= 8192, at least half a wave of tiles, whole-tile wave
+    // efficiency below 0.93.  Measured (GEMM, GB300): +4 to +7 % at
+    // K = 12288 with M = 1024 ... 16384; -3 to -76 % at K = 3072.
+    const int64_t units = tiles * p.total_kb;
+    const int64_t waves = (tiles + slots - 1) / slots;
+    const double wave_eff = static_cast<double>(tiles) / static_cast<double>(waves * slots);
+    const bool sk_table = p.total_kb >= 64 && 2 * tiles >= slots && wave_eff < 0.93;
+    if ((g_opt.stream_k == 2 || (g_opt.stream_k == 1 && sk_table)) && g_opt.force_splits == 0 &&
+        tiles % slots != 0 &&
+        units * slots < (int64_t(1) << 31)) {   // the kernel's unit arithmetic is 32-bit
+      const int pairs = static_cast<int>(std::min<int64_t>(slots, std::max<int64_t>(1, units / 4)));
+      const size_t arrive = (static_cast<size_t>(tiles) * 16 + 1023) / 1024 * 1024;
+      const size_t part = static_cast<size_t>(2 * pairs) * 256 * 256 * sizeof(int32_t);
+      if (arrive + part <= ws_cap) {
+        p.stream_k = true;
+        p.num_tiles = static_cast<int>(tiles);
+        p.kb_per_split = p.total_kb;
+        p.grid = 2 * pairs;
+        p.chunk_stages = g_opt.chunk_k / 64;
+        p.sk_arrive_bytes = arrive;
+        p.ws_bytes = arrive + part;
+        return p;
+      }
+    }
   } else {
     p.bn = (N >= 256 && ((M + 127) / 128) * ((N + 255) / 256) >= sms) ? 256 : 128;
     if (g_opt.force_bn == 128 || g_opt.force_bn == 256) p.bn = g_opt.force_bn;
@@ -355,10 +409,10 @@ int pair_cluster_capacity(DeviceInfo* d, int slot) {
 
 template <class Cfg>
 i8_status launch_pair_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my,
-                          const GemmParams& gp, int grid, cudaStream_t st) {
+                          const CUtensorMap& mp, const GemmParams& gp, int grid, cudaStream_t st) {
   auto kern = gemm_w8a8_pair_kernel<Cfg>;
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, st, ma, mb,
-                                my, gp));
+                                my, mp, gp));
 }
 
 using PairConv = PairCfg<3, 3, true, true>;    // int8 weights, CTA pair
@@ -369,9 +423,12 @@ using CfgConv256 = GemmCfg<256, 2, 2, true, true>;
 using CfgWide256 = GemmCfg<256, 3, 3, true, false>;
 
 // Common GEMM driver.  b16 = weights given as fp16 codes instead of int8.
+// ws_cap bounds the workspace the plan may ask for (the no-alloc entry's
+// fixed array); the plan falls back from stream-K when that is too small.
 i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int64_t N, int64_t K,
                       int out_mode, void* out, int64_t ldo, const float* s_a, const float* s_w,
-                      const void* bias, void* ws, size_t ws_bytes, cudaStream_t st) {
+                      const void* bias, void* ws, size_t ws_bytes, cudaStream_t st,
+                      size_t ws_cap = SIZE_MAX) {
   if (M < 0 || N < 0 || K <= 0) return I8_ERR_INVALID_ARG;
   if (K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX) return I8_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return I8_OK;
@@ -386,7 +443,7 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   if (i8_status e = device_info(&d, nullptr)) return e;
   const int clusters = b16 ? pair_cluster_capacity<PairWide>(d, 1)
                            : pair_cluster_capacity<PairConv>(d, 0);
-  const Plan pl = make_plan(M, N, K, d->sms, clusters, b16);
+  const Plan pl = make_plan(M, N, K, d->sms, clusters, b16, ws_cap);
   if (pl.ws_bytes > 0) {
     if (!ws || ws_bytes < pl.ws_bytes) return I8_ERR_WORKSPACE;
     if (!aligned16(ws)) return I8_ERR_ALIGNMENT;
@@ -480,10 +537,20 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
                   static_cast<uint64_t>(M), static_cast<uint64_t>(gp.ldo),
                   static_cast<uint64_t>(pl.splits)))
     return I8_ERR_CUDA;
+  // Stream-K partial slots: {256 columns, 256 rows, 2 per pair} int32.
+  CUtensorMap mp = my;
+  if (pl.stream_k) {
+    gp.stream_k = 1;
+    gp.sk_arrive = static_cast<unsigned long long*>(ws);
+    gp.sk_part = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(ws) + pl.sk_arrive_bytes);
+    gp.sk_epoch = next_sk_epoch();
+    if (!encode_out(&mp, false, gp.sk_part, 256, 256, 256, static_cast<uint64_t>(pl.grid)))
+      return I8_ERR_CUDA;
+  }
   i8_status e;
   if (pl.pair) {
-    e = b16 ? launch_pair_cfg<PairWide>(ma, mb, my, gp, pl.grid, st)
-            : launch_pair_cfg<PairConv>(ma, mb, my, gp, pl.grid, st);
+    e = b16 ? launch_pair_cfg<PairWide>(ma, mb, my, mp, gp, pl.grid, st)
+            : launch_pair_cfg<PairConv>(ma, mb, my, mp, gp, pl.grid, st);
   } else if (pl.bn == 256) {
     e = b16 ? launch_gemm_cfg<CfgWide256>(d, 3, ma, mb, my, gp, pl.grid, st)
             : launch_gemm_cfg<CfgConv256>(d, 2, ma, mb, my, gp, pl.grid, st);
@@ -601,13 +668,14 @@ i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a, 
       N <= INT32_MAX) {
     DeviceInfo* d;
     if (i8_status e = device_info(&d, nullptr)) return e;
-    if (make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0)).ws_bytes >
-        kStaticWsBytes)
+    if (make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0), false, kStaticWsBytes)
+            .ws_bytes > kStaticWsBytes)
       return I8_ERR_WORKSPACE;
     if (i8_status e = static_ws_address(&ws)) return e;
   }
   return gemm_common(aq, wq, false, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws,
-                     ws ? kStaticWsBytes : 0, reinterpret_cast<cudaStream_t>(stream));
+                     ws ? kStaticWsBytes : 0, reinterpret_cast<cudaStream_t>(stream),
+                     kStaticWsBytes);
 }
 
 i8_status i8_widen_weight_codes(const int8_t* wq, int64_t N, int64_t K, void* w16,
@@ -664,6 +732,10 @@ i8_status i8_set_option(i8_option opt, int64_t value) {
     case I8_OPT_PDL:
       if (value != 0 && value != 1) return I8_ERR_INVALID_ARG;
       g_opt.pdl = static_cast<int>(value);
+      return I8_OK;
+    case I8_OPT_STREAM_K:
+      if (value < 0 || value > 2) return I8_ERR_INVALID_ARG;
+      g_opt.stream_k = static_cast<int>(value);
       return I8_OK;
     case I8_OPT_QUANT_ROWS:
       if (value < 0 || value > 8) return I8_ERR_INVALID_ARG;

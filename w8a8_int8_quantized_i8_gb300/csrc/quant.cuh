@@ -93,7 +93,11 @@ __device__ __forceinline__ uint2 quant_vec8(uint4 v, float s, unsigned long long
   for (int i = 0; i < 4; ++i) {
     const unsigned long long x = f2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
     const unsigned long long t = f2_mul(x, rr);         // x * fl(1/s)
-    const unsigned long long y = f2_add(t, mm);         // rounds t to an integer (+ magic)
+    // y rounds t to an integer (+ magic).  If the compiler fuses the
+    // multiply into this add, y rounds the exact product x * fl(1/s)
+    // instead; that is also within 3 * 127 * 2^-24 of x / s, so the near-tie
+    // test below covers both forms.
+    const unsigned long long y = f2_add(t, mm);
     const unsigned long long d = f2_sub(t, f2_sub(y, mm));  // t - rint(t), exact
     float y0, y1, d0, d1;
     f2_split(y, y0, y1);
