@@ -64,6 +64,17 @@ def _load():
             lib.orc_gemm_s32.restype = ctypes.c_int
             lib.orc_dequant_bias.argtypes = [vp, i64, vp, vp, vp, i64, i64, vp, i64]
             lib.orc_dequant_bias.restype = ctypes.c_int
+            lib.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
+            lib.orc_f32_to_e4m3.restype = ctypes.c_uint8
+            lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_to_f64.restype = ctypes.c_double
+            lib.orc_quant_rows_e4m3.argtypes = [vp, i64, i64, i64, vp, i64, vp]
+            lib.orc_quant_rows_e4m3.restype = ctypes.c_int
+            lib.orc_gemm_e4m3_f64.argtypes = [vp, i64, vp, i64, i64, i64, i64,
+                                              ctypes.c_int, vp, i64]
+            lib.orc_gemm_e4m3_f64.restype = ctypes.c_int
+            lib.orc_dequant_bias_f64acc.argtypes = [vp, i64, vp, vp, vp, i64, i64, vp, i64]
+            lib.orc_dequant_bias_f64acc.restype = ctypes.c_int
             lib.orc_num_threads.argtypes = []
             lib.orc_num_threads.restype = ctypes.c_int
             lib.orc_set_num_threads.argtypes = [ctypes.c_int]
@@ -161,4 +172,80 @@ def linear(x_bits, w_bits, bias_bits):
     wq, s_w = quant_rows(w_bits)
     acc = gemm_s32(aq, wq)
     y = dequant_bias(acc, s_a, s_w, bias_bits)
+    return dict(aq=aq, s_a=s_a, wq=wq, s_w=s_w, acc=acc, y=y)
+
+
+# ---------------------------------------------------------------------- FP8
+# The E4M3 arm (see the FP8 section of i8_oracle.h for the reading): the same
+# per-row symmetric scheme with s = absmax / 448 and E4M3 codes, an exact
+# fp64 GEMM over the codes, and the same fp32 epilogue steps.
+
+def f32_to_e4m3_bits(f: float) -> int:
+    return int(_load().orc_f32_to_e4m3(float(f)))
+
+
+def e4m3_bits_to_f64(b: int) -> float:
+    return float(_load().orc_e4m3_to_f64(int(b)))
+
+
+def quant_rows_e4m3(x_bits):
+    """Per-row E4M3 quantization of a bf16 matrix (uint16 bits).
+
+    Returns ``(q uint8 [rows,K] E4M3 bit patterns, scale float32 [rows])``.
+    """
+    x = _c2d(x_bits, np.uint16)
+    rows, K = x.shape
+    q = np.zeros((rows, K), dtype=np.uint8)
+    s = np.zeros((rows,), dtype=np.float32)
+    rc = _load().orc_quant_rows_e4m3(_ptr(x), rows, K, K, _ptr(q), K, _ptr(s))
+    if rc != 0:
+        raise ValueError("orc_quant_rows_e4m3 rejected its arguments")
+    return q, s
+
+
+def gemm_e4m3_f64(a, w, absval: bool = False) -> np.ndarray:
+    """Exact fp64 ``a @ w.T`` over E4M3 codes (``|a| @ |w|.T`` if absval)."""
+    a = _c2d(a, np.uint8)
+    w = _c2d(w, np.uint8)
+    M, K = a.shape
+    N, K2 = w.shape
+    if K != K2:
+        raise ValueError("K mismatch")
+    c = np.zeros((M, N), dtype=np.float64)
+    rc = _load().orc_gemm_e4m3_f64(_ptr(a), K, _ptr(w), K, M, N, K,
+                                   1 if absval else 0, _ptr(c), N)
+    if rc != 0:
+        raise ValueError("orc_gemm_e4m3_f64 rejected its arguments")
+    return c
+
+
+def dequant_bias_f64acc(acc, s_a, s_w, bias_bits) -> np.ndarray:
+    """bf16 bits of ``fl32(acc) * s_a * s_w + bias`` with fp32 steps."""
+    c = _c2d(acc, np.float64)
+    M, N = c.shape
+    sa = np.ascontiguousarray(s_a, dtype=np.float32)
+    sw = np.ascontiguousarray(s_w, dtype=np.float32)
+    if sa.shape != (M,) or sw.shape != (N,):
+        raise ValueError("scale shapes")
+    b = None
+    if bias_bits is not None:
+        b = np.ascontiguousarray(bias_bits)
+        if b.dtype != np.uint16 or b.shape != (N,):
+            raise ValueError("bias must be uint16 bf16 bits of shape [N]")
+    y = np.zeros((M, N), dtype=np.uint16)
+    rc = _load().orc_dequant_bias_f64acc(_ptr(c), N, _ptr(sa), _ptr(sw), _ptr(b),
+                                         M, N, _ptr(y), N)
+    if rc != 0:
+        raise ValueError("orc_dequant_bias_f64acc rejected its arguments")
+    return y
+
+
+def linear_e4m3(x_bits, w_bits, bias_bits):
+    """The E4M3 path: per-row E4M3 quantization of X and W, the exact GEMM
+    over the codes, and the epilogue.  Returns ``aq, s_a, wq, s_w, acc, y``
+    (acc exact in fp64, y as bf16 bits)."""
+    aq, s_a = quant_rows_e4m3(x_bits)
+    wq, s_w = quant_rows_e4m3(w_bits)
+    acc = gemm_e4m3_f64(aq, wq)
+    y = dequant_bias_f64acc(acc, s_a, s_w, bias_bits)
     return dict(aq=aq, s_a=s_a, wq=wq, s_w=s_w, acc=acc, y=y)

@@ -137,3 +137,131 @@ void orc_set_num_threads(int n) {
   (void)n;
 #endif
 }
+
+/* ------------------------------------------------------------------ FP8
+ * E4M3 as the OCP 8-bit floating point specification defines it: sign bit,
+ * 4 exponent bits with bias 7, 3 mantissa bits.  Normal codes (exponent
+ * field e = 1..15) hold (8 + m) * 2^(e - 10); subnormal codes (e = 0) hold
+ * m * 2^-9; there is no infinity, and e = 15, m = 7 is NaN, so the largest
+ * finite magnitude is 14 * 2^5 = 448.
+ *
+ * Pins (tests/test_oracle_fp8.py): torch's float8_e4m3fn cast on every bf16
+ * value below the saturation point and on random fp32 patterns; the decode
+ * of all 256 codes against the format's closed form; midpoints between
+ * neighbouring codes (ties to the even code); the saturation rule; the
+ * quantizer against exact rational arithmetic; the fp64 GEMM against
+ * Python integer arithmetic on the codes scaled by 2^18; the epilogue against
+ * its int32 counterpart on integer-valued accumulators. */
+
+double orc_e4m3_to_f64(uint8_t b) {
+  int e = (b >> 3) & 15;
+  int m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  v = (e == 0) ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+  return (b & 0x80) ? -v : v;
+}
+
+uint8_t orc_f32_to_e4m3(float f) {
+  uint8_t sign;
+  double a, quantum, r;
+  int e2, lg, m;
+  if (isnan(f)) return 0x7F;
+  sign = signbit(f) ? 0x80 : 0x00;
+  if (isinf(f)) return (uint8_t)(sign | 0x7E); /* saturate: +-448 */
+  a = fabs((double)f);
+  if (a == 0.0) return sign;
+  /* The quantum of |f|'s binade: 2^(floor(log2 |f|) - 3) for normal
+   * magnitudes, 2^-9 (the subnormal spacing) below 2^-6. */
+  frexp(a, &e2);
+  lg = e2 - 1;
+  if (lg < -6) lg = -6;
+  quantum = ldexp(1.0, lg - 3);
+  /* a / quantum is exact (power-of-two divisor); nearbyint rounds half to
+   * even, and an even multiple of the quantum is an even mantissa. */
+  r = nearbyint(a / quantum) * quantum;
+  if (r > 448.0) r = 448.0; /* finite saturation */
+  if (r == 0.0) return sign;
+  if (r < ldexp(1.0, -6)) return (uint8_t)(sign | (int)(r / ldexp(1.0, -9)));
+  frexp(r, &e2);
+  lg = e2 - 1; /* r in [2^lg, 2^(lg+1)) */
+  m = (int)(r / ldexp(1.0, lg - 3)) - 8;
+  return (uint8_t)(sign | ((lg + 7) << 3) | m);
+}
+
+/* One row: absmax, scale = absmax / 448, q = E4M3(x / scale). */
+static void quant_one_row_e4m3(const uint16_t* x, int64_t K, uint8_t* q,
+                               float* scale) {
+  float amax = 0.0f;
+  for (int64_t k = 0; k < K; ++k) {
+    float v = fabsf(orc_bf16_to_f32(x[k]));
+    if (v > amax) amax = v;
+  }
+  if (amax == 0.0f) {
+    *scale = 0.0f;
+    for (int64_t k = 0; k < K; ++k) q[k] = 0;
+    return;
+  }
+  float s = amax / 448.0f; /* IEEE fp32 division, round to nearest even */
+  *scale = s;
+  for (int64_t k = 0; k < K; ++k) {
+    float t = orc_bf16_to_f32(x[k]) / s; /* a true fp32 division */
+    q[k] = orc_f32_to_e4m3(t);
+  }
+}
+
+int orc_quant_rows_e4m3(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
+                        uint8_t* q, int64_t ldq, float* scale) {
+  if (rows < 0 || K < 0 || ldx < K || ldq < K) return -1;
+  if (rows > 0 && K > 0 && (!x || !q)) return -1;
+  if (rows > 0 && !scale) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    quant_one_row_e4m3(x + r * ldx, K, q + r * ldq, scale + r);
+  }
+  return 0;
+}
+
+int orc_gemm_e4m3_f64(const uint8_t* a, int64_t lda, const uint8_t* w, int64_t ldw,
+                      int64_t M, int64_t N, int64_t K, int absval, double* c,
+                      int64_t ldc) {
+  double val[256];
+  if (M < 0 || N < 0 || K < 0 || K > 131072) return -1;
+  if (lda < K || ldw < K || ldc < N) return -1;
+  if (M > 0 && N > 0 && (!c || (K > 0 && (!a || !w)))) return -1;
+  for (int b = 0; b < 256; ++b) {
+    double v = orc_e4m3_to_f64((uint8_t)b);
+    val[b] = absval ? fabs(v) : v;
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    const uint8_t* arow = a + m * lda;
+    for (int64_t n = 0; n < N; ++n) {
+      const uint8_t* wrow = w + n * ldw;
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        acc += val[arow[k]] * val[wrow[k]];
+      }
+      c[m * ldc + n] = acc;
+    }
+  }
+  return 0;
+}
+
+int orc_dequant_bias_f64acc(const double* c, int64_t ldc, const float* s_a,
+                            const float* s_w, const uint16_t* bias, int64_t M,
+                            int64_t N, uint16_t* y, int64_t ldy) {
+  if (M < 0 || N < 0 || ldc < N || ldy < N) return -1;
+  if (M > 0 && N > 0 && (!c || !s_a || !s_w || !y)) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t n = 0; n < N; ++n) {
+      float t = (float)c[m * ldc + n]; /* fp64 -> fp32, nearest even */
+      t = t * s_a[m];
+      t = t * s_w[n];
+      t = t + (bias ? orc_bf16_to_f32(bias[n]) : 0.0f);
+      y[m * ldy + n] = orc_f32_to_bf16(t);
+    }
+  }
+  return 0;
+}

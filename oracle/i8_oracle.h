@@ -58,6 +58,43 @@ int orc_dequant_bias(const int32_t* c, int64_t ldc, const float* s_a,
                      const float* s_w, const uint16_t* bias, int64_t M,
                      int64_t N, uint16_t* y, int64_t ldy);
 
+/* ------------------------------------------------------------------ FP8
+ * The 8-bit floating-point arm: the pages set their INT8 kernel against an
+ * FP8 baseline ([ABS]: the 172.9 s single-card FP8 run at 1024px, and the
+ * closing remark that B200's native FP8 path beats the Ampere INT8 kernel).
+ * They never print that quantizer.  Reading (listed in the design doc): the same
+ * symmetric per-row scheme with the E4M3 format of the OCP 8-bit floating
+ * point specification -- s = absmax / 448 in IEEE fp32 (448 = largest finite
+ * E4M3 value), code = E4M3(fl32(x / s)) rounded to nearest, ties to even,
+ * with finite saturation to +-448; the zero row gives s = 0 and codes 0.
+ * E4M3 codes cross this interface as uint8_t bit patterns. */
+
+/* fp32 -> E4M3 bit pattern: round to nearest even; finite values whose
+ * rounded magnitude exceeds 448 saturate to +-448; NaN -> 0x7F. */
+uint8_t orc_f32_to_e4m3(float f);
+/* E4M3 bit pattern -> value (exact in fp64); the two NaN codes give NaN. */
+double orc_e4m3_to_f64(uint8_t b);
+
+/* Per-row E4M3 quantizer (same argument meaning as orc_quant_rows). */
+int orc_quant_rows_e4m3(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
+                        uint8_t* q, int64_t ldq, float* scale);
+
+/* c[m][n] = sum_k a[m][k] * w[n][k] over E4M3 codes, in fp64.  Exact for
+ * K <= 131072: every product is an integer multiple of 2^-18 below 2^18, so
+ * every partial sum is a multiple of 2^-18 below 2^35 and fits the 53-bit
+ * significand.  absval != 0 sums |a * w| instead (used for error bounds).
+ * Returns 0, or -1 on bad arguments. */
+int orc_gemm_e4m3_f64(const uint8_t* a, int64_t lda, const uint8_t* w, int64_t ldw,
+                      int64_t M, int64_t N, int64_t K, int absval, double* c,
+                      int64_t ldc);
+
+/* y[m][n] = bf16( ((float)c[m][n] * s_a[m]) * s_w[n] + bias[n] ): the same
+ * epilogue steps as orc_dequant_bias, from an fp64 accumulator rounded once
+ * to fp32 (nearest even).  bias may be NULL.  Returns 0, or -1. */
+int orc_dequant_bias_f64acc(const double* c, int64_t ldc, const float* s_a,
+                            const float* s_w, const uint16_t* bias, int64_t M,
+                            int64_t N, uint16_t* y, int64_t ldy);
+
 /* Threads the loops may use (OpenMP), or 1 when built without it. */
 int orc_num_threads(void);
 void orc_set_num_threads(int n);
