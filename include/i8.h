@@ -118,6 +118,49 @@ i8_status i8_gemm_dequant_bias_bf16(const int8_t* aq, const float* s_a,
                                     int64_t K, void* y, int64_t ldy, void* ws,
                                     size_t ws_bytes, i8_stream_t stream);
 
+/* ------------------------------------------------------------------ E4M3
+ * The 8-bit floating-point arm (arXiv 2606.14598, abstract: the INT8 kernel
+ * is set against an FP8 baseline, and the B200's native FP8 path beats it).
+ * The pages print no FP8 quantizer; this library reads it as the same
+ * symmetric per-row scheme with the E4M3 format of the OCP 8-bit floating
+ * point specification (largest finite value 448):
+ *   s = absmax / 448 (IEEE fp32), code = E4M3(fl32(x / s)) rounded to
+ *   nearest even with finite saturation; the zero row gives s = 0, codes 0.
+ * Codes are stored as their uint8_t bit patterns.  Same layouts, alignment
+ * and error behaviour as the int8 quantizers above.                        */
+i8_status i8_quant_weight_perchannel_e4m3(const void* w_bf16, int64_t N,
+                                          int64_t K, int64_t ldw,
+                                          uint8_t* wq, int64_t ldq,
+                                          float* s_w, i8_stream_t stream);
+i8_status i8_quant_act_pertoken_e4m3(const void* x_bf16, int64_t M,
+                                     int64_t K, int64_t ldx, uint8_t* aq,
+                                     int64_t ldq, float* s_a,
+                                     i8_stream_t stream);
+
+/* fp32 accumulators of the E4M3 GEMM, for checking:
+ *   c[m,n] = sum_k a[m,k] * w[n,k] over the decoded E4M3 codes, accumulated
+ *   by the tensor core in fp32 (rounded; the order of its additions is not
+ *   specified, so the result is within the fp32 accumulation bound of the
+ *   exact sum, not bit-identical to a sequential loop).
+ *   aq [M,K], wq [N,K] E4M3 codes, contiguous (row stride K bytes)
+ *   c  [M,N] fp32, row stride ldc elements (ldc >= N, ldc % 4 == 0)
+ *   K % 16 == 0, K <= 131072.  Needs no workspace.                         */
+i8_status i8_gemm_e4m3_f32(const uint8_t* aq, const uint8_t* wq, int64_t M,
+                           int64_t N, int64_t K, float* c, int64_t ldc,
+                           i8_stream_t stream);
+
+/* The fused E4M3 GEMM: the fp32 accumulator above, then the same epilogue
+ * as i8_gemm_dequant_bias_bf16:
+ *   y[m,n] = bf16_rne(((acc * s_a[m]) * s_w[n]) + bias[n]), fp32 steps.
+ *   aq [M,K] / wq [N,K] E4M3 codes contiguous, s_a [M] / s_w [N] fp32,
+ *   bias [N] bf16 or NULL, y [M,N] bf16 (ldy >= N, ldy % 8 == 0).
+ *   Needs no workspace.                                                    */
+i8_status i8_gemm_e4m3_dequant_bias_bf16(const uint8_t* aq, const float* s_a,
+                                         const uint8_t* wq, const float* s_w,
+                                         const void* bias, int64_t M,
+                                         int64_t N, int64_t K, void* y,
+                                         int64_t ldy, i8_stream_t stream);
+
 /* i8_gemm_dequant_bias_bf16 for callers that cannot allocate device memory
  * at call time -- for example a plugin running inside another runtime that
  * offers no workspace hook, an application whose device memory is all owned

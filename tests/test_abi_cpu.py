@@ -66,6 +66,26 @@ def test_gemm_argument_errors(lib):
     assert lib.i8_widen_weight_codes(ok, 4, 24, ok, None) == 3
 
 
+def test_e4m3_argument_errors(lib):
+    ok = P(0x10000)
+    for fn in (lib.i8_quant_act_pertoken_e4m3, lib.i8_quant_weight_perchannel_e4m3):
+        assert fn(ok, -1, 64, 64, ok, 64, ok, None) == 1
+        assert fn(ok, 4, 40, 40, ok, 48, ok, None) == 3             # K % 16
+        assert fn(P(0x10008), 4, 64, 64, ok, 64, ok, None) == 2
+        assert fn(ok, 0, 64, 64, ok, 64, ok, None) == 0
+    g = lib.i8_gemm_e4m3_dequant_bias_bf16
+    assert g(ok, ok, ok, ok, None, -1, 8, 16, ok, 8, None) == 1
+    assert g(ok, ok, ok, ok, None, 4, 8, 24, ok, 8, None) == 3             # K % 16
+    assert g(ok, ok, ok, ok, None, 0, 8, 16, ok, 8, None) == 0             # empty
+    assert g(ok, None, ok, ok, None, 4, 8, 16, ok, 8, None) == 1           # no scales
+    assert g(P(0x10001), ok, ok, ok, None, 4, 8, 16, ok, 8, None) == 2
+    assert g(ok, ok, ok, ok, None, 4, 12, 16, ok, 12, None) == 2           # ldy % 8
+    c = lib.i8_gemm_e4m3_f32
+    assert c(ok, ok, 4, 8, 16, ok, 6, None) == 1                           # ldc < N
+    assert c(ok, ok, 4, 8, 16, ok, 10, None) == 2                          # ldc % 4
+    assert c(ok, ok, 4, 8, 200000, ok, 8, None) == 3
+
+
 def test_options_validation(lib):
     assert lib.i8_set_option(1, 100) == 1
     assert lib.i8_set_option(1, 2048) == 1

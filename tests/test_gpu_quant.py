@@ -32,6 +32,9 @@ def _compare(orc, x: torch.Tensor, fn=i8.quant_act_pertoken, what=""):
     (33, 12288, "gelu", True),       # MLP down width: 4 warps per row
     (300, 1040, "normal", True),     # ragged vector tail inside a lane
     (17, 4096 + 16, "gelu", True),
+    (5, 32768, "normal", True),      # longest row the register-resident kernel holds
+    (9, 32768 + 16, "normal", True), # two-pass long-row kernel from here on
+    (6, 131072, "gelu", True),       # maximum K
 ])
 def test_quant_matches_oracle(orc, M, K, dist, outl):
     x = inputs.activations(M, K, torch.Generator().manual_seed(M * 7 + K), dist, outl)

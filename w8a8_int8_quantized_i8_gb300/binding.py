@@ -69,6 +69,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "i8_gemm_dequant_bias_bf16_w16": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, sz, vp], st),
             "i8_set_option": ([ctypes.c_int, i64], st),
             "i8_gemm_dequant_bias_bf16_noalloc": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp], st),
+            "i8_quant_weight_perchannel_e4m3": ([vp, i64, i64, i64, vp, i64, vp, vp], st),
+            "i8_quant_act_pertoken_e4m3": ([vp, i64, i64, i64, vp, i64, vp, vp], st),
+            "i8_gemm_e4m3_f32": ([vp, vp, i64, i64, i64, vp, i64, vp], st),
+            "i8_gemm_e4m3_dequant_bias_bf16": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp], st),
             "i8_sync_check": ([vp], st),
             "i8_selftest_timeout": ([ctypes.c_int, vp], st),
         }
@@ -211,6 +215,92 @@ def linear(x, wq, s_w, bias=None, out=None, workspace=None):
     """The whole W8A8 linear layer: per-token quant of x, then the fused GEMM."""
     aq, s_a = quant_act_pertoken(x)
     return gemm_dequant_bias_bf16(aq, s_a, wq, s_w, bias, out=out, workspace=workspace)
+
+
+# ---------------------------------------------------------------------- E4M3
+# The 8-bit floating-point arm: per-row E4M3 codes (s = absmax / 448) and the
+# fused E4M3 GEMM with the same epilogue.  Codes are float8_e4m3fn tensors
+# (uint8 tensors holding the same bit patterns are accepted too).
+
+def _codes(t: torch.Tensor, name: str) -> torch.Tensor:
+    if isinstance(t, torch.Tensor) and t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    _need(t, torch.uint8, name, 2)
+    return t
+
+
+def _quant_e4m3(fn_name: str, x: torch.Tensor, q=None, s=None):
+    _need(x, torch.bfloat16, "x", 2)
+    R, K = x.shape
+    if q is None:
+        q = torch.empty((R, K), dtype=torch.float8_e4m3fn, device=x.device)
+    if s is None:
+        s = torch.empty((R,), dtype=torch.float32, device=x.device)
+    qb = _codes(q, "q")
+    _need(s, torch.float32, "s", 1)
+    if tuple(qb.shape) != (R, K) or s.shape[0] != R:
+        raise ValueError("output shape")
+    lib = load()
+    with torch.cuda.device(x.device):
+        _check(getattr(lib, fn_name)(_ptr(x), R, K, K, _ptr(qb), K, _ptr(s), _stream(x)), fn_name)
+    return q, s
+
+
+def quant_act_pertoken_e4m3(x: torch.Tensor, q=None, s=None):
+    """bf16 [M,K] -> (E4M3 codes [M,K], fp32 per-token scales [M])."""
+    return _quant_e4m3("i8_quant_act_pertoken_e4m3", x, q, s)
+
+
+def quant_weight_perchannel_e4m3(w: torch.Tensor, q=None, s=None):
+    """bf16 [N,K] -> (E4M3 codes [N,K], fp32 per-channel scales [N])."""
+    return _quant_e4m3("i8_quant_weight_perchannel_e4m3", w, q, s)
+
+
+def gemm_e4m3_f32(aq, wq, out=None) -> torch.Tensor:
+    """fp32 tensor-core accumulators aq @ wq.T over E4M3 codes (for checking)."""
+    a = _codes(aq, "aq")
+    w = _codes(wq, "wq")
+    M, K = a.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("K mismatch")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _need(out, torch.float32, "out", 2)
+    with torch.cuda.device(a.device):
+        _check(load().i8_gemm_e4m3_f32(_ptr(a), _ptr(w), M, N, K, _ptr(out), out.stride(0),
+                                       _stream(a)), "i8_gemm_e4m3_f32")
+    return out
+
+
+def gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, bias=None, out=None):
+    """Fused E4M3 GEMM: bf16(acc * s_a[m] * s_w[n] + bias[n])."""
+    a = _codes(aq, "aq")
+    w = _codes(wq, "wq")
+    _need(s_a, torch.float32, "s_a", 1)
+    _need(s_w, torch.float32, "s_w", 1)
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = a.shape
+    N = w.shape[0]
+    if w.shape[1] != K or s_a.shape[0] != M or s_w.shape[0] != N:
+        raise ValueError("shape mismatch")
+    if bias is not None and bias.shape[0] != N:
+        raise ValueError("bias shape")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _need(out, torch.bfloat16, "out", 2)
+    fn = "i8_gemm_e4m3_dequant_bias_bf16"
+    with torch.cuda.device(a.device):
+        _check(getattr(load(), fn)(_ptr(a), _ptr(s_a), _ptr(w), _ptr(s_w), _ptr(bias), M, N, K,
+                                   _ptr(out), out.stride(0), _stream(a)), fn)
+    return out
+
+
+def linear_e4m3(x, wq, s_w, bias=None, out=None):
+    """The E4M3 linear layer: per-token E4M3 quant of x, then the fused GEMM."""
+    aq, s_a = quant_act_pertoken_e4m3(x)
+    return gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, bias, out=out)
 
 
 def set_option(name: str, value: int) -> None:

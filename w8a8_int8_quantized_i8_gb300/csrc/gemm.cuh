@@ -224,6 +224,12 @@ __device__ __forceinline__ float dequant_one(int acc, float sa, float sw, float 
   t = __fmul_rn(t, sw);
   return __fadd_rn(t, b);
 }
+// The same steps from an fp32 accumulator (the E4M3 arm).
+__device__ __forceinline__ float dequant_one(float acc, float sa, float sw, float b) {
+  float t = __fmul_rn(acc, sa);
+  t = __fmul_rn(t, sw);
+  return __fadd_rn(t, b);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -236,10 +242,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // columns, int32 groups 32.  Lane i holds row (m_base + i) in acc[0..127].
 // The tensor store clips rows >= M and columns >= N, so ragged tiles need no
 // masking.  tmY is 3-D {N, M, splits}; z selects the split-K partial.
-template <int COLS>
+template <int COLS, typename Acc = int>
 __device__ __forceinline__ void store_warp_tile_bf16(const GemmParams& p, const CUtensorMap* tmY,
                                                      uint32_t stage, int lane, int m_base, int n0,
-                                                     const int (&acc)[COLS]) {
+                                                     const Acc (&acc)[COLS]) {
   const uint32_t row = stage + static_cast<uint32_t>(lane) * 128u;
   const uint32_t x = static_cast<uint32_t>(lane & 7);
   const int m = m_base + lane;

@@ -1,0 +1,232 @@
+// gemm_fp8.cuh -- the E4M3 (FP8) arm of the W8A8 linear layer, on a CTA pair.
+//
+// Fused INT8 GEMM Kernel for Ideogram 4.0 (arXiv 2606.14598), abstract: the
+// INT8 kernel is measured against an FP8 baseline, and on B200 it loses to
+// the card's native FP8 path.  This is that native path on sm_103a, with the
+// same per-token x per-channel scales and the same fused epilogue:
+//   acc[m,n] = sum_k a[m,k] * w[n,k]      (E4M3 x E4M3 -> fp32, tensor core)
+//   y[m,n]   = bf16(acc * s_a[m] * s_w[n] + bias[n])
+// Unlike the int8 arm nothing is widened on chip and nothing is drained in
+// chunks: TMA brings the E4M3 codes into shared memory and tcgen05.mma
+// kind::f8f6f4 consumes them there; the fp32 accumulator of the whole K
+// range is read once per tile.  The tensor core's fp32 additions round (in
+// an order the hardware does not specify), so this arm agrees with the exact
+// oracle within an error bound rather than bit for bit.
+//
+// Structure: the two CTAs of a cluster compute one 256 x 256 output tile.
+//   * CTA r loads A rows [m0 + 128 r, +128) and B rows [n0 + 128 r, +128) of
+//     each 128-deep K block into its own shared memory (128-byte swizzle);
+//     both CTAs' loads complete on CTA 0's full barrier (cta_group::2 TMA),
+//     which CTA 0's producer armed with the stage's total byte count.
+//   * One thread of CTA 0 issues four M=256 N=256 K=32 MMAs per block; each
+//     CTA's 128 rows x 256 fp32 columns land in its own tensor memory, in
+//     one of two buffers, so a tile's epilogue overlaps the next mainloop.
+//     Its commits free the stage in both CTAs (multicast).
+//   * Eight epilogue warps per CTA (lane quarter = warp % 4, column half =
+//     (warp - 4) / 4) read the accumulator, hand the buffer back (CTA 1's
+//     warps arrive on CTA 0's barrier), dequantize + bias -> bf16 (or keep
+//     fp32 for the checking path) and write through swizzled shared-memory
+//     staging with bulk tensor stores.
+// Warps: 0 producer, 1 TMEM allocation + MMA issuer, 2-3 idle, 4-11 epilogue.
+// Every wait is bounded (ptx.cuh); a timeout aborts the CTA cleanly.
+#pragma once
+#include "gemm.cuh"
+
+namespace i8 {
+
+struct Fp8Cfg {
+  static constexpr int BM = 128;        // A rows loaded per CTA
+  static constexpr int BN = 128;        // B rows loaded per CTA
+  static constexpr int PAIR_M = 256;
+  static constexpr int PAIR_N = 256;
+  static constexpr int BK = 128;        // K per stage: one 128-byte swizzle row
+  static constexpr int STAGES = 6;
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_WARP0 = 4;
+  static constexpr int THREADS = 384;
+  static constexpr int OFF_STAGE = 0;
+  static constexpr int OFF_EPI = STAGES * STAGE_BYTES;          // 4 KB staging per epilogue warp
+  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 4096;
+  // full[S] empty[S] accfull[2] accempty[2] done
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int TMEM_COLS = 2 * PAIR_N;
+  static constexpr uint32_t TX = 2 * STAGE_BYTES;               // both CTAs' loads of a stage
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+};
+
+struct Fp8Bars {
+  uint32_t base;
+  __device__ uint32_t full(int s) const { return base + 8u * s; }
+  __device__ uint32_t empty(int s) const { return base + 8u * (Fp8Cfg::STAGES + s); }
+  __device__ uint32_t accfull(int b) const { return base + 8u * (2 * Fp8Cfg::STAGES + b); }
+  __device__ uint32_t accempty(int b) const { return base + 8u * (2 * Fp8Cfg::STAGES + 2 + b); }
+  __device__ uint32_t done() const { return base + 8u * (2 * Fp8Cfg::STAGES + 4); }
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
+    gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+  using Cfg = Fp8Cfg;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw_base);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  const Fp8Bars bars{sbase + Cfg::OFF_BAR};
+  auto stage = [&](int s) { return sbase + Cfg::OFF_STAGE + static_cast<uint32_t>(s * Cfg::STAGE_BYTES); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(bars.full(s), 1);        // CTA 0: its producer's arrive + both CTAs' bytes
+      mbar_init(bars.empty(s), 1);       // the MMA thread's commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars.accfull(b), 1);
+      mbar_init(bars.accempty(b), 2 * Cfg::EPI_WARPS);  // CTA 0: both CTAs' epilogue warps
+    }
+    mbar_init(bars.done(), 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmY);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers initialised before any remote signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // operands and outputs may belong to the previous kernel
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t full0 = mapa_shared(bars.full(0), 0);
+      Ring r;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+        const int mp = tile % p.num_m_blk;
+        const int nb = tile / p.num_m_blk;
+        const int m0 = mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM;
+        const int n0 = nb * Cfg::PAIR_N + static_cast<int>(rank) * Cfg::BN;
+        for (int kb = 0; kb < p.total_kb; ++kb) {
+          if (!(ok = mbar_wait(bars.empty(r.s), r.ph ^ 1u, abort_flag))) break;
+          if (rank == 0) mbar_arrive_expect_tx(bars.full(r.s), Cfg::TX);
+          const uint32_t fb = full0 + 8u * static_cast<uint32_t>(r.s);
+          tma_load_2d_pair(stage(r.s), &tmA, fb, kb * Cfg::BK, m0);
+          tma_load_2d_pair(stage(r.s) + Cfg::A_BYTES, &tmB, fb, kb * Cfg::BK, n0);
+          r.advance(Cfg::STAGES);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (CTA 0)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(Cfg::PAIR_M, Cfg::PAIR_N);
+      Ring r, racc;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+        if (!(ok = mbar_wait_cluster(bars.accempty(racc.s), racc.ph ^ 1u, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(racc.s * Cfg::PAIR_N);
+        for (int kb = 0; kb < p.total_kb; ++kb) {
+          if (!(ok = mbar_wait_cluster(bars.full(r.s), r.ph, abort_flag))) break;
+          tc_fence_after();
+          const uint64_t ad = smem_desc_sw128(stage(r.s));
+          const uint64_t bd = smem_desc_sw128(stage(r.s) + Cfg::A_BYTES);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {   // K = 32 per MMA: 32 bytes along the swizzled row
+            mma_f8_ss_pair(d, ad + 2u * j, bd + 2u * j, idesc, (kb > 0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit_pair(bars.empty(r.s), 0x3);
+          r.advance(Cfg::STAGES);
+        }
+        if (!ok) break;
+        mma_commit_pair(bars.accfull(racc.s), 0x3);
+        racc.advance(2);
+      }
+      mma_commit_pair(bars.done(), 0x1);
+      mbar_wait_bounded(bars.done(), 0u, 100000000ull);
+    }
+  } else if (warp >= Cfg::EPI_WARP0) {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - Cfg::EPI_WARP0;
+    const int quarter = warp & 3;
+    const int cg = ew >> 2;
+    const uint32_t stage_y = sbase + Cfg::OFF_EPI + static_cast<uint32_t>(ew) * 4096u;
+    const uint32_t accempty0 = rank == 0 ? bars.accempty(0) : mapa_shared(bars.accempty(0), 0);
+    Ring racc;
+    bool ok = true;
+    for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+      const int mp = tile % p.num_m_blk;
+      const int nb = tile / p.num_m_blk;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.accfull(racc.s), racc.ph, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(racc.s * Cfg::PAIR_N + cg * 128);
+      int acc[128];   // fp32 bit patterns
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + q4 * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[q4 * 32 + i] = static_cast<int>(r[i]);
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t bar = accempty0 + 8u * static_cast<uint32_t>(racc.s);
+        if (rank == 0) mbar_arrive(bar);
+        else mbar_arrive_cluster(bar);
+      }
+      racc.advance(2);
+      const int m_base = mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM + quarter * 32;
+      const int n_base = nb * Cfg::PAIR_N + cg * 128;
+      if (p.out_mode == kOutBf16) {
+        float f[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) f[i] = __int_as_float(acc[i]);
+        store_warp_tile_bf16<128, float>(p, &tmY, stage_y, lane, m_base, n_base, f);
+      } else {
+        store_warp_tile_s32<128>(&tmY, stage_y, lane, m_base, n_base, acc, 0);
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  __syncwarp();
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer's loads, MMAs and remote arrivals are finished
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace i8

@@ -14,6 +14,7 @@
 
 #include "../../include/i8.h"
 #include "gemm.cuh"
+#include "gemm_fp8.cuh"
 #include "gemm_pair.cuh"
 #include "skinny.cuh"
 #include "ptx.cuh"
@@ -145,14 +146,18 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 // ----------------------------------------------------------------- quant
 template <int V>
 cudaError_t launch_quant_v(const uint16_t* x, int64_t rows, int K, int64_t ldx, int8_t* q,
-                           int64_t ldq, float* s, int G, int R, cudaStream_t st) {
+                           int64_t ldq, float* s, int G, int R, int fmt, cudaStream_t st) {
   const int64_t grid = (rows + R - 1) / R;
+  if (fmt == kQuantE4M3)
+    return launch_pdl(quant_rows_kernel<V, kQuantE4M3>, dim3(static_cast<unsigned>(grid)),
+                      dim3(32 * G * R), 0, st, x, rows, K, ldx, q, ldq, s, G);
   return launch_pdl(quant_rows_kernel<V>, dim3(static_cast<unsigned>(grid)), dim3(32 * G * R), 0,
                     st, x, rows, K, ldx, q, ldq, s, G);
 }
 
+// fmt: kQuantInt8 (int8 codes) or kQuantE4M3 (E4M3 bit patterns).
 i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t* q, int64_t ldq,
-                     float* s, cudaStream_t st) {
+                     float* s, cudaStream_t st, int fmt = kQuantInt8) {
   if (rows < 0 || K <= 0 || ldx < K || ldq < K) return I8_ERR_INVALID_ARG;
   if (rows > 0 && (!x || !q || !s)) return I8_ERR_INVALID_ARG;
   if (K % 16 != 0 || K > 131072 || rows > INT32_MAX) return I8_ERR_UNSUPPORTED;
@@ -173,14 +178,24 @@ i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t
   const auto* xb = static_cast<const uint16_t*>(x);
   const int Ki = static_cast<int>(K);
   cudaError_t e;
-  if (need <= 1) e = launch_quant_v<1>(xb, rows, Ki, ldx, q, ldq, s, G, R, st);
-  else if (need <= 2) e = launch_quant_v<2>(xb, rows, Ki, ldx, q, ldq, s, G, R, st);
-  else if (need <= 3) e = launch_quant_v<3>(xb, rows, Ki, ldx, q, ldq, s, G, R, st);
-  else if (need <= 4) e = launch_quant_v<4>(xb, rows, Ki, ldx, q, ldq, s, G, R, st);
-  else if (need <= 6) e = launch_quant_v<6>(xb, rows, Ki, ldx, q, ldq, s, G, R, st);
-  else if (need <= 8) e = launch_quant_v<8>(xb, rows, Ki, ldx, q, ldq, s, G, R, st);
-  else if (need <= 12) e = launch_quant_v<12>(xb, rows, Ki, ldx, q, ldq, s, G, R, st);
-  else e = launch_quant_v<16>(xb, rows, Ki, ldx, q, ldq, s, G, R, st);
+  if (need > 16) {
+    // longer than 8 warps x 32 lanes x 16 vectors: the two-pass kernel
+    if (fmt == kQuantE4M3)
+      e = launch_pdl(quant_rows_long_kernel<kQuantE4M3>, dim3(static_cast<unsigned>(rows)),
+                     dim3(256), 0, st, xb, rows, Ki, ldx, q, ldq, s);
+    else
+      e = launch_pdl(quant_rows_long_kernel<kQuantInt8>, dim3(static_cast<unsigned>(rows)),
+                     dim3(256), 0, st, xb, rows, Ki, ldx, q, ldq, s);
+    return cuda_status(e);
+  }
+  if (need <= 1) e = launch_quant_v<1>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);
+  else if (need <= 2) e = launch_quant_v<2>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);
+  else if (need <= 3) e = launch_quant_v<3>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);
+  else if (need <= 4) e = launch_quant_v<4>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);
+  else if (need <= 6) e = launch_quant_v<6>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);
+  else if (need <= 8) e = launch_quant_v<8>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);
+  else if (need <= 12) e = launch_quant_v<12>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);
+  else e = launch_quant_v<16>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);  // need <= 16
   return cuda_status(e);
 }
 
@@ -573,6 +588,84 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   return I8_OK;
 }
 
+// ----------------------------------------------------------------- E4M3 GEMM
+int fp8_cluster_capacity(DeviceInfo* d) {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return d->sms / 2;
+  if (cached[dev] > 0) return cached[dev];
+  auto kern = gemm_fp8_pair_kernel;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Fp8Cfg::SMEM_BYTES) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (d->sms / 2), 1, 1);
+    cfg.blockDim = dim3(Fp8Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Fp8Cfg::SMEM_BYTES;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  if (n <= 0) n = d->sms / 2;
+  cached[dev] = n;
+  return n;
+}
+
+// E4M3 codes in, bf16 (dequant + bias) or fp32 accumulators out.  One
+// persistent launch of the pair kernel; every shape uses 256 x 256 tiles
+// (rows and columns beyond M, N are zero-filled on load and clipped on store).
+i8_status gemm_fp8_common(const uint8_t* aq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
+                          int out_mode, void* out, int64_t ldo, const float* s_a,
+                          const float* s_w, const void* bias, cudaStream_t st) {
+  if (M < 0 || N < 0 || K <= 0) return I8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX) return I8_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return I8_OK;
+  if (!aq || !wq || !out || ldo < N) return I8_ERR_INVALID_ARG;
+  if (out_mode == kOutBf16 && (!s_a || !s_w)) return I8_ERR_INVALID_ARG;
+  if (!aligned16(aq) || !aligned16(wq) || !aligned16(out)) return I8_ERR_ALIGNMENT;
+  if (out_mode == kOutBf16 && (ldo % 8 != 0 || !aligned4(s_a) || !aligned16(s_w) ||
+                               (bias && !aligned16(bias))))
+    return I8_ERR_ALIGNMENT;
+  if (out_mode != kOutBf16 && ldo % 4 != 0) return I8_ERR_ALIGNMENT;
+  DeviceInfo* d;
+  if (i8_status e = device_info(&d, nullptr)) return e;
+  CUtensorMap ma, mb, my;
+  if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M, K, Fp8Cfg::BK, Fp8Cfg::BM) ||
+      !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, K, N, K, Fp8Cfg::BK, Fp8Cfg::BN))
+    return I8_ERR_CUDA;
+  if (!encode_out(&my, out_mode == kOutBf16, out, static_cast<uint64_t>(N),
+                  static_cast<uint64_t>(M), static_cast<uint64_t>(ldo), 1))
+    return I8_ERR_CUDA;
+  GemmParams gp{};
+  gp.M = static_cast<int>(M);
+  gp.N = static_cast<int>(N);
+  gp.K = static_cast<int>(K);
+  gp.num_m_blk = static_cast<int>((M + Fp8Cfg::PAIR_M - 1) / Fp8Cfg::PAIR_M);
+  gp.num_n_blk = static_cast<int>((N + Fp8Cfg::PAIR_N - 1) / Fp8Cfg::PAIR_N);
+  gp.splits = 1;
+  gp.total_kb = static_cast<int>((K + Fp8Cfg::BK - 1) / Fp8Cfg::BK);
+  gp.kb_per_split = gp.total_kb;
+  const int64_t tiles = static_cast<int64_t>(gp.num_m_blk) * gp.num_n_blk;
+  if (tiles > INT32_MAX) return I8_ERR_UNSUPPORTED;
+  gp.num_tiles = static_cast<int>(tiles);
+  gp.out_mode = out_mode;
+  gp.out = out;
+  gp.ldo = ldo;
+  gp.s_a = s_a;
+  gp.s_w = s_w;
+  gp.bias = static_cast<const uint16_t*>(bias);
+  const int clusters = fp8_cluster_capacity(d);
+  const int grid = 2 * static_cast<int>(std::min<int64_t>(clusters, tiles));
+  return cuda_status(launch_pdl(gemm_fp8_pair_kernel, dim3(grid), dim3(Fp8Cfg::THREADS),
+                                Fp8Cfg::SMEM_BYTES, st, ma, mb, my, gp));
+}
+
 // ----------------------------------------------------------------- no-alloc variant
 // Split-K scratch for i8_gemm_dequant_bias_bf16_noalloc: a fixed array in the
 // library's own device memory, so that entry point never allocates.  Every
@@ -628,6 +721,33 @@ i8_status i8_quant_weight_perchannel(const void* w, int64_t N, int64_t K, int64_
 i8_status i8_quant_act_pertoken(const void* x, int64_t M, int64_t K, int64_t ldx, int8_t* aq,
                                 int64_t ldq, float* s_a, i8_stream_t stream) {
   return quant_rows(x, M, K, ldx, aq, ldq, s_a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_quant_weight_perchannel_e4m3(const void* w, int64_t N, int64_t K, int64_t ldw,
+                                          uint8_t* wq, int64_t ldq, float* s_w,
+                                          i8_stream_t stream) {
+  return quant_rows(w, N, K, ldw, reinterpret_cast<int8_t*>(wq), ldq, s_w,
+                    reinterpret_cast<cudaStream_t>(stream), kQuantE4M3);
+}
+
+i8_status i8_quant_act_pertoken_e4m3(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                     uint8_t* aq, int64_t ldq, float* s_a, i8_stream_t stream) {
+  return quant_rows(x, M, K, ldx, reinterpret_cast<int8_t*>(aq), ldq, s_a,
+                    reinterpret_cast<cudaStream_t>(stream), kQuantE4M3);
+}
+
+i8_status i8_gemm_e4m3_f32(const uint8_t* aq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
+                           float* c, int64_t ldc, i8_stream_t stream) {
+  return gemm_fp8_common(aq, wq, M, N, K, kOutInt32, c, ldc, nullptr, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_gemm_e4m3_dequant_bias_bf16(const uint8_t* aq, const float* s_a, const uint8_t* wq,
+                                         const float* s_w, const void* bias, int64_t M,
+                                         int64_t N, int64_t K, void* y, int64_t ldy,
+                                         i8_stream_t stream) {
+  return gemm_fp8_common(aq, wq, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {

@@ -123,6 +123,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* desc, uint
       : "memory");
 }
 
+// The same load issued by either CTA of a pair, with completion signalled
+// on an mbarrier that may sit in the peer CTA: `bar_cluster` is a
+// shared::cluster address (mapa_shared), so both CTAs' loads of a stage can
+// count against the one barrier the MMA-issuing CTA waits on.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* desc,
+                                                 uint32_t bar_cluster, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 // 3-D tiled bulk tensor store from this CTA's shared memory (bulk-group
 // completion).  Parts of the box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const void* desc, uint32_t src, int c0, int c1, int c2) {
@@ -279,6 +292,17 @@ __device__ __forceinline__ void mma_f16_ss_pair(uint32_t d_tmem, uint64_t adesc,
       : "memory");
 }
 
+// The E4M3 form of mma_f16_ss_pair: kind::f8f6f4 with both operands E4M3
+// (K = 32 per instruction, 32 bytes of each operand row), fp32 D.
+__device__ __forceinline__ void mma_f8_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the mbarrier at offset `bar` in every CTA of `cta_mask` when
 // all prior tcgen05 operations of this thread have completed.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
@@ -356,6 +380,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 // operands K-major: D format (bits 4-5) = 1 (f32), A/B format (bits 7-9,
 // 10-12) = 0 (f16), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B and fp32 D,
+// both operands K-major.  The A/B format fields (bits 7-9, 10-12) code E4M3
+// as 0, so the word has the same bits as the fp16 one above; only the
+// instruction kind differs.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }

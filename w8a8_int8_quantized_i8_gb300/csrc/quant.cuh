@@ -117,6 +117,27 @@ __device__ __forceinline__ uint2 quant_vec8(uint4 v, float s, unsigned long long
   return make_uint2(low_bytes4(b[0], b[1], b[2], b[3]), low_bytes4(b[4], b[5], b[6], b[7]));
 }
 
+// Two fp32 values -> two E4M3 codes (lo in byte 0), round to nearest even,
+// finite saturation to +-448.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// 8 bf16 (one 16-byte vector) -> 8 E4M3 codes packed in two words, each
+// from the correctly rounded fp32 quotient x / s.
+__device__ __forceinline__ uint2 quant_vec8_e4m3(uint4 v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    c[i] = e4m3x2(__fdiv_rn(__uint_as_float(w[i] << 16), s),
+                  __fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), s));
+  }
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
 // Lane-wise max of |a| and |b| over bf16 pairs; the result's sign bits are
 // the xor of the inputs' signs and are masked off by the caller.
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
@@ -125,9 +146,12 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+enum QuantFmt : int { kQuantInt8 = 0, kQuantE4M3 = 1 };
+
 // Grid: ceil(rows / R) CTAs of 32 * G * R threads (G * R <= 8); warp w of a
 // CTA serves row (blockIdx.x * R + w / G), slice (w % G) of that row.
-template <int V>
+// FMT selects the code format (int8 or E4M3, one byte per element either way).
+template <int V, int FMT = kQuantInt8>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ x,
                                                          int64_t rows, int K, int64_t ldx,
                                                          int8_t* __restrict__ q, int64_t ldq,
@@ -173,7 +197,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
     for (int j = 0; j < G; ++j) abits = max(abits, red[g0 + j]);
   }
   const float amax = __uint_as_float(abits << 16);
-  const float s = __fdiv_rn(amax, 127.0f);
+  const float s = __fdiv_rn(amax, FMT == kQuantE4M3 ? 448.0f : 127.0f);
   if (valid_row && wig == 0 && lane == 0) scale[row] = s;
   if (!valid_row) return;
 
@@ -183,6 +207,17 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
     for (int i = 0; i < V; ++i) {
       const int e = slice0 + (i * 32 + lane) * 8;
       if (e < K) st_v2(qr + e, 0u, 0u);
+    }
+    return;
+  }
+  if constexpr (FMT == kQuantE4M3) {
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = slice0 + (i * 32 + lane) * 8;
+      if (e < K) {
+        const uint2 c = quant_vec8_e4m3(v[i], s);
+        st_v2(qr + e, c.x, c.y);
+      }
     }
     return;
   }
@@ -197,6 +232,64 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
       st_v2(qr + e, c.x, c.y);
     }
   }
+}
+
+}  // namespace i8
+
+namespace i8 {
+
+// Rows longer than the register-resident kernel covers (8 warps x 32 lanes x
+// 16 vectors x 8 = 32768 elements): one CTA of 256 threads per row, two
+// passes over the row -- absmax, then the codes -- with the second pass's
+// loads served mostly by L2.  The per-vector arithmetic is the same as the
+// resident kernel's, so the codes are the same.
+template <int FMT = kQuantInt8>
+__global__ void __launch_bounds__(256) quant_rows_long_kernel(const uint16_t* __restrict__ x,
+                                                              int64_t rows, int K, int64_t ldx,
+                                                              int8_t* __restrict__ q,
+                                                              int64_t ldq,
+                                                              float* __restrict__ scale) {
+  __shared__ uint32_t red[8];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = blockIdx.x;
+  pdl_wait();
+  if (row >= rows) return;
+  const uint16_t* xr = x + row * ldx;
+  const int vecs = K / 8;
+  uint32_t amax2 = 0;
+  for (int i = threadIdx.x; i < vecs; i += 256) {
+    const uint4 v = ld_stream_v4(xr + 8 * i);
+    amax2 = absmax_bf16x2(amax2, v.x);
+    amax2 = absmax_bf16x2(amax2, v.y);
+    amax2 = absmax_bf16x2(amax2, v.z);
+    amax2 = absmax_bf16x2(amax2, v.w);
+  }
+  amax2 &= 0x7FFF7FFFu;
+  uint32_t abits = max(amax2 & 0xFFFFu, amax2 >> 16);
+  abits = __reduce_max_sync(0xFFFFFFFFu, abits);
+  if (lane == 0) red[warp] = abits;
+  __syncthreads();
+  abits = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) abits = max(abits, red[j]);
+  const float amax = __uint_as_float(abits << 16);
+  const float s = __fdiv_rn(amax, FMT == kQuantE4M3 ? 448.0f : 127.0f);
+  if (threadIdx.x == 0) scale[row] = s;
+  int8_t* qr = q + row * ldq;
+  const bool fast = s >= 0x1p-126f;
+  const float r = __frcp_rn(s);
+  const unsigned long long rr = f2(r, r);
+  for (int i = threadIdx.x; i < vecs; i += 256) {
+    uint2 c = make_uint2(0u, 0u);
+    if (amax != 0.0f) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + 8 * i);
+      if constexpr (FMT == kQuantE4M3) c = quant_vec8_e4m3(v, s);
+      else c = quant_vec8(v, s, rr, fast);
+    }
+    st_v2(qr + 8 * i, c.x, c.y);
+  }
+  pdl_trigger();
 }
 
 }  // namespace i8
