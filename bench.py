@@ -54,6 +54,9 @@ L2_BYTES = 129 * 1024 * 1024
 # Dense INT8 rate of this GB300's legacy warp MMA (mma.sync s8 -> s32), the
 # chip's INT8 engine, measured by bench_engines.py (profiles/engine_rates.md).
 INT8_ENGINE_TOPS = 158.4
+# Nominal dense fp8 / bf16 tensor rate on GB300 (4.5 / 2.25 PF/s): the E4M3
+# arm's peak is the measured bf16 peak times this ratio.
+FP8_OVER_BF16 = 2.0
 ROTATE_MIN_BYTES = 3 * L2_BYTES
 
 
@@ -66,22 +69,39 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+# Committed ncu summaries per (arm, workload) and the kernel sources each
+# capture was taken from: the DRAM traffic is quoted only while the sources
+# still hash to the value recorded in the summary.
 PROFILE_SUMMARIES = {
-    "dit_qkv_768px_M2560_K3072_N9216": "gemm_w8a8_qkv768_M2560_K3072_N9216.md",
+    ("int8", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_w8a8_qkv768_M2560_K3072_N9216.md",
+    ("e4m3", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_fp8_qkv768_M2560_K3072_N9216.md",
 }
-KERNEL_SOURCES = ("w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
-                  "w8a8_int8_quantized_i8_gb300/csrc/gemm_pair.cuh",
-                  "w8a8_int8_quantized_i8_gb300/csrc/ptx.cuh",
-                  "w8a8_int8_quantized_i8_gb300/csrc/quant.cuh")
+KERNEL_SOURCES = {
+    "int8": ("w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
+             "w8a8_int8_quantized_i8_gb300/csrc/gemm_pair.cuh",
+             "w8a8_int8_quantized_i8_gb300/csrc/ptx.cuh",
+             "w8a8_int8_quantized_i8_gb300/csrc/quant.cuh"),
+    "e4m3": ("w8a8_int8_quantized_i8_gb300/csrc/gemm_fp8.cuh",
+             "w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
+             "w8a8_int8_quantized_i8_gb300/csrc/ptx.cuh"),
+}
 
 
-def _profiled_traffic(workload: str, weights: str):
-    """DRAM bytes per launch of the GEMM from the committed ncu summary, or
-    None when no summary covers this workload or the kernel sources changed
-    since the capture."""
+def kernel_sources_sha256(arm: str) -> str:
     import hashlib
-    name = PROFILE_SUMMARIES.get(workload)
-    if weights != "int8" or name is None:
+    h = hashlib.sha256()
+    for src in KERNEL_SOURCES[arm]:
+        with open(os.path.join(ROOT, src), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _profiled_traffic(workload: str, arm: str):
+    """DRAM bytes per launch of the arm's GEMM from the committed ncu summary,
+    or None when no summary covers this workload or the kernel sources
+    changed since the capture."""
+    name = PROFILE_SUMMARIES.get((arm, workload))
+    if name is None:
         return None
     path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
@@ -94,11 +114,7 @@ def _profiled_traffic(workload: str, weights: str):
                 fields[k.strip()] = v.strip()
     if fields.get("workload") != workload:
         return None
-    h = hashlib.sha256()
-    for src in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, src), "rb") as fh:
-            h.update(fh.read())
-    if fields.get("kernel_sources_sha256") != h.hexdigest():
+    if fields.get("kernel_sources_sha256") != kernel_sources_sha256(arm):
         return None
     try:
         return int(fields["traffic_bytes_per_launch"])
@@ -408,6 +424,14 @@ def run_ours(args, shape, dist, rank, world, local):
     e2e_ms = _max_over_ranks(dist, (time.perf_counter() - t0) * 1e3 / e2e_steps)
     e2e_val = _sum_over_ranks(dist, ops) / (e2e_ms * 1e-3) / 1e12
 
+    # ---- the E4M3 (FP8) arm on the same workload: per-token E4M3 quant +
+    # the fused E4M3 GEMM, timed the same way (headline pass without events,
+    # then a pass with events around each GEMM), rotating the same number of
+    # buffer sets.  Reported beside the int8 line, against the FP8 peak.
+    e4m3 = None
+    if not args.no_e4m3:
+        e4m3 = _run_e4m3(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, local)
+
     # ---- oracle on the host cores (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -430,7 +454,8 @@ def run_ours(args, shape, dist, rank, world, local):
                        "k_split": splits, "replicas": world},
             "roofline": {"bound": "tensor", "achieved": gemm_tops, "peak": tc_peak,
                          "unit": "TFLOP/s", "frac": gemm_tops / tc_peak,
-                         "traffic": _profiled_traffic(shape.name, args.weights),
+                         "traffic": (_profiled_traffic(shape.name, "int8")
+                                     if args.weights == "int8" else None),
                          "traffic_unit": "bytes per launch (ncu dram read + write)",
                          "kernel": "gemm_w8a8 (CTA-pair or single-CTA per the shape table)",
                          "peak_note": f"{peak_kind} dense bf16 burst (same nominal rate as the "
@@ -444,6 +469,7 @@ def run_ours(args, shape, dist, rank, world, local):
                              "steps (the headline pass has no events between kernels)",
             "vs_int8_engine": {"int8_tops_measured": INT8_ENGINE_TOPS, "gemm_ratio": gemm_tops / INT8_ENGINE_TOPS,
                                "source": "mma.sync m16n8k32 s8 rate on this GB300 (bench_engines.py)"},
+            "e4m3": e4m3,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TOPS", "h2d_bytes_per_step": M * K * 2,
                     "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
@@ -456,6 +482,77 @@ def run_ours(args, shape, dist, rank, world, local):
     return 0
 
 
+def _run_e4m3(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, local):
+    """The E4M3 arm: quant + fused GEMM steps on device-resident inputs."""
+    from w8a8_int8_quantized_i8_gb300 import binding
+    M, K, N = shape.M, shape.K, shape.N
+    vp = ctypes.c_void_p
+    wq, s_w = i8.quant_weight_perchannel_e4m3(d["w"].to(dev))
+    wq = wq.view(torch.uint8)
+    b_dev = d["bias"].to(dev)
+    sets = [dict(x=d["x"].to(dev), aq=torch.empty(M, K, dtype=torch.uint8, device=dev),
+                 s_a=torch.empty(M, dtype=torch.float32, device=dev),
+                 w=wq.clone(), y=torch.empty(M, N, dtype=torch.bfloat16, device=dev))
+            for _ in range(R)]
+    calls = [((vp(t["x"].data_ptr()), M, K, K, vp(t["aq"].data_ptr()), K, vp(t["s_a"].data_ptr()), sp),
+              (vp(t["aq"].data_ptr()), vp(t["s_a"].data_ptr()), vp(t["w"].data_ptr()),
+               vp(s_w.data_ptr()), vp(b_dev.data_ptr()), M, N, K, vp(t["y"].data_ptr()), N, sp))
+             for t in sets]
+    qf, gf = lib.i8_quant_act_pertoken_e4m3, lib.i8_gemm_e4m3_dequant_bias_bf16
+
+    def step(i, evg=None):
+        qa, ga = calls[i % R]
+        st = qf(*qa)
+        if evg is not None:
+            evg[0].record(stream)
+        st |= gf(*ga)
+        if evg is not None:
+            evg[1].record(stream)
+        if st:
+            raise RuntimeError(f"libi8 E4M3 call failed with status {st}")
+
+    steps = max(10, min(args.steps, 1000))
+    for i in range(max(3, args.warmup)):
+        step(i)
+    binding.sync_check(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    evg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        step(i, evg[i])
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    binding.sync_check(dev)
+    ops = 2.0 * M * N * K
+    t_ms = e0.elapsed_time(e1) / steps
+    g_ms = statistics.mean(a.elapsed_time(b) for a, b in evg)
+    peak = tc_peak * FP8_OVER_BF16
+    g_tflops = ops / (g_ms * 1e-3) / 1e12
+    return {
+        "value": ops / (t_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": t_ms, "steps": steps,
+        "dtype": "e4m3", "gemm_us": g_ms * 1e3,
+        "roofline": {"bound": "tensor", "achieved": g_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": g_tflops / peak, "traffic": _profiled_traffic(shape.name, "e4m3"),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)",
+                     "kernel": "gemm_fp8_pair_kernel",
+                     "peak_note": f"{peak_kind} dense bf16 burst x {FP8_OVER_BF16:g} "
+                                  "(nominal dense fp8 / bf16 rate: 4.5 / 2.25 PF/s)"},
+        "parity": "codes bit-exact; fp32 accumulators within the derived rounding bound of the "
+                  "exact sum; bf16 = oracle epilogue of the GPU accumulators, bit for bit",
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,6 +562,7 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qkv768")
     ap.add_argument("--weights", choices=["int8", "w16"], default="int8")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-e4m3", action="store_true", help="skip the E4M3 (FP8) arm")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
