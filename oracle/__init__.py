@@ -75,6 +75,12 @@ def _load():
             lib.orc_gemm_e4m3_f64.restype = ctypes.c_int
             lib.orc_dequant_bias_f64acc.argtypes = [vp, i64, vp, vp, vp, i64, i64, vp, i64]
             lib.orc_dequant_bias_f64acc.restype = ctypes.c_int
+            lib.orc_f64_to_bf16.argtypes = [ctypes.c_double]
+            lib.orc_f64_to_bf16.restype = ctypes.c_uint16
+            lib.orc_layernorm_rows.argtypes = [vp, i64, i64, i64, ctypes.c_double, vp, i64]
+            lib.orc_layernorm_rows.restype = ctypes.c_int
+            lib.orc_gelu_rows.argtypes = [vp, i64, i64, i64, vp, i64]
+            lib.orc_gelu_rows.restype = ctypes.c_int
             lib.orc_num_threads.argtypes = []
             lib.orc_num_threads.restype = ctypes.c_int
             lib.orc_set_num_threads.argtypes = [ctypes.c_int]
@@ -249,3 +255,40 @@ def linear_e4m3(x_bits, w_bits, bias_bits):
     acc = gemm_e4m3_f64(aq, wq)
     y = dequant_bias_f64acc(acc, s_a, s_w, bias_bits)
     return dict(aq=aq, s_a=s_a, wq=wq, s_w=s_w, acc=acc, y=y)
+
+
+# ---------------------------------------------------------------------- fused
+# The producer of a linear layer's input (LayerNorm without affine, or GELU),
+# in fp64 with one rounding to bf16, followed by the per-row quantizer of that
+# bf16 row (see the fused section of i8_oracle.h).
+
+def f64_to_bf16_bits(v: float) -> int:
+    return int(_load().orc_f64_to_bf16(float(v)))
+
+
+def layernorm_rows(x_bits, eps: float = 1e-6) -> np.ndarray:
+    """bf16 bits of the row-wise LayerNorm (no affine) of a bf16 matrix."""
+    x = _c2d(x_bits, np.uint16)
+    rows, K = x.shape
+    y = np.zeros((rows, K), dtype=np.uint16)
+    if _load().orc_layernorm_rows(_ptr(x), rows, K, K, float(eps), _ptr(y), K) != 0:
+        raise ValueError("orc_layernorm_rows rejected its arguments")
+    return y
+
+
+def gelu_rows(x_bits) -> np.ndarray:
+    """bf16 bits of GELU (erf form) of a bf16 matrix."""
+    x = _c2d(x_bits, np.uint16)
+    rows, K = x.shape
+    y = np.zeros((rows, K), dtype=np.uint16)
+    if _load().orc_gelu_rows(_ptr(x), rows, K, K, _ptr(y), K) != 0:
+        raise ValueError("orc_gelu_rows rejected its arguments")
+    return y
+
+
+def producer_quant_rows(x_bits, op: str, fmt: str = "int8", eps: float = 1e-6):
+    """LayerNorm (op="layernorm") or GELU (op="gelu") then the per-row
+    quantizer ("int8" or "e4m3").  Returns ``(y bf16 bits, q, scale)``."""
+    y = layernorm_rows(x_bits, eps) if op == "layernorm" else gelu_rows(x_bits)
+    q, s = quant_rows(y) if fmt == "int8" else quant_rows_e4m3(y)
+    return y, q, s

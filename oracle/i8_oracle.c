@@ -265,3 +265,72 @@ int orc_dequant_bias_f64acc(const double* c, int64_t ldc, const float* s_a,
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------ fused
+ * Pins (tests/test_oracle_fused.py): orc_f64_to_bf16 against exact rational
+ * rounding; LayerNorm against torch's fp64 layer_norm, against closed forms
+ * (symmetric rows, constant rows, power-of-two scaling) and its zero-mean /
+ * unit-variance invariants; GELU against torch's fp64 gelu and the identity
+ * gelu(x) - gelu(-x) = x. */
+
+uint16_t orc_f64_to_bf16(double v) {
+  double a, q, r;
+  int e2, lg;
+  uint16_t sign;
+  if (isnan(v)) return 0x7FC0;
+  sign = signbit(v) ? 0x8000 : 0x0000;
+  a = fabs(v);
+  if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+  if (a == 0.0) return sign;
+  /* quantum of a's binade: 2^(floor(log2 a) - 7); subnormal spacing 2^-133 */
+  frexp(a, &e2);
+  lg = e2 - 1;
+  if (lg < -126) lg = -126;
+  q = ldexp(1.0, lg - 7);
+  r = nearbyint(a / q) * q; /* a / q exact; ties to the even multiple */
+  {
+    float f = (float)r; /* r has at most 8 significant bits: exact in fp32 */
+    uint32_t u;
+    if (r > 3.3895313892515355e38) return (uint16_t)(sign | 0x7F80); /* overflow */
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (u >> 16));
+  }
+}
+
+int orc_layernorm_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
+                       double eps, uint16_t* y, int64_t ldy) {
+  if (rows < 0 || K <= 0 || ldx < K || ldy < K || !(eps >= 0.0)) return -1;
+  if (rows > 0 && (!x || !y)) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint16_t* xr = x + r * ldx;
+    uint16_t* yr = y + r * ldy;
+    double mu = 0.0, var = 0.0, rs;
+    for (int64_t k = 0; k < K; ++k) mu += (double)orc_bf16_to_f32(xr[k]);
+    mu /= (double)K;
+    for (int64_t k = 0; k < K; ++k) {
+      double d = (double)orc_bf16_to_f32(xr[k]) - mu;
+      var += d * d;
+    }
+    var /= (double)K;
+    rs = sqrt(var + eps);
+    for (int64_t k = 0; k < K; ++k) {
+      yr[k] = orc_f64_to_bf16(((double)orc_bf16_to_f32(xr[k]) - mu) / rs);
+    }
+  }
+  return 0;
+}
+
+int orc_gelu_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
+                  uint16_t* y, int64_t ldy) {
+  if (rows < 0 || K <= 0 || ldx < K || ldy < K) return -1;
+  if (rows > 0 && (!x || !y)) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t k = 0; k < K; ++k) {
+      double v = (double)orc_bf16_to_f32(x[r * ldx + k]);
+      y[r * ldy + k] = orc_f64_to_bf16(0.5 * v * (1.0 + erf(v / sqrt(2.0))));
+    }
+  }
+  return 0;
+}

@@ -95,6 +95,31 @@ int orc_dequant_bias_f64acc(const double* c, int64_t ldc, const float* s_a,
                             const float* s_w, const uint16_t* bias, int64_t M,
                             int64_t N, uint16_t* y, int64_t ldy);
 
+/* ------------------------------------------------------------------ fused
+ * The step before the linear layer.  The pages' argument for folding the
+ * dequantization into the GEMM epilogue is the memory trip it saves ([NEWS]
+ * mechanism paragraph); the same argument moves the per-token quantizer into
+ * the kernel that produces the layer's input: the LayerNorm in front of the
+ * QKV, attention-out and MLP-up projections of a DiT block, and the GELU in
+ * front of the MLP down-projection.  Definition: the producer's bf16 output,
+ * then the per-row quantizer of that bf16 row -- so the fused path gives
+ * exactly the codes of the unfused one whenever the bf16 rows agree. */
+
+/* fp64 -> bf16 bit pattern with a single rounding (nearest, ties to even). */
+uint16_t orc_f64_to_bf16(double v);
+
+/* LayerNorm without affine parameters, per row, in fp64:
+ *   mu = sum_k x_k / K,  var = sum_k (x_k - mu)^2 / K,
+ *   y_k = bf16((x_k - mu) / sqrt(var + eps)), rounded once.
+ * x, y: rows x K bf16 (row strides ldx, ldy).  Returns 0, or -1. */
+int orc_layernorm_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
+                       double eps, uint16_t* y, int64_t ldy);
+
+/* GELU (erf form) per element, in fp64:
+ *   y = bf16(0.5 * x * (1 + erf(x / sqrt(2)))), rounded once.  Returns 0, or -1. */
+int orc_gelu_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
+                  uint16_t* y, int64_t ldy);
+
 /* Threads the loops may use (OpenMP), or 1 when built without it. */
 int orc_num_threads(void);
 void orc_set_num_threads(int n);
