@@ -270,7 +270,8 @@ int orc_dequant_bias_f64acc(const double* c, int64_t ldc, const float* s_a,
  * Pins (tests/test_oracle_fused.py): orc_f64_to_bf16 against exact rational
  * rounding; LayerNorm against torch's fp64 layer_norm, against closed forms
  * (symmetric rows, constant rows, power-of-two scaling) and its zero-mean /
- * unit-variance invariants; GELU against torch's fp64 gelu and the identity
+ * unit-variance invariants; GELU against torch's fp64 gelu where that is
+ * accurate (x > -8), against x * scipy's normal CDF below, and the identity
  * gelu(x) - gelu(-x) = x. */
 
 uint16_t orc_f64_to_bf16(double v) {
@@ -328,8 +329,13 @@ int orc_gelu_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t k = 0; k < K; ++k) {
+      /* GELU(v) = v * Phi(v), Phi the standard normal CDF.  Phi(v) is
+       * (1 + erf(v / sqrt 2)) / 2 = erfc(-v / sqrt 2) / 2; the second form
+       * has no cancellation for v < 0 (the first rounds to 0 below about
+       * v = -8.3 even in fp64). */
       double v = (double)orc_bf16_to_f32(x[r * ldx + k]);
-      y[r * ldy + k] = orc_f64_to_bf16(0.5 * v * (1.0 + erf(v / sqrt(2.0))));
+      double phi = v >= 0.0 ? 0.5 * (1.0 + erf(v / sqrt(2.0))) : 0.5 * erfc(-v / sqrt(2.0));
+      y[r * ldy + k] = orc_f64_to_bf16(v * phi);
     }
   }
   return 0;

@@ -116,7 +116,8 @@ int orc_layernorm_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
                        double eps, uint16_t* y, int64_t ldy);
 
 /* GELU (erf form) per element, in fp64:
- *   y = bf16(0.5 * x * (1 + erf(x / sqrt(2)))), rounded once.  Returns 0, or -1. */
+ *   y = bf16(x * Phi(x)), Phi(x) = (1 + erf(x / sqrt 2)) / 2, evaluated as
+ *   erfc(-x / sqrt 2) / 2 for x < 0; rounded once.  Returns 0, or -1. */
 int orc_gelu_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
                   uint16_t* y, int64_t ldy);
 

@@ -4,14 +4,18 @@ something other than the oracle: torch's fp64 layer_norm / gelu, closed forms,
 invariants and the ordering of neighbouring bf16 values.
 
 A plausible slip -- a biased variance (K - 1), eps outside the square root, a
-double rounding through fp32, the tanh form of GELU, a truncating round --
-fails at least one of them.
+double rounding through fp32, the tanh form of GELU, the cancelling
+1 + erf(x / sqrt 2) in the negative tail, a truncating round -- fails at least
+one of them.
 """
 import math
 
 import numpy as np
 import pytest
 import torch
+
+scipy = pytest.importorskip("scipy")
+import scipy.special  # noqa: E402
 
 from w8a8_int8_quantized_i8_gb300 import inputs
 
@@ -117,10 +121,20 @@ def test_gelu_matches_torch_fp64_and_identity(orc):
     keep = np.isfinite(xf) & (np.abs(xf) < 1e4)
     vals = vals[keep]
     y = orc.gelu_rows(vals[None, :])[0]
-    ref = torch.nn.functional.gelu(torch.from_numpy(_f64(vals)), approximate="none").numpy()
+    xv = _f64(vals)
+    # torch's fp64 gelu evaluates 1 + erf(x / sqrt 2), which loses relative
+    # accuracy as x falls (about 1e-16 / Phi(x)) and cancels to 0 below about
+    # x = -8.3; below x = -5 the pin is x * Phi(x) from scipy's normal CDF
+    ref = torch.nn.functional.gelu(torch.from_numpy(xv), approximate="none").numpy()
+    tail = xv < -5.0
+    ref[tail] = xv[tail] * scipy.special.ndtr(xv[tail])
     got = _f64(y)
     tol = 2.0 ** -8 * np.abs(ref) * (1 + 1e-9) + 2.0 ** -134   # half the subnormal spacing
     assert np.all(np.abs(got - ref) <= tol)
+    # the tail is not flushed: gelu(-9.25) = -1.0e-19, gelu(-13.25) ~ -2.6e-39
+    t = inputs.bits(torch.tensor([[-9.25, -13.25]]).to(torch.bfloat16))
+    yt = _f64(orc.gelu_rows(t))[0]
+    assert -1.1e-19 < yt[0] < -0.9e-19 and yt[1] < 0
     # the tanh form differs by far more than that on [1, 3]
     x = np.linspace(1, 3, 64)
     tanh_form = 0.5 * x * (1 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3)))
