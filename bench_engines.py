@@ -15,7 +15,8 @@ Prints one JSON object per line:
     then a bf16 matmul + bias (all torch ops);
   inputs rotate over enough buffer sets to exceed 3x the 129 MB L2;
 * ``stack`` (with --stack): the linear-layer time per denoising step of the
-  synthetic 28-block DiT stack at 1024px batch 2 (M = 8704), glue excluded.
+  synthetic 28-block DiT stack at 1024px batch 2 (M = 8704), int8 and E4M3
+  codes, with torch LN/GELU glue and with the fused producer-quantizers.
 
 Usage: python bench_engines.py [--sweep] [--stack] [--no-engines] [--iters N]
 """
@@ -201,13 +202,16 @@ def shape_row(shape, iters, full=True):
     print(json.dumps(res), flush=True)
 
 
-def stack_time(blocks=28, M=8704, iters=5):
+def stack_time(blocks=28, M=8704, iters=5, fused=False, fmt="int8"):
     """Linear-layer time per denoising step of the synthetic 28-block DiT
-    stack at 1024px batch 2 (M = 8704): the sum over 112 layers of per-token
-    quant + fused GEMM, timed with CUDA events around each layer; the glue
-    (LayerNorm, GELU, V slice) is excluded."""
+    stack at 1024px batch 2 (M = 8704): the sum over 112 layers of each
+    layer's quantizer and fused GEMM, timed with CUDA events around each
+    layer.  Unfused, the glue (LayerNorm, GELU, V slice) runs in torch between
+    the timed layers; fused, the LayerNorm / GELU in front of each layer runs
+    inside the timed producer-quantizer kernel and only the block-output LN
+    stays outside.  step_ms_with_glue is the whole forward either way."""
     from w8a8_int8_quantized_i8_gb300 import dit_stack
-    stack = dit_stack.build(blocks=blocks, seed=5)
+    stack = dit_stack.build(blocks=blocks, seed=5, fmt=fmt)
     h = inputs.activations(M, dit_stack.WIDTH, torch.Generator().manual_seed(5)).to("cuda")
     events = []
 
@@ -216,7 +220,7 @@ def stack_time(blocks=28, M=8704, iters=5):
         ev.record()
         events.append(ev)
 
-    dit_stack.forward(stack, h)  # warm-up
+    dit_stack.forward(stack, h, fused=fused)  # warm-up
     torch.cuda.synchronize()
     lin, tot = [], []
     for _ in range(iters):
@@ -224,17 +228,30 @@ def stack_time(blocks=28, M=8704, iters=5):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        dit_stack.forward(stack, h, timer=timer)
+        dit_stack.forward(stack, h, timer=timer, fused=fused)
         e1.record()
         torch.cuda.synchronize()
         lin.append(sum(events[i].elapsed_time(events[i + 1]) for i in range(0, len(events), 2)))
         tot.append(e0.elapsed_time(e1))
     i8.sync_check()
+    # whole forward without per-layer events
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        dit_stack.forward(stack, h, fused=fused)
+    e1.record()
+    torch.cuda.synchronize()
     ops = 2.0 * M * blocks * sum(K * N for _, K, N in dit_stack.LAYERS)
     lin_ms = sorted(lin)[len(lin) // 2]
-    print(json.dumps({"stack": f"dit_1024px_b2_{blocks}blocks_M{M}", "linear_ms_per_step": lin_ms,
-                      "step_ms_with_glue": sorted(tot)[len(tot) // 2], "layers": 4 * blocks,
+    print(json.dumps({"stack": f"dit_1024px_b2_{blocks}blocks_M{M}", "codes": fmt,
+                      "producers": "fused LN/GELU + quant" if fused else "torch LN/GELU, separate quant",
+                      "linear_ms_per_step": lin_ms,
+                      "step_ms_with_glue": sorted(tot)[len(tot) // 2],
+                      "step_ms_no_events": e0.elapsed_time(e1) / iters, "layers": 4 * blocks,
                       "linear_tops": ops / (lin_ms * 1e-3) / 1e12}), flush=True)
+    del stack
+    torch.cuda.empty_cache()
 
 
 def main(argv=None):
@@ -253,7 +270,9 @@ def main(argv=None):
         for shape in inputs.sweep_shapes():
             shape_row(shape, args.iters, full=True)
     if args.stack:
-        stack_time()
+        for fmt in ("int8", "e4m3"):
+            for fused in (False, True):
+                stack_time(fused=fused, fmt=fmt)
     return 0
 
 

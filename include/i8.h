@@ -161,6 +161,38 @@ i8_status i8_gemm_e4m3_dequant_bias_bf16(const uint8_t* aq, const float* s_a,
                                          int64_t N, int64_t K, void* y,
                                          int64_t ldy, i8_stream_t stream);
 
+/* ------------------------------------------------------------------ fused producers
+ * The per-token quantizer fused into the kernel that produces a linear
+ * layer's input (arXiv 2606.14598 folds the dequantization into the GEMM to
+ * save a memory trip -- aiexpert.news mechanism paragraph; the same argument
+ * applies to the step before the GEMM).  In a DiT block the QKV,
+ * attention-out and MLP-up inputs are LayerNorm outputs and the MLP-down
+ * input is a GELU output.
+ *   result:  y = bf16(producer(x)) per row, then the per-row quantizer of y
+ *            (int8 or E4M3 per fmt) -- the codes the separate quantizer gives
+ *            for that bf16 row.
+ *   LayerNorm: no affine parameters, mu and the biased variance over the row,
+ *            y = bf16((x - mu) / sqrt(var + eps)); reductions in fp32, so y may
+ *            differ from the exactly rounded value by one bf16 step where it
+ *            lies within fp32 noise of a rounding midpoint.
+ *   GELU:    erf form, y = bf16(0.5 x (1 + erf(x / sqrt 2))), fp32 arithmetic.
+ *   x [M,K] bf16 (row stride ldx elements, ldx % 8 == 0), q [M,K] codes (int8
+ *   or E4M3 bit patterns, row stride ldq bytes, ldq % 16 == 0), s_a [M] fp32;
+ *   y [M,K] bf16 or NULL: when given, receives the bf16 producer output (for
+ *   checking, or when the layer's input is also needed elsewhere).
+ *   K % 16 == 0 and K <= 32768 (the row is held in registers); larger K is
+ *   I8_ERR_UNSUPPORTED.  eps >= 0 and finite.  fmt: i8_code_format.        */
+typedef enum { I8_CODES_INT8 = 0, I8_CODES_E4M3 = 1 } i8_code_format;
+i8_status i8_layernorm_quant_act_pertoken(const void* x_bf16, int64_t M,
+                                          int64_t K, int64_t ldx, float eps,
+                                          int fmt, void* q, int64_t ldq,
+                                          float* s_a, void* y_bf16,
+                                          int64_t ldy, i8_stream_t stream);
+i8_status i8_gelu_quant_act_pertoken(const void* x_bf16, int64_t M, int64_t K,
+                                     int64_t ldx, int fmt, void* q,
+                                     int64_t ldq, float* s_a, void* y_bf16,
+                                     int64_t ldy, i8_stream_t stream);
+
 /* i8_gemm_dequant_bias_bf16 for callers that cannot allocate device memory
  * at call time -- for example a plugin running inside another runtime that
  * offers no workspace hook, an application whose device memory is all owned

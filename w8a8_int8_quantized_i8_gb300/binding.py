@@ -73,6 +73,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "i8_quant_act_pertoken_e4m3": ([vp, i64, i64, i64, vp, i64, vp, vp], st),
             "i8_gemm_e4m3_f32": ([vp, vp, i64, i64, i64, vp, i64, vp], st),
             "i8_gemm_e4m3_dequant_bias_bf16": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp], st),
+            "i8_layernorm_quant_act_pertoken": ([vp, i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                                                 vp, i64, vp, vp, i64, vp], st),
+            "i8_gelu_quant_act_pertoken": ([vp, i64, i64, i64, ctypes.c_int, vp, i64, vp, vp, i64,
+                                            vp], st),
             "i8_sync_check": ([vp], st),
             "i8_selftest_timeout": ([ctypes.c_int, vp], st),
         }
@@ -301,6 +305,51 @@ def linear_e4m3(x, wq, s_w, bias=None, out=None):
     """The E4M3 linear layer: per-token E4M3 quant of x, then the fused GEMM."""
     aq, s_a = quant_act_pertoken_e4m3(x)
     return gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, bias, out=out)
+
+
+# ---------------------------------------------------------------------- fused producers
+# LayerNorm (no affine) or GELU of each row, then the per-row quantizer of the
+# bf16 result, in one kernel: the codes of the next linear layer's input
+# without writing and re-reading that input in bf16.
+
+_FMT = {"int8": (0, torch.int8), "e4m3": (1, torch.float8_e4m3fn)}
+
+
+def _producer(fn_name, x, extra, fmt, want_y):
+    # x may be a row-strided view (e.g. a column slice of a wider output):
+    # unit stride along K, any row stride the library accepts
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise TypeError("x must be a 2-D bf16 CUDA tensor")
+    if x.shape[1] > 1 and x.stride(1) != 1:
+        raise ValueError("x must have unit stride along K")
+    ldx = x.stride(0) if x.shape[0] > 1 else x.shape[1]
+    if ldx < x.shape[1]:
+        raise ValueError("x rows overlap")
+    if fmt not in _FMT:
+        raise ValueError(f"fmt must be one of {sorted(_FMT)}")
+    code, dtype = _FMT[fmt]
+    R, K = x.shape
+    q = torch.empty((R, K), dtype=dtype, device=x.device)
+    s = torch.empty((R,), dtype=torch.float32, device=x.device)
+    y = torch.empty((R, K), dtype=torch.bfloat16, device=x.device) if want_y else None
+    lib = load()
+    with torch.cuda.device(x.device):
+        _check(getattr(lib, fn_name)(_ptr(x), R, K, ldx, *extra, code, _ptr(q), K, _ptr(s), _ptr(y),
+                                     K if want_y else 0, _stream(x)), fn_name)
+    return (q, s, y) if want_y else (q, s)
+
+
+def layernorm_quant_act_pertoken(x: torch.Tensor, eps: float = 1e-6, fmt: str = "int8",
+                                 want_y: bool = False):
+    """bf16 [M,K] -> codes of LayerNorm(x) (no affine) per token, with scales
+    (and the bf16 LayerNorm output when ``want_y``)."""
+    return _producer("i8_layernorm_quant_act_pertoken", x, (ctypes.c_float(eps),), fmt, want_y)
+
+
+def gelu_quant_act_pertoken(x: torch.Tensor, fmt: str = "int8", want_y: bool = False):
+    """bf16 [M,K] -> codes of GELU(x) (erf form) per token, with scales (and
+    the bf16 GELU output when ``want_y``)."""
+    return _producer("i8_gelu_quant_act_pertoken", x, (), fmt, want_y)
 
 
 def set_option(name: str, value: int) -> None:

@@ -16,6 +16,7 @@
 #include "gemm.cuh"
 #include "gemm_fp8.cuh"
 #include "gemm_pair.cuh"
+#include "producer.cuh"
 #include "skinny.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
@@ -196,6 +197,65 @@ i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t
   else if (need <= 8) e = launch_quant_v<8>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);
   else if (need <= 12) e = launch_quant_v<12>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);
   else e = launch_quant_v<16>(xb, rows, Ki, ldx, q, ldq, s, G, R, fmt, st);  // need <= 16
+  return cuda_status(e);
+}
+
+// ----------------------------------------------------------------- producer + quant
+template <int V, int FMT>
+cudaError_t launch_producer_v(int op, const uint16_t* x, int64_t rows, int K, int64_t ldx,
+                              float eps, int8_t* q, int64_t ldq, float* s, uint16_t* y,
+                              int64_t ldy, int G, cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>(rows)), block(32 * G);
+  if (op == kOpLayerNorm)
+    return launch_pdl(producer_quant_kernel<V, FMT, kOpLayerNorm>, grid, block, 0, st, x, rows, K,
+                      ldx, eps, q, ldq, s, y, ldy, G);
+  return launch_pdl(producer_quant_kernel<V, FMT, kOpGelu>, grid, block, 0, st, x, rows, K, ldx,
+                    eps, q, ldq, s, y, ldy, G);
+}
+
+template <int FMT>
+cudaError_t launch_producer(int op, const uint16_t* x, int64_t rows, int K, int64_t ldx, float eps,
+                            int8_t* q, int64_t ldq, float* s, uint16_t* y, int64_t ldy, int need,
+                            int G, cudaStream_t st) {
+  if (need <= 1) return launch_producer_v<1, FMT>(op, x, rows, K, ldx, eps, q, ldq, s, y, ldy, G, st);
+  if (need <= 2) return launch_producer_v<2, FMT>(op, x, rows, K, ldx, eps, q, ldq, s, y, ldy, G, st);
+  if (need <= 3) return launch_producer_v<3, FMT>(op, x, rows, K, ldx, eps, q, ldq, s, y, ldy, G, st);
+  if (need <= 4) return launch_producer_v<4, FMT>(op, x, rows, K, ldx, eps, q, ldq, s, y, ldy, G, st);
+  if (need <= 6) return launch_producer_v<6, FMT>(op, x, rows, K, ldx, eps, q, ldq, s, y, ldy, G, st);
+  if (need <= 8) return launch_producer_v<8, FMT>(op, x, rows, K, ldx, eps, q, ldq, s, y, ldy, G, st);
+  if (need <= 12) return launch_producer_v<12, FMT>(op, x, rows, K, ldx, eps, q, ldq, s, y, ldy, G, st);
+  return launch_producer_v<16, FMT>(op, x, rows, K, ldx, eps, q, ldq, s, y, ldy, G, st);
+}
+
+// LayerNorm / GELU of each row, then the per-row quantizer of the bf16
+// result; y (optional) receives that bf16 result.  Rows must fit the
+// register-resident layout: K <= 32768.
+i8_status producer_quant(int op, const void* x, int64_t rows, int64_t K, int64_t ldx, float eps,
+                         int fmt, void* q, int64_t ldq, float* s, void* y, int64_t ldy,
+                         cudaStream_t st) {
+  if (rows < 0 || K <= 0 || ldx < K || ldq < K || (y && ldy < K)) return I8_ERR_INVALID_ARG;
+  if (fmt != kQuantInt8 && fmt != kQuantE4M3) return I8_ERR_INVALID_ARG;
+  if (op == kOpLayerNorm && !(eps >= 0.0f && eps <= 3.0e38f)) return I8_ERR_INVALID_ARG;
+  if (rows > 0 && (!x || !q || !s)) return I8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || K > 32768 || rows > INT32_MAX) return I8_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(q) || !aligned4(s) || ldx % 8 != 0 || ldq % 16 != 0 ||
+      (y && (!aligned16(y) || ldy % 8 != 0)))
+    return I8_ERR_ALIGNMENT;
+  if (rows == 0) return I8_OK;
+  DeviceInfo* d;
+  if (i8_status e = device_info(&d, nullptr)) return e;
+  const int vecs = static_cast<int>(K / 8);
+  int G = 1;
+  while (G < 8 && (vecs + 32 * G - 1) / (32 * G) > g_opt.quant_vpl) G *= 2;
+  const int need = (vecs + 32 * G - 1) / (32 * G);
+  const auto* xb = static_cast<const uint16_t*>(x);
+  auto* qb = static_cast<int8_t*>(q);
+  auto* yb = static_cast<uint16_t*>(y);
+  const int Ki = static_cast<int>(K);
+  const cudaError_t e =
+      fmt == kQuantE4M3
+          ? launch_producer<kQuantE4M3>(op, xb, rows, Ki, ldx, eps, qb, ldq, s, yb, ldy, need, G, st)
+          : launch_producer<kQuantInt8>(op, xb, rows, Ki, ldx, eps, qb, ldq, s, yb, ldy, need, G, st);
   return cuda_status(e);
 }
 
@@ -748,6 +808,20 @@ i8_status i8_gemm_e4m3_dequant_bias_bf16(const uint8_t* aq, const float* s_a, co
                                          i8_stream_t stream) {
   return gemm_fp8_common(aq, wq, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_layernorm_quant_act_pertoken(const void* h, int64_t M, int64_t K, int64_t ldh,
+                                          float eps, int fmt, void* q, int64_t ldq, float* s_a,
+                                          void* y, int64_t ldy, i8_stream_t stream) {
+  return producer_quant(kOpLayerNorm, h, M, K, ldh, eps, fmt, q, ldq, s_a, y, ldy,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_gelu_quant_act_pertoken(const void* u, int64_t M, int64_t K, int64_t ldu, int fmt,
+                                     void* q, int64_t ldq, float* s_a, void* y, int64_t ldy,
+                                     i8_stream_t stream) {
+  return producer_quant(kOpGelu, u, M, K, ldu, 0.0f, fmt, q, ldq, s_a, y, ldy,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
