@@ -23,6 +23,7 @@ Usage: python bench_engines.py [--sweep] [--stack] [--no-engines] [--iters N]
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import subprocess
@@ -202,6 +203,55 @@ def shape_row(shape, iters, full=True):
     print(json.dumps(res), flush=True)
 
 
+def producer_rates(iters=20):
+    """The fused producer-quantizers against the unfused path they replace
+    (torch LayerNorm / GELU writing bf16, then the separate quantizer), at the
+    DiT inputs: LN at M = 8704, K = 3072 (QKV / out / up) and GELU at M = 8704,
+    K = 12288 (down), int8 codes.  Inputs rotate over sets larger than 3 x L2.
+    Fused bytes: 2 MK read + MK written + 4 M; unfused: the torch op's 2 MK
+    read + 2 MK written, then the quantizer's 3 MK + 4 M."""
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {"hbm_gbs": 6800.0}
+    hbm = float(peaks["hbm_gbs"])
+    for op, K in (("layernorm", 3072), ("gelu", 12288)):
+        M = 8704
+        R = max(2, -(-3 * 129 * 2 ** 20 // (M * K * 3)))
+        xs = [inputs.activations(M, K, torch.Generator().manual_seed(11 + r)).to("cuda") for r in range(R)]
+        qs = [torch.empty(M, K, dtype=torch.int8, device="cuda") for _ in range(R)]
+        ss = [torch.empty(M, dtype=torch.float32, device="cuda") for _ in range(R)]
+        lib = i8.load()
+        vp = ctypes.c_void_p
+
+        def fused(i):
+            st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            x, q, s = xs[i % R], qs[i % R], ss[i % R]
+            if op == "layernorm":
+                rc = lib.i8_layernorm_quant_act_pertoken(vp(x.data_ptr()), M, K, K, ctypes.c_float(1e-6), 0,
+                                                         vp(q.data_ptr()), K, vp(s.data_ptr()), None, 0, st)
+            else:
+                rc = lib.i8_gelu_quant_act_pertoken(vp(x.data_ptr()), M, K, K, 0, vp(q.data_ptr()), K,
+                                                    vp(s.data_ptr()), None, 0, st)
+            assert rc == 0
+
+        def unfused(i):
+            x = xs[i % R]
+            y = (torch.nn.functional.layer_norm(x, (K,), eps=1e-6) if op == "layernorm"
+                 else torch.nn.functional.gelu(x, approximate="none"))
+            i8.quant_act_pertoken(y, q=qs[i % R], s=ss[i % R])
+
+        t_f = _time(fused, iters)
+        t_u = _time(unfused, iters)
+        b_f = 3.0 * M * K + 4.0 * M
+        b_u = 4.0 * M * K + 3.0 * M * K + 4.0 * M
+        print(json.dumps({"producer": op, "M": M, "K": K, "codes": "int8",
+                          "fused_us": t_f * 1e6, "fused_gbs": b_f / t_f / 1e9,
+                          "fused_frac_hbm": b_f / t_f / 1e9 / hbm,
+                          "unfused_us": t_u * 1e6, "unfused_gbs": b_u / t_u / 1e9,
+                          "speedup": t_u / t_f, "hbm_peak_gbs": hbm}), flush=True)
+        del xs, qs, ss
+        torch.cuda.empty_cache()
+
+
 def stack_time(blocks=28, M=8704, iters=5, fused=False, fmt="int8"):
     """Linear-layer time per denoising step of the synthetic 28-block DiT
     stack at 1024px batch 2 (M = 8704): the sum over 112 layers of each
@@ -260,12 +310,18 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=30)
     ap.add_argument("--no-engines", action="store_true")
     ap.add_argument("--stack", action="store_true", help="time the 28-block DiT linear stack")
+    ap.add_argument("--producers", action="store_true",
+                    help="time the fused LayerNorm/GELU + quant kernels against the unfused path")
+    ap.add_argument("--no-shapes", action="store_true", help="skip the three DiT layer rows")
     args = ap.parse_args(argv)
     i8.load()
     if not args.no_engines:
         engine_rates()
-    for shape in (inputs.QKV_768, inputs.MLP_UP_1024, inputs.MLP_DOWN_1024):
-        shape_row(shape, args.iters)
+    if not args.no_shapes:
+        for shape in (inputs.QKV_768, inputs.MLP_UP_1024, inputs.MLP_DOWN_1024):
+            shape_row(shape, args.iters)
+    if args.producers:
+        producer_rates()
     if args.sweep:
         for shape in inputs.sweep_shapes():
             shape_row(shape, args.iters, full=True)

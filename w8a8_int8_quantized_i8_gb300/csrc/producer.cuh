@@ -14,7 +14,7 @@
 //   LayerNorm (no affine): mu = sum x / K, var = sum (x - mu)^2 / K,
 //                          y = bf16((x - mu) * (1 / sqrt(var + eps)))
 //   GELU (erf form):       y = bf16(0.5 x (1 + erf(x / sqrt 2))), evaluated as
-//                          0.5 x erfc(-x / sqrt 2) for x < 0 (no cancellation)
+//                          x * Phi(x) from one erfc(|x| / sqrt 2) (no cancellation)
 // The reductions run in fp32 (per-lane, then warp shuffles, then across the
 // row's warps), so y can differ from the oracle's fp64 value rounded once by
 // one bf16 step where that value lies within fp32 noise of a rounding
@@ -45,13 +45,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&t);
 }
 
-// GELU in erf form.  For x < 0 the factor 1 + erf(x / sqrt 2) cancels (it is
-// 6e-5 at x = -4 and 6e-7 at x = -5, where fp32 resolves only 6e-8 near 1),
-// so that branch uses the complementary function, erfc(-x / sqrt 2), which
-// equals it without the cancellation.
+// GELU in erf form, x * Phi(x) with Phi the standard normal CDF.  With
+// t = erfc(|x| / sqrt 2): Phi(x) = 1 - t / 2 for x >= 0 and t / 2 for x < 0.
+// One erfc per element, the same call on every lane (no divergent branch),
+// and no cancellation: the naive 1 + erf(x / sqrt 2) is 6e-7 at x = -5,
+// where fp32 resolves only 6e-8 near 1.
 __device__ __forceinline__ float gelu_erf(float x) {
   constexpr float kRsqrt2 = 0.70710678118654752f;
-  return x >= 0.0f ? 0.5f * x * (1.0f + erff(x * kRsqrt2)) : 0.5f * x * erfcf(-x * kRsqrt2);
+  const float t = erfcf(fabsf(x) * kRsqrt2);
+  const float phi = x >= 0.0f ? 1.0f - 0.5f * t : 0.5f * t;
+  return x * phi;
 }
 
 // Sum over the CTA's G warps (every warp gets the total).  Each reduction
