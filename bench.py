@@ -490,13 +490,16 @@ def _run_e4m3(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, l
     wq, s_w = i8.quant_weight_perchannel_e4m3(d["w"].to(dev))
     wq = wq.view(torch.uint8)
     b_dev = d["bias"].to(dev)
+    ws_bytes = i8.e4m3_workspace_bytes(M, N, K)
     sets = [dict(x=d["x"].to(dev), aq=torch.empty(M, K, dtype=torch.uint8, device=dev),
                  s_a=torch.empty(M, dtype=torch.float32, device=dev),
-                 w=wq.clone(), y=torch.empty(M, N, dtype=torch.bfloat16, device=dev))
+                 w=wq.clone(), y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+                 ws=torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev))
             for _ in range(R)]
     calls = [((vp(t["x"].data_ptr()), M, K, K, vp(t["aq"].data_ptr()), K, vp(t["s_a"].data_ptr()), sp),
               (vp(t["aq"].data_ptr()), vp(t["s_a"].data_ptr()), vp(t["w"].data_ptr()),
-               vp(s_w.data_ptr()), vp(b_dev.data_ptr()), M, N, K, vp(t["y"].data_ptr()), N, sp))
+               vp(s_w.data_ptr()), vp(b_dev.data_ptr()), M, N, K, vp(t["y"].data_ptr()), N,
+               vp(t["ws"].data_ptr()), ws_bytes, sp))
              for t in sets]
     qf, gf = lib.i8_quant_act_pertoken_e4m3, lib.i8_gemm_e4m3_dequant_bias_bf16
 

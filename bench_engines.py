@@ -187,6 +187,28 @@ def shape_row(shape, iters, full=True):
     res["gemm_int8_tops"] = ops / (res["gemm_int8_us"] * 1e-6) / 1e12
     res["gemm_w16_tops"] = ops / (res["gemm_w16_us"] * 1e-6) / 1e12
     res["step_int8_tops"] = ops / (res["step_int8_us"] * 1e-6) / 1e12
+    # the E4M3 arm on the same inputs
+    wq8, s_w8 = i8.quant_weight_perchannel_e4m3(w)
+    aq8 = [torch.empty(M, K, dtype=torch.float8_e4m3fn, device=dev) for _ in range(R)]
+    sa8 = [torch.empty(M, dtype=torch.float32, device=dev) for _ in range(R)]
+    for r in range(R):
+        i8.quant_act_pertoken_e4m3(xs[r], aq8[r], sa8[r])
+    ws8 = torch.empty(max(i8.e4m3_workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=dev)
+
+    def step8(i):
+        r = i % R
+        i8.quant_act_pertoken_e4m3(xs[r], aq8[r], sa8[r])
+        i8.gemm_e4m3_dequant_bias_bf16(aq8[r], sa8[r], wq8, s_w8, b, out=ys[r], workspace=ws8)
+
+    def gemm8(i):
+        r = i % R
+        i8.gemm_e4m3_dequant_bias_bf16(aq8[r], sa8[r], wq8, s_w8, b, out=ys[r], workspace=ws8)
+
+    res["step_e4m3_us"] = _time(step8, iters) * 1e6
+    res["gemm_e4m3_us"] = _time(gemm8, iters) * 1e6
+    i8.sync_check()
+    res["gemm_e4m3_tflops"] = ops / (res["gemm_e4m3_us"] * 1e-6) / 1e12
+    res["e4m3_k_splits"] = "yes" if i8.e4m3_workspace_bytes(M, N, K) else "no"
     if full:
         wt = w.t()
         res["torch_bf16_us"] = _time(lambda i: torch.addmm(b, xs[i % R], wt, out=ys[i % R]), iters) * 1e6

@@ -137,29 +137,41 @@ i8_status i8_quant_act_pertoken_e4m3(const void* x_bf16, int64_t M,
                                      int64_t ldq, float* s_a,
                                      i8_stream_t stream);
 
+/* Workspace bytes the two E4M3 GEMM calls below need for this shape on the
+ * current device: 0 when the shape runs without a K split, else the fp32
+ * partials of the split (splits x M x round_up(N, 4) x 4 bytes).  Returns 0
+ * for shapes the GEMM rejects. */
+size_t i8_gemm_e4m3_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
 /* fp32 accumulators of the E4M3 GEMM, for checking:
  *   c[m,n] = sum_k a[m,k] * w[n,k] over the decoded E4M3 codes, accumulated
  *   by the tensor core in fp32 (rounded; the order of its additions is not
  *   specified, so the result is within the fp32 accumulation bound of the
- *   exact sum, not bit-identical to a sequential loop).
+ *   exact sum, not bit-identical to a sequential loop).  When the shape's
+ *   plan splits K, the splits' fp32 partials are added in split order (a
+ *   fixed order: repeated calls give the same bits).
  *   aq [M,K], wq [N,K] E4M3 codes, contiguous (row stride K bytes)
  *   c  [M,N] fp32, row stride ldc elements (ldc >= N, ldc % 4 == 0)
- *   K % 16 == 0, K <= 131072.  Needs no workspace.                         */
+ *   ws / ws_bytes: device workspace of at least
+ *   i8_gemm_e4m3_workspace_bytes() (may be NULL when that is 0);
+ *   I8_ERR_WORKSPACE when it is too small.
+ *   K % 16 == 0, K <= 131072.                                              */
 i8_status i8_gemm_e4m3_f32(const uint8_t* aq, const uint8_t* wq, int64_t M,
                            int64_t N, int64_t K, float* c, int64_t ldc,
-                           i8_stream_t stream);
+                           void* ws, size_t ws_bytes, i8_stream_t stream);
 
 /* The fused E4M3 GEMM: the fp32 accumulator above, then the same epilogue
  * as i8_gemm_dequant_bias_bf16:
  *   y[m,n] = bf16_rne(((acc * s_a[m]) * s_w[n]) + bias[n]), fp32 steps.
  *   aq [M,K] / wq [N,K] E4M3 codes contiguous, s_a [M] / s_w [N] fp32,
- *   bias [N] bf16 or NULL, y [M,N] bf16 (ldy >= N, ldy % 8 == 0).
- *   Needs no workspace.                                                    */
+ *   bias [N] bf16 or NULL, y [M,N] bf16 (ldy >= N, ldy % 8 == 0);
+ *   ws / ws_bytes as for i8_gemm_e4m3_f32.                                 */
 i8_status i8_gemm_e4m3_dequant_bias_bf16(const uint8_t* aq, const float* s_a,
                                          const uint8_t* wq, const float* s_w,
                                          const void* bias, int64_t M,
                                          int64_t N, int64_t K, void* y,
-                                         int64_t ldy, i8_stream_t stream);
+                                         int64_t ldy, void* ws,
+                                         size_t ws_bytes, i8_stream_t stream);
 
 /* ------------------------------------------------------------------ fused producers
  * The per-token quantizer fused into the kernel that produces a linear

@@ -74,16 +74,17 @@ def test_e4m3_argument_errors(lib):
         assert fn(P(0x10008), 4, 64, 64, ok, 64, ok, None) == 2
         assert fn(ok, 0, 64, 64, ok, 64, ok, None) == 0
     g = lib.i8_gemm_e4m3_dequant_bias_bf16
-    assert g(ok, ok, ok, ok, None, -1, 8, 16, ok, 8, None) == 1
-    assert g(ok, ok, ok, ok, None, 4, 8, 24, ok, 8, None) == 3             # K % 16
-    assert g(ok, ok, ok, ok, None, 0, 8, 16, ok, 8, None) == 0             # empty
-    assert g(ok, None, ok, ok, None, 4, 8, 16, ok, 8, None) == 1           # no scales
-    assert g(P(0x10001), ok, ok, ok, None, 4, 8, 16, ok, 8, None) == 2
-    assert g(ok, ok, ok, ok, None, 4, 12, 16, ok, 12, None) == 2           # ldy % 8
+    assert g(ok, ok, ok, ok, None, -1, 8, 16, ok, 8, None, 0, None) == 1
+    assert g(ok, ok, ok, ok, None, 4, 8, 24, ok, 8, None, 0, None) == 3    # K % 16
+    assert g(ok, ok, ok, ok, None, 0, 8, 16, ok, 8, None, 0, None) == 0    # empty
+    assert g(ok, None, ok, ok, None, 4, 8, 16, ok, 8, None, 0, None) == 1  # no scales
+    assert g(P(0x10001), ok, ok, ok, None, 4, 8, 16, ok, 8, None, 0, None) == 2
+    assert g(ok, ok, ok, ok, None, 4, 12, 16, ok, 12, None, 0, None) == 2  # ldy % 8
     c = lib.i8_gemm_e4m3_f32
-    assert c(ok, ok, 4, 8, 16, ok, 6, None) == 1                           # ldc < N
-    assert c(ok, ok, 4, 8, 16, ok, 10, None) == 2                          # ldc % 4
-    assert c(ok, ok, 4, 8, 200000, ok, 8, None) == 3
+    assert c(ok, ok, 4, 8, 16, ok, 6, None, 0, None) == 1                  # ldc < N
+    assert c(ok, ok, 4, 8, 16, ok, 10, None, 0, None) == 2                 # ldc % 4
+    assert c(ok, ok, 4, 8, 200000, ok, 8, None, 0, None) == 3
+    assert lib.i8_gemm_e4m3_workspace_bytes(4, 8, 24) == 0
 
 
 def test_options_validation(lib):

@@ -4,9 +4,10 @@
   correctly rounded fp32 quotient x / s).
 * fp32 accumulators: the tensor core adds in fp32 in an unspecified order, so
   they are checked against the oracle's exact fp64 sum S with the bound
-      |acc - S| <= (ceil(K / 32) + 1) * 2 * 2^-24 * sum_k |a_k w_k|,
+      |acc - S| <= (ceil(K / 32) + 17) * 2 * 2^-24 * sum_k |a_k w_k|,
   i.e. at most one rounding (allowed 2 ulp, since the tensor core's adder
-  rounding mode is not documented) per K = 32 MMA step plus the final one.
+  rounding mode is not documented) per K = 32 MMA step, per addition of a
+  K split's partial in the fix-up (at most 16 splits), and the final one.
 * bf16 outputs: bit-identical to the oracle's epilogue applied to the GPU's
   own fp32 accumulators (the epilogue steps are the same fp32 operations);
   and against the oracle's exact path within one bf16 ulp plus the
@@ -33,7 +34,9 @@ def _codes(t: torch.Tensor) -> np.ndarray:
 
 
 def acc_bound(K: int, P: np.ndarray) -> np.ndarray:
-    return (math.ceil(K / 32) + 1) * 2 * U * P
+    # one rounding per K = 32 MMA step, plus up to 16 for a K split's
+    # partials being added in the fix-up, plus the final one
+    return (math.ceil(K / 32) + 17) * 2 * U * P
 
 
 def _check_acc(orc, aq, wq, c, what=""):
@@ -103,7 +106,9 @@ def test_quant_e4m3_weights_and_special_rows(orc):
 
 # ----------------------------------------------------------------- GEMM
 GEMM_SHAPES = [(64, 128, 256), (1, 8, 16), (7, 24, 48), (129, 136, 272), (300, 520, 1040),
-               (256, 256, 3072), (200, 304, 12288), (513, 264, 400)]
+               (256, 256, 3072), (200, 304, 12288), (513, 264, 400),
+               # few tiles: the plan splits K (fp32 partials + ordered fix-up)
+               (16, 3072, 3072), (256, 9216, 3072), (1, 3072, 12288), (2, 18432, 3072)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -115,6 +120,21 @@ def test_gemm_e4m3_f32_within_bound(orc, M, N, K):
     c = i8.gemm_e4m3_f32(aq, wq)
     i8.sync_check()
     _check_acc(orc, aq, wq, c, f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 3072, 3072), (1, 3072, 12288)])
+def test_gemm_e4m3_split_k_is_deterministic(M, N, K):
+    assert i8.e4m3_workspace_bytes(M, N, K) > 0          # these shapes split K
+    a = torch.randint(0, 0x7E, (M, K), dtype=torch.uint8, device="cuda")
+    w = torch.randint(0, 0x7E, (N, K), dtype=torch.uint8, device="cuda") | 0x80
+    c1 = i8.gemm_e4m3_f32(a, w)
+    ws = torch.full((i8.e4m3_workspace_bytes(M, N, K),), 0xFF, dtype=torch.uint8, device="cuda")
+    c2 = i8.gemm_e4m3_f32(a, w, workspace=ws)            # garbage in the workspace is fine
+    i8.sync_check()
+    assert torch.equal(c1.view(torch.int32), c2.view(torch.int32))
+    with pytest.raises(i8.I8Error) as e:
+        i8.gemm_e4m3_f32(a, w, workspace=ws[:-16])
+    assert e.value.status == 4
 
 
 def test_gemm_e4m3_closed_forms(orc):
@@ -154,7 +174,8 @@ def test_gemm_e4m3_mixed_magnitudes_within_bound(orc):
 
 @pytest.mark.parametrize("M,N,K,bias", [(64, 128, 256, True), (1, 8, 16, True), (7, 24, 48, False),
                                         (129, 136, 272, True), (300, 520, 1040, False),
-                                        (16, 3072, 3072, True)])
+                                        (16, 3072, 3072, True), (256, 9216, 3072, True),
+                                        (2, 12288, 3072, False)])
 def test_linear_e4m3_matches_oracle(orc, M, N, K, bias):
     shape = inputs.LinearShape("t", M, K, N, seed=M + N + K, outliers=K >= 256)
     d = inputs.linear_inputs(shape, with_bias=bias)

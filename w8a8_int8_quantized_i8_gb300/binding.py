@@ -71,8 +71,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "i8_gemm_dequant_bias_bf16_noalloc": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp], st),
             "i8_quant_weight_perchannel_e4m3": ([vp, i64, i64, i64, vp, i64, vp, vp], st),
             "i8_quant_act_pertoken_e4m3": ([vp, i64, i64, i64, vp, i64, vp, vp], st),
-            "i8_gemm_e4m3_f32": ([vp, vp, i64, i64, i64, vp, i64, vp], st),
-            "i8_gemm_e4m3_dequant_bias_bf16": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp], st),
+            "i8_gemm_e4m3_workspace_bytes": ([i64, i64, i64], sz),
+            "i8_gemm_e4m3_f32": ([vp, vp, i64, i64, i64, vp, i64, vp, sz, vp], st),
+            "i8_gemm_e4m3_dequant_bias_bf16": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, sz,
+                                                vp], st),
             "i8_layernorm_quant_act_pertoken": ([vp, i64, i64, i64, ctypes.c_float, ctypes.c_int,
                                                  vp, i64, vp, vp, i64, vp], st),
             "i8_gelu_quant_act_pertoken": ([vp, i64, i64, i64, ctypes.c_int, vp, i64, vp, vp, i64,
@@ -260,7 +262,20 @@ def quant_weight_perchannel_e4m3(w: torch.Tensor, q=None, s=None):
     return _quant_e4m3("i8_quant_weight_perchannel_e4m3", w, q, s)
 
 
-def gemm_e4m3_f32(aq, wq, out=None) -> torch.Tensor:
+def e4m3_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().i8_gemm_e4m3_workspace_bytes(M, N, K))
+
+
+def _e4m3_workspace(M, N, K, device, workspace):
+    need = e4m3_workspace_bytes(M, N, K)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def gemm_e4m3_f32(aq, wq, out=None, workspace=None) -> torch.Tensor:
     """fp32 tensor-core accumulators aq @ wq.T over E4M3 codes (for checking)."""
     a = _codes(aq, "aq")
     w = _codes(wq, "wq")
@@ -271,13 +286,14 @@ def gemm_e4m3_f32(aq, wq, out=None) -> torch.Tensor:
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=a.device)
     _need(out, torch.float32, "out", 2)
+    ws, wsb = _e4m3_workspace(M, N, K, a.device, workspace)
     with torch.cuda.device(a.device):
         _check(load().i8_gemm_e4m3_f32(_ptr(a), _ptr(w), M, N, K, _ptr(out), out.stride(0),
-                                       _stream(a)), "i8_gemm_e4m3_f32")
+                                       _ptr(ws), wsb, _stream(a)), "i8_gemm_e4m3_f32")
     return out
 
 
-def gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, bias=None, out=None):
+def gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, bias=None, out=None, workspace=None):
     """Fused E4M3 GEMM: bf16(acc * s_a[m] * s_w[n] + bias[n])."""
     a = _codes(aq, "aq")
     w = _codes(wq, "wq")
@@ -294,17 +310,18 @@ def gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, bias=None, out=None):
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
     _need(out, torch.bfloat16, "out", 2)
+    ws, wsb = _e4m3_workspace(M, N, K, a.device, workspace)
     fn = "i8_gemm_e4m3_dequant_bias_bf16"
     with torch.cuda.device(a.device):
         _check(getattr(load(), fn)(_ptr(a), _ptr(s_a), _ptr(w), _ptr(s_w), _ptr(bias), M, N, K,
-                                   _ptr(out), out.stride(0), _stream(a)), fn)
+                                   _ptr(out), out.stride(0), _ptr(ws), wsb, _stream(a)), fn)
     return out
 
 
-def linear_e4m3(x, wq, s_w, bias=None, out=None):
+def linear_e4m3(x, wq, s_w, bias=None, out=None, workspace=None):
     """The E4M3 linear layer: per-token E4M3 quant of x, then the fused GEMM."""
     aq, s_a = quant_act_pertoken_e4m3(x)
-    return gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, bias, out=out)
+    return gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, bias, out=out, workspace=workspace)
 
 
 # ---------------------------------------------------------------------- fused producers

@@ -28,6 +28,9 @@
 //     fp32 for the checking path) and write through swizzled shared-memory
 //     staging with bulk tensor stores.
 // Warps: 0 producer, 1 TMEM allocation + MMA issuer, 2-3 idle, 4-11 epilogue.
+// With few tiles (small M or N) the K range is split: each (tile, split) item
+// writes an fp32 partial into a workspace plane, and splitk_reduce_f32_kernel
+// adds the planes in split order and applies the epilogue.
 // Every wait is bounded (ptx.cuh); a timeout aborts the CTA cleanly.
 #pragma once
 #include "gemm.cuh"
@@ -59,6 +62,22 @@ struct Fp8Cfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
 };
+
+// Work item `item` of the schedule: K split ks of tile (mp, nb); the tile's
+// M blocks run fastest, so concurrently running pairs share weight tiles.
+struct Fp8Item {
+  int mp, nb, ks, kb0, kb1;
+};
+__device__ __forceinline__ Fp8Item fp8_item(const GemmParams& p, int item) {
+  Fp8Item t;
+  t.ks = item % p.splits;
+  const int tile = item / p.splits;
+  t.mp = tile % p.num_m_blk;
+  t.nb = tile / p.num_m_blk;
+  t.kb0 = t.ks * p.kb_per_split;
+  t.kb1 = min(t.kb0 + p.kb_per_split, p.total_kb);
+  return t;
+}
 
 struct Fp8Bars {
   uint32_t base;
@@ -125,12 +144,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
       const uint32_t full0 = mapa_shared(bars.full(0), 0);
       Ring r;
       bool ok = true;
-      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
-        const int mp = tile % p.num_m_blk;
-        const int nb = tile / p.num_m_blk;
-        const int m0 = mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM;
-        const int n0 = nb * Cfg::PAIR_N + static_cast<int>(rank) * Cfg::BN;
-        for (int kb = 0; kb < p.total_kb; ++kb) {
+      const int items = p.num_tiles * p.splits;
+      for (int item = pair; ok && item < items; item += npairs) {
+        const Fp8Item t = fp8_item(p, item);
+        const int m0 = t.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM;
+        const int n0 = t.nb * Cfg::PAIR_N + static_cast<int>(rank) * Cfg::BN;
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!(ok = mbar_wait(bars.empty(r.s), r.ph ^ 1u, abort_flag))) break;
           if (rank == 0) mbar_arrive_expect_tx(bars.full(r.s), Cfg::TX);
           const uint32_t fb = full0 + 8u * static_cast<uint32_t>(r.s);
@@ -146,18 +165,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
       constexpr uint32_t idesc = idesc_e4m3_f32(Cfg::PAIR_M, Cfg::PAIR_N);
       Ring r, racc;
       bool ok = true;
-      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+      const int items = p.num_tiles * p.splits;
+      for (int item = pair; ok && item < items; item += npairs) {
+        const Fp8Item t = fp8_item(p, item);
         if (!(ok = mbar_wait_cluster(bars.accempty(racc.s), racc.ph ^ 1u, abort_flag))) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(racc.s * Cfg::PAIR_N);
-        for (int kb = 0; kb < p.total_kb; ++kb) {
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!(ok = mbar_wait_cluster(bars.full(r.s), r.ph, abort_flag))) break;
           tc_fence_after();
           const uint64_t ad = smem_desc_sw128(stage(r.s));
           const uint64_t bd = smem_desc_sw128(stage(r.s) + Cfg::A_BYTES);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {   // K = 32 per MMA: 32 bytes along the swizzled row
-            mma_f8_ss_pair(d, ad + 2u * j, bd + 2u * j, idesc, (kb > 0 || j > 0) ? 1u : 0u);
+            mma_f8_ss_pair(d, ad + 2u * j, bd + 2u * j, idesc, (kb > t.kb0 || j > 0) ? 1u : 0u);
           }
           mma_commit_pair(bars.empty(r.s), 0x3);
           r.advance(Cfg::STAGES);
@@ -178,9 +199,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
     const uint32_t accempty0 = rank == 0 ? bars.accempty(0) : mapa_shared(bars.accempty(0), 0);
     Ring racc;
     bool ok = true;
-    for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
-      const int mp = tile % p.num_m_blk;
-      const int nb = tile / p.num_m_blk;
+    const int items = p.num_tiles * p.splits;
+    for (int item = pair; ok && item < items; item += npairs) {
+      const Fp8Item t = fp8_item(p, item);
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.accfull(racc.s), racc.ph, abort_flag));
       if (!ok) break;
       tc_fence_after();
@@ -203,15 +224,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
         else mbar_arrive_cluster(bar);
       }
       racc.advance(2);
-      const int m_base = mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM + quarter * 32;
-      const int n_base = nb * Cfg::PAIR_N + cg * 128;
+      const int m_base = t.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM + quarter * 32;
+      const int n_base = t.nb * Cfg::PAIR_N + cg * 128;
       if (p.out_mode == kOutBf16) {
         float f[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) f[i] = __int_as_float(acc[i]);
         store_warp_tile_bf16<128, float>(p, &tmY, stage_y, lane, m_base, n_base, f);
       } else {
-        store_warp_tile_s32<128>(&tmY, stage_y, lane, m_base, n_base, acc, 0);
+        // fp32 accumulators (checking path) or a K split's fp32 partial
+        // (plane ks of the workspace)
+        store_warp_tile_s32<128>(&tmY, stage_y, lane, m_base, n_base, acc,
+                                 p.out_mode == kOutPartial ? t.ks : 0);
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -226,6 +250,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// Split-K fix-up of the E4M3 GEMM: y = epilogue(sum_s partial[s]), the fp32
+// partials added in split order (a fixed order, so the result is
+// deterministic), then the same fp32 epilogue steps (or the raw sum for the
+// checking path).
+__global__ void __launch_bounds__(256) splitk_reduce_f32_kernel(const float* __restrict__ ws,
+                                                               int64_t split_stride, int64_t ldw,
+                                                               int splits, GemmParams p) {
+  pdl_wait();  // the partials come from the GEMM kernel just before
+  pdl_trigger();
+  const int groups_per_row = (p.N + 3) / 4;
+  const int64_t total = static_cast<int64_t>(p.M) * groups_per_row;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(g / groups_per_row);
+    const int n = static_cast<int>(g % groups_per_row) * 4;
+    const int cnt = min(4, p.N - n);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const float* src = ws + static_cast<int64_t>(m) * ldw + n;
+    for (int s = 0; s < splits; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(src + s * split_stride);  // ldw % 4 == 0
+      acc[0] = __fadd_rn(acc[0], v.x);
+      acc[1] = __fadd_rn(acc[1], v.y);
+      acc[2] = __fadd_rn(acc[2], v.z);
+      acc[3] = __fadd_rn(acc[3], v.w);
+    }
+    if (p.out_mode == kOutBf16) {
+      const float sa = p.s_a[m];
+      uint16_t* yrow = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(m) * p.ldo;
+      for (int i = 0; i < cnt; ++i) {
+        const float b = p.bias ? __uint_as_float(static_cast<uint32_t>(p.bias[n + i]) << 16) : 0.0f;
+        const __nv_bfloat16 v = __float2bfloat16_rn(dequant_one(acc[i], sa, p.s_w[n + i], b));
+        yrow[n + i] = *reinterpret_cast<const uint16_t*>(&v);
+      }
+    } else {
+      float* crow = static_cast<float*>(p.out) + static_cast<int64_t>(m) * p.ldo;
+      for (int i = 0; i < cnt; ++i) crow[n + i] = acc[i];
+    }
   }
 }
 

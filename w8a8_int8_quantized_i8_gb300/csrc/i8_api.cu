@@ -677,12 +677,40 @@ int fp8_cluster_capacity(DeviceInfo* d) {
   return n;
 }
 
+// Plan of the E4M3 GEMM: 256 x 256 tiles; when the tiles leave CTA pairs idle,
+// K splits of at least 4 blocks (512 K) by the same wave-efficiency rule as
+// the int8 table.  ws: fp32 partials [splits][M][round_up(N, 4)].
+struct Fp8Plan {
+  int num_m, num_n, total_kb, splits, kb_per_split;
+  int64_t tiles;
+  int64_t ldw;
+  size_t ws_bytes;
+};
+
+Fp8Plan plan_fp8(int64_t M, int64_t N, int64_t K, int pairs) {
+  Fp8Plan p{};
+  p.num_m = static_cast<int>((M + Fp8Cfg::PAIR_M - 1) / Fp8Cfg::PAIR_M);
+  p.num_n = static_cast<int>((N + Fp8Cfg::PAIR_N - 1) / Fp8Cfg::PAIR_N);
+  p.total_kb = static_cast<int>((K + Fp8Cfg::BK - 1) / Fp8Cfg::BK);
+  p.tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+  p.splits = best_splits(p.tiles, pairs, p.total_kb);
+  p.kb_per_split = (p.total_kb + p.splits - 1) / p.splits;
+  p.splits = (p.total_kb + p.kb_per_split - 1) / p.kb_per_split;
+  p.ldw = (N + 3) / 4 * 4;
+  p.ws_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * static_cast<size_t>(M) *
+                                  static_cast<size_t>(p.ldw) * sizeof(float)
+                            : 0;
+  return p;
+}
+
 // E4M3 codes in, bf16 (dequant + bias) or fp32 accumulators out.  One
-// persistent launch of the pair kernel; every shape uses 256 x 256 tiles
-// (rows and columns beyond M, N are zero-filled on load and clipped on store).
+// persistent launch of the pair kernel (plus the split-K fix-up when the
+// plan splits K); rows and columns beyond M, N are zero-filled on load and
+// clipped on store.
 i8_status gemm_fp8_common(const uint8_t* aq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
                           int out_mode, void* out, int64_t ldo, const float* s_a,
-                          const float* s_w, const void* bias, cudaStream_t st) {
+                          const float* s_w, const void* bias, void* ws, size_t ws_bytes,
+                          cudaStream_t st) {
   if (M < 0 || N < 0 || K <= 0) return I8_ERR_INVALID_ARG;
   if (K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX) return I8_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return I8_OK;
@@ -695,35 +723,62 @@ i8_status gemm_fp8_common(const uint8_t* aq, const uint8_t* wq, int64_t M, int64
   if (out_mode != kOutBf16 && ldo % 4 != 0) return I8_ERR_ALIGNMENT;
   DeviceInfo* d;
   if (i8_status e = device_info(&d, nullptr)) return e;
+  const int clusters = fp8_cluster_capacity(d);
+  const Fp8Plan pl = plan_fp8(M, N, K, clusters);
+  if (pl.tiles * pl.splits > INT32_MAX) return I8_ERR_UNSUPPORTED;
+  if (pl.ws_bytes > 0) {
+    if (!ws || ws_bytes < pl.ws_bytes) return I8_ERR_WORKSPACE;
+    if (!aligned16(ws)) return I8_ERR_ALIGNMENT;
+  }
   CUtensorMap ma, mb, my;
   if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M, K, Fp8Cfg::BK, Fp8Cfg::BM) ||
       !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, K, N, K, Fp8Cfg::BK, Fp8Cfg::BN))
-    return I8_ERR_CUDA;
-  if (!encode_out(&my, out_mode == kOutBf16, out, static_cast<uint64_t>(N),
-                  static_cast<uint64_t>(M), static_cast<uint64_t>(ldo), 1))
     return I8_ERR_CUDA;
   GemmParams gp{};
   gp.M = static_cast<int>(M);
   gp.N = static_cast<int>(N);
   gp.K = static_cast<int>(K);
-  gp.num_m_blk = static_cast<int>((M + Fp8Cfg::PAIR_M - 1) / Fp8Cfg::PAIR_M);
-  gp.num_n_blk = static_cast<int>((N + Fp8Cfg::PAIR_N - 1) / Fp8Cfg::PAIR_N);
-  gp.splits = 1;
-  gp.total_kb = static_cast<int>((K + Fp8Cfg::BK - 1) / Fp8Cfg::BK);
-  gp.kb_per_split = gp.total_kb;
-  const int64_t tiles = static_cast<int64_t>(gp.num_m_blk) * gp.num_n_blk;
-  if (tiles > INT32_MAX) return I8_ERR_UNSUPPORTED;
-  gp.num_tiles = static_cast<int>(tiles);
-  gp.out_mode = out_mode;
-  gp.out = out;
-  gp.ldo = ldo;
+  gp.num_m_blk = pl.num_m;
+  gp.num_n_blk = pl.num_n;
+  gp.splits = pl.splits;
+  gp.total_kb = pl.total_kb;
+  gp.kb_per_split = pl.kb_per_split;
+  gp.num_tiles = static_cast<int>(pl.tiles);
   gp.s_a = s_a;
   gp.s_w = s_w;
   gp.bias = static_cast<const uint16_t*>(bias);
-  const int clusters = fp8_cluster_capacity(d);
-  const int grid = 2 * static_cast<int>(std::min<int64_t>(clusters, tiles));
-  return cuda_status(launch_pdl(gemm_fp8_pair_kernel, dim3(grid), dim3(Fp8Cfg::THREADS),
-                                Fp8Cfg::SMEM_BYTES, st, ma, mb, my, gp));
+  if (pl.splits > 1) {
+    gp.out_mode = kOutPartial;
+    gp.out = ws;
+    gp.ldo = pl.ldw;
+    gp.split_stride = M * pl.ldw;
+    if (!encode_out(&my, false, ws, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                    static_cast<uint64_t>(pl.ldw), static_cast<uint64_t>(pl.splits)))
+      return I8_ERR_CUDA;
+  } else {
+    gp.out_mode = out_mode;
+    gp.out = out;
+    gp.ldo = ldo;
+    if (!encode_out(&my, out_mode == kOutBf16, out, static_cast<uint64_t>(N),
+                    static_cast<uint64_t>(M), static_cast<uint64_t>(ldo), 1))
+      return I8_ERR_CUDA;
+  }
+  const int grid = 2 * static_cast<int>(std::min<int64_t>(clusters, pl.tiles * pl.splits));
+  if (cudaError_t e = launch_pdl(gemm_fp8_pair_kernel, dim3(grid), dim3(Fp8Cfg::THREADS),
+                                 Fp8Cfg::SMEM_BYTES, st, ma, mb, my, gp))
+    return cuda_status(e);
+  if (pl.splits > 1) {
+    GemmParams rp = gp;
+    rp.out_mode = out_mode;
+    rp.out = out;
+    rp.ldo = ldo;
+    const int64_t groups = M * ((N + 3) / 4);
+    const int64_t blocks = std::min<int64_t>((groups + 255) / 256, static_cast<int64_t>(d->sms) * 16);
+    return cuda_status(launch_pdl(splitk_reduce_f32_kernel, dim3(static_cast<unsigned>(blocks)),
+                                  dim3(256), 0, st, static_cast<const float*>(ws),
+                                  gp.split_stride, pl.ldw, pl.splits, rp));
+  }
+  return I8_OK;
 }
 
 // ----------------------------------------------------------------- no-alloc variant
@@ -796,17 +851,26 @@ i8_status i8_quant_act_pertoken_e4m3(const void* x, int64_t M, int64_t K, int64_
                     reinterpret_cast<cudaStream_t>(stream), kQuantE4M3);
 }
 
+size_t i8_gemm_e4m3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX)
+    return 0;
+  DeviceInfo* d;
+  if (device_info(&d, nullptr) != I8_OK) return 0;
+  return plan_fp8(M, N, K, fp8_cluster_capacity(d)).ws_bytes;
+}
+
 i8_status i8_gemm_e4m3_f32(const uint8_t* aq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
-                           float* c, int64_t ldc, i8_stream_t stream) {
-  return gemm_fp8_common(aq, wq, M, N, K, kOutInt32, c, ldc, nullptr, nullptr, nullptr,
-                         reinterpret_cast<cudaStream_t>(stream));
+                           float* c, int64_t ldc, void* ws, size_t ws_bytes,
+                           i8_stream_t stream) {
+  return gemm_fp8_common(aq, wq, M, N, K, kOutInt32, c, ldc, nullptr, nullptr, nullptr, ws,
+                         ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 i8_status i8_gemm_e4m3_dequant_bias_bf16(const uint8_t* aq, const float* s_a, const uint8_t* wq,
                                          const float* s_w, const void* bias, int64_t M,
-                                         int64_t N, int64_t K, void* y, int64_t ldy,
-                                         i8_stream_t stream) {
-  return gemm_fp8_common(aq, wq, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias,
+                                         int64_t N, int64_t K, void* y, int64_t ldy, void* ws,
+                                         size_t ws_bytes, i8_stream_t stream) {
+  return gemm_fp8_common(aq, wq, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws, ws_bytes,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
