@@ -173,6 +173,50 @@ i8_status i8_gemm_e4m3_dequant_bias_bf16(const uint8_t* aq, const float* s_a,
                                          int64_t ldy, void* ws,
                                          size_t ws_bytes, i8_stream_t stream);
 
+/* ------------------------------------------------------------------ fp16 codes
+ * The exact W8A8 product with the int8 codes held in 16-bit containers: the
+ * activation quantizer writes each int8 code as the fp16 value of the same
+ * integer, and the weights are widened once offline (i8_widen_weight_codes).
+ * The GEMM then feeds both operands to the tensor core's fp16 kind straight
+ * from memory, with no on-chip widening; products are exact and the fp32
+ * accumulator restarts every chunk (i8_set_option I8_OPT_CHUNK_K), so the
+ * int32 result and the bf16 output are identical to the int8-code calls
+ * above (arXiv 2606.14598, abstract: int8 x int8 -> int32, per-token x
+ * per-channel dequantization and bias folded into the epilogue).  The codes
+ * take twice the memory of int8 codes.
+ *
+ * i8_quant_act_pertoken_f16codes: the quantizer of i8_quant_act_pertoken;
+ *   q16 [M,K] fp16 values (-127..127), row stride ldq elements
+ *   (ldq >= K, ldq % 8 == 0).                                              */
+i8_status i8_quant_act_pertoken_f16codes(const void* x_bf16, int64_t M,
+                                         int64_t K, int64_t ldx, void* q16,
+                                         int64_t ldq, float* s_a,
+                                         i8_stream_t stream);
+
+/* Workspace bytes of the two fp16-code GEMM calls below (0 when the shape
+ * runs without a K split; else int32 partials, splits x M x round_up(N, 4)
+ * x 4 bytes).  Returns 0 for shapes the GEMM rejects. */
+size_t i8_gemm_f16codes_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Exact int32 accumulators from fp16 codes, for checking.
+ *   a16 [M,K], w16 [N,K] fp16 code values, contiguous (row stride K)
+ *   c [M,N] int32 (ldc >= N, ldc % 4 == 0); ws as above.                    */
+i8_status i8_gemm_int32_f16codes(const void* a16, const void* w16, int64_t M,
+                                 int64_t N, int64_t K, int32_t* c,
+                                 int64_t ldc, void* ws, size_t ws_bytes,
+                                 i8_stream_t stream);
+
+/* The fused GEMM from fp16 codes: same result and epilogue as
+ * i8_gemm_dequant_bias_bf16; y [M,N] bf16 (ldy >= N, ldy % 8 == 0). */
+i8_status i8_gemm_dequant_bias_bf16_f16codes(const void* a16, const float* s_a,
+                                             const void* w16,
+                                             const float* s_w,
+                                             const void* bias, int64_t M,
+                                             int64_t N, int64_t K, void* y,
+                                             int64_t ldy, void* ws,
+                                             size_t ws_bytes,
+                                             i8_stream_t stream);
+
 /* ------------------------------------------------------------------ fused producers
  * The per-token quantizer fused into the kernel that produces a linear
  * layer's input (arXiv 2606.14598 folds the dequantization into the GEMM to

@@ -7,7 +7,9 @@ Consumer GPUs: A Fused INT8 GEMM Kernel for Ideogram 4.0", arXiv 2606.14598,
 abstract).  The computation lives in libi8.so (CUDA, include/i8.h); the
 functions below are its torch-tensor binding.
 """
-from .binding import (I8Error, e4m3_workspace_bytes, gelu_quant_act_pertoken, gemm_dequant_bias_bf16,
+from .binding import (I8Error, e4m3_workspace_bytes, f16codes_workspace_bytes,
+                      gelu_quant_act_pertoken, gemm_dequant_bias_bf16_f16codes,
+                      gemm_int32_f16codes, linear_f16codes, quant_act_pertoken_f16codes, gemm_dequant_bias_bf16,
                       gemm_e4m3_dequant_bias_bf16, gemm_e4m3_f32, gemm_int32,
                       layernorm_quant_act_pertoken, linear, linear_e4m3, load, quant_act_pertoken,
                       quant_act_pertoken_e4m3, quant_weight_perchannel,
@@ -15,7 +17,9 @@ from .binding import (I8Error, e4m3_workspace_bytes, gelu_quant_act_pertoken, ge
                       workspace_bytes)
 
 __all__ = [
-    "I8Error", "e4m3_workspace_bytes", "gelu_quant_act_pertoken", "gemm_dequant_bias_bf16", "gemm_e4m3_dequant_bias_bf16",
+    "I8Error", "e4m3_workspace_bytes", "f16codes_workspace_bytes", "gelu_quant_act_pertoken",
+    "gemm_dequant_bias_bf16_f16codes", "gemm_int32_f16codes", "linear_f16codes",
+    "quant_act_pertoken_f16codes", "gemm_dequant_bias_bf16", "gemm_e4m3_dequant_bias_bf16",
     "gemm_e4m3_f32", "gemm_int32", "layernorm_quant_act_pertoken", "linear", "linear_e4m3", "load", "quant_act_pertoken",
     "quant_act_pertoken_e4m3", "quant_weight_perchannel", "quant_weight_perchannel_e4m3",
     "set_option", "sync_check", "widen_weight_codes", "workspace_bytes",

@@ -75,6 +75,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "i8_gemm_e4m3_f32": ([vp, vp, i64, i64, i64, vp, i64, vp, sz, vp], st),
             "i8_gemm_e4m3_dequant_bias_bf16": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, sz,
                                                 vp], st),
+            "i8_quant_act_pertoken_f16codes": ([vp, i64, i64, i64, vp, i64, vp, vp], st),
+            "i8_gemm_f16codes_workspace_bytes": ([i64, i64, i64], sz),
+            "i8_gemm_int32_f16codes": ([vp, vp, i64, i64, i64, vp, i64, vp, sz, vp], st),
+            "i8_gemm_dequant_bias_bf16_f16codes": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp,
+                                                    sz, vp], st),
             "i8_layernorm_quant_act_pertoken": ([vp, i64, i64, i64, ctypes.c_float, ctypes.c_int,
                                                  vp, i64, vp, vp, i64, vp], st),
             "i8_gelu_quant_act_pertoken": ([vp, i64, i64, i64, ctypes.c_int, vp, i64, vp, vp, i64,
@@ -322,6 +327,91 @@ def linear_e4m3(x, wq, s_w, bias=None, out=None, workspace=None):
     """The E4M3 linear layer: per-token E4M3 quant of x, then the fused GEMM."""
     aq, s_a = quant_act_pertoken_e4m3(x)
     return gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, bias, out=out, workspace=workspace)
+
+
+# ---------------------------------------------------------------------- fp16 codes
+# The exact W8A8 product with the int8 codes held as fp16 values: the
+# quantizer writes them, weights come from widen_weight_codes, and the GEMM
+# feeds both to the tensor core without on-chip widening.  Results are
+# identical to the int8-code calls.
+
+def quant_act_pertoken_f16codes(x: torch.Tensor, q=None, s=None):
+    """bf16 [M,K] -> (int8 codes as fp16 values [M,K], fp32 per-token scales [M])."""
+    _need(x, torch.bfloat16, "x", 2)
+    R, K = x.shape
+    if q is None:
+        q = torch.empty((R, K), dtype=torch.float16, device=x.device)
+    if s is None:
+        s = torch.empty((R,), dtype=torch.float32, device=x.device)
+    _need(q, torch.float16, "q", 2)
+    _need(s, torch.float32, "s", 1)
+    with torch.cuda.device(x.device):
+        _check(load().i8_quant_act_pertoken_f16codes(_ptr(x), R, K, K, _ptr(q), K, _ptr(s),
+                                                     _stream(x)), "i8_quant_act_pertoken_f16codes")
+    return q, s
+
+
+def f16codes_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().i8_gemm_f16codes_workspace_bytes(M, N, K))
+
+
+def _f16_workspace(M, N, K, device, workspace):
+    need = f16codes_workspace_bytes(M, N, K)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def gemm_int32_f16codes(a16, w16, out=None, workspace=None) -> torch.Tensor:
+    """Exact int32 accumulators from fp16 code values ([M,K] x [N,K])."""
+    _need(a16, torch.float16, "a16", 2)
+    _need(w16, torch.float16, "w16", 2)
+    M, K = a16.shape
+    N = w16.shape[0]
+    if w16.shape[1] != K:
+        raise ValueError("K mismatch")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=a16.device)
+    _need(out, torch.int32, "out", 2)
+    ws, wsb = _f16_workspace(M, N, K, a16.device, workspace)
+    with torch.cuda.device(a16.device):
+        _check(load().i8_gemm_int32_f16codes(_ptr(a16), _ptr(w16), M, N, K, _ptr(out),
+                                             out.stride(0), _ptr(ws), wsb, _stream(a16)),
+               "i8_gemm_int32_f16codes")
+    return out
+
+
+def gemm_dequant_bias_bf16_f16codes(a16, s_a, w16, s_w, bias=None, out=None, workspace=None):
+    """The fused GEMM from fp16 code values: bf16(acc * s_a[m] * s_w[n] + bias[n])."""
+    _need(a16, torch.float16, "a16", 2)
+    _need(w16, torch.float16, "w16", 2)
+    _need(s_a, torch.float32, "s_a", 1)
+    _need(s_w, torch.float32, "s_w", 1)
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = a16.shape
+    N = w16.shape[0]
+    if w16.shape[1] != K or s_a.shape[0] != M or s_w.shape[0] != N:
+        raise ValueError("shape mismatch")
+    if bias is not None and bias.shape[0] != N:
+        raise ValueError("bias shape")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a16.device)
+    _need(out, torch.bfloat16, "out", 2)
+    ws, wsb = _f16_workspace(M, N, K, a16.device, workspace)
+    fn = "i8_gemm_dequant_bias_bf16_f16codes"
+    with torch.cuda.device(a16.device):
+        _check(getattr(load(), fn)(_ptr(a16), _ptr(s_a), _ptr(w16), _ptr(s_w), _ptr(bias), M, N, K,
+                                   _ptr(out), out.stride(0), _ptr(ws), wsb, _stream(a16)), fn)
+    return out
+
+
+def linear_f16codes(x, w16, s_w, bias=None, out=None, workspace=None):
+    """The W8A8 layer with fp16-held codes: quantize x, then the fused GEMM."""
+    a16, s_a = quant_act_pertoken_f16codes(x)
+    return gemm_dequant_bias_bf16_f16codes(a16, s_a, w16, s_w, bias, out=out, workspace=workspace)
 
 
 # ---------------------------------------------------------------------- fused producers

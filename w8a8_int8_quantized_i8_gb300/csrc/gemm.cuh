@@ -167,16 +167,7 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
                : "memory");
 }
 
-// Four int8 codes -> four fp16 values (exact).  x ^ 0x80 is x + 128 as an
-// unsigned byte u; the fp16 bit pattern 0x64uu is 1024 + u; subtracting
-// 1152 (0x6480) leaves x.
-__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
-  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
-}
+// s8x4_to_f16x4 (four int8 codes -> four fp16 values) lives in quant.cuh.
 
 // One conversion item = one 16-byte chunk (16 int8 codes) of one row of an
 // int8 stage, widened into two 16-byte chunks (16 fp16 codes) of the fp16

@@ -1,51 +1,64 @@
-// gemm_fp8.cuh -- the E4M3 (FP8) arm of the W8A8 linear layer, on a CTA pair.
+// gemm_direct.cuh -- the converter-free CTA-pair GEMM: operands go from HBM
+// to shared memory by TMA and straight into tcgen05.mma, nothing is widened
+// on chip.  Two modes of one kernel template:
 //
-// Fused INT8 GEMM Kernel for Ideogram 4.0 (arXiv 2606.14598), abstract: the
-// INT8 kernel is measured against an FP8 baseline, and on B200 it loses to
-// the card's native FP8 path.  This is that native path on sm_103a, with the
-// same per-token x per-channel scales and the same fused epilogue:
-//   acc[m,n] = sum_k a[m,k] * w[n,k]      (E4M3 x E4M3 -> fp32, tensor core)
-//   y[m,n]   = bf16(acc * s_a[m] * s_w[n] + bias[n])
-// Unlike the int8 arm nothing is widened on chip and nothing is drained in
-// chunks: TMA brings the E4M3 codes into shared memory and tcgen05.mma
-// kind::f8f6f4 consumes them there; the fp32 accumulator of the whole K
-// range is read once per tile.  The tensor core's fp32 additions round (in
-// an order the hardware does not specify), so this arm agrees with the exact
-// oracle within an error bound rather than bit for bit.
+// * E4M3 (the FP8 arm).  Fused INT8 GEMM Kernel for Ideogram 4.0 (arXiv
+//   2606.14598), abstract: the INT8 kernel is measured against an FP8
+//   baseline, and on B200 it loses to the card's native FP8 path.  This is
+//   that native path on sm_103a, with the same per-token x per-channel scales
+//   and the same fused epilogue:
+//     acc[m,n] = sum_k a[m,k] * w[n,k]    (E4M3 x E4M3 -> fp32, kind::f8f6f4)
+//     y[m,n]   = bf16(acc * s_a[m] * s_w[n] + bias[n])
+//   The tensor core's fp32 additions round (in an order the hardware does not
+//   specify), so this mode agrees with the exact oracle within an error bound.
+//
+// * F16 codes (the exact W8A8 path without on-chip widening).  The same
+//   int8 x int8 -> int32 product as gemm.cuh / gemm_pair.cuh, with both
+//   operands' int8 codes stored as fp16 values of the same integers (the
+//   quantizer's fp16-code output, and weights widened once offline).
+//   kind::f16 products are exact, and the fp32 accumulator is restarted every
+//   `chunk` K so that no partial sum reaches 2^24; the epilogue warps drain
+//   each chunk into int32 registers.  Bit-exact, like the int8-code kernels.
 //
 // Structure: the two CTAs of a cluster compute one 256 x 256 output tile.
 //   * CTA r loads A rows [m0 + 128 r, +128) and B rows [n0 + 128 r, +128) of
-//     each 128-deep K block into its own shared memory (128-byte swizzle);
-//     both CTAs' loads complete on CTA 0's full barrier (cta_group::2 TMA),
-//     which CTA 0's producer armed with the stage's total byte count.
-//   * One thread of CTA 0 issues four M=256 N=256 K=32 MMAs per block; each
-//     CTA's 128 rows x 256 fp32 columns land in its own tensor memory, in
-//     one of two buffers, so a tile's epilogue overlaps the next mainloop.
-//     Its commits free the stage in both CTAs (multicast).
+//     each 128-byte-deep K block (128 E4M3 or 64 fp16 codes) into its own
+//     shared memory (128-byte swizzle); both CTAs' loads complete on CTA 0's
+//     full barrier (cta_group::2 TMA), which CTA 0's producer armed with the
+//     stage's total byte count.
+//   * One thread of CTA 0 issues four M=256 N=256 MMAs per block (K = 32 E4M3
+//     or 16 fp16 codes each, 32 bytes along the swizzled row); each CTA's 128
+//     rows x 256 fp32 columns land in its own tensor memory, in one of two
+//     buffers, so the epilogue overlaps the next MMAs.  Its commits free the
+//     stage in both CTAs (multicast).
 //   * Eight epilogue warps per CTA (lane quarter = warp % 4, column half =
 //     (warp - 4) / 4) read the accumulator, hand the buffer back (CTA 1's
-//     warps arrive on CTA 0's barrier), dequantize + bias -> bf16 (or keep
-//     fp32 for the checking path) and write through swizzled shared-memory
-//     staging with bulk tensor stores.
+//     warps arrive on CTA 0's barrier), and write the tile through swizzled
+//     shared-memory staging with bulk tensor stores: dequant + bias -> bf16,
+//     or the raw accumulator (fp32 / int32) for the checking paths.
 // Warps: 0 producer, 1 TMEM allocation + MMA issuer, 2-3 idle, 4-11 epilogue.
 // With few tiles (small M or N) the K range is split: each (tile, split) item
-// writes an fp32 partial into a workspace plane, and splitk_reduce_f32_kernel
-// adds the planes in split order and applies the epilogue.
+// writes a partial into a workspace plane, and a fix-up kernel adds the
+// planes in split order (fp32 for E4M3, exact int32 for F16 codes) and
+// applies the epilogue.
 // Every wait is bounded (ptx.cuh); a timeout aborts the CTA cleanly.
 #pragma once
 #include "gemm.cuh"
 
 namespace i8 {
 
-struct Fp8Cfg {
+enum DirectKind : int { kDirectE4M3 = 0, kDirectF16 = 1 };
+
+template <int KIND>
+struct DirectCfg {
   static constexpr int BM = 128;        // A rows loaded per CTA
   static constexpr int BN = 128;        // B rows loaded per CTA
   static constexpr int PAIR_M = 256;
   static constexpr int PAIR_N = 256;
-  static constexpr int BK = 128;        // K per stage: one 128-byte swizzle row
+  static constexpr int BK = KIND == kDirectF16 ? 64 : 128;   // K per stage: one 128-byte row
   static constexpr int STAGES = 6;
-  static constexpr int A_BYTES = BM * BK;
-  static constexpr int B_BYTES = BN * BK;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_WARP0 = 4;
@@ -65,11 +78,11 @@ struct Fp8Cfg {
 
 // Work item `item` of the schedule: K split ks of tile (mp, nb); the tile's
 // M blocks run fastest, so concurrently running pairs share weight tiles.
-struct Fp8Item {
+struct DirectItem {
   int mp, nb, ks, kb0, kb1;
 };
-__device__ __forceinline__ Fp8Item fp8_item(const GemmParams& p, int item) {
-  Fp8Item t;
+__device__ __forceinline__ DirectItem direct_item(const GemmParams& p, int item) {
+  DirectItem t;
   t.ks = item % p.splits;
   const int tile = item / p.splits;
   t.mp = tile % p.num_m_blk;
@@ -79,20 +92,22 @@ __device__ __forceinline__ Fp8Item fp8_item(const GemmParams& p, int item) {
   return t;
 }
 
-struct Fp8Bars {
+template <int STAGES>
+struct DirectBars {
   uint32_t base;
   __device__ uint32_t full(int s) const { return base + 8u * s; }
-  __device__ uint32_t empty(int s) const { return base + 8u * (Fp8Cfg::STAGES + s); }
-  __device__ uint32_t accfull(int b) const { return base + 8u * (2 * Fp8Cfg::STAGES + b); }
-  __device__ uint32_t accempty(int b) const { return base + 8u * (2 * Fp8Cfg::STAGES + 2 + b); }
-  __device__ uint32_t done() const { return base + 8u * (2 * Fp8Cfg::STAGES + 4); }
+  __device__ uint32_t empty(int s) const { return base + 8u * (STAGES + s); }
+  __device__ uint32_t accfull(int b) const { return base + 8u * (2 * STAGES + b); }
+  __device__ uint32_t accempty(int b) const { return base + 8u * (2 * STAGES + 2 + b); }
+  __device__ uint32_t done() const { return base + 8u * (2 * STAGES + 4); }
 };
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
-    gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
-  using Cfg = Fp8Cfg;
+template <int KIND>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DirectCfg<KIND>::THREADS, 1)
+    gemm_direct_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+  using Cfg = DirectCfg<KIND>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -104,7 +119,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
 
-  const Fp8Bars bars{sbase + Cfg::OFF_BAR};
+  const DirectBars<Cfg::STAGES> bars{sbase + Cfg::OFF_BAR};
   auto stage = [&](int s) { return sbase + Cfg::OFF_STAGE + static_cast<uint32_t>(s * Cfg::STAGE_BYTES); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
@@ -146,7 +161,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
       bool ok = true;
       const int items = p.num_tiles * p.splits;
       for (int item = pair; ok && item < items; item += npairs) {
-        const Fp8Item t = fp8_item(p, item);
+        const DirectItem t = direct_item(p, item);
         const int m0 = t.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM;
         const int n0 = t.nb * Cfg::PAIR_N + static_cast<int>(rank) * Cfg::BN;
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
@@ -162,30 +177,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (CTA 0)
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(Cfg::PAIR_M, Cfg::PAIR_N);
+      constexpr uint32_t idesc = KIND == kDirectF16 ? idesc_f16_f32(Cfg::PAIR_M, Cfg::PAIR_N)
+                                                    : idesc_e4m3_f32(Cfg::PAIR_M, Cfg::PAIR_N);
       Ring r, racc;
       bool ok = true;
       const int items = p.num_tiles * p.splits;
       for (int item = pair; ok && item < items; item += npairs) {
-        const Fp8Item t = fp8_item(p, item);
-        if (!(ok = mbar_wait_cluster(bars.accempty(racc.s), racc.ph ^ 1u, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(racc.s * Cfg::PAIR_N);
-        for (int kb = t.kb0; kb < t.kb1; ++kb) {
-          if (!(ok = mbar_wait_cluster(bars.full(r.s), r.ph, abort_flag))) break;
+        const DirectItem t = direct_item(p, item);
+        // F16 codes: the fp32 accumulator restarts every chunk_stages blocks
+        // (exactness); E4M3: one accumulation over the item's K range
+        const int chunk = KIND == kDirectF16 ? p.chunk_stages : t.kb1 - t.kb0;
+        for (int kc = t.kb0; ok && kc < t.kb1; kc += chunk) {
+          const int kc1 = min(t.kb1, kc + chunk);
+          if (!(ok = mbar_wait_cluster(bars.accempty(racc.s), racc.ph ^ 1u, abort_flag))) break;
           tc_fence_after();
-          const uint64_t ad = smem_desc_sw128(stage(r.s));
-          const uint64_t bd = smem_desc_sw128(stage(r.s) + Cfg::A_BYTES);
+          const uint32_t d = tmem_base + static_cast<uint32_t>(racc.s * Cfg::PAIR_N);
+          for (int kb = kc; kb < kc1; ++kb) {
+            if (!(ok = mbar_wait_cluster(bars.full(r.s), r.ph, abort_flag))) break;
+            tc_fence_after();
+            const uint64_t ad = smem_desc_sw128(stage(r.s));
+            const uint64_t bd = smem_desc_sw128(stage(r.s) + Cfg::A_BYTES);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {   // K = 32 per MMA: 32 bytes along the swizzled row
-            mma_f8_ss_pair(d, ad + 2u * j, bd + 2u * j, idesc, (kb > t.kb0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < 4; ++j) {   // 32 bytes of K per MMA along the swizzled row
+              const uint32_t accum = (kb > kc || j > 0) ? 1u : 0u;
+              if constexpr (KIND == kDirectF16) mma_f16_ss_pair(d, ad + 2u * j, bd + 2u * j, idesc, accum);
+              else mma_f8_ss_pair(d, ad + 2u * j, bd + 2u * j, idesc, accum);
+            }
+            mma_commit_pair(bars.empty(r.s), 0x3);
+            r.advance(Cfg::STAGES);
           }
-          mma_commit_pair(bars.empty(r.s), 0x3);
-          r.advance(Cfg::STAGES);
+          if (!ok) break;
+          mma_commit_pair(bars.accfull(racc.s), 0x3);
+          racc.advance(2);
         }
-        if (!ok) break;
-        mma_commit_pair(bars.accfull(racc.s), 0x3);
-        racc.advance(2);
       }
       mma_commit_pair(bars.done(), 0x1);
       mbar_wait_bounded(bars.done(), 0u, 100000000ull);
@@ -201,41 +225,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
     bool ok = true;
     const int items = p.num_tiles * p.splits;
     for (int item = pair; ok && item < items; item += npairs) {
-      const Fp8Item t = fp8_item(p, item);
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.accfull(racc.s), racc.ph, abort_flag));
+      const DirectItem t = direct_item(p, item);
+      const int chunk = KIND == kDirectF16 ? p.chunk_stages : t.kb1 - t.kb0;
+      // F16: exact int32 sum of the chunks; E4M3: the fp32 bit patterns
+      int acc[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0;
+      for (int kc = t.kb0; kc < t.kb1; kc += chunk) {
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.accfull(racc.s), racc.ph, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(racc.s * Cfg::PAIR_N + cg * 128);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + q4 * 32, r);
+          if constexpr (KIND == kDirectF16) {
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[q4 * 32 + i] += f32_exact_int_to_s32(r[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[q4 * 32 + i] = static_cast<int>(r[i]);
+          }
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t bar = accempty0 + 8u * static_cast<uint32_t>(racc.s);
+          if (rank == 0) mbar_arrive(bar);
+          else mbar_arrive_cluster(bar);
+        }
+        racc.advance(2);
+      }
       if (!ok) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                             static_cast<uint32_t>(racc.s * Cfg::PAIR_N + cg * 128);
-      int acc[128];   // fp32 bit patterns
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + q4 * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[q4 * 32 + i] = static_cast<int>(r[i]);
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        const uint32_t bar = accempty0 + 8u * static_cast<uint32_t>(racc.s);
-        if (rank == 0) mbar_arrive(bar);
-        else mbar_arrive_cluster(bar);
-      }
-      racc.advance(2);
       const int m_base = t.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM + quarter * 32;
       const int n_base = t.nb * Cfg::PAIR_N + cg * 128;
-      if (p.out_mode == kOutBf16) {
-        float f[128];
-#pragma unroll
-        for (int i = 0; i < 128; ++i) f[i] = __int_as_float(acc[i]);
-        store_warp_tile_bf16<128, float>(p, &tmY, stage_y, lane, m_base, n_base, f);
+      const int z = p.out_mode == kOutPartial ? t.ks : 0;
+      if constexpr (KIND == kDirectF16) {
+        // int32 results, or a K split's exact int32 partial (plane ks)
+        if (p.out_mode == kOutBf16) store_warp_tile_bf16<128, int>(p, &tmY, stage_y, lane, m_base, n_base, acc);
+        else store_warp_tile_s32<128>(&tmY, stage_y, lane, m_base, n_base, acc, z);
       } else {
-        // fp32 accumulators (checking path) or a K split's fp32 partial
-        // (plane ks of the workspace)
-        store_warp_tile_s32<128>(&tmY, stage_y, lane, m_base, n_base, acc,
-                                 p.out_mode == kOutPartial ? t.ks : 0);
+        if (p.out_mode == kOutBf16) {
+          float f[128];
+#pragma unroll
+          for (int i = 0; i < 128; ++i) f[i] = __int_as_float(acc[i]);
+          store_warp_tile_bf16<128, float>(p, &tmY, stage_y, lane, m_base, n_base, f);
+        } else {
+          // fp32 accumulators (checking path) or a K split's fp32 partial
+          store_warp_tile_s32<128>(&tmY, stage_y, lane, m_base, n_base, acc, z);
+        }
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -253,7 +295,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Fp8Cfg::THREADS, 1)
   }
 }
 
-// Split-K fix-up of the E4M3 GEMM: y = epilogue(sum_s partial[s]), the fp32
+// Split-K fix-up of the E4M3 mode (the F16-code mode's int32 partials use
+// splitk_reduce_kernel of gemm.cuh): y = epilogue(sum_s partial[s]), the fp32
 // partials added in split order (a fixed order, so the result is
 // deterministic), then the same fp32 epilogue steps (or the raw sum for the
 // checking path).

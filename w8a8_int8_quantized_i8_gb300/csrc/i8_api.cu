@@ -14,7 +14,7 @@
 
 #include "../../include/i8.h"
 #include "gemm.cuh"
-#include "gemm_fp8.cuh"
+#include "gemm_direct.cuh"
 #include "gemm_pair.cuh"
 #include "producer.cuh"
 #include "skinny.cuh"
@@ -152,17 +152,22 @@ cudaError_t launch_quant_v(const uint16_t* x, int64_t rows, int K, int64_t ldx, 
   if (fmt == kQuantE4M3)
     return launch_pdl(quant_rows_kernel<V, kQuantE4M3>, dim3(static_cast<unsigned>(grid)),
                       dim3(32 * G * R), 0, st, x, rows, K, ldx, q, ldq, s, G);
+  if (fmt == kQuantF16)
+    return launch_pdl(quant_rows_kernel<V, kQuantF16>, dim3(static_cast<unsigned>(grid)),
+                      dim3(32 * G * R), 0, st, x, rows, K, ldx, q, ldq, s, G);
   return launch_pdl(quant_rows_kernel<V>, dim3(static_cast<unsigned>(grid)), dim3(32 * G * R), 0,
                     st, x, rows, K, ldx, q, ldq, s, G);
 }
 
-// fmt: kQuantInt8 (int8 codes) or kQuantE4M3 (E4M3 bit patterns).
+// fmt: kQuantInt8 (int8 codes), kQuantE4M3 (E4M3 bit patterns) or kQuantF16
+// (the int8 codes as fp16 values; ldq then counts fp16 elements).
 i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t* q, int64_t ldq,
                      float* s, cudaStream_t st, int fmt = kQuantInt8) {
   if (rows < 0 || K <= 0 || ldx < K || ldq < K) return I8_ERR_INVALID_ARG;
   if (rows > 0 && (!x || !q || !s)) return I8_ERR_INVALID_ARG;
   if (K % 16 != 0 || K > 131072 || rows > INT32_MAX) return I8_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(q) || !aligned4(s) || ldx % 8 != 0 || ldq % 16 != 0)
+  if (!aligned16(x) || !aligned16(q) || !aligned4(s) || ldx % 8 != 0 ||
+      ldq % (fmt == kQuantF16 ? 8 : 16) != 0)
     return I8_ERR_ALIGNMENT;
   if (rows == 0) return I8_OK;
   DeviceInfo* d;
@@ -183,6 +188,9 @@ i8_status quant_rows(const void* x, int64_t rows, int64_t K, int64_t ldx, int8_t
     // longer than 8 warps x 32 lanes x 16 vectors: the two-pass kernel
     if (fmt == kQuantE4M3)
       e = launch_pdl(quant_rows_long_kernel<kQuantE4M3>, dim3(static_cast<unsigned>(rows)),
+                     dim3(256), 0, st, xb, rows, Ki, ldx, q, ldq, s);
+    else if (fmt == kQuantF16)
+      e = launch_pdl(quant_rows_long_kernel<kQuantF16>, dim3(static_cast<unsigned>(rows)),
                      dim3(256), 0, st, xb, rows, Ki, ldx, q, ldq, s);
     else
       e = launch_pdl(quant_rows_long_kernel<kQuantInt8>, dim3(static_cast<unsigned>(rows)),
@@ -648,20 +656,22 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   return I8_OK;
 }
 
-// ----------------------------------------------------------------- E4M3 GEMM
-int fp8_cluster_capacity(DeviceInfo* d) {
+// ----------------------------------------------------------------- direct (converter-free) GEMM
+template <int KIND>
+int direct_cluster_capacity(DeviceInfo* d) {
   static int cached[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return d->sms / 2;
   if (cached[dev] > 0) return cached[dev];
-  auto kern = gemm_fp8_pair_kernel;
+  using Cfg = DirectCfg<KIND>;
+  auto kern = gemm_direct_pair_kernel<KIND>;
   int n = 0;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Fp8Cfg::SMEM_BYTES) == cudaSuccess) {
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) ==
+      cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (d->sms / 2), 1, 1);
-    cfg.blockDim = dim3(Fp8Cfg::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Fp8Cfg::SMEM_BYTES;
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
@@ -677,40 +687,44 @@ int fp8_cluster_capacity(DeviceInfo* d) {
   return n;
 }
 
-// Plan of the E4M3 GEMM: 256 x 256 tiles; when the tiles leave CTA pairs idle,
-// K splits of at least 4 blocks (512 K) by the same wave-efficiency rule as
-// the int8 table.  ws: fp32 partials [splits][M][round_up(N, 4)].
-struct Fp8Plan {
+// Plan of the direct GEMM: 256 x 256 tiles of 128-byte-deep K blocks (128
+// E4M3 or 64 fp16 codes); when the tiles leave CTA pairs idle, K splits of
+// at least 4 blocks by the same wave-efficiency rule as the int8 table.
+// ws: 4-byte partials (fp32 or int32) [splits][M][round_up(N, 4)].
+struct DirectPlan {
   int num_m, num_n, total_kb, splits, kb_per_split;
   int64_t tiles;
   int64_t ldw;
   size_t ws_bytes;
 };
 
-Fp8Plan plan_fp8(int64_t M, int64_t N, int64_t K, int pairs) {
-  Fp8Plan p{};
-  p.num_m = static_cast<int>((M + Fp8Cfg::PAIR_M - 1) / Fp8Cfg::PAIR_M);
-  p.num_n = static_cast<int>((N + Fp8Cfg::PAIR_N - 1) / Fp8Cfg::PAIR_N);
-  p.total_kb = static_cast<int>((K + Fp8Cfg::BK - 1) / Fp8Cfg::BK);
+DirectPlan plan_direct(int64_t M, int64_t N, int64_t K, int pairs, int bk) {
+  DirectPlan p{};
+  p.num_m = static_cast<int>((M + 255) / 256);
+  p.num_n = static_cast<int>((N + 255) / 256);
+  p.total_kb = static_cast<int>((K + bk - 1) / bk);
   p.tiles = static_cast<int64_t>(p.num_m) * p.num_n;
   p.splits = best_splits(p.tiles, pairs, p.total_kb);
   p.kb_per_split = (p.total_kb + p.splits - 1) / p.splits;
   p.splits = (p.total_kb + p.kb_per_split - 1) / p.kb_per_split;
   p.ldw = (N + 3) / 4 * 4;
   p.ws_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * static_cast<size_t>(M) *
-                                  static_cast<size_t>(p.ldw) * sizeof(float)
+                                  static_cast<size_t>(p.ldw) * 4
                             : 0;
   return p;
 }
 
-// E4M3 codes in, bf16 (dequant + bias) or fp32 accumulators out.  One
-// persistent launch of the pair kernel (plus the split-K fix-up when the
-// plan splits K); rows and columns beyond M, N are zero-filled on load and
-// clipped on store.
-i8_status gemm_fp8_common(const uint8_t* aq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
-                          int out_mode, void* out, int64_t ldo, const float* s_a,
-                          const float* s_w, const void* bias, void* ws, size_t ws_bytes,
-                          cudaStream_t st) {
+// The direct GEMM: E4M3 codes (KIND = kDirectE4M3) or fp16 values of int8
+// codes (kDirectF16) in; bf16 (dequant + bias) or the raw accumulator (fp32
+// for E4M3, exact int32 for fp16 codes) out.  One persistent launch of the
+// pair kernel, plus the split-K fix-up when the plan splits K; rows and
+// columns beyond M, N are zero-filled on load and clipped on store.
+template <int KIND>
+i8_status gemm_direct_common(const void* aq, const void* wq, int64_t M, int64_t N, int64_t K,
+                             int out_mode, void* out, int64_t ldo, const float* s_a,
+                             const float* s_w, const void* bias, void* ws, size_t ws_bytes,
+                             cudaStream_t st) {
+  using Cfg = DirectCfg<KIND>;
   if (M < 0 || N < 0 || K <= 0) return I8_ERR_INVALID_ARG;
   if (K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX) return I8_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return I8_OK;
@@ -723,16 +737,19 @@ i8_status gemm_fp8_common(const uint8_t* aq, const uint8_t* wq, int64_t M, int64
   if (out_mode != kOutBf16 && ldo % 4 != 0) return I8_ERR_ALIGNMENT;
   DeviceInfo* d;
   if (i8_status e = device_info(&d, nullptr)) return e;
-  const int clusters = fp8_cluster_capacity(d);
-  const Fp8Plan pl = plan_fp8(M, N, K, clusters);
+  const int clusters = direct_cluster_capacity<KIND>(d);
+  const DirectPlan pl = plan_direct(M, N, K, clusters, Cfg::BK);
   if (pl.tiles * pl.splits > INT32_MAX) return I8_ERR_UNSUPPORTED;
   if (pl.ws_bytes > 0) {
     if (!ws || ws_bytes < pl.ws_bytes) return I8_ERR_WORKSPACE;
     if (!aligned16(ws)) return I8_ERR_ALIGNMENT;
   }
   CUtensorMap ma, mb, my;
-  if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M, K, Fp8Cfg::BK, Fp8Cfg::BM) ||
-      !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, K, N, K, Fp8Cfg::BK, Fp8Cfg::BN))
+  const CUtensorMapDataType dt =
+      KIND == kDirectF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint64_t row_bytes = KIND == kDirectF16 ? 2 * K : K;
+  if (!encode_2d(&ma, dt, aq, K, M, row_bytes, Cfg::BK, Cfg::BM) ||
+      !encode_2d(&mb, dt, wq, K, N, row_bytes, Cfg::BK, Cfg::BN))
     return I8_ERR_CUDA;
   GemmParams gp{};
   gp.M = static_cast<int>(M);
@@ -744,6 +761,7 @@ i8_status gemm_fp8_common(const uint8_t* aq, const uint8_t* wq, int64_t M, int64
   gp.total_kb = pl.total_kb;
   gp.kb_per_split = pl.kb_per_split;
   gp.num_tiles = static_cast<int>(pl.tiles);
+  gp.chunk_stages = g_opt.chunk_k / 64;   // fp16 codes: 64 K per block
   gp.s_a = s_a;
   gp.s_w = s_w;
   gp.bias = static_cast<const uint16_t*>(bias);
@@ -764,8 +782,8 @@ i8_status gemm_fp8_common(const uint8_t* aq, const uint8_t* wq, int64_t M, int64
       return I8_ERR_CUDA;
   }
   const int grid = 2 * static_cast<int>(std::min<int64_t>(clusters, pl.tiles * pl.splits));
-  if (cudaError_t e = launch_pdl(gemm_fp8_pair_kernel, dim3(grid), dim3(Fp8Cfg::THREADS),
-                                 Fp8Cfg::SMEM_BYTES, st, ma, mb, my, gp))
+  if (cudaError_t e = launch_pdl(gemm_direct_pair_kernel<KIND>, dim3(grid), dim3(Cfg::THREADS),
+                                 Cfg::SMEM_BYTES, st, ma, mb, my, gp))
     return cuda_status(e);
   if (pl.splits > 1) {
     GemmParams rp = gp;
@@ -774,6 +792,10 @@ i8_status gemm_fp8_common(const uint8_t* aq, const uint8_t* wq, int64_t M, int64
     rp.ldo = ldo;
     const int64_t groups = M * ((N + 3) / 4);
     const int64_t blocks = std::min<int64_t>((groups + 255) / 256, static_cast<int64_t>(d->sms) * 16);
+    if (KIND == kDirectF16)
+      return cuda_status(launch_pdl(splitk_reduce_kernel, dim3(static_cast<unsigned>(blocks)),
+                                    dim3(256), 0, st, static_cast<const int32_t*>(ws),
+                                    gp.split_stride, pl.ldw, pl.splits, rp));
     return cuda_status(launch_pdl(splitk_reduce_f32_kernel, dim3(static_cast<unsigned>(blocks)),
                                   dim3(256), 0, st, static_cast<const float*>(ws),
                                   gp.split_stride, pl.ldw, pl.splits, rp));
@@ -856,22 +878,56 @@ size_t i8_gemm_e4m3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return 0;
   DeviceInfo* d;
   if (device_info(&d, nullptr) != I8_OK) return 0;
-  return plan_fp8(M, N, K, fp8_cluster_capacity(d)).ws_bytes;
+  return plan_direct(M, N, K, direct_cluster_capacity<kDirectE4M3>(d),
+                     DirectCfg<kDirectE4M3>::BK).ws_bytes;
 }
 
 i8_status i8_gemm_e4m3_f32(const uint8_t* aq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
                            float* c, int64_t ldc, void* ws, size_t ws_bytes,
                            i8_stream_t stream) {
-  return gemm_fp8_common(aq, wq, M, N, K, kOutInt32, c, ldc, nullptr, nullptr, nullptr, ws,
-                         ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+  return gemm_direct_common<kDirectE4M3>(aq, wq, M, N, K, kOutInt32, c, ldc, nullptr, nullptr,
+                                         nullptr, ws, ws_bytes,
+                                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 i8_status i8_gemm_e4m3_dequant_bias_bf16(const uint8_t* aq, const float* s_a, const uint8_t* wq,
                                          const float* s_w, const void* bias, int64_t M,
                                          int64_t N, int64_t K, void* y, int64_t ldy, void* ws,
                                          size_t ws_bytes, i8_stream_t stream) {
-  return gemm_fp8_common(aq, wq, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws, ws_bytes,
-                         reinterpret_cast<cudaStream_t>(stream));
+  return gemm_direct_common<kDirectE4M3>(aq, wq, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws,
+                                         ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_quant_act_pertoken_f16codes(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                         void* q16, int64_t ldq, float* s_a,
+                                         i8_stream_t stream) {
+  return quant_rows(x, M, K, ldx, static_cast<int8_t*>(q16), ldq, s_a,
+                    reinterpret_cast<cudaStream_t>(stream), kQuantF16);
+}
+
+size_t i8_gemm_f16codes_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX)
+    return 0;
+  DeviceInfo* d;
+  if (device_info(&d, nullptr) != I8_OK) return 0;
+  return plan_direct(M, N, K, direct_cluster_capacity<kDirectF16>(d),
+                     DirectCfg<kDirectF16>::BK).ws_bytes;
+}
+
+i8_status i8_gemm_int32_f16codes(const void* a16, const void* w16, int64_t M, int64_t N,
+                                 int64_t K, int32_t* c, int64_t ldc, void* ws, size_t ws_bytes,
+                                 i8_stream_t stream) {
+  return gemm_direct_common<kDirectF16>(a16, w16, M, N, K, kOutInt32, c, ldc, nullptr, nullptr,
+                                        nullptr, ws, ws_bytes,
+                                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+i8_status i8_gemm_dequant_bias_bf16_f16codes(const void* a16, const float* s_a, const void* w16,
+                                             const float* s_w, const void* bias, int64_t M,
+                                             int64_t N, int64_t K, void* y, int64_t ldy,
+                                             void* ws, size_t ws_bytes, i8_stream_t stream) {
+  return gemm_direct_common<kDirectF16>(a16, w16, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws,
+                                        ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 i8_status i8_layernorm_quant_act_pertoken(const void* h, int64_t M, int64_t K, int64_t ldh,

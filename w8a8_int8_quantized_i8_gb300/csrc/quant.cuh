@@ -117,6 +117,22 @@ __device__ __forceinline__ uint2 quant_vec8(uint4 v, float s, unsigned long long
   return make_uint2(low_bytes4(b[0], b[1], b[2], b[3]), low_bytes4(b[4], b[5], b[6], b[7]));
 }
 
+// Four int8 codes -> four fp16 values (exact).  x ^ 0x80 is x + 128 as an
+// unsigned byte u; the fp16 bit pattern 0x64uu is 1024 + u; subtracting
+// 1152 (0x6480) leaves x.
+__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+// Stores 8 codes at element e of a code row: one byte each, or, for the
+// fp16-code format, the same integers as fp16 values (16 bytes).
+template <int FMT>
+__device__ __forceinline__ void store_codes8(int8_t* qrow, int e, uint2 c);
+
 // Two fp32 values -> two E4M3 codes (lo in byte 0), round to nearest even,
 // finite saturation to +-448.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -146,11 +162,28 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-enum QuantFmt : int { kQuantInt8 = 0, kQuantE4M3 = 1 };
+// kQuantF16: the int8 decision, each code stored as the fp16 value of the
+// same integer (2 bytes per code), ready for the tensor core's fp16 kind.
+enum QuantFmt : int { kQuantInt8 = 0, kQuantE4M3 = 1, kQuantF16 = 2 };
+
+template <int FMT>
+__device__ __forceinline__ void store_codes8(int8_t* qrow, int e, uint2 c) {
+  if constexpr (FMT == kQuantF16) {
+    uint4 o;
+    s8x4_to_f16x4(c.x, o.x, o.y);
+    s8x4_to_f16x4(c.y, o.z, o.w);
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(qrow + 2 * e), "r"(o.x),
+                 "r"(o.y), "r"(o.z), "r"(o.w)
+                 : "memory");
+  } else {
+    st_v2(qrow + e, c.x, c.y);
+  }
+}
 
 // Grid: ceil(rows / R) CTAs of 32 * G * R threads (G * R <= 8); warp w of a
 // CTA serves row (blockIdx.x * R + w / G), slice (w % G) of that row.
-// FMT selects the code format (int8 or E4M3, one byte per element either way).
+// FMT selects the code format: int8 or E4M3 (one byte per code), or fp16
+// values of the int8 codes (two bytes; ldq then counts fp16 elements).
 template <int V, int FMT = kQuantInt8>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ x,
                                                          int64_t rows, int K, int64_t ldx,
@@ -201,12 +234,12 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   if (valid_row && wig == 0 && lane == 0) scale[row] = s;
   if (!valid_row) return;
 
-  int8_t* qr = q + row * ldq;
+  int8_t* qr = q + row * ldq * (FMT == kQuantF16 ? 2 : 1);
   if (amax == 0.0f) {
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int e = slice0 + (i * 32 + lane) * 8;
-      if (e < K) st_v2(qr + e, 0u, 0u);
+      if (e < K) store_codes8<FMT>(qr, e, make_uint2(0u, 0u));
     }
     return;
   }
@@ -229,7 +262,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
     const int e = slice0 + (i * 32 + lane) * 8;
     if (e < K) {
       const uint2 c = quant_vec8(v[i], s, rr, fast);
-      st_v2(qr + e, c.x, c.y);
+      store_codes8<FMT>(qr, e, c);
     }
   }
 }
@@ -276,7 +309,7 @@ __global__ void __launch_bounds__(256) quant_rows_long_kernel(const uint16_t* __
   const float amax = __uint_as_float(abits << 16);
   const float s = __fdiv_rn(amax, FMT == kQuantE4M3 ? 448.0f : 127.0f);
   if (threadIdx.x == 0) scale[row] = s;
-  int8_t* qr = q + row * ldq;
+  int8_t* qr = q + row * ldq * (FMT == kQuantF16 ? 2 : 1);
   const bool fast = s >= 0x1p-126f;
   const float r = __frcp_rn(s);
   const unsigned long long rr = f2(r, r);
@@ -287,7 +320,7 @@ __global__ void __launch_bounds__(256) quant_rows_long_kernel(const uint16_t* __
       if constexpr (FMT == kQuantE4M3) c = quant_vec8_e4m3(v, s);
       else c = quant_vec8(v, s, rr, fast);
     }
-    st_v2(qr + 8 * i, c.x, c.y);
+    store_codes8<FMT>(qr, 8 * i, c);
   }
   pdl_trigger();
 }
