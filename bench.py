@@ -74,16 +74,20 @@ def _peaks():
 # still hash to the value recorded in the summary.
 PROFILE_SUMMARIES = {
     ("int8", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_w8a8_qkv768_M2560_K3072_N9216.md",
-    ("e4m3", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_fp8_qkv768_M2560_K3072_N9216.md",
+    ("e4m3", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_direct_e4m3_qkv768_M2560_K3072_N9216.md",
+    ("f16codes", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_direct_f16codes_qkv768_M2560_K3072_N9216.md",
 }
 KERNEL_SOURCES = {
     "int8": ("w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
              "w8a8_int8_quantized_i8_gb300/csrc/gemm_pair.cuh",
              "w8a8_int8_quantized_i8_gb300/csrc/ptx.cuh",
              "w8a8_int8_quantized_i8_gb300/csrc/quant.cuh"),
-    "e4m3": ("w8a8_int8_quantized_i8_gb300/csrc/gemm_fp8.cuh",
+    "e4m3": ("w8a8_int8_quantized_i8_gb300/csrc/gemm_direct.cuh",
              "w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
              "w8a8_int8_quantized_i8_gb300/csrc/ptx.cuh"),
+    "f16codes": ("w8a8_int8_quantized_i8_gb300/csrc/gemm_direct.cuh",
+                 "w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
+                 "w8a8_int8_quantized_i8_gb300/csrc/ptx.cuh"),
 }
 
 
@@ -431,6 +435,11 @@ def run_ours(args, shape, dist, rank, world, local):
     e4m3 = None
     if not args.no_e4m3:
         e4m3 = _run_e4m3(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, local)
+    # ---- the same exact W8A8 product with the codes held as fp16 values
+    # (quantizer fp16-code output, weights widened offline), no on-chip widening
+    f16codes = None
+    if not args.no_e4m3:
+        f16codes = _run_f16codes(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, local)
 
     # ---- oracle on the host cores (rank 0, N = 1 only)
     cpu = None
@@ -470,6 +479,7 @@ def run_ours(args, shape, dist, rank, world, local):
             "vs_int8_engine": {"int8_tops_measured": INT8_ENGINE_TOPS, "gemm_ratio": gemm_tops / INT8_ENGINE_TOPS,
                                "source": "mma.sync m16n8k32 s8 rate on this GB300 (bench_engines.py)"},
             "e4m3": e4m3,
+            "f16codes": f16codes,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TOPS", "h2d_bytes_per_step": M * K * 2,
                     "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
@@ -547,11 +557,85 @@ def _run_e4m3(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, l
         "roofline": {"bound": "tensor", "achieved": g_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": g_tflops / peak, "traffic": _profiled_traffic(shape.name, "e4m3"),
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
-                     "kernel": "gemm_fp8_pair_kernel",
+                     "kernel": "gemm_direct_pair_kernel<E4M3>",
                      "peak_note": f"{peak_kind} dense bf16 burst x {FP8_OVER_BF16:g} "
                                   "(nominal dense fp8 / bf16 rate: 4.5 / 2.25 PF/s)"},
         "parity": "codes bit-exact; fp32 accumulators within the derived rounding bound of the "
                   "exact sum; bf16 = oracle epilogue of the GPU accumulators, bit for bit",
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+    }
+
+
+def _run_f16codes(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, local):
+    """The exact path with fp16-held codes: quant (fp16 codes) + fused GEMM."""
+    from w8a8_int8_quantized_i8_gb300 import binding
+    M, K, N = shape.M, shape.K, shape.N
+    vp = ctypes.c_void_p
+    wq, s_w = i8.quant_weight_perchannel(d["w"].to(dev))
+    w16 = i8.widen_weight_codes(wq)
+    del wq
+    b_dev = d["bias"].to(dev)
+    ws_bytes = i8.f16codes_workspace_bytes(M, N, K)
+    sets = [dict(x=d["x"].to(dev), aq=torch.empty(M, K, dtype=torch.float16, device=dev),
+                 s_a=torch.empty(M, dtype=torch.float32, device=dev),
+                 w=w16.clone(), y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+                 ws=torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev))
+            for _ in range(R)]
+    del w16
+    calls = [((vp(t["x"].data_ptr()), M, K, K, vp(t["aq"].data_ptr()), K, vp(t["s_a"].data_ptr()), sp),
+              (vp(t["aq"].data_ptr()), vp(t["s_a"].data_ptr()), vp(t["w"].data_ptr()),
+               vp(s_w.data_ptr()), vp(b_dev.data_ptr()), M, N, K, vp(t["y"].data_ptr()), N,
+               vp(t["ws"].data_ptr()), ws_bytes, sp))
+             for t in sets]
+    qf, gf = lib.i8_quant_act_pertoken_f16codes, lib.i8_gemm_dequant_bias_bf16_f16codes
+
+    def step(i, evg=None):
+        qa, ga = calls[i % R]
+        st = qf(*qa)
+        if evg is not None:
+            evg[0].record(stream)
+        st |= gf(*ga)
+        if evg is not None:
+            evg[1].record(stream)
+        if st:
+            raise RuntimeError(f"libi8 fp16-code call failed with status {st}")
+
+    steps = max(10, min(args.steps, 1000))
+    for i in range(max(3, args.warmup)):
+        step(i)
+    binding.sync_check(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    evg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        step(i, evg[i])
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    binding.sync_check(dev)
+    ops = 2.0 * M * N * K
+    t_ms = e0.elapsed_time(e1) / steps
+    g_ms = statistics.mean(a.elapsed_time(b) for a, b in evg)
+    g_tops = ops / (g_ms * 1e-3) / 1e12
+    return {
+        "value": ops / (t_ms * 1e-3) / 1e12, "unit": "TOPS", "ms_per_step": t_ms, "steps": steps,
+        "dtype": "int8 codes held as fp16 (exact int32 accumulation)", "gemm_us": g_ms * 1e3,
+        "bytes_note": "activation codes 2 B (written by the quantizer), weight codes 2 B (widened offline)",
+        "roofline": {"bound": "tensor", "achieved": g_tops, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": g_tops / tc_peak, "traffic": _profiled_traffic(shape.name, "f16codes"),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)",
+                     "kernel": "gemm_direct_pair_kernel<F16 codes>",
+                     "peak_note": f"{peak_kind} dense bf16 burst (the fp16 kind's nominal rate)"},
+        "parity": "int32 and bf16 bit-identical to the oracle and to the int8-code kernels",
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
     }
 
@@ -565,7 +649,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qkv768")
     ap.add_argument("--weights", choices=["int8", "w16"], default="int8")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--no-e4m3", action="store_true", help="skip the E4M3 (FP8) arm")
+    ap.add_argument("--no-e4m3", action="store_true",
+                    help="skip the E4M3 (FP8) arm and the fp16-code variant")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
