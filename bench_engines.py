@@ -348,7 +348,7 @@ def main(argv=None):
         for shape in inputs.sweep_shapes():
             shape_row(shape, args.iters, full=True)
     if args.stack:
-        for fmt in ("int8", "e4m3"):
+        for fmt in ("int8", "f16codes", "e4m3"):
             for fused in (False, True):
                 stack_time(fused=fused, fmt=fmt)
     return 0

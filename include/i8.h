@@ -232,13 +232,15 @@ i8_status i8_gemm_dequant_bias_bf16_f16codes(const void* a16, const float* s_a,
  *            differ from the exactly rounded value by one bf16 step where it
  *            lies within fp32 noise of a rounding midpoint.
  *   GELU:    erf form, y = bf16(0.5 x (1 + erf(x / sqrt 2))), fp32 arithmetic.
- *   x [M,K] bf16 (row stride ldx elements, ldx % 8 == 0), q [M,K] codes (int8
- *   or E4M3 bit patterns, row stride ldq bytes, ldq % 16 == 0), s_a [M] fp32;
+ *   x [M,K] bf16 (row stride ldx elements, ldx % 8 == 0), q [M,K] codes: int8
+ *   or E4M3 bit patterns (row stride ldq bytes, ldq % 16 == 0), or, for
+ *   I8_CODES_F16, the int8 codes as fp16 values (row stride ldq elements,
+ *   ldq % 8 == 0); s_a [M] fp32;
  *   y [M,K] bf16 or NULL: when given, receives the bf16 producer output (for
  *   checking, or when the layer's input is also needed elsewhere).
  *   K % 16 == 0 and K <= 32768 (the row is held in registers); larger K is
  *   I8_ERR_UNSUPPORTED.  eps >= 0 and finite.  fmt: i8_code_format.        */
-typedef enum { I8_CODES_INT8 = 0, I8_CODES_E4M3 = 1 } i8_code_format;
+typedef enum { I8_CODES_INT8 = 0, I8_CODES_E4M3 = 1, I8_CODES_F16 = 2 } i8_code_format;
 i8_status i8_layernorm_quant_act_pertoken(const void* x_bf16, int64_t M,
                                           int64_t K, int64_t ldx, float eps,
                                           int fmt, void* q, int64_t ldq,

@@ -24,7 +24,11 @@ pytestmark = pytest.mark.gpu
 
 
 def _codes(t: torch.Tensor) -> np.ndarray:
-    return t.view(torch.uint8).cpu().numpy() if t.dtype == torch.float8_e4m3fn else t.cpu().numpy()
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).cpu().numpy()
+    if t.dtype == torch.float16:                 # fp16-held int8 codes
+        return t.cpu().float().numpy().astype(np.int8)
+    return t.cpu().numpy()
 
 
 def _run(op, x, fmt, want_y):
@@ -58,16 +62,19 @@ def _check(orc, op, x_cpu, fmt, min_exact=0.999):
     frac = float((yb == y_ref).mean())
     assert frac >= min_exact, f"only {frac:.5f} of the producer outputs equal the oracle's"
     # codes and scales from the GPU's own bf16 row, bit for bit
-    qo, so = orc.quant_rows(yb) if fmt == "int8" else orc.quant_rows_e4m3(yb)
+    qo, so = orc.quant_rows_e4m3(yb) if fmt == "e4m3" else orc.quant_rows(yb)
     assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
     bad = np.argwhere(_codes(q) != qo)
     assert bad.size == 0, f"{len(bad)} codes differ, first {bad[:4].tolist()}"
     # the optional output does not change the codes
     assert torch.equal(q.view(torch.uint8), q2.view(torch.uint8)) and torch.equal(s, s2)
+    if fmt == "f16codes":                         # exact integers, +0.0 for zero
+        qf = q.cpu().float().numpy()
+        assert np.array_equal(qf, np.round(qf)) and not np.signbit(qf[qf == 0]).any()
     return frac
 
 
-@pytest.mark.parametrize("fmt", ["int8", "e4m3"])
+@pytest.mark.parametrize("fmt", ["int8", "e4m3", "f16codes"])
 @pytest.mark.parametrize("op", ["layernorm", "gelu"])
 @pytest.mark.parametrize("M,K", [(64, 256), (7, 48), (1, 16), (129, 3072), (33, 12288),
                                  (5, 32768), (2560, 3072)])
@@ -141,3 +148,17 @@ def test_fused_dit_stack_layers_sampled(orc):
         wq, s_w = orc.quant_rows(inputs.bits(w.cpu()))
         want = orc.dequant_bias(orc.gemm_s32(aq, wq), s_a, s_w, inputs.bits(b.cpu()))
         assert_bf16_exact(gpu_bf16_bits(y), want, f"block {blk} {name}")
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_f16codes_stack_is_bit_identical_to_int8_stack(fused):
+    """The fp16-held codes change the storage, not the arithmetic: two blocks of
+    the DiT stack give the same bits through either path."""
+    M = 1024
+    h = inputs.activations(M, dit_stack.WIDTH, torch.Generator().manual_seed(9)).cuda()
+    s8 = dit_stack.build(blocks=2, seed=7, fmt="int8")
+    s16 = dit_stack.build(blocks=2, seed=7, fmt="f16codes")
+    o8 = dit_stack.forward(s8, h, fused=fused)
+    o16 = dit_stack.forward(s16, h, fused=fused)
+    i8.sync_check()
+    assert torch.equal(o8.view(torch.int16), o16.view(torch.int16))

@@ -419,7 +419,7 @@ def linear_f16codes(x, w16, s_w, bias=None, out=None, workspace=None):
 # bf16 result, in one kernel: the codes of the next linear layer's input
 # without writing and re-reading that input in bf16.
 
-_FMT = {"int8": (0, torch.int8), "e4m3": (1, torch.float8_e4m3fn)}
+_FMT = {"int8": (0, torch.int8), "e4m3": (1, torch.float8_e4m3fn), "f16codes": (2, torch.float16)}
 
 
 def _producer(fn_name, x, extra, fmt, want_y):

@@ -242,12 +242,12 @@ i8_status producer_quant(int op, const void* x, int64_t rows, int64_t K, int64_t
                          int fmt, void* q, int64_t ldq, float* s, void* y, int64_t ldy,
                          cudaStream_t st) {
   if (rows < 0 || K <= 0 || ldx < K || ldq < K || (y && ldy < K)) return I8_ERR_INVALID_ARG;
-  if (fmt != kQuantInt8 && fmt != kQuantE4M3) return I8_ERR_INVALID_ARG;
+  if (fmt != kQuantInt8 && fmt != kQuantE4M3 && fmt != kQuantF16) return I8_ERR_INVALID_ARG;
   if (op == kOpLayerNorm && !(eps >= 0.0f && eps <= 3.0e38f)) return I8_ERR_INVALID_ARG;
   if (rows > 0 && (!x || !q || !s)) return I8_ERR_INVALID_ARG;
   if (K % 16 != 0 || K > 32768 || rows > INT32_MAX) return I8_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(q) || !aligned4(s) || ldx % 8 != 0 || ldq % 16 != 0 ||
-      (y && (!aligned16(y) || ldy % 8 != 0)))
+  if (!aligned16(x) || !aligned16(q) || !aligned4(s) || ldx % 8 != 0 ||
+      ldq % (fmt == kQuantF16 ? 8 : 16) != 0 || (y && (!aligned16(y) || ldy % 8 != 0)))
     return I8_ERR_ALIGNMENT;
   if (rows == 0) return I8_OK;
   DeviceInfo* d;
@@ -263,6 +263,8 @@ i8_status producer_quant(int op, const void* x, int64_t rows, int64_t K, int64_t
   const cudaError_t e =
       fmt == kQuantE4M3
           ? launch_producer<kQuantE4M3>(op, xb, rows, Ki, ldx, eps, qb, ldq, s, yb, ldy, need, G, st)
+      : fmt == kQuantF16
+          ? launch_producer<kQuantF16>(op, xb, rows, Ki, ldx, eps, qb, ldq, s, yb, ldy, need, G, st)
           : launch_producer<kQuantInt8>(op, xb, rows, Ki, ldx, eps, qb, ldq, s, yb, ldy, need, G, st);
   return cuda_status(e);
 }

@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(256) producer_quant_kernel(
       if (e < K) *reinterpret_cast<uint4*>(yr + e) = v[i];
     }
   }
-  int8_t* qr = q + row * ldq;
+  int8_t* qr = q + row * ldq * (FMT == kQuantF16 ? 2 : 1);
   const bool fast = s >= 0x1p-126f;
   const float r = __frcp_rn(s);
   const unsigned long long rr = f2(r, r);
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(256) producer_quant_kernel(
         if constexpr (FMT == kQuantE4M3) c = quant_vec8_e4m3(v[i], s);
         else c = quant_vec8(v[i], s, rr, fast);
       }
-      st_v2(qr + e, c.x, c.y);
+      store_codes8<FMT>(qr, e, c);
     }
   }
 }

@@ -20,8 +20,9 @@ LN is a LayerNorm without affine parameters (eps 1e-6).  Two ways to run it:
   directly (the bf16 layer input is never written); only the block-output LN
   and the V slice (a strided view, no copy) stay outside.
 
-``fmt`` picks the codes: "int8" (the exact int8 path) or "e4m3" (the FP8
-arm).  Weights are drawn with a seeded CUDA generator, ~N(0, 0.02), bias
+``fmt`` picks the codes: "int8" (the exact int8 path), "f16codes" (the same
+exact path with the codes held as fp16 values, weights widened offline) or
+"e4m3" (the FP8 arm).  Weights are drawn with a seeded CUDA generator, ~N(0, 0.02), bias
 ~N(0, 0.01), and quantized per output channel once (offline).
 """
 from __future__ import annotations
@@ -55,7 +56,7 @@ def layer_weight(seed: int, N: int, K: int, device) -> tuple[torch.Tensor, torch
 
 def build(blocks: int = 28, seed: int = 5, device="cuda", fmt: str = "int8") -> list[dict[str, Linear]]:
     """Quantized weights of `blocks` blocks (each layer's seed is derived from `seed`)."""
-    quant = i8.quant_weight_perchannel if fmt == "int8" else i8.quant_weight_perchannel_e4m3
+    quant = i8.quant_weight_perchannel_e4m3 if fmt == "e4m3" else i8.quant_weight_perchannel
     stack = []
     for blk in range(blocks):
         layers = {}
@@ -63,6 +64,8 @@ def build(blocks: int = 28, seed: int = 5, device="cuda", fmt: str = "int8") -> 
             s = seed * 100003 + blk * 8 + li
             w, b = layer_weight(s, N, K, device)
             wq, s_w = quant(w)
+            if fmt == "f16codes":
+                wq = i8.widen_weight_codes(wq)
             del w
             layers[name] = Linear(wq, s_w, b, s, fmt)
         stack.append(layers)
@@ -76,6 +79,8 @@ def layer_norm(x: torch.Tensor) -> torch.Tensor:
 def _gemm(lin: Linear, aq, s_a):
     if lin.fmt == "int8":
         return i8.gemm_dequant_bias_bf16(aq, s_a, lin.wq, lin.s_w, lin.bias)
+    if lin.fmt == "f16codes":
+        return i8.gemm_dequant_bias_bf16_f16codes(aq, s_a, lin.wq, lin.s_w, lin.bias)
     return i8.gemm_e4m3_dequant_bias_bf16(aq, s_a, lin.wq, lin.s_w, lin.bias)
 
 
@@ -94,6 +99,8 @@ def forward(stack, h: torch.Tensor, record=None, timer=None, fused: bool = False
                 timer(True)
             if lin.fmt == "int8":
                 y = i8.linear(x, lin.wq, lin.s_w, lin.bias)
+            elif lin.fmt == "f16codes":
+                y = i8.linear_f16codes(x, lin.wq, lin.s_w, lin.bias)
             else:
                 y = i8.linear_e4m3(x, lin.wq, lin.s_w, lin.bias)
             if timer:
