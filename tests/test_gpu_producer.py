@@ -1,11 +1,12 @@
 """GPU parity of the fused producer-quantizers (LayerNorm or GELU, then the
 per-token quantizer, in one kernel) against the oracle.
 
-* The bf16 producer output y (the kernel's optional output): within one bf16
-  step of the oracle's fp64 value rounded once (plus, for the LayerNorm, the
+* The bf16 producer output y (the kernel's optional output).  GELU: equal to
+  the oracle's fp64 value rounded once, everywhere (the kernel reads a table
+  of exactly those values).  LayerNorm: within one bf16 step of it (plus the
   fp32 mean's rounding bound, which matters only where y is near 0), and
-  equal to it almost everywhere (the kernel reduces in fp32, so values within
-  fp32 noise of a rounding midpoint may round the other way).
+  equal almost everywhere (the kernel reduces in fp32, so values within fp32
+  noise of a rounding midpoint may round the other way).
 * Codes and scales: bit-exact against the oracle's quantizer applied to the
   GPU's own y (the integer decision is taken from the same bf16 row).
 * Asking for y does not change the codes.
@@ -60,6 +61,10 @@ def _check(orc, op, x_cpu, fmt, min_exact=0.999):
     bad = np.abs(g - w) > tol
     assert not bad.any(), f"{int(bad.sum())} producer outputs beyond one bf16 step"
     frac = float((yb == y_ref).mean())
+    if op == "gelu":
+        # the GELU producer reads a table of the fp64 value rounded once: the
+        # oracle's definition, so every output is equal
+        min_exact = 1.0
     assert frac >= min_exact, f"only {frac:.5f} of the producer outputs equal the oracle's"
     # codes and scales from the GPU's own bf16 row, bit for bit
     qo, so = orc.quant_rows_e4m3(yb) if fmt == "e4m3" else orc.quant_rows(yb)
@@ -101,6 +106,20 @@ def test_layernorm_special_rows(orc, fmt):
     i8.sync_check()
     assert s[0].item() == 0.0 and s[1].item() == 0.0
     assert (_codes(q)[:2] == 0).all()
+
+
+def test_gelu_every_bf16_input_matches_oracle(orc):
+    """All 65536 bf16 patterns (finite ones) through the GELU producer: each
+    output is the oracle's correctly rounded GELU."""
+    pats = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):
+        keep = np.isfinite((pats.astype(np.uint32) << 16).view(np.float32))
+    pats = pats[keep]
+    pats = pats[: len(pats) // 256 * 256].reshape(-1, 256)
+    x = inputs.from_bits(pats)
+    _, _, y = i8.gelu_quant_act_pertoken(to_dev(x), want_y=True)
+    i8.sync_check()
+    assert np.array_equal(gpu_bf16_bits(y), orc.gelu_rows(pats))
 
 
 def test_producer_strided_input_and_errors(orc):

@@ -235,6 +235,62 @@ cudaError_t launch_producer(int op, const uint16_t* x, int64_t rows, int K, int6
   return launch_producer_v<16, FMT>(op, x, rows, K, ldx, eps, q, ldq, s, y, ldy, G, st);
 }
 
+// The GELU table is built once per device, by the first GELU call, on that
+// call's stream, which is then synchronized (so the first call must not be
+// made during stream capture).
+bool g_gelu_table_ready[kMaxDevices] = {};
+
+i8_status ensure_gelu_table(cudaStream_t st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return I8_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_gelu_table_ready[dev]) return I8_OK;
+  gelu_table_kernel<<<65536 / 256, 256, 0, st>>>();
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return I8_ERR_CUDA;
+  g_gelu_table_ready[dev] = true;
+  return I8_OK;
+}
+
+template <int V, int FMT>
+cudaError_t launch_gelu_table_v(const uint16_t* x, int64_t rows, int K, int64_t ldx, int8_t* q,
+                                int64_t ldq, float* s, uint16_t* y, int64_t ldy, int G, int sms,
+                                cudaStream_t st) {
+  auto kern = gelu_table_quant_kernel<V, FMT>;
+  constexpr int kSmem = 65536 * 2;   // the table
+  static bool smem_set[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!smem_set[dev]) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      if (e != cudaSuccess) return e;
+      smem_set[dev] = true;
+    }
+  }
+  const int R = 16 / G;
+  const int64_t groups = (rows + R - 1) / R;
+  const int grid = static_cast<int>(std::min<int64_t>(groups, sms));
+  return launch_pdl(kern, dim3(grid), dim3(512), kSmem, st, x, rows, K, ldx, q, ldq, s, y, ldy, G);
+}
+
+template <int FMT>
+cudaError_t launch_gelu_table(const uint16_t* x, int64_t rows, int K, int64_t ldx, int8_t* q,
+                              int64_t ldq, float* s, uint16_t* y, int64_t ldy, int need, int G,
+                              int sms, cudaStream_t st) {
+  if (need <= 1) return launch_gelu_table_v<1, FMT>(x, rows, K, ldx, q, ldq, s, y, ldy, G, sms, st);
+  if (need <= 2) return launch_gelu_table_v<2, FMT>(x, rows, K, ldx, q, ldq, s, y, ldy, G, sms, st);
+  if (need <= 3) return launch_gelu_table_v<3, FMT>(x, rows, K, ldx, q, ldq, s, y, ldy, G, sms, st);
+  if (need <= 4) return launch_gelu_table_v<4, FMT>(x, rows, K, ldx, q, ldq, s, y, ldy, G, sms, st);
+  if (need <= 6) return launch_gelu_table_v<6, FMT>(x, rows, K, ldx, q, ldq, s, y, ldy, G, sms, st);
+  if (need <= 8) return launch_gelu_table_v<8, FMT>(x, rows, K, ldx, q, ldq, s, y, ldy, G, sms, st);
+  if (need <= 12) return launch_gelu_table_v<12, FMT>(x, rows, K, ldx, q, ldq, s, y, ldy, G, sms, st);
+  return launch_gelu_table_v<16, FMT>(x, rows, K, ldx, q, ldq, s, y, ldy, G, sms, st);
+}
+
 // LayerNorm / GELU of each row, then the per-row quantizer of the bf16
 // result; y (optional) receives that bf16 result.  Rows must fit the
 // register-resident layout: K <= 32768.
@@ -260,6 +316,16 @@ i8_status producer_quant(int op, const void* x, int64_t rows, int64_t K, int64_t
   auto* qb = static_cast<int8_t*>(q);
   auto* yb = static_cast<uint16_t*>(y);
   const int Ki = static_cast<int>(K);
+  if (op == kOpGelu) {
+    if (i8_status e = ensure_gelu_table(st)) return e;
+    const cudaError_t e =
+        fmt == kQuantE4M3
+            ? launch_gelu_table<kQuantE4M3>(xb, rows, Ki, ldx, qb, ldq, s, yb, ldy, need, G, d->sms, st)
+        : fmt == kQuantF16
+            ? launch_gelu_table<kQuantF16>(xb, rows, Ki, ldx, qb, ldq, s, yb, ldy, need, G, d->sms, st)
+            : launch_gelu_table<kQuantInt8>(xb, rows, Ki, ldx, qb, ldq, s, yb, ldy, need, G, d->sms, st);
+    return cuda_status(e);
+  }
   const cudaError_t e =
       fmt == kQuantE4M3
           ? launch_producer<kQuantE4M3>(op, xb, rows, Ki, ldx, eps, qb, ldq, s, yb, ldy, need, G, st)

@@ -189,4 +189,115 @@ __global__ void __launch_bounds__(256) producer_quant_kernel(
   }
 }
 
+// ----------------------------------------------------------------- GELU by table
+// bf16 has 65536 bit patterns, so the correctly rounded GELU of every input
+// fits a 128 KB table: g_gelu_table[b] = bf16_rne(x * Phi(x)) for x = the bf16
+// with bits b, evaluated in fp64 (Phi(x) = erfc(-x / sqrt 2) / 2, no
+// cancellation) and rounded once.  gelu_table_kernel fills it on the device,
+// once per device; the GELU producer then streams rows through a copy of the
+// table in shared memory.  The output is exactly the fp64 value rounded once,
+// which is the oracle's definition.
+static __device__ __align__(16) uint16_t g_gelu_table[65536];
+
+__global__ void __launch_bounds__(256) gelu_table_kernel() {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= 65536) return;
+  const double x = static_cast<double>(__uint_as_float(static_cast<uint32_t>(b) << 16));
+  const double phi = 0.5 * erfc(-x * 0.70710678118654752440);
+  const __nv_bfloat16 y = __double2bfloat16(x * phi);
+  g_gelu_table[b] = *reinterpret_cast<const uint16_t*>(&y);
+}
+
+// Persistent: grid = SMs, 16 warps per CTA; the table is copied into shared
+// memory once per CTA, then rows are processed R = 16 / G at a time (G warps
+// per row, V 16-byte vectors per lane, as quant_rows_kernel).
+template <int V, int FMT>
+__global__ void __launch_bounds__(512, 1) gelu_table_quant_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int K, int64_t ldx, int8_t* __restrict__ q,
+    int64_t ldq, float* __restrict__ scale, uint16_t* __restrict__ y_out, int64_t ldy, int G) {
+  extern __shared__ __align__(16) uint16_t tab[];
+  __shared__ uint32_t red_m[16];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int R = 16 / G;
+  const int sub = warp / G;            // which row of the group of R
+  const int wig = warp % G;
+  const int slice0 = wig * (32 * 8 * V);
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(g_gelu_table);
+    uint4* dst = reinterpret_cast<uint4*>(tab);
+    for (int i = threadIdx.x; i < 65536 / 8; i += 512) dst[i] = src[i];
+  }
+  __syncthreads();
+  pdl_wait();  // X may be the previous kernel's output
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * R; base < rows;
+       base += static_cast<int64_t>(gridDim.x) * R) {
+    const int64_t row = base + sub;
+    const bool valid = row < rows;
+    const uint16_t* xr = x + (valid ? row : 0) * ldx;
+    uint4 v[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = slice0 + (i * 32 + lane) * 8;
+      v[i] = (valid && e < K) ? ld_stream_v4(xr + e) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint32_t amax2 = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w[j] = static_cast<uint32_t>(tab[w[j] & 0xFFFFu]) |
+               (static_cast<uint32_t>(tab[w[j] >> 16]) << 16);
+      v[i] = make_uint4(w[0], w[1], w[2], w[3]);
+      const int e = slice0 + (i * 32 + lane) * 8;
+      if (e < K) {
+        amax2 = absmax_bf16x2(amax2, v[i].x);
+        amax2 = absmax_bf16x2(amax2, v[i].y);
+        amax2 = absmax_bf16x2(amax2, v[i].z);
+        amax2 = absmax_bf16x2(amax2, v[i].w);
+      }
+    }
+    amax2 &= 0x7FFF7FFFu;
+    uint32_t abits = max(amax2 & 0xFFFFu, amax2 >> 16);
+    abits = __reduce_max_sync(0xFFFFFFFFu, abits);
+    if (G > 1) {
+      if (lane == 0) red_m[warp] = abits;
+      __syncthreads();
+      abits = 0;
+      for (int j = 0; j < G; ++j) abits = max(abits, red_m[sub * G + j]);
+      __syncthreads();   // red_m is rewritten by the next group of rows
+    }
+    if (!valid) continue;
+    const float amax = __uint_as_float(abits << 16);
+    const float s = __fdiv_rn(amax, FMT == kQuantE4M3 ? 448.0f : 127.0f);
+    if (wig == 0 && lane == 0) scale[row] = s;
+    if (y_out) {
+      uint16_t* yr = y_out + row * ldy;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int e = slice0 + (i * 32 + lane) * 8;
+        if (e < K) *reinterpret_cast<uint4*>(yr + e) = v[i];
+      }
+    }
+    int8_t* qr = q + row * ldq * (FMT == kQuantF16 ? 2 : 1);
+    const bool fast = s >= 0x1p-126f;
+    const float r = __frcp_rn(s);
+    const unsigned long long rr = f2(r, r);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = slice0 + (i * 32 + lane) * 8;
+      if (e < K) {
+        uint2 c = make_uint2(0u, 0u);
+        if (amax != 0.0f) {
+          if constexpr (FMT == kQuantE4M3) c = quant_vec8_e4m3(v[i], s);
+          else c = quant_vec8(v[i], s, rr, fast);
+        }
+        store_codes8<FMT>(qr, e, c);
+      }
+    }
+  }
+  pdl_trigger();
+}
+
 }  // namespace i8
