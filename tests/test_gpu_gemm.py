@@ -415,3 +415,37 @@ def test_stream_k_workspace_garbage_and_graph_replay(stream_k_option):
         torch.cuda.synchronize()
         assert torch.equal(out, want)
     i8.sync_check()
+
+
+@pytest.mark.parametrize("M,N,K", [(2, 9216, 3072), (16, 3072, 12288)])
+def test_skinny_split_k_workspace_garbage_and_graph_replay(orc, M, N, K):
+    """The skinny kernel's K splits: a workspace full of random bytes,
+    back-to-back calls and CUDA-graph replays (the call clears its
+    accumulator on the stream, so the clear is captured too) all give the
+    exact result."""
+    a = inputs.random_int8(M, K, seed=M + 11)
+    w = inputs.random_int8(N, K, seed=N + 12)
+    want = orc.gemm_s32(a.numpy(), w.numpy())
+    a, w = a.cuda(), w.cuda()
+    nbytes = i8.workspace_bytes(M, N, K)
+    assert nbytes > 0
+    ws = torch.randint(-128, 128, (nbytes,), dtype=torch.int8, device="cuda").view(torch.uint8)
+    out = torch.empty(M, N, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        out.fill_(7)
+        i8.gemm_int32(a, w, out=out, workspace=ws)
+        i8.sync_check()
+        assert np.array_equal(out.cpu().numpy(), want)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            i8.gemm_int32(a, w, out=out, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        out.fill_(7)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), want)
+    i8.sync_check()

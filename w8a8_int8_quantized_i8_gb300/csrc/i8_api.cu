@@ -401,19 +401,22 @@ int best_splits(int64_t tiles, int slots, int total_kb) {
 //   * split-K (exact int32 partials + a reduction) when the tiles cannot fill
 //     every worker.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
-               bool b16 = false, size_t ws_cap = SIZE_MAX) {
+               bool b16 = false, size_t ws_cap = SIZE_MAX, int skinny_slots = 0) {
   Plan p;
   if (pair_clusters <= 0) pair_clusters = sms / 2;
+  if (skinny_slots <= 0) skinny_slots = 2 * sms;
   p.total_kb = static_cast<int>((K + 127) / 128);
   if (M <= g_opt.skinny_max_m) {
-    // int32 [M, N] accumulator + one completion counter per 64-row N-block
-    // K split for about two CTAs per SM; each split owns whole 512-K chunks.
+    // K split so that the whole grid is resident at once (skinny_slots CTAs):
+    // a second wave would stream its weights only after the first finished.
+    // Each split owns whole 512-K chunks.  Workspace: an int32 [M, N]
+    // accumulator + one completion counter per 64-row N-block, zeroed by the
+    // call before the launch.
     p.skinny = true;
     p.num_n = static_cast<int>((N + kSkinnyRows - 1) / kSkinnyRows);
     p.num_m = 1;
     const int chunks = static_cast<int>((K + kSkinnyK - 1) / kSkinnyK);
-    int splits = g_opt.force_splits > 0 ? g_opt.force_splits
-                                        : static_cast<int>((2 * sms + p.num_n - 1) / p.num_n);
+    int splits = g_opt.force_splits > 0 ? g_opt.force_splits : skinny_slots / p.num_n;
     splits = std::max(1, std::min(splits, chunks));
     p.kb_per_split = (chunks + splits - 1) / splits;          // chunks per split
     p.splits = (chunks + p.kb_per_split - 1) / p.kb_per_split;
@@ -566,6 +569,34 @@ i8_status launch_pair_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const CU
                                 my, mp, gp));
 }
 
+// CTAs of the skinny kernel resident at once on this device (its split
+// choice keeps the grid within one wave).
+int skinny_slots(DeviceInfo* d, bool b16) {
+  static int cached[kMaxDevices][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 2 * d->sms;
+  if (cached[dev][b16] > 0) return cached[dev][b16];
+  int n = 0;
+  cudaError_t e;
+  if (b16) {
+    e = cudaFuncSetAttribute(gemm_skinny_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SkinnyCfg<true>::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_skinny_kernel<true>, 128,
+                                                        SkinnyCfg<true>::SMEM_BYTES);
+  } else {
+    e = cudaFuncSetAttribute(gemm_skinny_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SkinnyCfg<false>::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_skinny_kernel<false>, 128,
+                                                        SkinnyCfg<false>::SMEM_BYTES);
+  }
+  cudaGetLastError();
+  if (e != cudaSuccess || n <= 0) n = 2;
+  cached[dev][b16] = n * d->sms;
+  return cached[dev][b16];
+}
+
 using PairConv = PairCfg<3, 3, true, true>;    // int8 weights, CTA pair
 using PairWide = PairCfg<4, 4, true, false>;   // pre-widened weights, CTA pair
 using CfgConv128 = GemmCfg<128, 3, 3, true, true>;   // int8 weights
@@ -594,7 +625,7 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   if (i8_status e = device_info(&d, nullptr)) return e;
   const int clusters = b16 ? pair_cluster_capacity<PairWide>(d, 1)
                            : pair_cluster_capacity<PairConv>(d, 0);
-  const Plan pl = make_plan(M, N, K, d->sms, clusters, b16, ws_cap);
+  const Plan pl = make_plan(M, N, K, d->sms, clusters, b16, ws_cap, skinny_slots(d, b16));
   if (pl.ws_bytes > 0) {
     if (!ws || ws_bytes < pl.ws_bytes) return I8_ERR_WORKSPACE;
     if (!aligned16(ws)) return I8_ERR_ALIGNMENT;
@@ -1018,8 +1049,10 @@ size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   DeviceInfo* d;
   if (device_info(&d, nullptr) != I8_OK) return 0;
   // the larger of the two weight formats' plans, so one query serves both
-  const size_t a = make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0), false).ws_bytes;
-  const size_t b = make_plan(M, N, K, d->sms, pair_cluster_capacity<PairWide>(d, 1), true).ws_bytes;
+  const size_t a = make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0), false,
+                             SIZE_MAX, skinny_slots(d, false)).ws_bytes;
+  const size_t b = make_plan(M, N, K, d->sms, pair_cluster_capacity<PairWide>(d, 1), true,
+                             SIZE_MAX, skinny_slots(d, true)).ws_bytes;
   return a > b ? a : b;
 }
 
@@ -1050,7 +1083,8 @@ i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a, 
       N <= INT32_MAX) {
     DeviceInfo* d;
     if (i8_status e = device_info(&d, nullptr)) return e;
-    if (make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0), false, kStaticWsBytes)
+    if (make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0), false, kStaticWsBytes,
+                  skinny_slots(d, false))
             .ws_bytes > kStaticWsBytes)
       return I8_ERR_WORKSPACE;
     if (i8_status e = static_ws_address(&ws)) return e;
