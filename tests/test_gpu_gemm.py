@@ -16,6 +16,8 @@ from tests._util import assert_bf16_exact, gpu_bf16_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
+SKINNY_DEFAULT = 8     # the library's default weight-streaming threshold
+
 INT_SHAPES = [
     (64, 128, 256),
     (1, 8, 16),
@@ -24,7 +26,7 @@ INT_SHAPES = [
     (256, 384, 1024),
     (300, 200, 1040),
     (2, 9216, 3072),       # skinny: split-K
-    (16, 3072, 12288),     # skinny, deep: split-K
+    (16, 3072, 12288),     # few tokens, deep: split-K
     (1024, 1024, 4096),
 ]
 
@@ -245,12 +247,17 @@ def test_linear_both_kernels_qkv_sampled(orc, cta_pair_option, mode, widened):
 
 @pytest.mark.parametrize("M,N,K", [(1, 200, 8192), (16, 520, 8192), (9, 64, 131072)])
 def test_skinny_kernel_adversarial_exact(orc, M, N, K):
-    """Few tokens (M <= 16) take the weight-streaming kernel: per-CTA partial
-    sums over 512 K in fp32 (< 2^24 for +-127 operands) plus int32 atomics."""
+    """Few tokens take the weight-streaming kernel (forced up to M = 16 here):
+    per-CTA partial sums over 512 K in fp32 (< 2^24 for +-127 operands) plus
+    int32 atomics."""
     a, w = _adversarial(max(M, 4), N, K, seed=M + N)
     a = a[:M].contiguous()
-    c = i8.gemm_int32(to_dev(a), to_dev(w))
-    i8.sync_check()
+    i8.set_option("skinny_max_m", 16)
+    try:
+        c = i8.gemm_int32(to_dev(a), to_dev(w))
+        i8.sync_check()
+    finally:
+        i8.set_option("skinny_max_m", SKINNY_DEFAULT)
     got = c.cpu().numpy()
     want = orc.gemm_s32(a.numpy(), w.numpy())
     bad = np.argwhere(got != want)
@@ -263,13 +270,17 @@ def test_skinny_kernel_widened_weights_and_off_switch(orc, M):
     d = inputs.linear_inputs(shape)
     rows = np.arange(M)
     want = _oracle_linear_rows(orc, d["x"], d["w"], d["bias"], rows)
-    y16 = _gpu_linear(d["x"], d["w"], d["bias"], widened=True)
+    i8.set_option("skinny_max_m", 16)  # the weight-streaming kernel, forced up to M = 16
+    try:
+        y16 = _gpu_linear(d["x"], d["w"], d["bias"], widened=True)
+    finally:
+        i8.set_option("skinny_max_m", SKINNY_DEFAULT)
     assert_bf16_exact(gpu_bf16_bits(y16), want, "skinny w16")
     i8.set_option("skinny_max_m", 0)   # the tiled kernels for the same shape
     try:
         y8 = _gpu_linear(d["x"], d["w"], d["bias"], widened=False)
     finally:
-        i8.set_option("skinny_max_m", 16)
+        i8.set_option("skinny_max_m", SKINNY_DEFAULT)
     assert_bf16_exact(gpu_bf16_bits(y8), want, "tiled")
 
 

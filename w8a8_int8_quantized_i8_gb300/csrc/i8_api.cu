@@ -67,7 +67,7 @@ struct Options {
   int force_bn = 0;        // 0 = table, else 128 or 256
   int quant_vpl = 6;       // max 16-byte vectors per lane in the quantizer
   int cta_pair = 0;        // 0 = table, 1 = never, 2 = whenever the shape allows
-  int skinny_max_m = 16;   // token counts up to this use the weight-streaming kernel (0 = off)
+  int skinny_max_m = 8;    // token counts up to this use the weight-streaming kernel (0 = off)
   int pdl = 1;             // launch with programmatic stream serialization
   int quant_rows = 0;      // quantizer rows per CTA (0 = by shape)
   int stream_k = 1;        // CTA-pair stream-K: 0 never, 1 by the table, 2 whenever pairs idle
@@ -406,7 +406,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
   if (pair_clusters <= 0) pair_clusters = sms / 2;
   if (skinny_slots <= 0) skinny_slots = 2 * sms;
   p.total_kb = static_cast<int>((K + 127) / 128);
-  if (M <= g_opt.skinny_max_m) {
+  // Few tokens: the weight-streaming kernel, which measured faster than the
+  // tiled kernels up to M = 8 (up to M = 2 for weights above 48 M codes).
+  if (M <= g_opt.skinny_max_m && (M <= 2 || N * K <= (int64_t(48) << 20))) {
     // K split so that the whole grid is resident at once (skinny_slots CTAs):
     // a second wave would stream its weights only after the first finished.
     // Each split owns whole 512-K chunks.  Workspace: an int32 [M, N]
