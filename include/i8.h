@@ -326,7 +326,17 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *                       gain (K >= 8192 and whole tiles leave many pairs
  *                       idle), 2 whenever whole tiles leave pairs idle,
  *                       0 never.
- * Changing FORCE_SPLITS changes i8_gemm_workspace_bytes(). */
+ *   I8_OPT_NVTX         1: every call of this header opens an NVTX range
+ *                       named after the call (visible in Nsight timelines;
+ *                       free when no tool is attached); 0 (default): none.
+ * Changing FORCE_SPLITS changes i8_gemm_workspace_bytes().
+ *
+ * The environment variable I8_OPTIONS, read once when the library is
+ * loaded, sets options without code changes: a comma-separated list of
+ * name=value pairs with the names chunk_k, force_splits, max_ctas, tile_n,
+ * quant_vpl, cta_pair, skinny_max_m, pdl, quant_rows, stream_k, nvtx (for
+ * example "chunk_k=512,stream_k=0").  Entries with an unknown name or an
+ * invalid value are ignored. */
 typedef enum {
   I8_OPT_CHUNK_K = 1,
   I8_OPT_FORCE_SPLITS = 2,
@@ -337,9 +347,13 @@ typedef enum {
   I8_OPT_SKINNY_MAX_M = 7,
   I8_OPT_PDL = 8,
   I8_OPT_QUANT_ROWS = 9,
-  I8_OPT_STREAM_K = 10
+  I8_OPT_STREAM_K = 10,
+  I8_OPT_NVTX = 11
 } i8_option;
 i8_status i8_set_option(i8_option opt, int64_t value);
+/* Current value of an option (I8_ERR_INVALID_ARG for an unknown option or a
+ * NULL value pointer). */
+i8_status i8_get_option(i8_option opt, int64_t* value);
 
 /* Failure-detection self-test: queues a one-thread kernel that waits on a
  * pipeline barrier nothing will ever complete, through the same bounded wait

@@ -108,6 +108,34 @@ def test_options_validation(lib):
     assert lib.i8_selftest_timeout(0, None) == 1
 
 
+def test_get_option_and_nvtx_ranges(lib):
+    v = ctypes.c_int64(-1)
+    assert lib.i8_get_option(1, ctypes.byref(v)) == 0 and v.value == 1024
+    assert lib.i8_get_option(77, ctypes.byref(v)) == 1
+    assert lib.i8_get_option(1, None) == 1
+    assert lib.i8_set_option(11, 1) == 0                  # NVTX ranges on
+    assert lib.i8_get_option(11, ctypes.byref(v)) == 0 and v.value == 1
+    # calls rejected on the host still open and close their range cleanly
+    assert lib.i8_gemm_int32(P(0x10000), P(0x10000), 4, 8, 24, P(0x10000), 8, None, 0, None) == 3
+    assert lib.i8_set_option(11, 2) == 1
+    assert lib.i8_set_option(11, 0) == 0
+
+
+def test_options_from_the_environment(tmp_path):
+    """I8_OPTIONS is read when the library loads; bad entries are ignored."""
+    import subprocess
+    import sys
+    code = ("import ctypes, sys; sys.path.insert(0, %r); "
+            "from w8a8_int8_quantized_i8_gb300 import binding; "
+            "print(binding.get_option('chunk_k'), binding.get_option('stream_k'), "
+            "binding.get_option('nvtx'), binding.get_option('pdl'))") % str(build.ROOT)
+    env = dict(__import__("os").environ,
+               I8_OPTIONS="chunk_k=512,stream_k=0,nvtx=1,pdl=7,bogus=3,tile_n=abc")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         check=True).stdout.split()
+    assert out == ["512", "0", "1", "1"]
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(OSError):
         binding.load(str(tmp_path / "missing_libi8.so"))

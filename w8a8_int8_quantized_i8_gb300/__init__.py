@@ -9,7 +9,8 @@ functions below are its torch-tensor binding.
 """
 from .binding import (I8Error, e4m3_workspace_bytes, f16codes_workspace_bytes,
                       gelu_quant_act_pertoken, gemm_dequant_bias_bf16_f16codes,
-                      gemm_int32_f16codes, linear_f16codes, quant_act_pertoken_f16codes, gemm_dequant_bias_bf16,
+                      gemm_int32_f16codes, get_option, linear_f16codes,
+                      quant_act_pertoken_f16codes, gemm_dequant_bias_bf16,
                       gemm_e4m3_dequant_bias_bf16, gemm_e4m3_f32, gemm_int32,
                       layernorm_quant_act_pertoken, linear, linear_e4m3, load, quant_act_pertoken,
                       quant_act_pertoken_e4m3, quant_weight_perchannel,
@@ -18,7 +19,7 @@ from .binding import (I8Error, e4m3_workspace_bytes, f16codes_workspace_bytes,
 
 __all__ = [
     "I8Error", "e4m3_workspace_bytes", "f16codes_workspace_bytes", "gelu_quant_act_pertoken",
-    "gemm_dequant_bias_bf16_f16codes", "gemm_int32_f16codes", "linear_f16codes",
+    "gemm_dequant_bias_bf16_f16codes", "gemm_int32_f16codes", "get_option", "linear_f16codes",
     "quant_act_pertoken_f16codes", "gemm_dequant_bias_bf16", "gemm_e4m3_dequant_bias_bf16",
     "gemm_e4m3_f32", "gemm_int32", "layernorm_quant_act_pertoken", "linear", "linear_e4m3", "load", "quant_act_pertoken",
     "quant_act_pertoken_e4m3", "quant_weight_perchannel", "quant_weight_perchannel_e4m3",

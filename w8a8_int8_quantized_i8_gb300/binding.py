@@ -25,7 +25,7 @@ STATUS = {
     4: "I8_ERR_WORKSPACE", 5: "I8_ERR_CUDA", 6: "I8_ERR_DEVICE_TIMEOUT",
 }
 OPTIONS = {"chunk_k": 1, "force_splits": 2, "max_ctas": 3, "tile_n": 4, "quant_vpl": 5, "cta_pair": 6,
-           "skinny_max_m": 7, "pdl": 8, "quant_rows": 9, "stream_k": 10}
+           "skinny_max_m": 7, "pdl": 8, "quant_rows": 9, "stream_k": 10, "nvtx": 11}
 
 
 class I8Error(RuntimeError):
@@ -68,6 +68,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "i8_widen_weight_codes": ([vp, i64, i64, vp, vp], st),
             "i8_gemm_dequant_bias_bf16_w16": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, sz, vp], st),
             "i8_set_option": ([ctypes.c_int, i64], st),
+            "i8_get_option": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int64)], st),
             "i8_gemm_dequant_bias_bf16_noalloc": ([vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp], st),
             "i8_quant_weight_perchannel_e4m3": ([vp, i64, i64, i64, vp, i64, vp, vp], st),
             "i8_quant_act_pertoken_e4m3": ([vp, i64, i64, i64, vp, i64, vp, vp], st),
@@ -461,6 +462,12 @@ def gelu_quant_act_pertoken(x: torch.Tensor, fmt: str = "int8", want_y: bool = F
 
 def set_option(name: str, value: int) -> None:
     _check(load().i8_set_option(OPTIONS[name], int(value)), f"i8_set_option({name})")
+
+
+def get_option(name: str) -> int:
+    v = ctypes.c_int64(0)
+    _check(load().i8_get_option(OPTIONS[name], ctypes.byref(v)), f"i8_get_option({name})")
+    return int(v.value)
 
 
 def sync_check(device=None) -> None:

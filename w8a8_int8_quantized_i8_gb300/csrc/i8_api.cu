@@ -3,6 +3,7 @@
 // the launches.  The whole library is this one translation unit.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
 #include <cstdlib>
@@ -71,8 +72,21 @@ struct Options {
   int pdl = 1;             // launch with programmatic stream serialization
   int quant_rows = 0;      // quantizer rows per CTA (0 = by shape)
   int stream_k = 1;        // CTA-pair stream-K: 0 never, 1 by the table, 2 whenever pairs idle
+  int nvtx = 0;            // NVTX range around every ABI call
 };
 Options g_opt;
+
+// NVTX range for the lifetime of one ABI call (when I8_OPT_NVTX is on).
+struct NvtxScope {
+  bool on;
+  explicit NvtxScope(const char* name) : on(g_opt.nvtx != 0) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~NvtxScope() {
+    if (on) nvtxRangePop();
+  }
+};
+#define I8_NVTX() NvtxScope i8_nvtx_scope_(__func__)
 
 struct DeviceInfo {
   bool init = false;
@@ -953,28 +967,33 @@ const char* i8_version(void) { return "i8 0.1.0 sm_103a"; }
 
 i8_status i8_quant_weight_perchannel(const void* w, int64_t N, int64_t K, int64_t ldw, int8_t* wq,
                                      int64_t ldq, float* s_w, i8_stream_t stream) {
+  I8_NVTX();
   return quant_rows(w, N, K, ldw, wq, ldq, s_w, reinterpret_cast<cudaStream_t>(stream));
 }
 
 i8_status i8_quant_act_pertoken(const void* x, int64_t M, int64_t K, int64_t ldx, int8_t* aq,
                                 int64_t ldq, float* s_a, i8_stream_t stream) {
+  I8_NVTX();
   return quant_rows(x, M, K, ldx, aq, ldq, s_a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 i8_status i8_quant_weight_perchannel_e4m3(const void* w, int64_t N, int64_t K, int64_t ldw,
                                           uint8_t* wq, int64_t ldq, float* s_w,
                                           i8_stream_t stream) {
+  I8_NVTX();
   return quant_rows(w, N, K, ldw, reinterpret_cast<int8_t*>(wq), ldq, s_w,
                     reinterpret_cast<cudaStream_t>(stream), kQuantE4M3);
 }
 
 i8_status i8_quant_act_pertoken_e4m3(const void* x, int64_t M, int64_t K, int64_t ldx,
                                      uint8_t* aq, int64_t ldq, float* s_a, i8_stream_t stream) {
+  I8_NVTX();
   return quant_rows(x, M, K, ldx, reinterpret_cast<int8_t*>(aq), ldq, s_a,
                     reinterpret_cast<cudaStream_t>(stream), kQuantE4M3);
 }
 
 size_t i8_gemm_e4m3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  I8_NVTX();
   if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX)
     return 0;
   DeviceInfo* d;
@@ -986,6 +1005,7 @@ size_t i8_gemm_e4m3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 i8_status i8_gemm_e4m3_f32(const uint8_t* aq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
                            float* c, int64_t ldc, void* ws, size_t ws_bytes,
                            i8_stream_t stream) {
+  I8_NVTX();
   return gemm_direct_common<kDirectE4M3>(aq, wq, M, N, K, kOutInt32, c, ldc, nullptr, nullptr,
                                          nullptr, ws, ws_bytes,
                                          reinterpret_cast<cudaStream_t>(stream));
@@ -995,6 +1015,7 @@ i8_status i8_gemm_e4m3_dequant_bias_bf16(const uint8_t* aq, const float* s_a, co
                                          const float* s_w, const void* bias, int64_t M,
                                          int64_t N, int64_t K, void* y, int64_t ldy, void* ws,
                                          size_t ws_bytes, i8_stream_t stream) {
+  I8_NVTX();
   return gemm_direct_common<kDirectE4M3>(aq, wq, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws,
                                          ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1002,11 +1023,13 @@ i8_status i8_gemm_e4m3_dequant_bias_bf16(const uint8_t* aq, const float* s_a, co
 i8_status i8_quant_act_pertoken_f16codes(const void* x, int64_t M, int64_t K, int64_t ldx,
                                          void* q16, int64_t ldq, float* s_a,
                                          i8_stream_t stream) {
+  I8_NVTX();
   return quant_rows(x, M, K, ldx, static_cast<int8_t*>(q16), ldq, s_a,
                     reinterpret_cast<cudaStream_t>(stream), kQuantF16);
 }
 
 size_t i8_gemm_f16codes_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  I8_NVTX();
   if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX)
     return 0;
   DeviceInfo* d;
@@ -1018,6 +1041,7 @@ size_t i8_gemm_f16codes_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 i8_status i8_gemm_int32_f16codes(const void* a16, const void* w16, int64_t M, int64_t N,
                                  int64_t K, int32_t* c, int64_t ldc, void* ws, size_t ws_bytes,
                                  i8_stream_t stream) {
+  I8_NVTX();
   return gemm_direct_common<kDirectF16>(a16, w16, M, N, K, kOutInt32, c, ldc, nullptr, nullptr,
                                         nullptr, ws, ws_bytes,
                                         reinterpret_cast<cudaStream_t>(stream));
@@ -1027,6 +1051,7 @@ i8_status i8_gemm_dequant_bias_bf16_f16codes(const void* a16, const float* s_a, 
                                              const float* s_w, const void* bias, int64_t M,
                                              int64_t N, int64_t K, void* y, int64_t ldy,
                                              void* ws, size_t ws_bytes, i8_stream_t stream) {
+  I8_NVTX();
   return gemm_direct_common<kDirectF16>(a16, w16, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws,
                                         ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1034,6 +1059,7 @@ i8_status i8_gemm_dequant_bias_bf16_f16codes(const void* a16, const float* s_a, 
 i8_status i8_layernorm_quant_act_pertoken(const void* h, int64_t M, int64_t K, int64_t ldh,
                                           float eps, int fmt, void* q, int64_t ldq, float* s_a,
                                           void* y, int64_t ldy, i8_stream_t stream) {
+  I8_NVTX();
   return producer_quant(kOpLayerNorm, h, M, K, ldh, eps, fmt, q, ldq, s_a, y, ldy,
                         reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1041,11 +1067,13 @@ i8_status i8_layernorm_quant_act_pertoken(const void* h, int64_t M, int64_t K, i
 i8_status i8_gelu_quant_act_pertoken(const void* u, int64_t M, int64_t K, int64_t ldu, int fmt,
                                      void* q, int64_t ldq, float* s_a, void* y, int64_t ldy,
                                      i8_stream_t stream) {
+  I8_NVTX();
   return producer_quant(kOpGelu, u, M, K, ldu, 0.0f, fmt, q, ldq, s_a, y, ldy,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  I8_NVTX();
   if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX)
     return 0;
   DeviceInfo* d;
@@ -1060,6 +1088,7 @@ size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 
 i8_status i8_gemm_int32(const int8_t* aq, const int8_t* wq, int64_t M, int64_t N, int64_t K,
                         int32_t* c, int64_t ldc, void* ws, size_t ws_bytes, i8_stream_t stream) {
+  I8_NVTX();
   return gemm_common(aq, wq, false, M, N, K, kOutInt32, c, ldc, nullptr, nullptr, nullptr, ws,
                      ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1068,6 +1097,7 @@ i8_status i8_gemm_dequant_bias_bf16(const int8_t* aq, const float* s_a, const in
                                     const float* s_w, const void* bias, int64_t M, int64_t N,
                                     int64_t K, void* y, int64_t ldy, void* ws, size_t ws_bytes,
                                     i8_stream_t stream) {
+  I8_NVTX();
   return gemm_common(aq, wq, false, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1076,6 +1106,7 @@ i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a, 
                                             const float* s_w, const void* bias, int64_t M,
                                             int64_t N, int64_t K, void* y, int64_t ldy,
                                             i8_stream_t stream) {
+  I8_NVTX();
   // Same checks and kernels as i8_gemm_dequant_bias_bf16; only the split-K
   // scratch comes from the library's fixed device array.  The split partials
   // are written in full before the reduction reads them, so nothing in the
@@ -1098,6 +1129,7 @@ i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a, 
 
 i8_status i8_widen_weight_codes(const int8_t* wq, int64_t N, int64_t K, void* w16,
                                 i8_stream_t stream) {
+  I8_NVTX();
   if (N < 0 || K <= 0) return I8_ERR_INVALID_ARG;
   if (K % 16 != 0 || K > 131072) return I8_ERR_UNSUPPORTED;
   if (N == 0) return I8_OK;
@@ -1117,6 +1149,7 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a, cons
                                         const float* s_w, const void* bias, int64_t M, int64_t N,
                                         int64_t K, void* y, int64_t ldy, void* ws,
                                         size_t ws_bytes, i8_stream_t stream) {
+  I8_NVTX();
   return gemm_common(aq, w16, true, M, N, K, kOutBf16, y, ldy, s_a, s_w, bias, ws, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1163,11 +1196,34 @@ i8_status i8_set_option(i8_option opt, int64_t value) {
       if (value != 0 && value != 128 && value != 256) return I8_ERR_INVALID_ARG;
       g_opt.force_bn = static_cast<int>(value);
       return I8_OK;
+    case I8_OPT_NVTX:
+      if (value != 0 && value != 1) return I8_ERR_INVALID_ARG;
+      g_opt.nvtx = static_cast<int>(value);
+      return I8_OK;
+  }
+  return I8_ERR_INVALID_ARG;
+}
+
+i8_status i8_get_option(i8_option opt, int64_t* value) {
+  if (!value) return I8_ERR_INVALID_ARG;
+  switch (opt) {
+    case I8_OPT_CHUNK_K: *value = g_opt.chunk_k; return I8_OK;
+    case I8_OPT_FORCE_SPLITS: *value = g_opt.force_splits; return I8_OK;
+    case I8_OPT_MAX_CTAS: *value = g_opt.max_ctas; return I8_OK;
+    case I8_OPT_TILE_N: *value = g_opt.force_bn; return I8_OK;
+    case I8_OPT_QUANT_VPL: *value = g_opt.quant_vpl; return I8_OK;
+    case I8_OPT_CTA_PAIR: *value = g_opt.cta_pair; return I8_OK;
+    case I8_OPT_SKINNY_MAX_M: *value = g_opt.skinny_max_m; return I8_OK;
+    case I8_OPT_PDL: *value = g_opt.pdl; return I8_OK;
+    case I8_OPT_QUANT_ROWS: *value = g_opt.quant_rows; return I8_OK;
+    case I8_OPT_STREAM_K: *value = g_opt.stream_k; return I8_OK;
+    case I8_OPT_NVTX: *value = g_opt.nvtx; return I8_OK;
   }
   return I8_ERR_INVALID_ARG;
 }
 
 i8_status i8_selftest_timeout(int limit_ms, i8_stream_t stream) {
+  I8_NVTX();
   if (limit_ms < 1 || limit_ms > 5000) return I8_ERR_INVALID_ARG;
   selftest_timeout_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       static_cast<unsigned long long>(limit_ms) * 1000000ull);
@@ -1175,6 +1231,7 @@ i8_status i8_selftest_timeout(int limit_ms, i8_stream_t stream) {
 }
 
 i8_status i8_sync_check(i8_stream_t stream) {
+  I8_NVTX();
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return I8_ERR_CUDA;
   unsigned int word = 0;
@@ -1189,3 +1246,43 @@ i8_status i8_sync_check(i8_stream_t stream) {
 }
 
 }  // extern "C"
+
+namespace {
+
+// I8_OPTIONS="name=value,..." applied once when the library is loaded.
+struct EnvOptions {
+  EnvOptions() {
+    const char* env = std::getenv("I8_OPTIONS");
+    if (!env) return;
+    static const struct {
+      const char* name;
+      i8_option opt;
+    } kNames[] = {{"chunk_k", I8_OPT_CHUNK_K},       {"force_splits", I8_OPT_FORCE_SPLITS},
+                  {"max_ctas", I8_OPT_MAX_CTAS},     {"tile_n", I8_OPT_TILE_N},
+                  {"quant_vpl", I8_OPT_QUANT_VPL},   {"cta_pair", I8_OPT_CTA_PAIR},
+                  {"skinny_max_m", I8_OPT_SKINNY_MAX_M}, {"pdl", I8_OPT_PDL},
+                  {"quant_rows", I8_OPT_QUANT_ROWS}, {"stream_k", I8_OPT_STREAM_K},
+                  {"nvtx", I8_OPT_NVTX}};
+    const char* p = env;
+    while (*p) {
+      const char* end = std::strchr(p, ',');
+      const size_t len = end ? static_cast<size_t>(end - p) : std::strlen(p);
+      const char* eq = static_cast<const char*>(std::memchr(p, '=', len));
+      if (eq) {
+        const size_t nlen = static_cast<size_t>(eq - p);
+        char* vend = nullptr;
+        const long long v = std::strtoll(eq + 1, &vend, 10);
+        if (vend == p + len) {
+          for (const auto& n : kNames)
+            if (std::strlen(n.name) == nlen && std::strncmp(n.name, p, nlen) == 0)
+              i8_set_option(n.opt, v);
+        }
+      }
+      if (!end) break;
+      p = end + 1;
+    }
+  }
+};
+EnvOptions g_env_options;
+
+}  // namespace
