@@ -206,6 +206,24 @@ def shape_row(shape, iters, full=True):
 
     res["step_e4m3_us"] = _time(step8, iters) * 1e6
     res["gemm_e4m3_us"] = _time(gemm8, iters) * 1e6
+    # the exact path with fp16-held codes (weights widened offline)
+    a16 = [torch.empty(M, K, dtype=torch.float16, device=dev) for _ in range(R)]
+    for r in range(R):
+        i8.quant_act_pertoken_f16codes(xs[r], a16[r], sas[r])
+    ws16 = torch.empty(max(i8.f16codes_workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=dev)
+
+    def step16(i):
+        r = i % R
+        i8.quant_act_pertoken_f16codes(xs[r], a16[r], sas[r])
+        i8.gemm_dequant_bias_bf16_f16codes(a16[r], sas[r], w16, s_w, b, out=ys[r], workspace=ws16)
+
+    def gemm16(i):
+        r = i % R
+        i8.gemm_dequant_bias_bf16_f16codes(a16[r], sas[r], w16, s_w, b, out=ys[r], workspace=ws16)
+
+    res["step_f16codes_us"] = _time(step16, iters) * 1e6
+    res["gemm_f16codes_us"] = _time(gemm16, iters) * 1e6
+    res["gemm_f16codes_tops"] = ops / (res["gemm_f16codes_us"] * 1e-6) / 1e12
     i8.sync_check()
     res["gemm_e4m3_tflops"] = ops / (res["gemm_e4m3_us"] * 1e-6) / 1e12
     res["e4m3_k_splits"] = "yes" if i8.e4m3_workspace_bytes(M, N, K) else "no"

@@ -299,7 +299,9 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *   I8_OPT_CHUNK_K      K-elements per exact fp32 accumulation chunk inside
  *                       the GEMM: a multiple of 64 in [64, 1024] (default
  *                       1024: partial sums stay below 127*127*1024 < 2^24).
- *   I8_OPT_FORCE_SPLITS K-splits to use for every shape (0 = the table).
+ *   I8_OPT_FORCE_SPLITS K-splits to use for every shape, on every GEMM route
+ *                       (int8, fp16-held and E4M3 codes; at most one split
+ *                       per K block); 0 = the plan's own choice.
  *   I8_OPT_MAX_CTAS     cap on the persistent grid (0 = one CTA per SM).
  *   I8_OPT_TILE_N       GEMM tile width, 128 or 256 (0 = the table).
  *   I8_OPT_CTA_PAIR     GEMM on CTA pairs (256 x 256 tiles per cluster of 2):
@@ -329,7 +331,7 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *   I8_OPT_NVTX         1: every call of this header opens an NVTX range
  *                       named after the call (visible in Nsight timelines;
  *                       free when no tool is attached); 0 (default): none.
- * Changing FORCE_SPLITS changes i8_gemm_workspace_bytes().
+ * Changing FORCE_SPLITS changes the *_workspace_bytes() results.
  *
  * The environment variable I8_OPTIONS, read once when the library is
  * loaded, sets options without code changes: a comma-separated list of

@@ -107,7 +107,8 @@ def test_quant_e4m3_weights_and_special_rows(orc):
 # ----------------------------------------------------------------- GEMM
 GEMM_SHAPES = [(64, 128, 256), (1, 8, 16), (7, 24, 48), (129, 136, 272), (300, 520, 1040),
                (256, 256, 3072), (200, 304, 12288), (513, 264, 400),
-               # few tiles: the plan splits K (fp32 partials + ordered fix-up)
+               # few tiles: the plan's cost model splits K (fp32 partials + ordered
+               # fix-up) for the first and third, not for the others
                (16, 3072, 3072), (256, 9216, 3072), (1, 3072, 12288), (2, 18432, 3072)]
 
 
@@ -247,3 +248,26 @@ def test_e4m3_error_paths():
                          torch.zeros(8, 24, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 3
     i8.sync_check()
+
+
+@pytest.mark.parametrize("splits", [2, 5, 16])
+def test_gemm_e4m3_forced_splits_within_bound(orc, splits):
+    """Any split count (uneven K ranges included) keeps the accumulators
+    within the bound and gives the same bf16 outputs as the oracle's
+    epilogue on those accumulators."""
+    M, N, K = 300, 520, 3072
+    shape = inputs.LinearShape("t", M, K, N, seed=splits, outliers=True)
+    d = inputs.linear_inputs(shape)
+    aq, s_a = i8.quant_act_pertoken_e4m3(to_dev(d["x"]))
+    wq, s_w = i8.quant_weight_perchannel_e4m3(to_dev(d["w"]))
+    i8.set_option("force_splits", splits)
+    try:
+        assert i8.e4m3_workspace_bytes(M, N, K) > 0
+        c = i8.gemm_e4m3_f32(aq, wq)
+        y = i8.gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, to_dev(d["bias"]))
+        i8.sync_check()
+    finally:
+        i8.set_option("force_splits", 0)
+    exact, P, got = _check_acc(orc, aq, wq, c, f"splits {splits}")
+    _check_bf16(orc, gpu_bf16_bits(y), exact, P, got, s_a.cpu().numpy(), s_w.cpu().numpy(),
+                inputs.bits(d["bias"]), K, f"splits {splits}")

@@ -37,7 +37,7 @@ def test_quant_f16codes_are_the_int8_codes(orc, M, K):
 
 SHAPES = [(64, 128, 256), (1, 8, 16), (7, 24, 48), (129, 136, 272), (256, 384, 1024),
           (300, 200, 1040), (1024, 1024, 4096), (513, 264, 400),
-          # few tiles: exact int32 split-K partials
+          # few tiles: the plan splits K (exact int32 partials)
           (2, 9216, 3072), (16, 3072, 12288), (256, 3072, 3072)]
 
 
@@ -115,3 +115,26 @@ def test_f16codes_workspace_errors():
         i8.gemm_int32_f16codes(a, w, workspace=torch.empty(need - 16, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 4
     i8.sync_check()
+
+
+@pytest.mark.parametrize("splits", [2, 5, 16])
+def test_f16codes_forced_splits_exact(orc, splits):
+    """Any split count, also one whose K ranges do not line up with the
+    accumulator restarts, gives the oracle's int32 sums and bf16 outputs."""
+    M, N, K = 300, 520, 3072
+    a = inputs.random_int8(M, K, seed=splits)
+    w = inputs.random_int8(N, K, seed=splits + 1)
+    shape = inputs.LinearShape("t", M, K, N, seed=splits, outliers=True)
+    d = inputs.linear_inputs(shape)
+    wq, s_w = i8.quant_weight_perchannel(to_dev(d["w"]))
+    i8.set_option("force_splits", splits)
+    try:
+        assert i8.f16codes_workspace_bytes(M, N, K) > 0
+        c = i8.gemm_int32_f16codes(to_dev(a).half(), to_dev(w).half())
+        y = i8.linear_f16codes(to_dev(d["x"]), i8.widen_weight_codes(wq), s_w, to_dev(d["bias"]))
+        i8.sync_check()
+    finally:
+        i8.set_option("force_splits", 0)
+    assert np.array_equal(c.cpu().numpy(), orc.gemm_s32(a.numpy(), w.numpy()))
+    want = orc.linear(inputs.bits(d["x"]), inputs.bits(d["w"]), inputs.bits(d["bias"]))["y"]
+    assert_bf16_exact(gpu_bf16_bits(y), want, f"splits {splits}")

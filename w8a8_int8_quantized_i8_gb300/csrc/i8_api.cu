@@ -813,13 +813,50 @@ struct DirectPlan {
   size_t ws_bytes;
 };
 
+// Modelled time (us) of a direct-kernel plan with `splits` K splits, up to a
+// start-up cost common to every plan.  Grid fill alone favours many short
+// items, but an item cannot retire faster than its epilogue (the accumulator
+// is double-buffered, so an item's epilogue overlaps the next item's MMAs),
+// and a split plan writes and re-reads fp32/int32 partial planes.  Per CTA
+// pair on GB300: a 256 x 256 tile advances one 128-byte K block in 0.31 us
+// (either kind); an epilogue takes 2 us for bf16 and 3 us for a 4-byte
+// partial; the fix-up costs 2 us plus 8 bytes per partial element at 15 TB/s
+// while the planes fit in L2 (64 MB), else at 6.5 TB/s.  The constants were
+// fitted to timings of both kinds over the DiT layer shapes.
+double direct_plan_us(int64_t tiles, int pairs, int total_kb, int splits, int64_t M, int64_t N) {
+  const int kbps = (total_kb + splits - 1) / splits;
+  const int s = (total_kb + kbps - 1) / kbps;
+  const int64_t rounds = (tiles * s + pairs - 1) / pairs;
+  const double t_epi = s > 1 ? 3.0 : 2.0;
+  double t = static_cast<double>(rounds) * std::max(0.31 * kbps, t_epi) + t_epi;
+  if (s > 1) {
+    const double bytes = 8.0 * s * static_cast<double>(M) * static_cast<double>(N);
+    t += 2.0 + bytes / (bytes <= 128.0 * (1 << 20) ? 15e6 : 6.5e6);
+  }
+  return t;
+}
+
 DirectPlan plan_direct(int64_t M, int64_t N, int64_t K, int pairs, int bk) {
   DirectPlan p{};
   p.num_m = static_cast<int>((M + 255) / 256);
   p.num_n = static_cast<int>((N + 255) / 256);
   p.total_kb = static_cast<int>((K + bk - 1) / bk);
   p.tiles = static_cast<int64_t>(p.num_m) * p.num_n;
-  p.splits = best_splits(p.tiles, pairs, p.total_kb);
+  // splits: the cheapest plan under direct_plan_us, only when the tiles
+  // leave pairs idle, and never below four K blocks per split
+  p.splits = 1;
+  if (p.tiles < pairs) {
+    double best = direct_plan_us(p.tiles, pairs, p.total_kb, 1, M, N);
+    const int max_s = std::max(1, std::min(16, p.total_kb / 4));
+    for (int s = 2; s <= max_s; ++s) {
+      const double t = direct_plan_us(p.tiles, pairs, p.total_kb, s, M, N);
+      if (t < best - 1e-9) {
+        best = t;
+        p.splits = s;
+      }
+    }
+  }
+  if (g_opt.force_splits > 0) p.splits = std::min(g_opt.force_splits, p.total_kb);
   p.kb_per_split = (p.total_kb + p.splits - 1) / p.splits;
   p.splits = (p.total_kb + p.kb_per_split - 1) / p.kb_per_split;
   p.ldw = (N + 3) / 4 * 4;
