@@ -331,13 +331,17 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *   I8_OPT_NVTX         1: every call of this header opens an NVTX range
  *                       named after the call (visible in Nsight timelines;
  *                       free when no tool is attached); 0 (default): none.
+ *   I8_OPT_PAIR_STAGE_K K covered by one fp16 stage of the int8-code CTA-pair
+ *                       GEMM, i.e. by one converter-to-MMA hand-off: 128
+ *                       (two 64-K sub-tiles) or 64; 0 (default) = 128
+ *                       whenever CHUNK_K is a multiple of 128, else 64.
  * Changing FORCE_SPLITS changes the *_workspace_bytes() results.
  *
  * The environment variable I8_OPTIONS, read once when the library is
  * loaded, sets options without code changes: a comma-separated list of
  * name=value pairs with the names chunk_k, force_splits, max_ctas, tile_n,
- * quant_vpl, cta_pair, skinny_max_m, pdl, quant_rows, stream_k, nvtx (for
- * example "chunk_k=512,stream_k=0").  Entries with an unknown name or an
+ * quant_vpl, cta_pair, skinny_max_m, pdl, quant_rows, stream_k, nvtx,
+ * pair_stage_k (for example "chunk_k=512,stream_k=0").  Entries with an unknown name or an
  * invalid value are ignored. */
 typedef enum {
   I8_OPT_CHUNK_K = 1,
@@ -350,7 +354,8 @@ typedef enum {
   I8_OPT_PDL = 8,
   I8_OPT_QUANT_ROWS = 9,
   I8_OPT_STREAM_K = 10,
-  I8_OPT_NVTX = 11
+  I8_OPT_NVTX = 11,
+  I8_OPT_PAIR_STAGE_K = 12
 } i8_option;
 i8_status i8_set_option(i8_option opt, int64_t value);
 /* Current value of an option (I8_ERR_INVALID_ARG for an unknown option or a

@@ -73,6 +73,7 @@ struct Options {
   int quant_rows = 0;      // quantizer rows per CTA (0 = by shape)
   int stream_k = 1;        // CTA-pair stream-K: 0 never, 1 by the table, 2 whenever pairs idle
   int nvtx = 0;            // NVTX range around every ABI call
+  int pair_stage_k = 0;    // K per fp16 stage of the int8-code pair kernel: 0 (table) / 64 / 128
 };
 Options g_opt;
 
@@ -613,12 +614,21 @@ int skinny_slots(DeviceInfo* d, bool b16) {
   return cached[dev][b16];
 }
 
-using PairConv = PairCfg<3, 3, true, true>;    // int8 weights, CTA pair
+using PairConv = PairCfg<3, 3, true, true>;    // int8 weights, CTA pair, 64-K fp16 stages
+using PairConvWide = PairCfg<2, 2, true, true, 2, true>;  // the same with 128-K fp16 stages
 using PairWide = PairCfg<4, 4, true, false>;   // pre-widened weights, CTA pair
 using CfgConv128 = GemmCfg<128, 3, 3, true, true>;   // int8 weights
 using CfgWide128 = GemmCfg<128, 4, 4, true, false>;  // weights pre-widened to fp16 codes
 using CfgConv256 = GemmCfg<256, 2, 2, true, true>;
 using CfgWide256 = GemmCfg<256, 3, 3, true, false>;
+
+// The int8-code pair kernel stages 128 K of fp16 codes per hand-off unless the
+// option asks for 64 or the fp32 chunk is not a whole number of 128-K stages.
+bool pair_wide_stages() { return g_opt.pair_stage_k != 64 && g_opt.chunk_k % 128 == 0; }
+int conv_pair_clusters(DeviceInfo* d) {
+  return pair_wide_stages() ? pair_cluster_capacity<PairConvWide>(d, 2)
+                            : pair_cluster_capacity<PairConv>(d, 0);
+}
 
 // Common GEMM driver.  b16 = weights given as fp16 codes instead of int8.
 // ws_cap bounds the workspace the plan may ask for (the no-alloc entry's
@@ -640,7 +650,7 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   DeviceInfo* d;
   if (i8_status e = device_info(&d, nullptr)) return e;
   const int clusters = b16 ? pair_cluster_capacity<PairWide>(d, 1)
-                           : pair_cluster_capacity<PairConv>(d, 0);
+                           : conv_pair_clusters(d);
   const Plan pl = make_plan(M, N, K, d->sms, clusters, b16, ws_cap, skinny_slots(d, b16));
   if (pl.ws_bytes > 0) {
     if (!ws || ws_bytes < pl.ws_bytes) return I8_ERR_WORKSPACE;
@@ -748,7 +758,8 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   i8_status e;
   if (pl.pair) {
     e = b16 ? launch_pair_cfg<PairWide>(ma, mb, my, mp, gp, pl.grid, st)
-            : launch_pair_cfg<PairConv>(ma, mb, my, mp, gp, pl.grid, st);
+            : (pair_wide_stages() ? launch_pair_cfg<PairConvWide>(ma, mb, my, mp, gp, pl.grid, st)
+                                  : launch_pair_cfg<PairConv>(ma, mb, my, mp, gp, pl.grid, st));
   } else if (pl.bn == 256) {
     e = b16 ? launch_gemm_cfg<CfgWide256>(d, 3, ma, mb, my, gp, pl.grid, st)
             : launch_gemm_cfg<CfgConv256>(d, 2, ma, mb, my, gp, pl.grid, st);
@@ -1116,7 +1127,7 @@ size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   DeviceInfo* d;
   if (device_info(&d, nullptr) != I8_OK) return 0;
   // the larger of the two weight formats' plans, so one query serves both
-  const size_t a = make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0), false,
+  const size_t a = make_plan(M, N, K, d->sms, conv_pair_clusters(d), false,
                              SIZE_MAX, skinny_slots(d, false)).ws_bytes;
   const size_t b = make_plan(M, N, K, d->sms, pair_cluster_capacity<PairWide>(d, 1), true,
                              SIZE_MAX, skinny_slots(d, true)).ws_bytes;
@@ -1153,7 +1164,7 @@ i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a, 
       N <= INT32_MAX) {
     DeviceInfo* d;
     if (i8_status e = device_info(&d, nullptr)) return e;
-    if (make_plan(M, N, K, d->sms, pair_cluster_capacity<PairConv>(d, 0), false, kStaticWsBytes,
+    if (make_plan(M, N, K, d->sms, conv_pair_clusters(d), false, kStaticWsBytes,
                   skinny_slots(d, false))
             .ws_bytes > kStaticWsBytes)
       return I8_ERR_WORKSPACE;
@@ -1237,6 +1248,10 @@ i8_status i8_set_option(i8_option opt, int64_t value) {
       if (value != 0 && value != 1) return I8_ERR_INVALID_ARG;
       g_opt.nvtx = static_cast<int>(value);
       return I8_OK;
+    case I8_OPT_PAIR_STAGE_K:
+      if (value != 0 && value != 64 && value != 128) return I8_ERR_INVALID_ARG;
+      g_opt.pair_stage_k = static_cast<int>(value);
+      return I8_OK;
   }
   return I8_ERR_INVALID_ARG;
 }
@@ -1255,6 +1270,7 @@ i8_status i8_get_option(i8_option opt, int64_t* value) {
     case I8_OPT_QUANT_ROWS: *value = g_opt.quant_rows; return I8_OK;
     case I8_OPT_STREAM_K: *value = g_opt.stream_k; return I8_OK;
     case I8_OPT_NVTX: *value = g_opt.nvtx; return I8_OK;
+    case I8_OPT_PAIR_STAGE_K: *value = g_opt.pair_stage_k; return I8_OK;
   }
   return I8_ERR_INVALID_ARG;
 }
@@ -1299,7 +1315,7 @@ struct EnvOptions {
                   {"quant_vpl", I8_OPT_QUANT_VPL},   {"cta_pair", I8_OPT_CTA_PAIR},
                   {"skinny_max_m", I8_OPT_SKINNY_MAX_M}, {"pdl", I8_OPT_PDL},
                   {"quant_rows", I8_OPT_QUANT_ROWS}, {"stream_k", I8_OPT_STREAM_K},
-                  {"nvtx", I8_OPT_NVTX}};
+                  {"nvtx", I8_OPT_NVTX},             {"pair_stage_k", I8_OPT_PAIR_STAGE_K}};
     const char* p = env;
     while (*p) {
       const char* end = std::strchr(p, ',');
