@@ -119,6 +119,13 @@ def test_get_option_and_nvtx_ranges(lib):
     assert lib.i8_gemm_int32(P(0x10000), P(0x10000), 4, 8, 24, P(0x10000), 8, None, 0, None) == 3
     assert lib.i8_set_option(11, 2) == 1
     assert lib.i8_set_option(11, 0) == 0
+    # K per fp16 stage of the pair kernel: 0 (by the chunk length), 64 or 128
+    assert lib.i8_get_option(12, ctypes.byref(v)) == 0 and v.value == 0
+    for bad in (1, 32, 96, 192, 256):
+        assert lib.i8_set_option(12, bad) == 1
+    assert lib.i8_set_option(12, 64) == 0
+    assert lib.i8_get_option(12, ctypes.byref(v)) == 0 and v.value == 64
+    assert lib.i8_set_option(12, 0) == 0
 
 
 def test_options_from_the_environment(tmp_path):

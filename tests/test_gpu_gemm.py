@@ -460,3 +460,46 @@ def test_skinny_split_k_workspace_garbage_and_graph_replay(orc, M, N, K):
         torch.cuda.synchronize()
         assert np.array_equal(out.cpu().numpy(), want)
     i8.sync_check()
+
+
+@pytest.fixture
+def stage_k_option():
+    yield
+    i8.set_option("pair_stage_k", 0)
+    i8.set_option("stream_k", 1)
+    i8.set_option("cta_pair", 0)
+    i8.set_option("chunk_k", 1024)
+
+
+@pytest.mark.parametrize("stream_k", [0, 2])
+@pytest.mark.parametrize("chunk_k", [1024, 384, 128])
+@pytest.mark.parametrize("M,N,K", [(512, 768, 4096), (300, 520, 1040), (2560, 9216, 3072)])
+def test_pair_stage_k_128_matches_64(orc, stage_k_option, stream_k, chunk_k, M, N, K):
+    """The pair kernel with one fp16 stage per 128 K (two 64-K sub-tiles)
+    gives the 64-K-stage kernel's int32 sums bit for bit, with whole tiles and
+    with stream-K, and with accumulator restarts every 128, 384 or 1024 K; the
+    int32 sums are also checked against the oracle on the small shapes."""
+    i8.set_option("cta_pair", 2)
+    i8.set_option("stream_k", stream_k)
+    i8.set_option("chunk_k", chunk_k)
+    a = inputs.random_int8(M, K, seed=M + K + chunk_k)
+    w = inputs.random_int8(N, K, seed=N + K)
+    a[:3], w[:3] = _adversarial(3, 3, K, seed=M)[0], _adversarial(3, 3, K, seed=N)[1]
+    res = {}
+    for sk in (64, 128):
+        i8.set_option("pair_stage_k", sk)
+        res[sk] = i8.gemm_int32(to_dev(a), to_dev(w))
+        i8.sync_check()
+    assert torch.equal(res[64], res[128])
+    if M * N <= 512 * 768:
+        assert np.array_equal(res[128].cpu().numpy(), orc.gemm_s32(a.numpy(), w.numpy()))
+
+
+def test_pair_stage_k_option_values():
+    assert i8.get_option("pair_stage_k") == 0
+    for bad in (32, 96, 256, -1):
+        with pytest.raises(i8.I8Error):
+            i8.set_option("pair_stage_k", bad)
+    i8.set_option("pair_stage_k", 64)
+    assert i8.get_option("pair_stage_k") == 64
+    i8.set_option("pair_stage_k", 0)
