@@ -95,7 +95,7 @@ struct PairCfg {
   static constexpr uint32_t TX16 = (CONV_A ? 0 : A16_BYTES) + (CONV_B ? 0 : B16_BYTES);
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(STAGE8 % 1024 == 0 && STAGE16 % 1024 == 0, "stage alignment");
-  static_assert(!WIDE || (CONV_A && CONV_B && A16_SUB == B16_SUB), "wide stages: both operands widened");
+  static_assert(!WIDE || A16_SUB == B16_SUB, "wide stages: equal sub-tiles");
 };
 
 struct PairBars {
@@ -422,14 +422,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
             r8.advance(Cfg::S8);
           }
           if constexpr (Cfg::ANY_DIRECT) {
-            for (int h = 0; h < 2; ++h) {
+            // the fp16 operand: one stage per 64-K half, or (WIDE) both
+            // halves as the two sub-tiles of one stage
+            for (int h = 0; h < 2; h += Cfg::K64_PER_STAGE) {
               if (!(ok = mbar_wait(bars.empty16(r16.s), r16.ph ^ 1u, abort_flag))) break;
               mbar_arrive_expect_tx(bars.tma16(r16.s), Cfg::TX16);
-              const int k16 = kb * Cfg::BK8 + h * Cfg::BK16;
-              if constexpr (!Cfg::CONV_A)
-                tma_load_2d(stage16(r16.s), &tmA, bars.tma16(r16.s), k16, m0);
-              if constexpr (!Cfg::CONV_B)
-                tma_load_2d(stage16(r16.s) + Cfg::A16_BYTES, &tmB, bars.tma16(r16.s), k16, n0);
+#pragma unroll
+              for (int q = 0; q < Cfg::K64_PER_STAGE; ++q) {
+                const int k16 = kb * Cfg::BK8 + (h + q) * Cfg::BK16;
+                if constexpr (!Cfg::CONV_A)
+                  tma_load_2d(stage16(r16.s) + q * Cfg::A16_SUB, &tmA, bars.tma16(r16.s), k16, m0);
+                if constexpr (!Cfg::CONV_B)
+                  tma_load_2d(stage16(r16.s) + Cfg::A16_BYTES + q * Cfg::B16_SUB, &tmB,
+                              bars.tma16(r16.s), k16, n0);
+              }
               r16.advance(Cfg::S16);
             }
           }
@@ -565,6 +571,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
             }
           }
           fence_proxy_async_smem();
+          if constexpr (Cfg::ANY_DIRECT) {
+            // this CTA's directly loaded operand of the stage must have landed
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.tma16(r16.s), r16.ph, abort_flag));
+            if (!ok) break;
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(bars.full16(r16.s));
           r16.advance(Cfg::S16);

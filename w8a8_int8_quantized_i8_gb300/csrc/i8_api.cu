@@ -617,6 +617,7 @@ int skinny_slots(DeviceInfo* d, bool b16) {
 using PairConv = PairCfg<3, 3, true, true>;    // int8 weights, CTA pair, 64-K fp16 stages
 using PairConvWide = PairCfg<2, 2, true, true, 2, true>;  // the same with 128-K fp16 stages
 using PairWide = PairCfg<4, 4, true, false>;   // pre-widened weights, CTA pair
+using PairWideW = PairCfg<4, 2, true, false, 2, true>;  // the same with 128-K fp16 stages
 using CfgConv128 = GemmCfg<128, 3, 3, true, true>;   // int8 weights
 using CfgWide128 = GemmCfg<128, 4, 4, true, false>;  // weights pre-widened to fp16 codes
 using CfgConv256 = GemmCfg<256, 2, 2, true, true>;
@@ -628,6 +629,10 @@ bool pair_wide_stages() { return g_opt.pair_stage_k != 64 && g_opt.chunk_k % 128
 int conv_pair_clusters(DeviceInfo* d) {
   return pair_wide_stages() ? pair_cluster_capacity<PairConvWide>(d, 2)
                             : pair_cluster_capacity<PairConv>(d, 0);
+}
+int wide_pair_clusters(DeviceInfo* d) {
+  return pair_wide_stages() ? pair_cluster_capacity<PairWideW>(d, 3)
+                            : pair_cluster_capacity<PairWide>(d, 1);
 }
 
 // Common GEMM driver.  b16 = weights given as fp16 codes instead of int8.
@@ -649,7 +654,7 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   if (out_mode == kOutInt32 && ldo % 4 != 0) return I8_ERR_ALIGNMENT;
   DeviceInfo* d;
   if (i8_status e = device_info(&d, nullptr)) return e;
-  const int clusters = b16 ? pair_cluster_capacity<PairWide>(d, 1)
+  const int clusters = b16 ? wide_pair_clusters(d)
                            : conv_pair_clusters(d);
   const Plan pl = make_plan(M, N, K, d->sms, clusters, b16, ws_cap, skinny_slots(d, b16));
   if (pl.ws_bytes > 0) {
@@ -757,7 +762,8 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   }
   i8_status e;
   if (pl.pair) {
-    e = b16 ? launch_pair_cfg<PairWide>(ma, mb, my, mp, gp, pl.grid, st)
+    e = b16 ? (pair_wide_stages() ? launch_pair_cfg<PairWideW>(ma, mb, my, mp, gp, pl.grid, st)
+                                  : launch_pair_cfg<PairWide>(ma, mb, my, mp, gp, pl.grid, st))
             : (pair_wide_stages() ? launch_pair_cfg<PairConvWide>(ma, mb, my, mp, gp, pl.grid, st)
                                   : launch_pair_cfg<PairConv>(ma, mb, my, mp, gp, pl.grid, st));
   } else if (pl.bn == 256) {
@@ -1129,7 +1135,7 @@ size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   // the larger of the two weight formats' plans, so one query serves both
   const size_t a = make_plan(M, N, K, d->sms, conv_pair_clusters(d), false,
                              SIZE_MAX, skinny_slots(d, false)).ws_bytes;
-  const size_t b = make_plan(M, N, K, d->sms, pair_cluster_capacity<PairWide>(d, 1), true,
+  const size_t b = make_plan(M, N, K, d->sms, wide_pair_clusters(d), true,
                              SIZE_MAX, skinny_slots(d, true)).ws_bytes;
   return a > b ? a : b;
 }
