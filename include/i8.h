@@ -335,13 +335,17 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *                       GEMM, i.e. by one converter-to-MMA hand-off: 128
  *                       (two 64-K sub-tiles) or 64; 0 (default) = 128
  *                       whenever CHUNK_K is a multiple of 128, else 64.
+ *   I8_OPT_RASTER       order of the output tiles in the tiled kernels: 1 M
+ *                       blocks fastest, 2 N blocks fastest, 0 (default) N
+ *                       fastest when M > N, else M fastest.  Results do not
+ *                       depend on it.
  * Changing FORCE_SPLITS changes the *_workspace_bytes() results.
  *
  * The environment variable I8_OPTIONS, read once when the library is
  * loaded, sets options without code changes: a comma-separated list of
  * name=value pairs with the names chunk_k, force_splits, max_ctas, tile_n,
  * quant_vpl, cta_pair, skinny_max_m, pdl, quant_rows, stream_k, nvtx,
- * pair_stage_k (for example "chunk_k=512,stream_k=0").  Entries with an unknown name or an
+ * pair_stage_k, raster (for example "chunk_k=512,stream_k=0").  Entries with an unknown name or an
  * invalid value are ignored. */
 typedef enum {
   I8_OPT_CHUNK_K = 1,
@@ -355,7 +359,8 @@ typedef enum {
   I8_OPT_QUANT_ROWS = 9,
   I8_OPT_STREAM_K = 10,
   I8_OPT_NVTX = 11,
-  I8_OPT_PAIR_STAGE_K = 12
+  I8_OPT_PAIR_STAGE_K = 12,
+  I8_OPT_RASTER = 13
 } i8_option;
 i8_status i8_set_option(i8_option opt, int64_t value);
 /* Current value of an option (I8_ERR_INVALID_ARG for an unknown option or a

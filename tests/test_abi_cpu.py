@@ -126,6 +126,10 @@ def test_get_option_and_nvtx_ranges(lib):
     assert lib.i8_set_option(12, 64) == 0
     assert lib.i8_get_option(12, ctypes.byref(v)) == 0 and v.value == 64
     assert lib.i8_set_option(12, 0) == 0
+    # tile order: 0 (by shape), 1 M blocks fastest, 2 N blocks fastest
+    assert lib.i8_get_option(13, ctypes.byref(v)) == 0 and v.value == 0
+    assert lib.i8_set_option(13, 3) == 1 and lib.i8_set_option(13, -1) == 1
+    assert lib.i8_set_option(13, 2) == 0 and lib.i8_set_option(13, 0) == 0
 
 
 def test_options_from_the_environment(tmp_path):

@@ -503,3 +503,40 @@ def test_pair_stage_k_option_values():
     i8.set_option("pair_stage_k", 64)
     assert i8.get_option("pair_stage_k") == 64
     i8.set_option("pair_stage_k", 0)
+
+
+@pytest.fixture
+def raster_option():
+    yield
+    i8.set_option("raster", 0)
+    i8.set_option("stream_k", 1)
+    i8.set_option("cta_pair", 0)
+
+
+@pytest.mark.parametrize("route", ["int8", "int8_stream_k", "e4m3", "f16codes"])
+@pytest.mark.parametrize("M,N,K", [(1280, 520, 2048), (300, 1040, 1040), (2560, 768, 4096)])
+def test_tile_order_does_not_change_results(raster_option, route, M, N, K):
+    """M-blocks-fastest and N-blocks-fastest tile orders give the same bits on
+    every route (ragged edges, split-K and stream-K included)."""
+    g = torch.Generator().manual_seed(M + N + K)
+    x = inputs.activations(M, K, g, "normal", True).cuda()
+    w = inputs.random_bf16(N, K, seed=N + K, std=0.02).cuda()
+    b = inputs.random_bf16(1, N, seed=K, std=0.1)[0].cuda()
+    if route == "int8_stream_k":
+        i8.set_option("cta_pair", 2)
+        i8.set_option("stream_k", 2)
+    outs = []
+    for order in (1, 2):
+        i8.set_option("raster", order)
+        if route.startswith("int8"):
+            wq, s_w = i8.quant_weight_perchannel(w)
+            y = i8.linear(x, wq, s_w, b)
+        elif route == "e4m3":
+            wq, s_w = i8.quant_weight_perchannel_e4m3(w)
+            y = i8.linear_e4m3(x, wq, s_w, b)
+        else:
+            wq, s_w = i8.quant_weight_perchannel(w)
+            y = i8.linear_f16codes(x, i8.widen_weight_codes(wq), s_w, b)
+        i8.sync_check()
+        outs.append(y.view(torch.int16))
+    assert torch.equal(outs[0], outs[1])

@@ -26,7 +26,7 @@ STATUS = {
 }
 OPTIONS = {"chunk_k": 1, "force_splits": 2, "max_ctas": 3, "tile_n": 4, "quant_vpl": 5, "cta_pair": 6,
            "skinny_max_m": 7, "pdl": 8, "quant_rows": 9, "stream_k": 10, "nvtx": 11,
-           "pair_stage_k": 12}
+           "pair_stage_k": 12, "raster": 13}
 
 
 class I8Error(RuntimeError):

@@ -64,7 +64,22 @@ struct GemmParams {
   unsigned long long* sk_arrive;       // [num_tiles][2] arrival words: epoch << 16 | count
   const int32_t* sk_part;              // [2 P][256][256] int32 partial slots
   unsigned long long sk_epoch;         // this launch's tag, in [1, 2^48)
+  int n_fastest;                       // tile order: 0 M blocks fastest, 1 N blocks fastest
 };
+
+// Block coordinates of output tile `tile` in the schedule's order.  M blocks
+// fastest: workers running at the same time share weight columns; N blocks
+// fastest: they share activation rows.  The host picks the order that keeps
+// the larger operand's reused part in L2.
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& mb, int& nb) {
+  if (p.n_fastest) {
+    nb = tile % p.num_n_blk;
+    mb = tile / p.num_n_blk;
+  } else {
+    mb = tile % p.num_m_blk;
+    nb = tile / p.num_m_blk;
+  }
+}
 
 // Kernel configuration.  CONV_A / CONV_B: the operand arrives as int8 codes
 // and is widened to fp16 on chip; otherwise it arrives as fp16 codes through
@@ -146,8 +161,7 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int tile) 
   TileCoord t;
   t.ks = tile % p.splits;
   const int rest = tile / p.splits;
-  t.mb = rest % p.num_m_blk;
-  t.nb = rest / p.num_m_blk;
+  tile_coords(p, rest, t.mb, t.nb);
   t.kb0 = t.ks * p.kb_per_split;
   t.kb1 = min(t.kb0 + p.kb_per_split, p.total_kb);
   return t;

@@ -77,7 +77,7 @@ struct DirectCfg {
 };
 
 // Work item `item` of the schedule: K split ks of tile (mp, nb); the tile's
-// M blocks run fastest, so concurrently running pairs share weight tiles.
+// tiles run in tile_coords order (M or N blocks fastest, by the host's choice).
 struct DirectItem {
   int mp, nb, ks, kb0, kb1;
 };
@@ -85,8 +85,7 @@ __device__ __forceinline__ DirectItem direct_item(const GemmParams& p, int item)
   DirectItem t;
   t.ks = item % p.splits;
   const int tile = item / p.splits;
-  t.mp = tile % p.num_m_blk;
-  t.nb = tile / p.num_m_blk;
+  tile_coords(p, tile, t.mp, t.nb);
   t.kb0 = t.ks * p.kb_per_split;
   t.kb1 = min(t.kb0 + p.kb_per_split, p.total_kb);
   return t;

@@ -128,8 +128,7 @@ __device__ __forceinline__ PairTile decode_pair_tile(const GemmParams& p, int ti
   PairTile t;
   t.ks = tile % p.splits;
   const int rest = tile / p.splits;
-  t.mp = rest % p.num_m_blk;
-  t.nb = rest / p.num_m_blk;
+  tile_coords(p, rest, t.mp, t.nb);
   t.kb0 = t.ks * p.kb_per_split;
   t.kb1 = min(t.kb0 + p.kb_per_split, p.total_kb);
   return t;
@@ -171,8 +170,7 @@ __device__ __forceinline__ bool pair_item(const GemmParams& p, int pair, int npa
   if (u0 >= u1 || t0 >= u1) return false;
   t.tile = static_cast<int>(tile);
   t.ks = 0;
-  t.mp = t.tile % p.num_m_blk;
-  t.nb = t.tile / p.num_m_blk;
+  tile_coords(p, t.tile, t.mp, t.nb);
   t.kb0 = static_cast<int>((u0 > t0 ? u0 : t0) - t0);
   t.kb1 = static_cast<int>((u1 < t0 + kb ? u1 : t0 + kb) - t0);
   t.partial = t.kb0 > 0 || t.kb1 < p.total_kb;

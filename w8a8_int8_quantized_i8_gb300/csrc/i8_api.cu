@@ -74,6 +74,7 @@ struct Options {
   int stream_k = 1;        // CTA-pair stream-K: 0 never, 1 by the table, 2 whenever pairs idle
   int nvtx = 0;            // NVTX range around every ABI call
   int pair_stage_k = 0;    // K per fp16 stage of the int8-code pair kernel: 0 (table) / 64 / 128
+  int raster = 0;          // tile order: 0 table, 1 M blocks fastest, 2 N blocks fastest
 };
 Options g_opt;
 
@@ -407,6 +408,16 @@ int best_splits(int64_t tiles, int slots, int total_kb) {
   return best;
 }
 
+// Tile order.  The tiles running at the same time share weight columns when
+// M blocks run fastest and activation rows when N blocks do; the reused
+// operand should be the larger one, which must otherwise be re-read from HBM
+// once it outgrows L2 (MLP down-projection, 8704 x 12288 activations: M-fastest
+// read 513 MB from DRAM per call for 145 MB of operands).
+int tile_order_n_fastest(int64_t M, int64_t N) {
+  if (g_opt.raster != 0) return g_opt.raster == 2 ? 1 : 0;
+  return M > N ? 1 : 0;
+}
+
 // Shape -> configuration (replaces per-shape autotuning).
 //   * CTA pairs (one 256 x 256 tile per cluster of two SMs, each SM staging
 //     and widening half of B) for int8 weights whenever M, N >= 256; with
@@ -463,12 +474,16 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
     // partial out, partials back in), so the table takes it only where a
     // tile carries far more MMA time than that and whole tiles leave many
     // pairs idle: K >= 8192, at least half a wave of tiles, whole-tile wave
-    // efficiency below 0.93.  Measured (GEMM, GB300): +4 to +7 % at
-    // K = 12288 with M = 1024 ... 16384; -3 to -76 % at K = 3072.
+    // efficiency below 0.93, and only in the M-blocks-fastest tile order.
+    // Measured (GEMM, GB300): +4 to +7 % at K = 12288 with M-fastest tiles;
+    // -3 to -76 % at K = 3072; with N blocks fastest (M > N) the whole-tile
+    // schedule is faster (MLP down-projection 482 -> 461 us with the order
+    // change, stream-K under N-fastest 525 us).
     const int64_t units = tiles * p.total_kb;
     const int64_t waves = (tiles + slots - 1) / slots;
     const double wave_eff = static_cast<double>(tiles) / static_cast<double>(waves * slots);
-    const bool sk_table = p.total_kb >= 64 && 2 * tiles >= slots && wave_eff < 0.93;
+    const bool sk_table = p.total_kb >= 64 && 2 * tiles >= slots && wave_eff < 0.93 &&
+                          !tile_order_n_fastest(M, N);
     if ((g_opt.stream_k == 2 || (g_opt.stream_k == 1 && sk_table)) && g_opt.force_splits == 0 &&
         tiles % slots != 0 &&
         units * slots < (int64_t(1) << 31)) {   // the kernel's unit arithmetic is 32-bit
@@ -626,6 +641,8 @@ using CfgWide256 = GemmCfg<256, 3, 3, true, false>;
 // The int8-code pair kernel stages 128 K of fp16 codes per hand-off unless the
 // option asks for 64 or the fp32 chunk is not a whole number of 128-K stages.
 bool pair_wide_stages() { return g_opt.pair_stage_k != 64 && g_opt.chunk_k % 128 == 0; }
+
+
 int conv_pair_clusters(DeviceInfo* d) {
   return pair_wide_stages() ? pair_cluster_capacity<PairConvWide>(d, 2)
                             : pair_cluster_capacity<PairConv>(d, 0);
@@ -726,6 +743,7 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   gp.K = static_cast<int>(K);
   gp.num_m_blk = pl.num_m;
   gp.num_n_blk = pl.num_n;
+  gp.n_fastest = tile_order_n_fastest(M, N);
   gp.splits = pl.splits;
   gp.kb_per_split = pl.kb_per_split;
   gp.total_kb = pl.total_kb;
@@ -926,6 +944,7 @@ i8_status gemm_direct_common(const void* aq, const void* wq, int64_t M, int64_t 
   gp.K = static_cast<int>(K);
   gp.num_m_blk = pl.num_m;
   gp.num_n_blk = pl.num_n;
+  gp.n_fastest = tile_order_n_fastest(M, N);
   gp.splits = pl.splits;
   gp.total_kb = pl.total_kb;
   gp.kb_per_split = pl.kb_per_split;
@@ -1258,6 +1277,10 @@ i8_status i8_set_option(i8_option opt, int64_t value) {
       if (value != 0 && value != 64 && value != 128) return I8_ERR_INVALID_ARG;
       g_opt.pair_stage_k = static_cast<int>(value);
       return I8_OK;
+    case I8_OPT_RASTER:
+      if (value < 0 || value > 2) return I8_ERR_INVALID_ARG;
+      g_opt.raster = static_cast<int>(value);
+      return I8_OK;
   }
   return I8_ERR_INVALID_ARG;
 }
@@ -1277,6 +1300,7 @@ i8_status i8_get_option(i8_option opt, int64_t* value) {
     case I8_OPT_STREAM_K: *value = g_opt.stream_k; return I8_OK;
     case I8_OPT_NVTX: *value = g_opt.nvtx; return I8_OK;
     case I8_OPT_PAIR_STAGE_K: *value = g_opt.pair_stage_k; return I8_OK;
+    case I8_OPT_RASTER: *value = g_opt.raster; return I8_OK;
   }
   return I8_ERR_INVALID_ARG;
 }
@@ -1321,7 +1345,8 @@ struct EnvOptions {
                   {"quant_vpl", I8_OPT_QUANT_VPL},   {"cta_pair", I8_OPT_CTA_PAIR},
                   {"skinny_max_m", I8_OPT_SKINNY_MAX_M}, {"pdl", I8_OPT_PDL},
                   {"quant_rows", I8_OPT_QUANT_ROWS}, {"stream_k", I8_OPT_STREAM_K},
-                  {"nvtx", I8_OPT_NVTX},             {"pair_stage_k", I8_OPT_PAIR_STAGE_K}};
+                  {"nvtx", I8_OPT_NVTX},             {"pair_stage_k", I8_OPT_PAIR_STAGE_K},
+                  {"raster", I8_OPT_RASTER}};
     const char* p = env;
     while (*p) {
       const char* end = std::strchr(p, ',');
