@@ -230,17 +230,34 @@ __global__ void __launch_bounds__(512, 1) gelu_table_quant_kernel(
   }
   __syncthreads();
   pdl_wait();  // X may be the previous kernel's output
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * R; base < rows;
-       base += static_cast<int64_t>(gridDim.x) * R) {
-    const int64_t row = base + sub;
+  // One group of R rows at a time; the next group's loads are issued before
+  // the current group is processed, so HBM stays busy during the table
+  // lookups and reductions (one 512-thread CTA per SM holds few loads).
+  auto load_rows = [&](int64_t b, uint4 (&dst)[V]) {
+    const int64_t row = b + sub;
     const bool valid = row < rows;
     const uint16_t* xr = x + (valid ? row : 0) * ldx;
-    uint4 v[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int e = slice0 + (i * 32 + lane) * 8;
-      v[i] = (valid && e < K) ? ld_stream_v4(xr + e) : make_uint4(0u, 0u, 0u, 0u);
+      dst[i] = (valid && e < K) ? ld_stream_v4(xr + e) : make_uint4(0u, 0u, 0u, 0u);
     }
+  };
+  // (rows of more than 8 vectors per lane keep a single buffer: two would
+  // not fit the registers)
+  constexpr bool kPrefetch = V <= 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * R;
+  uint4 v[V], vn[kPrefetch ? V : 1];
+  int64_t base = static_cast<int64_t>(blockIdx.x) * R;
+  if (kPrefetch && base < rows) load_rows(base, v);
+  for (; base < rows; base += stride) {
+    if constexpr (kPrefetch) {
+      if (base + stride < rows) load_rows(base + stride, vn);
+    } else {
+      load_rows(base, v);
+    }
+    const int64_t row = base + sub;
+    const bool valid = row < rows;
     uint32_t amax2 = 0;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
@@ -268,33 +285,38 @@ __global__ void __launch_bounds__(512, 1) gelu_table_quant_kernel(
       for (int j = 0; j < G; ++j) abits = max(abits, red_m[sub * G + j]);
       __syncthreads();   // red_m is rewritten by the next group of rows
     }
-    if (!valid) continue;
-    const float amax = __uint_as_float(abits << 16);
-    const float s = __fdiv_rn(amax, FMT == kQuantE4M3 ? 448.0f : 127.0f);
-    if (wig == 0 && lane == 0) scale[row] = s;
-    if (y_out) {
-      uint16_t* yr = y_out + row * ldy;
+    if (valid) {
+      const float amax = __uint_as_float(abits << 16);
+      const float s = __fdiv_rn(amax, FMT == kQuantE4M3 ? 448.0f : 127.0f);
+      if (wig == 0 && lane == 0) scale[row] = s;
+      if (y_out) {
+        uint16_t* yr = y_out + row * ldy;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+          const int e = slice0 + (i * 32 + lane) * 8;
+          if (e < K) *reinterpret_cast<uint4*>(yr + e) = v[i];
+        }
+      }
+      int8_t* qr = q + row * ldq * (FMT == kQuantF16 ? 2 : 1);
+      const bool fast = s >= 0x1p-126f;
+      const float r = __frcp_rn(s);
+      const unsigned long long rr = f2(r, r);
 #pragma unroll
       for (int i = 0; i < V; ++i) {
         const int e = slice0 + (i * 32 + lane) * 8;
-        if (e < K) *reinterpret_cast<uint4*>(yr + e) = v[i];
+        if (e < K) {
+          uint2 c = make_uint2(0u, 0u);
+          if (amax != 0.0f) {
+            if constexpr (FMT == kQuantE4M3) c = quant_vec8_e4m3(v[i], s);
+            else c = quant_vec8(v[i], s, rr, fast);
+          }
+          store_codes8<FMT>(qr, e, c);
+        }
       }
     }
-    int8_t* qr = q + row * ldq * (FMT == kQuantF16 ? 2 : 1);
-    const bool fast = s >= 0x1p-126f;
-    const float r = __frcp_rn(s);
-    const unsigned long long rr = f2(r, r);
+    if constexpr (kPrefetch) {
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const int e = slice0 + (i * 32 + lane) * 8;
-      if (e < K) {
-        uint2 c = make_uint2(0u, 0u);
-        if (amax != 0.0f) {
-          if constexpr (FMT == kQuantE4M3) c = quant_vec8_e4m3(v[i], s);
-          else c = quant_vec8(v[i], s, rr, fast);
-        }
-        store_codes8<FMT>(qr, e, c);
-      }
+      for (int i = 0; i < V; ++i) v[i] = vn[i];
     }
   }
   pdl_trigger();
