@@ -104,6 +104,40 @@ def test_quant_e4m3_weights_and_special_rows(orc):
     assert (_codes(q)[:2] == 0).all()
 
 
+def _all_bf16_up_to(amax_bits: int) -> np.ndarray:
+    """Every finite bf16 bit pattern of magnitude <= the bf16 amax, both signs."""
+    mags = np.arange(0, amax_bits + 1, dtype=np.uint32)
+    return np.concatenate([mags, mags | 0x8000]).astype(np.uint16)
+
+
+@pytest.mark.parametrize("amax", [1.0, 300.0, 0.0173, 3.0e38, 5.0e-37, 448.0])
+def test_quant_e4m3_every_bf16_input(orc, amax):
+    """Exhaustive over the inputs: every bf16 value up to amax in magnitude,
+    quantized with the scale amax / 448 (rows that start with amax), gives
+    the oracle's code.  Covers exact E4M3 ties, values within a few fp32 ulps
+    of a rounding boundary (where the fast path must defer to the division),
+    saturation at 448, a subnormal scale (5e-37 / 448) and scale 1."""
+    K = 4096
+    a_bits = int(np.array([amax], dtype=np.float32).view(np.uint32)[0] >> 16)
+    amax_bf16 = float(np.array([a_bits << 16], dtype=np.uint32).view(np.float32)[0])
+    vals = _all_bf16_up_to(a_bits)
+    per_row = K - 1
+    rows = -(-vals.size // per_row)
+    xb = np.zeros((rows, K), dtype=np.uint16)
+    xb[:, 0] = a_bits                                  # every row's absmax is amax
+    flat = np.zeros(rows * per_row, dtype=np.uint16)
+    flat[:vals.size] = vals
+    xb[:, 1:] = flat.reshape(rows, per_row)
+    x = inputs.from_bits(xb)
+    q, s = i8.quant_act_pertoken_e4m3(to_dev(x))
+    i8.sync_check()
+    qo, so = orc.quant_rows_e4m3(xb)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
+    assert float(so[0]) == np.float32(amax_bf16) / np.float32(448.0)
+    bad = np.argwhere(_codes(q) != qo)
+    assert bad.size == 0, f"amax {amax_bf16}: {len(bad)} codes differ, first {bad[:4].tolist()}"
+
+
 # ----------------------------------------------------------------- GEMM
 GEMM_SHAPES = [(64, 128, 256), (1, 8, 16), (7, 24, 48), (129, 136, 272), (300, 520, 1040),
                (256, 256, 3072), (200, 304, 12288), (513, 264, 400),
