@@ -91,3 +91,41 @@ def test_quant_launch_shapes_identical(orc, rows, vpl):
     finally:
         i8.set_option("quant_rows", 0)
         i8.set_option("quant_vpl", 6)
+
+
+def _all_bf16_up_to(amax_bits: int) -> np.ndarray:
+    """Every finite bf16 bit pattern of magnitude <= the bf16 amax, both signs."""
+    mags = np.arange(0, amax_bits + 1, dtype=np.uint32)
+    return np.concatenate([mags, mags | 0x8000]).astype(np.uint16)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "f16codes"])
+@pytest.mark.parametrize("amax", [127.0, 1.0, 300.0, 0.0173, 3.0e38, 1.0e-36])
+def test_quant_every_bf16_input(orc, fmt, amax):
+    """Exhaustive over the inputs: every bf16 value up to amax in magnitude,
+    quantized with the scale amax / 127 (rows that start with amax), gives the
+    oracle's code.  Covers the exact ties x / s = k + 1/2, quotients within a
+    few fp32 ulps of a tie (where the reciprocal fast path must defer to the
+    division), scale 1 (amax 127), and a subnormal scale (1e-36 / 127)."""
+    K = 4096
+    a_bits = int(np.array([amax], dtype=np.float32).view(np.uint32)[0] >> 16)
+    vals = _all_bf16_up_to(a_bits)
+    per_row = K - 1
+    rows = -(-vals.size // per_row)
+    xb = np.zeros((rows, K), dtype=np.uint16)
+    xb[:, 0] = a_bits
+    flat = np.zeros(rows * per_row, dtype=np.uint16)
+    flat[:vals.size] = vals
+    xb[:, 1:] = flat.reshape(rows, per_row)
+    x = to_dev(inputs.from_bits(xb))
+    if fmt == "int8":
+        q, s = i8.quant_act_pertoken(x)
+        got = q.cpu().numpy()
+    else:
+        q, s = i8.quant_act_pertoken_f16codes(x)
+        got = q.cpu().float().numpy().astype(np.int8)
+    i8.sync_check()
+    qo, so = orc.quant_rows(xb)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
+    bad = np.argwhere(got != qo)
+    assert bad.size == 0, f"{len(bad)} codes differ, first {bad[:4].tolist()}"
