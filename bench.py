@@ -20,7 +20,7 @@ pipelined across consecutive steps on separate streams).
 build) on the host cores instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload qkv768|mlp_up1024|mlp_down1024|tiny] [--weights int8|w16]
+                       [--workload qkv768|mlp_up1024|mlp_down1024|tiny|sweep_M<M>_K<K>_N<N>] [--weights int8|w16]
 """
 from __future__ import annotations
 
@@ -50,6 +50,9 @@ WORKLOADS = {
     "mlp_down1024": inputs.MLP_DOWN_1024,
     "tiny": inputs.TINY,
 }
+# the sweep's shapes as workloads too (sweep_M<M>_K<K>_N<N>), e.g. the
+# few-token ones that run the weight-streaming kernel
+WORKLOADS.update({sh.name: sh for sh in inputs.sweep_shapes()})
 L2_BYTES = 129 * 1024 * 1024
 # Dense INT8 rate of this GB300's legacy warp MMA (mma.sync s8 -> s32), the
 # chip's INT8 engine, measured by bench_engines.py (profiles/engine_rates.md).
@@ -58,6 +61,16 @@ INT8_ENGINE_TOPS = 158.4
 # arm's peak is the measured bf16 peak times this ratio.
 FP8_OVER_BF16 = 2.0
 ROTATE_MIN_BYTES = 3 * L2_BYTES
+
+
+def _bound(ops, alg_bytes, t_s, tc_peak, hbm_peak):
+    """Roofline side of one GEMM launch: "tensor" when its flops at the tensor
+    peak take longer than its algorithmic bytes at the HBM peak (the DiT
+    shapes), else "hbm" (few tokens: the weights dominate).  Returns
+    (bound, achieved, peak, unit)."""
+    if ops / (tc_peak * 1e12) >= alg_bytes / (hbm_peak * 1e9):
+        return "tensor", ops / t_s / 1e12, tc_peak, "TFLOP/s"
+    return "hbm", alg_bytes / t_s / 1e9, hbm_peak, "GB/s"
 
 
 def _peaks():
@@ -74,10 +87,16 @@ def _peaks():
 # still hash to the value recorded in the summary.
 PROFILE_SUMMARIES = {
     ("int8", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_w8a8_qkv768_M2560_K3072_N9216.md",
+    # few tokens: the int8 arm runs the weight-streaming kernel
+    ("int8", "sweep_M1_K3072_N9216"): ("gemm_skinny_M1_K3072_N9216.md", "int8_skinny"),
     ("e4m3", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_direct_e4m3_qkv768_M2560_K3072_N9216.md",
     ("f16codes", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_direct_f16codes_qkv768_M2560_K3072_N9216.md",
 }
 KERNEL_SOURCES = {
+    "int8_skinny": ("w8a8_int8_quantized_i8_gb300/csrc/skinny.cuh",
+                    "w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
+                    "w8a8_int8_quantized_i8_gb300/csrc/ptx.cuh",
+                    "w8a8_int8_quantized_i8_gb300/csrc/quant.cuh"),
     "int8": ("w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
              "w8a8_int8_quantized_i8_gb300/csrc/gemm_pair.cuh",
              "w8a8_int8_quantized_i8_gb300/csrc/ptx.cuh",
@@ -107,6 +126,9 @@ def _profiled_traffic(workload: str, arm: str):
     name = PROFILE_SUMMARIES.get((arm, workload))
     if name is None:
         return None
+    src_arm = arm
+    if isinstance(name, tuple):      # (summary, the source set its kernel is built from)
+        name, src_arm = name
     path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
@@ -118,7 +140,7 @@ def _profiled_traffic(workload: str, arm: str):
                 fields[k.strip()] = v.strip()
     if fields.get("workload") != workload:
         return None
-    if fields.get("kernel_sources_sha256") != kernel_sources_sha256(arm):
+    if fields.get("kernel_sources_sha256") != kernel_sources_sha256(src_arm):
         return None
     try:
         return int(fields["traffic_bytes_per_launch"])
@@ -449,6 +471,11 @@ def run_ours(args, shape, dist, rank, world, local):
                "sample": (f"{o['rows']} of {M} token rows (all N={N} channels, K={K}): "
                           f"quant + int32 GEMM + epilogue in {o['seconds']:.2f} s")}
 
+    # algorithmic bytes of one GEMM launch: codes of A and W, bf16 Y, the
+    # scales and the bias
+    wbytes = 2 if args.weights == "w16" else 1
+    alg_bytes = M * K + wbytes * N * K + 2 * M * N + 4 * M + 6 * N
+    rb, ra, rp, ru = _bound(ops, alg_bytes, gemm_ms * 1e-3, tc_peak, hbm_peak)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
@@ -461,8 +488,8 @@ def run_ours(args, shape, dist, rank, world, local):
                        "l2": f"rotating {R} buffer sets of {set_bytes / 1e6:.0f} MB "
                              f"(inputs of a step last touched {R - 1} steps earlier)",
                        "k_split": splits, "replicas": world},
-            "roofline": {"bound": "tensor", "achieved": gemm_tops, "peak": tc_peak,
-                         "unit": "TFLOP/s", "frac": gemm_tops / tc_peak,
+            "roofline": {"bound": rb, "achieved": ra, "peak": rp, "unit": ru, "frac": ra / rp,
+                         "alg_bytes": alg_bytes,
                          "traffic": (_profiled_traffic(shape.name, "int8")
                                      if args.weights == "int8" else None),
                          "traffic_unit": "bytes per launch (ncu dram read + write)",
@@ -551,11 +578,13 @@ def _run_e4m3(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, l
     g_ms = statistics.mean(a.elapsed_time(b) for a, b in evg)
     peak = tc_peak * FP8_OVER_BF16
     g_tflops = ops / (g_ms * 1e-3) / 1e12
+    alg_bytes = M * K + N * K + 2 * M * N + 4 * M + 6 * N
+    rb, ra, rp, ru = _bound(ops, alg_bytes, g_ms * 1e-3, peak, _peaks()[0])
     return {
         "value": ops / (t_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": t_ms, "steps": steps,
         "dtype": "e4m3", "gemm_us": g_ms * 1e3,
-        "roofline": {"bound": "tensor", "achieved": g_tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": g_tflops / peak, "traffic": _profiled_traffic(shape.name, "e4m3"),
+        "roofline": {"bound": rb, "achieved": ra, "peak": rp, "unit": ru, "frac": ra / rp,
+                     "alg_bytes": alg_bytes, "traffic": _profiled_traffic(shape.name, "e4m3"),
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
                      "kernel": "gemm_direct_pair_kernel<E4M3>",
                      "peak_note": f"{peak_kind} dense bf16 burst x {FP8_OVER_BF16:g} "
@@ -626,12 +655,14 @@ def _run_f16codes(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kin
     t_ms = e0.elapsed_time(e1) / steps
     g_ms = statistics.mean(a.elapsed_time(b) for a, b in evg)
     g_tops = ops / (g_ms * 1e-3) / 1e12
+    alg_bytes = 2 * M * K + 2 * N * K + 2 * M * N + 4 * M + 6 * N
+    rb, ra, rp, ru = _bound(ops, alg_bytes, g_ms * 1e-3, tc_peak, _peaks()[0])
     return {
         "value": ops / (t_ms * 1e-3) / 1e12, "unit": "TOPS", "ms_per_step": t_ms, "steps": steps,
         "dtype": "int8 codes held as fp16 (exact int32 accumulation)", "gemm_us": g_ms * 1e3,
         "bytes_note": "activation codes 2 B (written by the quantizer), weight codes 2 B (widened offline)",
-        "roofline": {"bound": "tensor", "achieved": g_tops, "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": g_tops / tc_peak, "traffic": _profiled_traffic(shape.name, "f16codes"),
+        "roofline": {"bound": rb, "achieved": ra, "peak": rp, "unit": ru, "frac": ra / rp,
+                     "alg_bytes": alg_bytes, "traffic": _profiled_traffic(shape.name, "f16codes"),
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
                      "kernel": "gemm_direct_pair_kernel<F16 codes>",
                      "peak_note": f"{peak_kind} dense bf16 burst (the fp16 kind's nominal rate)"},
