@@ -680,7 +680,13 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   }
   if (pl.skinny) {
     const size_t acc_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 15) / 16 * 16;
-    if (pl.splits > 1 && cudaMemsetAsync(ws, 0, pl.ws_bytes, st) != cudaSuccess) return I8_ERR_CUDA;
+    if (pl.splits > 1) {   // ws_bytes is a multiple of 16 (the plan rounds both parts)
+      const int64_t n16 = static_cast<int64_t>(pl.ws_bytes / 16);
+      const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n16 + 255) / 256, 4 * d->sms));
+      if (cudaError_t e = launch_pdl(zero_ws_kernel, dim3(blocks), dim3(256), 0, st,
+                                     static_cast<uint4*>(ws), n16))
+        return cuda_status(e);
+    }
     CUtensorMap mw;
     if (b16) {
       if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wb, K, N, 2 * K, 64, kSkinnyRows))

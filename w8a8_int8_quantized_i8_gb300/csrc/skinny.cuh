@@ -43,6 +43,19 @@ struct SkinnyParams {
   unsigned int* counters;     // [ceil(N / 64)], zeroed before the launch
 };
 
+// Zeroes the split-K workspace (n16 16-byte words) before the skinny kernel.
+// A kernel rather than a memset so that it joins the stream's programmatic
+// dependent launches: it waits for the previous kernel (which may still be
+// reading this workspace) before writing, and lets the GEMM's prologue start
+// early; the GEMM waits for it to finish before touching the workspace.
+__global__ void __launch_bounds__(256) zero_ws_kernel(uint4* __restrict__ ws, int64_t n16) {
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    ws[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 constexpr int kSkinnyRows = 64;
 constexpr int kSkinnyK = 512;
 
