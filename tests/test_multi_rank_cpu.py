@@ -76,3 +76,38 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert rc0 == 0 and rc1 == 0
     assert '"impl": "reference"' in s0 and s0.count("\n") == 1
     assert s1 == ""
+
+
+def test_roofline_side_follows_arithmetic_intensity():
+    """The bench reports a GEMM against the tensor peak when its flops at that
+    peak outlast its bytes at the HBM peak, else against HBM bandwidth."""
+    import bench
+    tc, hbm = 1924.1, 6794.5
+    # DiT QKV at 768px: 145 GOP, 83 MB -> tensor side
+    side, achieved, peak, unit = bench._bound(2 * 2560 * 9216 * 3072, 83.4e6, 112.6e-6, tc, hbm)
+    assert (side, unit, peak) == ("tensor", "TFLOP/s", tc)
+    assert abs(achieved - 2 * 2560 * 9216 * 3072 / 112.6e-6 / 1e12) < 1e-6
+    # one token against the same weights: 57 MOP, 28 MB -> HBM side
+    side, achieved, peak, unit = bench._bound(2 * 1 * 9216 * 3072, 28.4e6, 13e-6, tc, hbm)
+    assert (side, unit, peak) == ("hbm", "GB/s", hbm)
+    assert abs(achieved - 28.4e6 / 13e-6 / 1e9) < 1e-6
+
+
+def test_profile_lookup_uses_the_summarys_source_set(tmp_path, monkeypatch):
+    """A summary quotes its DRAM traffic only while the kernel sources it names
+    still hash to the recorded value."""
+    import bench
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    for src in set(bench.KERNEL_SOURCES["int8_skinny"]):
+        p = tmp_path / src
+        p.parent.mkdir(parents=True, exist_ok=True)
+        p.write_text("// " + src)
+    sha = bench.kernel_sources_sha256("int8_skinny")
+    (prof / "gemm_skinny_M1_K3072_N9216.md").write_text(
+        f"workload: sweep_M1_K3072_N9216\ntraffic_bytes_per_launch: 123\nkernel_sources_sha256: {sha}\n")
+    assert bench._profiled_traffic("sweep_M1_K3072_N9216", "int8") == 123
+    (tmp_path / bench.KERNEL_SOURCES["int8_skinny"][0]).write_text("// changed")
+    assert bench._profiled_traffic("sweep_M1_K3072_N9216", "int8") is None
+    assert bench._profiled_traffic("no_such_workload", "int8") is None
