@@ -155,3 +155,39 @@ def test_binding_fails_loudly_without_library(tmp_path):
 def test_workspace_query_rejects_bad_shapes(lib):
     assert lib.i8_gemm_workspace_bytes(4, 8, 24) == 0
     assert lib.i8_gemm_workspace_bytes(-4, 8, 16) == 0
+
+
+def test_empty_inputs_are_no_ops(lib):
+    """M = 0 (and N = 0 for the GEMMs) is a valid call that does nothing: each
+    entry point returns I8_OK before touching a pointer or the device (this
+    runs without a GPU, with null pointers)."""
+    N0 = None
+    K = 64
+    calls = {
+        "i8_quant_act_pertoken": lambda: lib.i8_quant_act_pertoken(N0, 0, K, K, N0, K, N0, N0),
+        "i8_quant_weight_perchannel": lambda: lib.i8_quant_weight_perchannel(N0, 0, K, K, N0, K, N0, N0),
+        "i8_quant_act_pertoken_e4m3": lambda: lib.i8_quant_act_pertoken_e4m3(N0, 0, K, K, N0, K, N0, N0),
+        "i8_quant_weight_perchannel_e4m3": lambda: lib.i8_quant_weight_perchannel_e4m3(N0, 0, K, K, N0, K, N0, N0),
+        "i8_quant_act_pertoken_f16codes": lambda: lib.i8_quant_act_pertoken_f16codes(N0, 0, K, K, N0, K, N0, N0),
+        "i8_layernorm_quant_act_pertoken": lambda: lib.i8_layernorm_quant_act_pertoken(
+            N0, 0, K, K, ctypes.c_float(1e-6), 0, N0, K, N0, N0, K, N0),
+        "i8_gelu_quant_act_pertoken": lambda: lib.i8_gelu_quant_act_pertoken(N0, 0, K, K, 0, N0, K, N0, N0, K, N0),
+        "i8_widen_weight_codes": lambda: lib.i8_widen_weight_codes(N0, 0, K, N0, N0),
+    }
+    for M, N in ((0, 8), (4, 0), (0, 0)):
+        calls[f"i8_gemm_int32 {M}x{N}"] = lambda M=M, N=N: lib.i8_gemm_int32(N0, N0, M, N, K, N0, max(N, 1), N0, 0, N0)
+        calls[f"i8_gemm_dequant_bias_bf16 {M}x{N}"] = lambda M=M, N=N: lib.i8_gemm_dequant_bias_bf16(
+            N0, N0, N0, N0, N0, M, N, K, N0, max(N, 8), N0, 0, N0)
+        calls[f"i8_gemm_dequant_bias_bf16_w16 {M}x{N}"] = lambda M=M, N=N: lib.i8_gemm_dequant_bias_bf16_w16(
+            N0, N0, N0, N0, N0, M, N, K, N0, max(N, 8), N0, 0, N0)
+        calls[f"i8_gemm_e4m3_f32 {M}x{N}"] = lambda M=M, N=N: lib.i8_gemm_e4m3_f32(N0, N0, M, N, K, N0, max(N, 4), N0, 0, N0)
+        calls[f"i8_gemm_e4m3_dequant_bias_bf16 {M}x{N}"] = lambda M=M, N=N: lib.i8_gemm_e4m3_dequant_bias_bf16(
+            N0, N0, N0, N0, N0, M, N, K, N0, max(N, 8), N0, 0, N0)
+        calls[f"i8_gemm_int32_f16codes {M}x{N}"] = lambda M=M, N=N: lib.i8_gemm_int32_f16codes(
+            N0, N0, M, N, K, N0, max(N, 4), N0, 0, N0)
+        calls[f"i8_gemm_dequant_bias_bf16_f16codes {M}x{N}"] = lambda M=M, N=N: lib.i8_gemm_dequant_bias_bf16_f16codes(
+            N0, N0, N0, N0, N0, M, N, K, N0, max(N, 8), N0, 0, N0)
+        calls[f"i8_gemm_dequant_bias_bf16_noalloc {M}x{N}"] = lambda M=M, N=N: lib.i8_gemm_dequant_bias_bf16_noalloc(
+            N0, N0, N0, N0, N0, M, N, K, N0, max(N, 8), N0)
+    bad = {name: rc for name, rc in ((name, fn()) for name, fn in calls.items()) if rc != 0}
+    assert not bad, bad

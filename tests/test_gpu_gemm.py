@@ -540,3 +540,31 @@ def test_tile_order_does_not_change_results(raster_option, route, M, N, K):
         i8.sync_check()
         outs.append(y.view(torch.int16))
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("route", ["int8", "f16codes", "e4m3", "layernorm", "gelu"])
+def test_empty_token_batch(route):
+    """No tokens: every route returns an empty [0, N] output (and empty codes
+    and scales), with no launch failure and no device error."""
+    K, N = 256, 128
+    x = torch.empty(0, K, dtype=torch.bfloat16, device="cuda")
+    w = inputs.random_bf16(N, K, seed=1, std=0.02).cuda()
+    b = inputs.random_bf16(1, N, seed=2, std=0.1)[0].cuda()
+    if route == "int8":
+        wq, s_w = i8.quant_weight_perchannel(w)
+        y = i8.linear(x, wq, s_w, b)
+        q, s = i8.quant_act_pertoken(x)
+        assert q.shape == (0, K) and s.shape == (0,)
+    elif route == "f16codes":
+        wq, s_w = i8.quant_weight_perchannel(w)
+        y = i8.linear_f16codes(x, i8.widen_weight_codes(wq), s_w, b)
+    elif route == "e4m3":
+        wq, s_w = i8.quant_weight_perchannel_e4m3(w)
+        y = i8.linear_e4m3(x, wq, s_w, b)
+    else:
+        fn = i8.layernorm_quant_act_pertoken if route == "layernorm" else i8.gelu_quant_act_pertoken
+        q, s = fn(x)
+        y = q
+        assert s.shape == (0,)
+    i8.sync_check()
+    assert y.shape[0] == 0
