@@ -568,3 +568,36 @@ def test_empty_token_batch(route):
         assert s.shape == (0,)
     i8.sync_check()
     assert y.shape[0] == 0
+
+
+@pytest.mark.parametrize("route", ["int8", "e4m3", "f16codes"])
+def test_output_beyond_two_to_the_31_elements(orc, route):
+    """Y with 65536 x 32768 = 2^31 elements (4 GiB of bf16): offsets past the
+    32-bit range.  Sampled rows, the last row and the last column included,
+    match the oracle bit for bit (exact routes) or within the bound (E4M3)."""
+    M, N, K = 65536, 32768, 16
+    g = torch.Generator().manual_seed(7)
+    x = inputs.activations(M, K, g, "normal", False)
+    w = inputs.random_bf16(N, K, seed=8, std=0.02)
+    b = inputs.random_bf16(1, N, seed=9, std=0.1)[0]
+    xd, wd, bd = to_dev(x), to_dev(w), to_dev(b)
+    if route == "e4m3":
+        wq, s_w = i8.quant_weight_perchannel_e4m3(wd)
+        y = i8.linear_e4m3(xd, wq, s_w, bd)
+    else:
+        wq, s_w = i8.quant_weight_perchannel(wd)
+        y = (i8.linear(xd, wq, s_w, bd) if route == "int8"
+             else i8.linear_f16codes(xd, i8.widen_weight_codes(wq), s_w, bd))
+    i8.sync_check()
+    rows = np.array([0, 1, 32767, 32768, 65534, 65535])
+    got = y[torch.from_numpy(rows).cuda()].cpu().view(torch.int16).numpy().view(np.uint16)
+    del y
+    torch.cuda.empty_cache()
+    if route == "e4m3":
+        ref = orc.linear_e4m3(inputs.bits(x[rows]), inputs.bits(w), inputs.bits(b))["y"]
+        r = (ref.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        gg = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        assert np.all(np.abs(gg - r) <= 2.0 ** -6 * np.abs(r) + 1e-5)
+    else:
+        ref = orc.linear(inputs.bits(x[rows]), inputs.bits(w), inputs.bits(b))["y"]
+        assert np.array_equal(got, ref)
