@@ -11,8 +11,9 @@
 //   of the B tile it multiplies, which halves the shared-memory traffic per
 //   MAC spent on B compared with a 128 x 256 tile on one SM.
 // Stages: TMA fills int8 stages of 128 K; converter warps widen each into
-// fp16 stages of 64 K, or (WIDE, the default for int8 weights) one fp16 stage
-// of 128 K made of two 64-K swizzled sub-tiles.  Every fp16 stage costs a
+// fp16 stages of 64 K, or (WIDE, the default whenever the fp32 chunk is a
+// whole number of 128-K stages) one fp16 stage of 128 K made of two 64-K
+// swizzled sub-tiles.  Every fp16 stage costs a
 // fixed round of hand-offs (converter arrivals, the relay, the MMA thread's
 // waits and its commit); at 64 K that round cost as much as the stage's MMAs,
 // so the wide stage paid once per 128 K ran 8-14 % faster at DiT shapes.
@@ -20,8 +21,9 @@
 //   * converters arrive on their own CTA's full16[s] and epilogue warps on
 //     their own accempty[b] (CTA-scope release: cheap);
 //   * in CTA 1 one relay thread forwards each completed phase of those two
-//     barriers to CTA 0's pfull16[s] / paccempty[b] (one cluster-scope
-//     release per phase instead of one per warp);
+//     barriers to CTA 0's pfull16[s] / paccempty[b]: one remote arrive per
+//     phase instead of one per warp (a CTA-scope release by default, SYNC
+//     below; arrivals straight from CTA 1's warps measured 1-3.5 % slower);
 //   * the MMA thread of CTA 0 waits on its own barrier and the forwarded one,
 //     and commits to empty16[s] / accfull[b] of both CTAs (multicast).
 #pragma once

@@ -419,13 +419,15 @@ int tile_order_n_fastest(int64_t M, int64_t N) {
 }
 
 // Shape -> configuration (replaces per-shape autotuning).
+//   * few tokens (M <= 8 by default): the weight-streaming kernel;
 //   * CTA pairs (one 256 x 256 tile per cluster of two SMs, each SM staging
 //     and widening half of B) for int8 weights whenever M, N >= 256; with
-//     pre-widened weights the single-CTA kernel measured slightly faster.
+//     pre-widened weights the single-CTA kernel measured slightly faster;
 //   * otherwise one CTA per 128 x 256 tile (128 x 128 when the wider tiles
 //     would leave SMs idle);
-//   * split-K (exact int32 partials + a reduction) when the tiles cannot fill
-//     every worker.
+//   * stream-K on CTA pairs by the rule below, else split-K (exact int32
+//     partials + a reduction) when the tiles cannot fill every worker;
+//   * the tile order from tile_order_n_fastest, applied by the caller.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
                bool b16 = false, size_t ws_cap = SIZE_MAX, int skinny_slots = 0) {
   Plan p;
