@@ -163,6 +163,8 @@ def widen_weight_codes(wq: torch.Tensor) -> torch.Tensor:
 
 
 def workspace_bytes(M: int, N: int, K: int) -> int:
+    """Workspace bytes the int8-code GEMMs need for this shape (0: none): the
+    larger of the int8-weight and pre-widened-weight plans."""
     return int(load().i8_gemm_workspace_bytes(M, N, K))
 
 
@@ -270,6 +272,7 @@ def quant_weight_perchannel_e4m3(w: torch.Tensor, q=None, s=None):
 
 
 def e4m3_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Workspace bytes the E4M3 GEMMs need for this shape (0: none)."""
     return int(load().i8_gemm_e4m3_workspace_bytes(M, N, K))
 
 
@@ -354,6 +357,7 @@ def quant_act_pertoken_f16codes(x: torch.Tensor, q=None, s=None):
 
 
 def f16codes_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Workspace bytes the fp16-held-code GEMMs need for this shape (0: none)."""
     return int(load().i8_gemm_f16codes_workspace_bytes(M, N, K))
 
 
@@ -462,10 +466,13 @@ def gelu_quant_act_pertoken(x: torch.Tensor, fmt: str = "int8", want_y: bool = F
 
 
 def set_option(name: str, value: int) -> None:
+    """Set a process-wide tuning option by name (the keys of OPTIONS, which
+    mirror i8_option in include/i8.h)."""
     _check(load().i8_set_option(OPTIONS[name], int(value)), f"i8_set_option({name})")
 
 
 def get_option(name: str) -> int:
+    """Current value of a tuning option by name."""
     v = ctypes.c_int64(0)
     _check(load().i8_get_option(OPTIONS[name], ctypes.byref(v)), f"i8_get_option({name})")
     return int(v.value)
