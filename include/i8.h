@@ -325,9 +325,9 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *                       (tile, K-block) shares per pair, tiles cut between
  *                       pairs finished from exact int32 partials; it needs
  *                       workspace): 1 (default) where the table predicts a
- *                       gain (K >= 8192 and whole tiles leave many pairs
- *                       idle), 2 whenever whole tiles leave pairs idle,
- *                       0 never.
+ *                       gain (K >= 8192, whole tiles leave many pairs idle
+ *                       and the tiles run M blocks fastest), 2 whenever
+ *                       whole tiles leave pairs idle, 0 never.
  *   I8_OPT_NVTX         1: every call of this header opens an NVTX range
  *                       named after the call (visible in Nsight timelines;
  *                       free when no tool is attached); 0 (default): none.
@@ -345,8 +345,8 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  * loaded, sets options without code changes: a comma-separated list of
  * name=value pairs with the names chunk_k, force_splits, max_ctas, tile_n,
  * quant_vpl, cta_pair, skinny_max_m, pdl, quant_rows, stream_k, nvtx,
- * pair_stage_k, raster (for example "chunk_k=512,stream_k=0").  Entries with an unknown name or an
- * invalid value are ignored. */
+ * pair_stage_k, raster (for example "chunk_k=512,stream_k=0").  Entries with
+ * an unknown name or an invalid value are ignored. */
 typedef enum {
   I8_OPT_CHUNK_K = 1,
   I8_OPT_FORCE_SPLITS = 2,
