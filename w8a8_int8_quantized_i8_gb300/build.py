@@ -20,6 +20,9 @@ MAIN = os.path.join(CSRC, "i8_api.cu")
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-lineinfo", "-O3", "-std=c++17",
+    # IEEE fp32 behaviour (nvcc's defaults, stated so no flag set can drop
+    # them): no flush to zero, correctly rounded division and square root
+    "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
     "-Xcompiler", "-fPIC", "-shared",
     "-I", os.path.join(ROOT, "include"),
 ]
