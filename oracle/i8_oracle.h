@@ -15,7 +15,7 @@
  *          the mechanism -- operands stay INT8, accumulation is int32, the
  *          epilogue dequantizes and adds the bias before writing bf16.
  *
- * Readings where the pages are silent (each one is listed in the design doc):
+ * Readings where the pages are silent (the plainest reading the rest supports):
  *   symmetric quantizer, no zero point; range +-127 (-128 never produced);
  *   scale = absmax / 127 in IEEE fp32; q = round-half-even(x / scale) with a
  *   true fp32 division; an all-zero row has scale 0 and codes 0; epilogue
@@ -62,7 +62,7 @@ int orc_dequant_bias(const int32_t* c, int64_t ldc, const float* s_a,
  * The 8-bit floating-point arm: the pages set their INT8 kernel against an
  * FP8 baseline ([ABS]: the 172.9 s single-card FP8 run at 1024px, and the
  * closing remark that B200's native FP8 path beats the Ampere INT8 kernel).
- * They never print that quantizer.  Reading (listed in the design doc): the same
+ * They never print that quantizer.  Reading: the same
  * symmetric per-row scheme with the E4M3 format of the OCP 8-bit floating
  * point specification -- s = absmax / 448 in IEEE fp32 (448 = largest finite
  * E4M3 value), code = E4M3(fl32(x / s)) rounded to nearest, ties to even,
