@@ -191,3 +191,29 @@ def test_empty_inputs_are_no_ops(lib):
             N0, N0, N0, N0, N0, M, N, K, N0, max(N, 8), N0)
     bad = {name: rc for name, rc in ((name, fn()) for name, fn in calls.items()) if rc != 0}
     assert not bad, bad
+
+
+def test_option_tables_agree(lib, tmp_path):
+    """The binding's option names and numbers are the header's i8_option enum,
+    and every name is accepted through I8_OPTIONS when the library loads."""
+    import os
+    import re
+    import subprocess
+    import sys
+    hdr = open(os.path.join(build.ROOT, "include", "i8.h")).read()
+    enum = {m.group(1).lower(): int(m.group(2))
+            for m in re.finditer(r"I8_OPT_([A-Z0-9_]+)\s*=\s*(\d+)", hdr)}
+    assert enum == binding.OPTIONS
+    # a value each option accepts that differs from its default
+    probe = {"chunk_k": 512, "force_splits": 3, "max_ctas": 64, "tile_n": 128, "quant_vpl": 4,
+             "cta_pair": 1, "skinny_max_m": 4, "pdl": 0, "quant_rows": 2, "stream_k": 0,
+             "nvtx": 1, "pair_stage_k": 64, "raster": 2}
+    assert set(probe) == set(binding.OPTIONS)
+    env = dict(os.environ, I8_OPTIONS=",".join(f"{k}={v}" for k, v in probe.items()))
+    code = ("import sys, json; sys.path.insert(0, %r); "
+            "from w8a8_int8_quantized_i8_gb300 import binding; "
+            "print(json.dumps({n: binding.get_option(n) for n in binding.OPTIONS}))") % str(build.ROOT)
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         check=True).stdout.strip().splitlines()[-1]
+    import json
+    assert json.loads(out) == probe
