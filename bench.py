@@ -38,7 +38,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from w8a8_int8_quantized_i8_gb300 import inputs  # noqa: E402

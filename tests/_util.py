@@ -3,7 +3,6 @@ comparing results with the oracle.  No method arithmetic lives here."""
 import numpy as np
 import torch
 
-from w8a8_int8_quantized_i8_gb300 import inputs
 
 # bf16 parity bar: |gpu - oracle| <= 2^-7 * |oracle| + 1e-6 per element (one
 # bf16 ulp), cosine >= 0.99999, no NaN/Inf.

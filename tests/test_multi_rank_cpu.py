@@ -8,7 +8,6 @@ only.  No GPU is involved.
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 
