@@ -367,6 +367,57 @@ i8_status i8_set_option(i8_option opt, int64_t value);
  * NULL value pointer). */
 i8_status i8_get_option(i8_option opt, int64_t* value);
 
+/* The launch plan a GEMM entry point would choose for a shape: the library's
+ * fixed shape -> configuration table, which stands where the pages' Triton
+ * kernel autotunes per shape (arXiv 2606.14598, abstract: an autotuned
+ * Triton kernel).  Nothing is launched and no memory is touched.
+ *   route   the entry points the plan is for (i8_route).
+ *   sms     > 0: describe the machine by hand, and the call needs no GPU:
+ *           `pairs` = CTA pairs of the route's pair kernel resident at once
+ *           (0 = sms / 2), `skinny_slots` = weight-streaming CTAs resident
+ *           at once (0 = 2 * sms).  0: use the current device's own figures
+ *           (needs the device; pairs and skinny_slots are then ignored).
+ *   ws_cap  workspace bytes the plan may use (0 = unbounded; the no-alloc
+ *           entry point plans with its fixed 16 MiB).
+ *   out     host pointer, filled on I8_OK.
+ * The options set with i8_set_option apply exactly as in the GEMM calls.
+ * Errors: I8_ERR_INVALID_ARG (NULL out, M or N < 1, an unknown route, a
+ * negative machine figure), I8_ERR_UNSUPPORTED (a K or size the GEMM
+ * rejects), I8_ERR_CUDA (sms = 0 without a usable device). */
+typedef enum {
+  I8_ROUTE_INT8 = 0,      /* i8_gemm_int32, i8_gemm_dequant_bias_bf16(_noalloc) */
+  I8_ROUTE_W16 = 1,       /* i8_gemm_dequant_bias_bf16_w16 */
+  I8_ROUTE_F16CODES = 2,  /* i8_gemm_int32_f16codes, i8_gemm_dequant_bias_bf16_f16codes */
+  I8_ROUTE_E4M3 = 3       /* i8_gemm_e4m3_f32, i8_gemm_e4m3_dequant_bias_bf16 */
+} i8_route;
+
+typedef enum {
+  I8_KERNEL_SKINNY = 0,         /* weight-streaming kernel for a few tokens */
+  I8_KERNEL_TILE = 1,           /* one CTA per 128 x tile_n output tile */
+  I8_KERNEL_PAIR = 2,           /* CTA pairs, one 256 x 256 tile per pair */
+  I8_KERNEL_PAIR_STREAM_K = 3,  /* the same with the stream-K schedule */
+  I8_KERNEL_DIRECT = 4          /* CTA pairs fed fp16 or E4M3 codes by TMA */
+} i8_kernel;
+
+typedef struct {
+  int32_t kernel;        /* i8_kernel */
+  int32_t tile_m;        /* output rows of one work item (M for the skinny kernel) */
+  int32_t tile_n;        /* output columns of one work item */
+  int32_t num_m, num_n;  /* work items along M and along N */
+  int32_t block_k;       /* K per K block (skinny kernel: per 512-K chunk) */
+  int32_t total_kb;      /* K blocks */
+  int32_t splits;        /* K splits (1 = none; stream-K reports 1) */
+  int32_t kb_per_split;  /* K blocks per split (the last may hold fewer) */
+  int32_t grid;          /* CTAs of the GEMM launch */
+  int32_t n_fastest;     /* tile order: 1 = N blocks fastest, 0 = M blocks */
+  int64_t ws_bytes;      /* workspace the call needs (0 = none) */
+  double model_us;       /* direct kernels: the split cost model's time (us,
+                            up to a constant) for this plan; else 0 */
+} i8_plan_info;
+
+i8_status i8_plan_query(int64_t M, int64_t N, int64_t K, i8_route route, int sms,
+                        int pairs, int skinny_slots, size_t ws_cap, i8_plan_info* out);
+
 /* Failure-detection self-test: queues a one-thread kernel that waits on a
  * pipeline barrier nothing will ever complete, through the same bounded wait
  * the GEMM uses, with a limit of limit_ms (1..5000).  The wait runs out, the

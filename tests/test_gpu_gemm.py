@@ -601,3 +601,19 @@ def test_output_beyond_two_to_the_31_elements(orc, route):
     else:
         ref = orc.linear(inputs.bits(x[rows]), inputs.bits(w), inputs.bits(b))["y"]
         assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(2, 9216, 3072), (16, 3072, 12288), (300, 200, 1040),
+                                   (512, 3072, 12288), (2304, 3072, 12288), (8704, 9216, 3072)])
+def test_plan_query_on_the_device_matches_the_workspace_queries(M, N, K):
+    """i8_plan_query with the current device's figures reports the workspace
+    that each route's *_workspace_bytes asks for."""
+    p8 = i8.plan_query(M, N, K, "int8")
+    p16 = i8.plan_query(M, N, K, "w16")
+    assert i8.workspace_bytes(M, N, K) == max(p8["ws_bytes"], p16["ws_bytes"])
+    assert i8.e4m3_workspace_bytes(M, N, K) == i8.plan_query(M, N, K, "e4m3")["ws_bytes"]
+    assert i8.f16codes_workspace_bytes(M, N, K) == i8.plan_query(M, N, K, "f16codes")["ws_bytes"]
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    for p in (p8, p16):
+        if p["kernel"] != "skinny":          # tiled grids: at most one CTA per SM
+            assert p["grid"] <= sms

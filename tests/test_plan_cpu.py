@@ -1,0 +1,252 @@
+"""The shape -> configuration table (i8_plan_query), on the host.
+
+The pages autotune their Triton kernel per shape ("Realizing Native INT8
+Compute for Diffusion Transformers on Consumer GPUs", abstract); the library
+instead picks tiles, split counts, schedules and tile order from a fixed
+table.  These tests run that table for hand-described machines (no GPU) and
+check what must hold for every plan -- every output tile and every K block
+covered exactly once, no empty split, a grid that fits the machine, the
+workspace the partials need -- plus each rule of the table and each option.
+"""
+import ctypes
+import math
+
+import pytest
+import torch
+
+from w8a8_int8_quantized_i8_gb300 import binding as i8
+
+GB300 = dict(sms=152, pairs=74, skinny_slots=304)
+MACHINES = [GB300, dict(sms=152, pairs=0, skinny_slots=0), dict(sms=20, pairs=9, skinny_slots=40)]
+ROUTES = ["int8", "w16", "f16codes", "e4m3"]
+MS = [1, 2, 3, 8, 9, 64, 127, 255, 256, 257, 1024, 4096, 4352, 8704]
+NS = [16, 200, 256, 768, 3072, 9216, 12288]
+KS = [16, 112, 512, 3072, 12288, 131072]
+
+
+@pytest.fixture(autouse=True)
+def restore_options():
+    saved = {k: i8.get_option(k) for k in i8.OPTIONS}
+    yield
+    for k, v in saved.items():
+        i8.set_option(k, v)
+
+
+def _eff(items, slots):
+    return items / (math.ceil(items / slots) * slots)
+
+
+def _check_plan(p, M, N, K, route, m):
+    sms = m["sms"]
+    pairs = m["pairs"] or sms // 2
+    slots = m["skinny_slots"] or 2 * sms
+    assert p["num_m"] >= 1 and p["num_n"] >= 1
+    # every output row and column in exactly one work item
+    if p["kernel"] == "skinny":
+        assert p["num_m"] == 1 and p["tile_m"] == M
+    else:
+        assert (p["num_m"] - 1) * p["tile_m"] < M <= p["num_m"] * p["tile_m"]
+    assert (p["num_n"] - 1) * p["tile_n"] < N <= p["num_n"] * p["tile_n"]
+    # every K block in exactly one split, no split empty
+    assert p["total_kb"] == -(-K // p["block_k"])
+    s, kbs = p["splits"], p["kb_per_split"]
+    assert s >= 1 and (s - 1) * kbs < p["total_kb"] <= s * kbs
+    # the grid fits the machine
+    items = p["num_m"] * p["num_n"] * s
+    if p["kernel"] == "skinny":
+        assert p["grid"] == p["num_n"] * s and p["grid"] <= max(p["num_n"], slots)
+    elif p["kernel"] == "tile":
+        assert 1 <= p["grid"] <= min(sms, items)
+    elif p["kernel"] == "pair_stream_k":
+        assert s == 1 and kbs == p["total_kb"] and p["grid"] % 2 == 0
+        assert 2 <= p["grid"] <= 2 * pairs
+    else:
+        assert p["grid"] % 2 == 0 and 2 <= p["grid"] <= 2 * min(pairs, items)
+    # the workspace the partials need
+    if p["kernel"] == "skinny":
+        want = (-(-M * N * 4 // 16) * 16 + -(-p["num_n"] * 4 // 16) * 16) if s > 1 else 0
+        assert p["ws_bytes"] == want
+    elif p["kernel"] == "pair_stream_k":
+        tiles = p["num_m"] * p["num_n"]
+        arrive = -(-tiles * 16 // 1024) * 1024
+        assert p["ws_bytes"] == arrive + p["grid"] * 256 * 256 * 4
+    else:
+        assert p["ws_bytes"] == (s * M * (-(-N // 4) * 4) * 4 if s > 1 else 0)
+    assert p["n_fastest"] == (1 if M > N else 0)
+    assert (p["model_us"] > 0) == (p["kernel"] == "direct")
+
+
+def test_every_plan_covers_the_output_once_and_fits_the_machine():
+    n = 0
+    for m in MACHINES:
+        for route in ROUTES:
+            for M in MS:
+                for N in NS:
+                    for K in KS:
+                        p = i8.plan_query(M, N, K, route, **m)
+                        _check_plan(p, M, N, K, route, m)
+                        n += 1
+    assert n == len(MACHINES) * len(ROUTES) * len(MS) * len(NS) * len(KS)
+
+
+def test_kernel_choice_table():
+    for M in MS:
+        for N in NS:
+            for K in KS:
+                few = M <= 8 and (M <= 2 or N * K <= 48 << 20)
+                k8 = i8.plan_query(M, N, K, "int8", **GB300)["kernel"]
+                k16 = i8.plan_query(M, N, K, "w16", **GB300)["kernel"]
+                if few:
+                    assert k8 == k16 == "skinny", (M, N, K)
+                    continue
+                # CTA pairs for int8 codes once both sides hold a 256 x 256 tile;
+                # the pre-widened weights stay on the single-CTA kernel
+                assert k8 in (("pair", "pair_stream_k") if M >= 256 and N >= 256 else ("tile",))
+                assert k16 == "tile"
+                for r in ("f16codes", "e4m3"):
+                    assert i8.plan_query(M, N, K, r, **GB300)["kernel"] == "direct"
+
+
+def test_block_k_per_route():
+    assert i8.plan_query(4096, 3072, 3072, "int8", **GB300)["block_k"] == 128
+    assert i8.plan_query(4096, 3072, 3072, "e4m3", **GB300)["block_k"] == 128
+    assert i8.plan_query(4096, 3072, 3072, "f16codes", **GB300)["block_k"] == 64
+    assert i8.plan_query(1, 3072, 3072, "int8", **GB300)["block_k"] == 512
+
+
+def test_tiled_splits_maximise_the_last_wave():
+    """int8 / w16 tiled plans: no split while the tiles fill every worker;
+    otherwise the split count maximises the filled fraction of the last wave
+    among the counts with at least 4 K blocks per split (smallest on ties)."""
+    for route, slots_key in (("int8", "pairs"), ("w16", "sms")):
+        for M in (256, 512, 1024, 4096):
+            for N in (256, 768, 3072):
+                for K in (512, 3072, 12288):
+                    i8.set_option("force_splits", 0)
+                    p = i8.plan_query(M, N, K, route, **GB300)
+                    if p["kernel"] in ("skinny", "pair_stream_k"):
+                        continue
+                    slots = GB300[slots_key] if p["kernel"] == "pair" else GB300["sms"]
+                    tiles = p["num_m"] * p["num_n"]
+                    if tiles >= slots:
+                        assert p["splits"] == 1
+                        continue
+                    best = _eff(tiles * p["splits"], slots)
+                    for s in range(1, max(1, min(16, p["total_kb"] // 4)) + 1):
+                        i8.set_option("force_splits", s)
+                        q = i8.plan_query(M, N, K, route, **GB300)
+                        assert q["num_m"] * q["num_n"] == tiles
+                        e = _eff(tiles * q["splits"], slots)
+                        assert e <= best + 1e-9, (route, M, N, K, s)
+                        if e > best - 1e-9:
+                            assert q["splits"] >= p["splits"]
+
+
+def test_direct_splits_minimise_the_cost_model():
+    """Direct plans: no split while the 256 x 256 tiles fill every pair;
+    otherwise the chosen split count has the lowest modelled time among the
+    counts with at least 4 K blocks per split."""
+    for route in ("f16codes", "e4m3"):
+        for M in (1, 8, 64, 256, 512, 1024, 4096):
+            for N in (768, 3072, 9216):
+                for K in (512, 3072, 12288):
+                    i8.set_option("force_splits", 0)
+                    p = i8.plan_query(M, N, K, route, **GB300)
+                    tiles = p["num_m"] * p["num_n"]
+                    if tiles >= GB300["pairs"]:
+                        assert p["splits"] == 1
+                        continue
+                    for s in range(1, max(1, min(16, p["total_kb"] // 4)) + 1):
+                        i8.set_option("force_splits", s)
+                        q = i8.plan_query(M, N, K, route, **GB300)
+                        assert q["model_us"] >= p["model_us"] - 1e-9, (route, M, N, K, s)
+
+
+def test_stream_k_rule():
+    # QKV-like K = 3072: never; K = 12288 with M-fastest tiles and a ragged
+    # last wave: stream-K; the same shape with M > N (N-fastest): split-K or whole tiles
+    assert i8.plan_query(2304, 3072, 3072, "int8", **GB300)["kernel"] == "pair"
+    p = i8.plan_query(2304, 3072, 12288, "int8", **GB300)
+    assert p["kernel"] == "pair_stream_k" and p["grid"] == 2 * GB300["pairs"]
+    assert i8.plan_query(3328, 3072, 12288, "int8", **GB300)["kernel"] == "pair"
+    # a whole number of waves: no stream-K
+    assert i8.plan_query(74 * 256, 256, 12288, "int8", **GB300)["kernel"] == "pair"
+    # the no-alloc entry's 16 MiB cannot hold the partial slots: falls back
+    capped = i8.plan_query(2304, 3072, 12288, "int8", ws_cap=16 << 20, **GB300)
+    assert capped["kernel"] == "pair"
+    i8.set_option("stream_k", 0)
+    assert i8.plan_query(2304, 3072, 12288, "int8", **GB300)["kernel"] == "pair"
+    i8.set_option("stream_k", 2)
+    assert i8.plan_query(2304, 3072, 3072, "int8", **GB300)["kernel"] == "pair_stream_k"
+    assert i8.plan_query(3328, 3072, 12288, "int8", **GB300)["kernel"] == "pair_stream_k"
+    i8.set_option("force_splits", 2)      # a forced split count wins over stream-K
+    assert i8.plan_query(2304, 3072, 12288, "int8", **GB300)["kernel"] == "pair"
+
+
+def test_options_change_the_plan():
+    i8.set_option("force_splits", 5)
+    for route in ROUTES:
+        p = i8.plan_query(4096, 3072, 3072, route, **GB300)
+        assert p["splits"] == 5, route
+    # six 512-K chunks in 5 splits: 2 chunks per split, so 3 splits (none empty)
+    one = i8.plan_query(1, 3072, 3072, "int8", **GB300)
+    assert (one["splits"], one["kb_per_split"]) == (3, 2)
+    assert i8.plan_query(4096, 3072, 16, "int8", **GB300)["splits"] == 1  # one K block
+    i8.set_option("force_splits", 0)
+    for raster, want in ((1, 0), (2, 1)):
+        i8.set_option("raster", raster)
+        for M, N in ((8704, 3072), (512, 9216)):
+            assert i8.plan_query(M, N, 3072, "int8", **GB300)["n_fastest"] == want
+    i8.set_option("raster", 0)
+    i8.set_option("skinny_max_m", 0)
+    assert i8.plan_query(1, 3072, 3072, "int8", **GB300)["kernel"] == "tile"
+    i8.set_option("skinny_max_m", 16)
+    assert i8.plan_query(16, 3072, 3072, "int8", **GB300)["kernel"] == "skinny"
+    i8.set_option("skinny_max_m", 8)
+    i8.set_option("cta_pair", 1)
+    assert i8.plan_query(4096, 3072, 3072, "int8", **GB300)["kernel"] == "tile"
+    i8.set_option("cta_pair", 2)
+    assert i8.plan_query(4096, 3072, 3072, "w16", **GB300)["kernel"] == "pair"
+    i8.set_option("cta_pair", 0)
+    i8.set_option("tile_n", 128)
+    assert i8.plan_query(4096, 3072, 3072, "w16", **GB300)["tile_n"] == 128
+    i8.set_option("tile_n", 0)
+    i8.set_option("max_ctas", 64)
+    assert i8.plan_query(4096, 3072, 3072, "w16", **GB300)["grid"] == 64
+    assert i8.plan_query(4096, 3072, 3072, "int8", **GB300)["grid"] == 64
+
+
+def test_bench_workloads():
+    """The plans behind the timed workloads (DiT-XL-like layers at 4096 and
+    8704 tokens, GB300 figures)."""
+    qkv = i8.plan_query(8704, 9216, 3072, "int8", **GB300)
+    assert (qkv["kernel"], qkv["splits"], qkv["n_fastest"], qkv["ws_bytes"]) == ("pair", 1, 0, 0)
+    down = i8.plan_query(8704, 3072, 12288, "int8", **GB300)
+    assert (down["kernel"], down["splits"], down["n_fastest"]) == ("pair", 1, 1)
+    one = i8.plan_query(1, 9216, 3072, "int8", **GB300)
+    assert (one["kernel"], one["splits"], one["grid"]) == ("skinny", 2, 288)
+
+
+def test_plan_query_errors():
+    lib = i8.load()
+    info = i8.PlanInfo()
+    call = lambda *a: lib.i8_plan_query(*a)  # noqa: E731
+    ok = (64, 64, 64, 0, 152, 0, 0, 0)
+    assert call(*ok, ctypes.byref(info)) == 0
+    assert call(*ok, None) == 1
+    assert call(0, 64, 64, 0, 152, 0, 0, 0, ctypes.byref(info)) == 1
+    assert call(64, 0, 64, 0, 152, 0, 0, 0, ctypes.byref(info)) == 1
+    assert call(64, 64, 64, 4, 152, 0, 0, 0, ctypes.byref(info)) == 1
+    assert call(64, 64, 64, -1, 152, 0, 0, 0, ctypes.byref(info)) == 1
+    assert call(64, 64, 64, 0, -1, 0, 0, 0, ctypes.byref(info)) == 1
+    assert call(64, 64, 64, 0, 152, -1, 0, 0, ctypes.byref(info)) == 1
+    assert call(64, 64, 100, 0, 152, 0, 0, 0, ctypes.byref(info)) == 3
+    assert call(64, 64, 131072 + 16, 0, 152, 0, 0, 0, ctypes.byref(info)) == 3
+    assert call(1 << 31, 64, 64, 0, 152, 0, 0, 0, ctypes.byref(info)) == 3
+    if not torch.cuda.is_available():
+        # the current device's figures need a device
+        assert call(64, 64, 64, 0, 0, 0, 0, 0, ctypes.byref(info)) == 5
+    with pytest.raises(i8.I8Error):
+        i8.plan_query(64, 64, 100, "int8", sms=152)
+    with pytest.raises(KeyError):
+        i8.plan_query(64, 64, 64, "int4", sms=152)

@@ -12,7 +12,8 @@ from .binding import (I8Error, e4m3_workspace_bytes, f16codes_workspace_bytes,
                       gemm_int32_f16codes, get_option, linear_f16codes,
                       quant_act_pertoken_f16codes, gemm_dequant_bias_bf16,
                       gemm_e4m3_dequant_bias_bf16, gemm_e4m3_f32, gemm_int32,
-                      layernorm_quant_act_pertoken, linear, linear_e4m3, load, quant_act_pertoken,
+                      layernorm_quant_act_pertoken, linear, linear_e4m3, load, plan_query,
+                      quant_act_pertoken,
                       quant_act_pertoken_e4m3, quant_weight_perchannel,
                       quant_weight_perchannel_e4m3, set_option, sync_check, widen_weight_codes,
                       workspace_bytes)
@@ -21,7 +22,7 @@ __all__ = [
     "I8Error", "e4m3_workspace_bytes", "f16codes_workspace_bytes", "gelu_quant_act_pertoken",
     "gemm_dequant_bias_bf16_f16codes", "gemm_int32_f16codes", "get_option", "linear_f16codes",
     "quant_act_pertoken_f16codes", "gemm_dequant_bias_bf16", "gemm_e4m3_dequant_bias_bf16",
-    "gemm_e4m3_f32", "gemm_int32", "layernorm_quant_act_pertoken", "linear", "linear_e4m3", "load", "quant_act_pertoken",
+    "gemm_e4m3_f32", "gemm_int32", "layernorm_quant_act_pertoken", "linear", "linear_e4m3", "load", "plan_query", "quant_act_pertoken",
     "quant_act_pertoken_e4m3", "quant_weight_perchannel", "quant_weight_perchannel_e4m3",
     "set_option", "sync_check", "widen_weight_codes", "workspace_bytes",
 ]

@@ -29,6 +29,21 @@ OPTIONS = {"chunk_k": 1, "force_splits": 2, "max_ctas": 3, "tile_n": 4, "quant_v
            "pair_stage_k": 12, "raster": 13}
 
 
+ROUTES = {"int8": 0, "w16": 1, "f16codes": 2, "e4m3": 3}
+KERNELS = {0: "skinny", 1: "tile", 2: "pair", 3: "pair_stream_k", 4: "direct"}
+
+
+class PlanInfo(ctypes.Structure):
+    """i8_plan_info of include/i8.h."""
+    _fields_ = [("kernel", ctypes.c_int32), ("tile_m", ctypes.c_int32),
+                ("tile_n", ctypes.c_int32), ("num_m", ctypes.c_int32),
+                ("num_n", ctypes.c_int32), ("block_k", ctypes.c_int32),
+                ("total_kb", ctypes.c_int32), ("splits", ctypes.c_int32),
+                ("kb_per_split", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("n_fastest", ctypes.c_int32), ("ws_bytes", ctypes.c_int64),
+                ("model_us", ctypes.c_double)]
+
+
 class I8Error(RuntimeError):
     def __init__(self, status: int, what: str):
         super().__init__(f"{what}: {STATUS.get(status, status)}")
@@ -88,6 +103,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                             vp], st),
             "i8_sync_check": ([vp], st),
             "i8_selftest_timeout": ([ctypes.c_int, vp], st),
+            "i8_plan_query": ([i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_int, sz, ctypes.POINTER(PlanInfo)], st),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -476,6 +493,21 @@ def get_option(name: str) -> int:
     v = ctypes.c_int64(0)
     _check(load().i8_get_option(OPTIONS[name], ctypes.byref(v)), f"i8_get_option({name})")
     return int(v.value)
+
+
+def plan_query(M: int, N: int, K: int, route: str = "int8", sms: int = 0, pairs: int = 0,
+               skinny_slots: int = 0, ws_cap: int = 0) -> dict:
+    """The launch plan the route's GEMM calls would choose for an M x N x K
+    shape (i8_plan_query).  With sms > 0 the machine is described by hand and
+    no GPU is needed; sms = 0 uses the current device.  Returns the fields of
+    i8_plan_info, with ``kernel`` as a name (KERNELS)."""
+    info = PlanInfo()
+    _check(load().i8_plan_query(int(M), int(N), int(K), ROUTES[route], int(sms), int(pairs),
+                                int(skinny_slots), int(ws_cap), ctypes.byref(info)),
+           "i8_plan_query")
+    out = {name: getattr(info, name) for name, _ in PlanInfo._fields_}
+    out["kernel"] = KERNELS[out["kernel"]]
+    return out
 
 
 def sync_check(device=None) -> None:

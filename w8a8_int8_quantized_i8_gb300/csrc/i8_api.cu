@@ -1313,6 +1313,72 @@ i8_status i8_get_option(i8_option opt, int64_t* value) {
   return I8_ERR_INVALID_ARG;
 }
 
+// The same planners the GEMM calls run (make_plan, plan_direct), fed either
+// the caller's machine figures or the current device's.
+i8_status i8_plan_query(int64_t M, int64_t N, int64_t K, i8_route route, int sms, int pairs,
+                        int skinny_slots_in, size_t ws_cap, i8_plan_info* out) {
+  if (!out || M <= 0 || N <= 0 || K <= 0 || sms < 0 || pairs < 0 || skinny_slots_in < 0)
+    return I8_ERR_INVALID_ARG;
+  if (route != I8_ROUTE_INT8 && route != I8_ROUTE_W16 && route != I8_ROUTE_F16CODES &&
+      route != I8_ROUTE_E4M3)
+    return I8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX) return I8_ERR_UNSUPPORTED;
+  const bool b16 = route == I8_ROUTE_W16;
+  if (sms == 0) {
+    DeviceInfo* d;
+    if (i8_status e = device_info(&d, nullptr)) return e;
+    sms = d->sms;
+    pairs = route == I8_ROUTE_E4M3       ? direct_cluster_capacity<kDirectE4M3>(d)
+            : route == I8_ROUTE_F16CODES ? direct_cluster_capacity<kDirectF16>(d)
+            : b16                        ? wide_pair_clusters(d)
+                                         : conv_pair_clusters(d);
+    skinny_slots_in = skinny_slots(d, b16);
+  }
+  if (pairs == 0) pairs = std::max(1, sms / 2);
+  i8_plan_info r{};
+  r.n_fastest = tile_order_n_fastest(M, N);
+  if (route == I8_ROUTE_F16CODES || route == I8_ROUTE_E4M3) {
+    const int bk = route == I8_ROUTE_E4M3 ? DirectCfg<kDirectE4M3>::BK : DirectCfg<kDirectF16>::BK;
+    const DirectPlan pl = plan_direct(M, N, K, pairs, bk);
+    if (pl.tiles * pl.splits > INT32_MAX) return I8_ERR_UNSUPPORTED;
+    r.kernel = I8_KERNEL_DIRECT;
+    r.tile_m = r.tile_n = 256;
+    r.num_m = pl.num_m;
+    r.num_n = pl.num_n;
+    r.block_k = bk;
+    r.total_kb = pl.total_kb;
+    r.splits = pl.splits;
+    r.kb_per_split = pl.kb_per_split;
+    r.grid = 2 * static_cast<int>(std::min<int64_t>(pairs, pl.tiles * pl.splits));
+    r.ws_bytes = static_cast<int64_t>(pl.ws_bytes);
+    r.model_us = direct_plan_us(pl.tiles, pairs, pl.total_kb, pl.splits, M, N);
+  } else {
+    const Plan pl = make_plan(M, N, K, sms, pairs, b16, ws_cap ? ws_cap : SIZE_MAX,
+                              skinny_slots_in);
+    r.num_m = pl.num_m;
+    r.num_n = pl.num_n;
+    r.total_kb = pl.total_kb;
+    r.splits = pl.splits;
+    r.kb_per_split = pl.kb_per_split;
+    r.ws_bytes = static_cast<int64_t>(pl.ws_bytes);
+    if (pl.skinny) {
+      r.kernel = I8_KERNEL_SKINNY;
+      r.tile_m = static_cast<int>(M);
+      r.tile_n = kSkinnyRows;
+      r.block_k = kSkinnyK;
+      r.grid = pl.num_n * pl.splits;
+    } else {
+      r.kernel = pl.stream_k ? I8_KERNEL_PAIR_STREAM_K : pl.pair ? I8_KERNEL_PAIR : I8_KERNEL_TILE;
+      r.tile_m = pl.pair ? 256 : 128;
+      r.tile_n = pl.bn;
+      r.block_k = 128;
+      r.grid = pl.grid;
+    }
+  }
+  *out = r;
+  return I8_OK;
+}
+
 i8_status i8_selftest_timeout(int limit_ms, i8_stream_t stream) {
   I8_NVTX();
   if (limit_ms < 1 || limit_ms > 5000) return I8_ERR_INVALID_ARG;
