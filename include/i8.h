@@ -98,7 +98,11 @@ size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   aq [M,K] int8 contiguous (row stride K), wq [N,K] int8 contiguous
  *   c  [M,N] int32, row stride ldc elements (ldc >= N, ldc % 4 == 0)
  *   ws / ws_bytes: device workspace of at least i8_gemm_workspace_bytes()
- *   (may be NULL when that is 0).  The result is exact for every input.   */
+ *   (may be NULL when that is 0).  The result is exact whenever the true
+ *   sum fits in int32: always for codes in -127..127, the quantizers' range
+ *   (127 * 127 * 131072 < 2^31).  A -128 code is accepted too; the one sum
+ *   that cannot be represented is +2^31, reached only when all 131072
+ *   products of a row pair are (-128)^2, and that output is unspecified.  */
 i8_status i8_gemm_int32(const int8_t* aq, const int8_t* wq, int64_t M,
                         int64_t N, int64_t K, int32_t* c, int64_t ldc,
                         void* ws, size_t ws_bytes, i8_stream_t stream);
