@@ -96,3 +96,35 @@ def test_model_restates_the_kernel_sources():
                 f"tile_coords(p, {rest}, {coords}); t.kb0 = t.ks * p.kb_per_split; "
                 f"t.kb1 = min(t.kb0 + p.kb_per_split, p.total_kb);")
         assert body in text(name), name
+
+
+def test_skinny_splits_partition_the_k_chunks():
+    """The weight-streaming kernel: CTA (x, y) streams 64 weight rows of
+    N-block x over K chunks [y * kc_per_cta, min((y + 1) * kc_per_cta,
+    num_kc)); with several splits the CTA whose arrival finds the block's
+    counter at splits - 1 is the last and applies the epilogue."""
+    n = 0
+    for M in (1, 2, 3, 8):
+        for N in (16, 200, 768, 3072, 9216, 18432):
+            for K in (16, 512, 528, 3072, 12288, 131072):
+                p = i8.plan_query(M, N, K, "int8", **GB300)
+                if p["kernel"] != "skinny":
+                    continue
+                s, per, nkc = p["splits"], p["kb_per_split"], p["total_kb"]
+                assert nkc == -(-K // 512) and p["num_n"] == -(-N // 64)
+                ranges = [(y * per, min(y * per + per, nkc)) for y in range(s)]
+                assert all(a < b for a, b in ranges)
+                assert ranges[0][0] == 0 and ranges[-1][1] == nkc
+                assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
+                # arrivals 0..s-1 at a block's counter: exactly one sees s - 1
+                assert sum(prev == s - 1 for prev in range(s)) == 1
+                n += 1
+    assert n > 50
+    src_path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "w8a8_int8_quantized_i8_gb300", "csrc", "skinny.cuh")
+    with open(src_path) as fh:
+        src = " ".join(fh.read().split())
+    for text in ["const int kc0 = blockIdx.y * p.kc_per_cta;",
+                 "const int kc1 = min(kc0 + p.kc_per_cta, p.num_kc);",
+                 "last_cta = (prev == gridDim.y - 1) ? 1 : 0;"]:
+        assert text in src, text
