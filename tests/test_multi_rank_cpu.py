@@ -110,3 +110,31 @@ def test_profile_lookup_uses_the_summarys_source_set(tmp_path, monkeypatch):
     (tmp_path / bench.KERNEL_SOURCES["int8_skinny"][0]).write_text("// changed")
     assert bench._profiled_traffic("sweep_M1_K3072_N9216", "int8") is None
     assert bench._profiled_traffic("no_such_workload", "int8") is None
+
+
+def test_reference_arm_line_keeps_the_contract(capsys, monkeypatch):
+    """One process: the reference arm's JSON line carries every key of the
+    bench contract, with the oracle's own figures in cpu_baseline and e2e."""
+    import json
+    import bench
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    rc = bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1"])
+    assert rc == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2
+    assert d["warmup"] >= 3                      # raised to the contract's minimum
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
+    assert d["vs_baseline"] is None and d["data"] == "synthetic"
+    assert "workload" in d["config"]
+    cb, e2e = d["cpu_baseline"], d["e2e"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
+    assert cb["value"] == d["value"] and cb["unit"] == d["unit"]
+    assert e2e == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}
