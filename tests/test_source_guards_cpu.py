@@ -71,3 +71,50 @@ def test_build_keeps_ieee_fp32():
     assert not any(f in ("--use_fast_math", "-use_fast_math") or f.startswith("-ftz=true")
                    for f in flags)
     assert "arch=compute_103a,code=sm_103a" in flags
+
+
+KERNEL_SOURCES = ["gemm.cuh", "gemm_pair.cuh", "gemm_direct.cuh", "skinny.cuh", "quant.cuh",
+                  "producer.cuh", "ptx.cuh", "i8_api.cu"]
+
+
+def test_every_pipeline_wait_is_bounded():
+    """Raw mbarrier polls appear only inside the bounded wait helpers, each of
+    which gives up after a time limit (2 s) with the abort flag and the
+    device status word set; no kernel source has another unbounded loop."""
+    ptx = _code("ptx.cuh")
+    assert "constexpr unsigned long long kWaitLimitNs = 2000000000ull;" in ptx
+    helpers = {}
+    for name in ("mbar_wait", "mbar_wait_bounded", "mbar_wait_cluster"):
+        m = re.search(rf"bool {name}\((.*?)\) {{(.*?)\}} (?=__device__|//|$)", ptx)
+        assert m, name
+        helpers[name] = m.group(2)
+        assert "globaltimer_ns() - t0 >" in m.group(2), name
+        assert "return false;" in m.group(2) and "atomicOr(&g_status, 1u << 6);" in m.group(2)
+    for name in KERNEL_SOURCES:
+        src = _code(name)
+        # every raw poll sits inside a helper body
+        polls = len(re.findall(r"\bmbar_try_wait(?:_cluster)?\(bar, parity\)", src))
+        if name == "ptx.cuh":
+            inside = sum(len(re.findall(r"\bmbar_try_wait(?:_cluster)?\(bar, parity\)", b))
+                         for b in helpers.values())
+            assert polls == inside
+        else:
+            assert "mbar_try_wait" not in src, name
+        # no other unbounded loop shapes in device code
+        if name != "i8_api.cu":
+            assert "for (;;)" not in src and "do {" not in src, name
+            if name != "ptx.cuh":
+                assert not re.search(r"\bwhile\s*\(", src), name
+
+
+def test_stream_k_arrival_loop_is_capped():
+    src = _code("gemm_pair.cuh")
+    m = re.search(r"bool sk_arrive\((.*?)\) \{(.*?)\n?\}", src)
+    assert m and "for (int i = 0; i < 4096; ++i)" in m.group(2)
+
+
+def test_no_device_code_traps_or_asserts():
+    for name in KERNEL_SOURCES:
+        src = _code(name)
+        assert "__trap" not in src and "trap;" not in src, name
+        assert not re.search(r"(?<!static_)\bassert\(", src), name
