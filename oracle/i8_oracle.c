@@ -18,6 +18,11 @@
  *   orc_dequant_bias   fp64 evaluation rounded to bf16 (within 1 ulp), zero
  *                      accumulator gives the bias, unit scales give
  *                      bf16(acc + bias) exactly
+ *
+ * The pins are tested in turn: tests/test_oracle_mutants.py plants one
+ * plausible mistake at a time in a copy of this file or of its wrapper (a
+ * wrong constant, rounding mode, sign, index or operand order, a dropped
+ * term) and requires each copy to fail at least one pin.
  */
 #include "i8_oracle.h"
 
