@@ -118,3 +118,39 @@ def test_no_device_code_traps_or_asserts():
         src = _code(name)
         assert "__trap" not in src and "trap;" not in src, name
         assert not re.search(r"(?<!static_)\bassert\(", src), name
+
+
+def test_tma_inner_coordinates_are_16_byte_multiples():
+    """A tiled TMA copy must start its innermost coordinate on a 16-byte
+    boundary.  Every x argument in the kernels is one of the expressions
+    below, each a whole number of 128-byte rows: K-block starts (128 int8 /
+    E4M3 codes, 64 fp16 codes, 512-code chunks of 128- or 64-element boxes)
+    and output column starts (64 bf16 or 32 int32 columns from a multiple of
+    128)."""
+    allowed_x = {"kb * Cfg::BK8", "k16", "kb * Cfg::BK", "kc * kSkinnyK + b * Cfg::BOX_K",
+                 "nb", "n0 + g * 32"}
+    calls = 0
+    for name in GEMM_SOURCES:
+        src = _code(name)
+        for m in re.finditer(r"\b(tma_load_2d(?:_pair)?|tma_store_3d)\(([^;]*)\);", src):
+            args = [a.strip() for a in m.group(2).split(",")]
+            x = args[3] if m.group(1).startswith("tma_load") else args[2]
+            assert x in allowed_x, (name, m.group(0))
+            calls += 1
+    assert calls >= 12
+    gemm, pair, skinny = _code("gemm.cuh"), _code("gemm_pair.cuh"), _code("skinny.cuh")
+    direct = _code("gemm_direct.cuh")
+    # the expressions' parts
+    assert "static constexpr int BK8 = 128;" in gemm and "static constexpr int BK16 = 64;" in gemm
+    assert "static constexpr int BK8 = 128;" in pair and "static constexpr int BK16 = 64;" in pair
+    assert "static constexpr int BK = KIND == kDirectF16 ? 64 : 128;" in direct
+    assert "constexpr int kSkinnyK = 512;" in skinny
+    assert "static constexpr int BOX_K = W16 ? 64 : 128;" in skinny
+    assert "const int k16 = kb * Cfg::BK8 + h * Cfg::BK16;" in gemm
+    assert "const int k16 = kb * Cfg::BK8 + (h + q) * Cfg::BK16;" in pair
+    assert "const int nb = n0 + g * 64;" in gemm
+    # output column starts passed to the store helpers: multiples of 128
+    for src, expr in ((gemm, "tc.nb * Cfg::BN + cg * 128"),
+                      (direct, "const int n_base = t.nb * Cfg::PAIR_N + cg * 128;"),
+                      (pair, "const int n_loc = cg * 128;")):
+        assert expr in src, expr
