@@ -90,3 +90,29 @@ def test_model_restates_the_sources():
     for text in ["const int slice0 = wig * (32 * 8 * V);",
                  "const int e = slice0 + (i * 32 + lane) * 8; if (valid_row && e < K) {"]:
         assert text in quant, text
+
+
+def test_layernorm_producer_uses_the_same_split():
+    """The LayerNorm producer-quantizer (one row per CTA of G warps) takes
+    the same host choice of G and V and the same element index, and accepts
+    only K <= 32768, so the coverage checked above holds for it too."""
+    root = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "w8a8_int8_quantized_i8_gb300", "csrc")
+
+    def code(name):
+        with open(os.path.join(root, name)) as fh:
+            return " ".join(fh.read().split())
+
+    api, prod = code("i8_api.cu"), code("producer.cuh")
+    assert "if (K % 16 != 0 || K > 32768 || rows > INT32_MAX) return I8_ERR_UNSUPPORTED;" in api
+    assert api.count("while (G < 8 && (vecs + 32 * G - 1) / (32 * G) > g_opt.quant_vpl) G *= 2;") == 2
+    for v in V_SIZES[:-1]:
+        assert f"if (need <= {v}) return launch_producer_v<{v}, FMT>(" in api
+    assert "return launch_producer_v<16, FMT>(" in api
+    assert "const int slice0 = warp * (32 * 8 * V);" in prod
+    assert "const int e = slice0 + (i * 32 + lane) * 8;" in prod
+    for vpl in range(1, 17):
+        for K in (16, 3072, 12288, 32768):
+            G, V, _ = host_choice(K, vpl, 0)
+            owned = _starts(G, V)[_starts(G, V) < K]
+            assert np.array_equal(owned, np.arange(0, K, 8))
