@@ -217,3 +217,32 @@ def test_option_tables_agree(lib, tmp_path):
                          check=True).stdout.strip().splitlines()[-1]
     import json
     assert json.loads(out) == probe
+
+
+def test_every_compute_entry_point_cites_its_passage():
+    """Each compute call in include/i8.h is documented by the comment block
+    above it (or by its section's comment), and that text cites the passage
+    that defines the operation, or says that the pages have none."""
+    import os
+    import re
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "i8.h")
+    with open(hdr) as fh:
+        text = fh.read()
+    cites = re.compile(r"arXiv 2606\.14598|aiexpert\.news|OCP 8-bit|no counterpart|not on the pages|"
+                       r"The pages (?:print|do not|never)", re.I)
+    names = re.findall(r"^(?:i8_status|size_t)\s+(i8_[a-z0-9_]+)\(", text, re.M)
+    compute = [n for n in names if re.search(r"quant|gemm|widen|layernorm|gelu", n)
+               and not n.endswith("_workspace_bytes")]
+    assert len(compute) >= 15
+    missing = []
+    for name in compute:
+        pos = re.search(rf"^(?:i8_status|size_t)\s+{name}\(", text, re.M).start()
+        # the nearest comment blocks above the declaration (its own and its section's)
+        before = text[:pos]
+        blocks = re.findall(r"/\*.*?\*/", before, re.S)
+        assert blocks, name
+        own = blocks[-1]
+        section = next((b for b in reversed(blocks) if "----" in b), "")
+        if not (cites.search(own) or cites.search(section)):
+            missing.append(name)
+    assert not missing, missing
