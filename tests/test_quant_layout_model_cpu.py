@@ -116,3 +116,39 @@ def test_layernorm_producer_uses_the_same_split():
             G, V, _ = host_choice(K, vpl, 0)
             owned = _starts(G, V)[_starts(G, V) < K]
             assert np.array_equal(owned, np.arange(0, K, 8))
+
+
+def test_gelu_kernel_row_walk_with_prefetch():
+    """The GELU producer walks groups of R rows with a grid stride and, for
+    rows of at most 8 vectors per lane, loads the next group before
+    processing the current one.  Simulated for many row counts, grids and R:
+    every row is processed exactly once, from the data loaded for that row."""
+    for rows in (1, 2, 7, 8, 9, 100, 1023, 4096):
+        for grid in (1, 3, 152, 304):
+            for R in (1, 2, 4, 8):
+                for prefetch in (True, False):
+                    stride = grid * R
+                    done = []
+                    for blk in range(grid):
+                        base = blk * R
+                        cur = base if (prefetch and base < rows) else None
+                        while base < rows:
+                            nxt = base + stride if (prefetch and base + stride < rows) else None
+                            if not prefetch:
+                                cur = base
+                            assert cur == base             # the loaded group is this group
+                            done.extend(r for r in range(base, base + R) if r < rows)
+                            cur = nxt
+                            base += stride
+                    assert sorted(done) == list(range(rows))
+    src_path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "w8a8_int8_quantized_i8_gb300", "csrc", "producer.cuh")
+    with open(src_path) as fh:
+        src = " ".join(fh.read().split())
+    for text in ["const int64_t stride = static_cast<int64_t>(gridDim.x) * R;",
+                 "int64_t base = static_cast<int64_t>(blockIdx.x) * R;",
+                 "if (kPrefetch && base < rows) load_rows(base, v);",
+                 "for (; base < rows; base += stride) {",
+                 "if (base + stride < rows) load_rows(base + stride, vn);",
+                 "for (int i = 0; i < V; ++i) v[i] = vn[i];"]:
+        assert text in src, text
