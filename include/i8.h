@@ -264,14 +264,21 @@ i8_status i8_gelu_quant_act_pertoken(const void* x_bf16, int64_t M, int64_t K,
  *   Same arguments and result as i8_gemm_dequant_bias_bf16, without ws and
  *   ws_bytes.  The split-K scratch lives in a fixed 16 MiB (16777216-byte)
  *   array inside the library, held on every GPU
- *   that loads the library until the process exits.  A shape whose split-K
- *   scratch (i8_gemm_workspace_bytes) exceeds that size is rejected with
- *   I8_ERR_WORKSPACE before anything is queued.
+ *   that loads the library until the process exits.  The launch plan is
+ *   capped to that size: where the regular plan's scratch
+ *   (i8_gemm_workspace_bytes) is larger, the call splits K fewer times, or
+ *   not at all, and falls back from stream-K to whole tiles, with the same
+ *   result bit for bit.  Only a plan that still needs more (a split count
+ *   forced with I8_OPT_FORCE_SPLITS) is rejected with I8_ERR_WORKSPACE,
+ *   before anything is queued.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any
  *   stream capture.  The call itself allocates nothing.
- *   All calls share the one array and it keeps the last call's contents;
- *   the call clears (on its stream) the part that must start at zero.  Calls whose
+ *   All calls share the one array and it keeps the last call's contents.
+ *   Split-K partials are written in full before they are read; the
+ *   few-token kernel's accumulator and counters, the part that must start
+ *   at zero, are cleared by the call on its stream; stream-K arrival words
+ *   carry a per-launch tag, so old words count as zero.  Calls whose
  *   kernels overlap on the GPU -- on different streams, or from different
  *   host threads -- race on the array; serialize them.                      */
 i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a,

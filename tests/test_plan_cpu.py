@@ -142,6 +142,39 @@ def test_tiled_splits_maximise_the_last_wave():
                             assert q["splits"] >= p["splits"]
 
 
+def test_capped_workspace_plans_fit_the_cap():
+    """A workspace cap (the no-alloc entry's fixed 16 MiB array) lowers the
+    split count until the partials fit, down to one split that needs none;
+    it never rejects a sweep shape.  Without a cap the plan is unchanged, and
+    under the cap every plan still covers the output once."""
+    cap = 16 << 20
+    from w8a8_int8_quantized_i8_gb300 import inputs
+    shapes = [(s.M, s.N, s.K) for s in inputs.sweep_shapes()]
+    shapes += [(2560, 9216, 3072), (8704, 12288, 3072), (8704, 3072, 12288), (64, 128, 256)]
+    lowered = 0
+    for m in MACHINES:
+        for M, N, K in shapes:
+            free = i8.plan_query(M, N, K, "int8", **m)
+            p = i8.plan_query(M, N, K, "int8", ws_cap=cap, **m)
+            _check_plan(p, M, N, K, "int8", m)
+            assert p["ws_bytes"] <= cap, (m, M, N, K, p)
+            assert p["splits"] <= free["splits"]
+            if free["ws_bytes"] <= cap:
+                assert p == free, (m, M, N, K)
+            else:
+                lowered += 1
+                # the largest split count whose partials fit
+                if p["kernel"] == "pair" or p["kernel"] == "tile":
+                    plane = M * (-(-N // 4) * 4) * 4
+                    assert p["splits"] == 1 or p["splits"] * plane <= cap
+                    i8.set_option("force_splits", p["splits"] + 1)
+                    more = i8.plan_query(M, N, K, "int8", **m)
+                    i8.set_option("force_splits", 0)
+                    if more["splits"] > p["splits"] and more["splits"] <= free["splits"]:
+                        assert more["ws_bytes"] > cap
+    assert lowered >= 6        # M = 256 at every (K, N), and M = 1024 at N = 3072
+
+
 def test_direct_splits_minimise_the_cost_model():
     """Direct plans: no split while the 256 x 256 tiles fill every pair;
     otherwise the chosen split count has the lowest modelled time among the

@@ -448,6 +448,11 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
     const int chunks = static_cast<int>((K + kSkinnyK - 1) / kSkinnyK);
     int splits = g_opt.force_splits > 0 ? g_opt.force_splits : skinny_slots / p.num_n;
     splits = std::max(1, std::min(splits, chunks));
+    // a capped workspace too small for the accumulator: one split, none needed
+    if (g_opt.force_splits == 0 &&
+        (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 15) / 16 * 16 +
+                (static_cast<size_t>(p.num_n) * 4 + 15) / 16 * 16 > ws_cap)
+      splits = 1;
     p.kb_per_split = (chunks + splits - 1) / splits;          // chunks per split
     p.splits = (chunks + p.kb_per_split - 1) / p.kb_per_split;
     p.total_kb = chunks;
@@ -515,6 +520,16 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
   splits = std::max(1, std::min(splits, p.total_kb));
   p.kb_per_split = (p.total_kb + splits - 1) / splits;
   p.splits = (p.total_kb + p.kb_per_split - 1) / p.kb_per_split;
+  // A capped workspace (the no-alloc entry's fixed array): fewer splits until
+  // the int32 partial planes fit, down to one split, which needs none.
+  if (g_opt.force_splits == 0) {
+    const size_t plane = static_cast<size_t>(M) * static_cast<size_t>((N + 3) / 4 * 4) * 4;
+    while (p.splits > 1 && static_cast<size_t>(p.splits) * plane > ws_cap) {
+      splits = p.splits - 1;
+      p.kb_per_split = (p.total_kb + splits - 1) / splits;
+      p.splits = (p.total_kb + p.kb_per_split - 1) / p.kb_per_split;
+    }
+  }
   p.num_tiles = static_cast<int>(tiles * p.splits);
   p.grid = std::max(1, static_cast<int>(std::min<int64_t>(p.num_tiles, slots)));
   if (p.pair) p.grid *= 2;
@@ -1189,9 +1204,13 @@ i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a, 
                                             i8_stream_t stream) {
   I8_NVTX();
   // Same checks and kernels as i8_gemm_dequant_bias_bf16; only the split-K
-  // scratch comes from the library's fixed device array.  The split partials
-  // are written in full before the reduction reads them, so nothing in the
-  // array has to start at zero.
+  // scratch comes from the library's fixed device array, and the plan is
+  // capped to its size (fewer K splits, or none).  What the array must hold
+  // at the start of a call: the tiled kernels' split-K partials are written
+  // in full before the reduction reads them; the few-token kernel's int32
+  // accumulator and completion counters are zeroed on the stream before its
+  // launch; the stream-K arrival words carry a per-launch epoch tag, so words
+  // left by an earlier call count as zero.
   void* ws = nullptr;
   if (M > 0 && N > 0 && K > 0 && K % 16 == 0 && K <= 131072 && M <= INT32_MAX &&
       N <= INT32_MAX) {
