@@ -229,34 +229,6 @@ def test_linear_e4m3_matches_oracle(orc, M, N, K, bias):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
-SAMPLE_ROWS = lambda M: np.unique(np.concatenate([np.arange(0, 16), np.arange(M // 2, M // 2 + 16),
-                                                  np.arange(M - 24, M)]))
-
-
-@pytest.mark.parametrize("shape", [inputs.QKV_768, inputs.MLP_UP_1024, inputs.MLP_DOWN_1024],
-                         ids=lambda s: s.name)
-def test_full_size_e4m3_sampled_rows(orc, shape):
-    d = inputs.linear_inputs(shape)
-    x = to_dev(d["x"])
-    wq, s_w = i8.quant_weight_perchannel_e4m3(to_dev(d["w"]))
-    aq, s_a = i8.quant_act_pertoken_e4m3(x)
-    y = i8.gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, to_dev(d["bias"]))
-    c = i8.gemm_e4m3_f32(aq, wq)
-    i8.sync_check()
-    rows = SAMPLE_ROWS(shape.M)
-    # codes and scales of the whole matrices, bit-exact
-    qo, so = orc.quant_rows_e4m3(inputs.bits(d["x"]))
-    assert np.array_equal(_codes(aq), qo)
-    assert np.array_equal(s_a.cpu().numpy().view(np.uint32), so.view(np.uint32))
-    wo, swo = orc.quant_rows_e4m3(inputs.bits(d["w"]))
-    assert np.array_equal(_codes(wq), wo)
-    # accumulators and outputs on the sampled rows
-    a_rows = aq[torch.as_tensor(rows, device="cuda")]
-    exact, P, got = _check_acc(orc, a_rows, wq, c[torch.as_tensor(rows, device="cuda")], shape.name)
-    _check_bf16(orc, gpu_bf16_bits(y)[rows], exact, P, got, s_a.cpu().numpy()[rows],
-                s_w.cpu().numpy(), inputs.bits(d["bias"]), shape.K, shape.name)
-
-
 def test_e4m3_zero_rows_give_bias():
     M, N, K = 5, 64, 128
     x = torch.zeros(M, K, dtype=torch.bfloat16)

@@ -93,19 +93,6 @@ def test_linear_f16codes_matches_oracle_and_int8_path(orc, M, N, K, bias):
     assert_bf16_exact(gpu_bf16_bits(y16), want, f"{M}x{N}x{K}")
 
 
-def test_full_size_qkv_f16codes_sampled_rows(orc):
-    shape = inputs.QKV_768
-    d = inputs.linear_inputs(shape)
-    wq, s_w = i8.quant_weight_perchannel(to_dev(d["w"]))
-    y = i8.linear_f16codes(to_dev(d["x"]), i8.widen_weight_codes(wq), s_w, to_dev(d["bias"]))
-    i8.sync_check()
-    rows = np.unique(np.concatenate([np.arange(16), np.arange(1272, 1288), np.arange(2536, 2560)]))
-    aq, s_a = orc.quant_rows(inputs.bits(d["x"][rows]))
-    wo, swo = orc.quant_rows(inputs.bits(d["w"]))
-    want = orc.dequant_bias(orc.gemm_s32(aq, wo), s_a, swo, inputs.bits(d["bias"]))
-    assert_bf16_exact(gpu_bf16_bits(y)[rows], want, shape.name)
-
-
 def test_f16codes_workspace_errors():
     a = torch.zeros(2, 3072, dtype=torch.float16, device="cuda")
     w = torch.zeros(9216, 3072, dtype=torch.float16, device="cuda")

@@ -138,10 +138,13 @@ def test_producer_strided_input_and_errors(orc):
 
 
 def _rows(M):
-    return np.unique(np.concatenate([np.arange(8), np.arange(M // 2 - 4, M // 2 + 4), np.arange(M - 8, M)]))
+    """First, middle and last eight rows plus one row of every 256-row M tile."""
+    per_tile = np.array([256 * t + (97 * t + 13) % 256 for t in range(-(-M // 256))])
+    return np.unique(np.concatenate([np.arange(8), np.arange(M // 2 - 4, M // 2 + 4),
+                                     np.arange(M - 8, M), per_tile[per_tile < M]]))
 
 
-def test_fused_dit_stack_layers_sampled(orc):
+def test_fused_dit_stack_every_layer_every_m_tile(orc):
     M = 8704
     stack = dit_stack.build(blocks=4, seed=5)
     h = inputs.activations(M, dit_stack.WIDTH, torch.Generator().manual_seed(5)).cuda()
