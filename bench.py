@@ -16,6 +16,20 @@ the host cores, `e2e` repeats the metric through the public API with host
 buffers (H2D of X and D2H of Y of every step inside the timed region,
 pipelined across consecutive steps on separate streams).
 
+Beside the headline the line carries, from the same process:
+* ``configs``: the DiT MLP pair at 1024px, batch 2 (up 8704 x 3072 x 12288,
+  down 8704 x 12288 x 3072 on GELU inputs) timed the same way, each with its
+  GEMM and quantizer rooflines; one few-token shape (1 x 3072 x 9216, the
+  weight-streaming kernel) against HBM; and the synthetic 28-block DiT linear
+  stack at 1024px, batch 2 (linear-layer time per denoising step);
+* ``library``: torch bf16 ``addmm`` (cuBLAS), ``torch._int_mm`` and the
+  "fake INT8" forward (both operands dequantized to bf16, then a bf16 matmul)
+  on the same inputs, at the headline workload and at the MLP pair;
+* ``int8_engine``: the rate of this GPU's int8 tensor instruction (the legacy
+  warp MMA, mma.sync s8), measured in this run;
+* ``cosine``: the headline output against the fake-INT8 forward and against
+  the unquantized bf16 product, with NaN/Inf counts.
+
 `--impl reference` times the oracle (the reference implementation of this
 build) on the host cores instead.
 
@@ -53,9 +67,6 @@ WORKLOADS = {
 # few-token ones that run the weight-streaming kernel
 WORKLOADS.update({sh.name: sh for sh in inputs.sweep_shapes()})
 L2_BYTES = 129 * 1024 * 1024
-# Dense INT8 rate of this GB300's legacy warp MMA (mma.sync s8 -> s32), the
-# chip's INT8 engine, measured by bench_engines.py (profiles/engine_rates.md).
-INT8_ENGINE_TOPS = 158.4
 # Nominal dense fp8 / bf16 tensor rate on GB300 (4.5 / 2.25 PF/s): the E4M3
 # arm's peak is the measured bf16 peak times this ratio.
 FP8_OVER_BF16 = 2.0
@@ -81,16 +92,9 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-# Committed ncu summaries per (arm, workload) and the kernel sources each
-# capture was taken from: the DRAM traffic is quoted only while the sources
-# still hash to the value recorded in the summary.
-PROFILE_SUMMARIES = {
-    ("int8", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_w8a8_qkv768_M2560_K3072_N9216.md",
-    # few tokens: the int8 arm runs the weight-streaming kernel
-    ("int8", "sweep_M1_K3072_N9216"): ("gemm_skinny_M1_K3072_N9216.md", "int8_skinny"),
-    ("e4m3", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_direct_e4m3_qkv768_M2560_K3072_N9216.md",
-    ("f16codes", "dit_qkv_768px_M2560_K3072_N9216"): "gemm_direct_f16codes_qkv768_M2560_K3072_N9216.md",
-}
+# DRAM traffic per launch of each arm's GEMM from the committed ncu captures
+# (profiles/traffic.json), quoted only while the kernel sources still hash to
+# the value recorded with the capture.
 KERNEL_SOURCES = {
     "int8_skinny": ("w8a8_int8_quantized_i8_gb300/csrc/skinny.cuh",
                     "w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
@@ -107,6 +111,8 @@ KERNEL_SOURCES = {
                  "w8a8_int8_quantized_i8_gb300/csrc/gemm.cuh",
                  "w8a8_int8_quantized_i8_gb300/csrc/ptx.cuh"),
 }
+TRAFFIC_NOTE = ("ncu dram read + write bytes of one captured launch; ncu flushes the caches "
+                "before the launch, so output still held in L2 when the kernel ends is not counted")
 
 
 def kernel_sources_sha256(arm: str) -> str:
@@ -119,32 +125,20 @@ def kernel_sources_sha256(arm: str) -> str:
 
 
 def _profiled_traffic(workload: str, arm: str):
-    """DRAM bytes per launch of the arm's GEMM from the committed ncu summary,
-    or None when no summary covers this workload or the kernel sources
+    """DRAM bytes per launch of the arm's GEMM on this workload from the
+    committed captures, or None when none covers it or the kernel sources
     changed since the capture."""
-    name = PROFILE_SUMMARIES.get((arm, workload))
-    if name is None:
-        return None
-    src_arm = arm
-    if isinstance(name, tuple):      # (summary, the source set its kernel is built from)
-        name, src_arm = name
-    path = os.path.join(ROOT, "profiles", name)
-    if not os.path.exists(path):
-        return None
-    fields = {}
-    with open(path) as fh:
-        for line in fh:
-            if ":" in line and not line.startswith(("|", "#", " ")):
-                k, v = line.split(":", 1)
-                fields[k.strip()] = v.strip()
-    if fields.get("workload") != workload:
-        return None
-    if fields.get("kernel_sources_sha256") != kernel_sources_sha256(src_arm):
-        return None
     try:
-        return int(fields["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            entries = json.load(fh)["entries"]
+    except (OSError, ValueError, KeyError):
         return None
+    for e in entries:
+        if e.get("arm") == arm and e.get("workload") == workload:
+            if e.get("kernel_sources_sha256") != kernel_sources_sha256(e.get("source_set", arm)):
+                return None
+            return int(e["traffic_bytes_per_launch"])
+    return None
 
 
 def _dist():
@@ -307,6 +301,276 @@ def run_reference(args, shape, dist, rank, world):
 
 
 # --------------------------------------------------------------------- GPU arm
+def _setup_int8(i8, lib, shape, d, dev, stream, weights="int8"):
+    """Device buffers for the int8 path on one workload: weights quantized
+    once (offline), and enough rotating sets of (X, A_q, s_a, W_q, Y,
+    workspace) that a step's inputs were last touched more than 3 x L2 of
+    traffic earlier.  Returns the context the timers use."""
+    M, K, N = shape.M, shape.K, shape.N
+    set_bytes = M * K * 2 + M * K + M * 4 + M * N * 2 + N * K * (2 if weights == "w16" else 1)
+    R = max(2, min(8, -(-ROTATE_MIN_BYTES // set_bytes)))
+    w_dev = d["w"].to(dev)
+    b_dev = d["bias"].to(dev)
+    wq0, s_w = i8.quant_weight_perchannel(w_dev)
+    del w_dev
+    if weights == "w16":
+        wq0 = i8.widen_weight_codes(wq0)
+    ws_bytes = i8.workspace_bytes(M, N, K)
+    x_dev = d["x"].to(dev)
+    sets = []
+    for r in range(R):
+        sets.append(dict(
+            x=x_dev if r == 0 else x_dev.clone(),
+            aq=torch.empty(M, K, dtype=torch.int8, device=dev),
+            s_a=torch.empty(M, dtype=torch.float32, device=dev),
+            w=wq0 if r == 0 else wq0.clone(), y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+            ws=torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)))
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    vp = ctypes.c_void_p
+    calls = []
+    for t in sets:
+        calls.append((
+            (vp(t["x"].data_ptr()), M, K, K, vp(t["aq"].data_ptr()), K, vp(t["s_a"].data_ptr()), sp),
+            (vp(t["aq"].data_ptr()), vp(t["s_a"].data_ptr()), vp(t["w"].data_ptr()),
+             vp(s_w.data_ptr()), vp(b_dev.data_ptr()), M, N, K, vp(t["y"].data_ptr()), N,
+             vp(t["ws"].data_ptr()), ws_bytes, sp)))
+    gemm_fn = lib.i8_gemm_dequant_bias_bf16_w16 if weights == "w16" else lib.i8_gemm_dequant_bias_bf16
+    return dict(shape=shape, sets=sets, calls=calls, R=R, set_bytes=set_bytes, ws_bytes=ws_bytes,
+                s_w=s_w, b_dev=b_dev, weights=weights, quant_fn=lib.i8_quant_act_pertoken,
+                gemm_fn=gemm_fn)
+
+
+def _time_int8(ctx, stream, dev, steps, warmup, dist=None):
+    """Time `steps` steps (per-token quant + fused GEMM) back to back with no
+    event between kernels, then the same steps again with events around each
+    kernel.  Returns (ms per step, sorted GEMM ms, mean quant ms)."""
+    calls, R = ctx["calls"], ctx["R"]
+    qf, gf = ctx["quant_fn"], ctx["gemm_fn"]
+
+    def step(i, evq=None, evg=None):
+        qa, ga = calls[i % R]
+        if evq is not None:
+            evq.record(stream)
+        st = qf(*qa)
+        if evg is not None:
+            evg[0].record(stream)
+        st |= gf(*ga)
+        if evg is not None:
+            evg[1].record(stream)
+        if st:
+            raise RuntimeError(f"libi8 call failed with status {st}")
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    ev_q = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev_g = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(steps)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    _barrier(dist)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(dist)
+    # Per-kernel durations: the same steps again with an event before and
+    # after each kernel.  An event between two kernels keeps the second from
+    # being scheduled while the first drains, so the headline pass records none.
+    for i in range(steps):
+        step(i, ev_q[i], ev_g[i])
+    torch.cuda.synchronize(dev)
+    t_ms = e0.elapsed_time(e1) / steps
+    gemm_all = sorted(a.elapsed_time(b) for a, b in ev_g)
+    quant_ms = statistics.mean(q.elapsed_time(g[0]) for q, g in zip(ev_q, ev_g))
+    return t_ms, gemm_all, quant_ms
+
+
+def _gemm_roofline(shape, gemm_ms, tc_peak, hbm_peak, peak_kind, wbytes=1, arm="int8"):
+    M, K, N = shape.M, shape.K, shape.N
+    ops = 2.0 * M * N * K
+    # algorithmic bytes of one GEMM launch: codes of A and W, bf16 Y, the
+    # scales and the bias
+    alg_bytes = M * K + wbytes * N * K + 2 * M * N + 4 * M + 6 * N
+    rb, ra, rp, ru = _bound(ops, alg_bytes, gemm_ms * 1e-3, tc_peak, hbm_peak)
+    return {"bound": rb, "achieved": ra, "peak": rp, "unit": ru, "frac": ra / rp,
+            "alg_bytes": alg_bytes,
+            "traffic": _profiled_traffic(shape.name, arm) if wbytes == 1 else None,
+            "traffic_unit": "bytes per launch", "traffic_note": TRAFFIC_NOTE,
+            "kernel": "gemm_w8a8 (CTA-pair, single-CTA or few-token kernel per the shape table)",
+            "peak_note": (f"{peak_kind} dense bf16 burst (same nominal rate as the fp16 kind the "
+                          "int8 codes run through)" if rb == "tensor" else f"{peak_kind} HBM copy")}
+
+
+def _quant_roofline(shape, quant_ms, hbm_peak):
+    qb = 3.0 * shape.M * shape.K + 4.0 * shape.M
+    gbs = qb / (quant_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+            "alg_bytes": qb, "kernel": "quant_rows_kernel", "us": quant_ms * 1e3}
+
+
+def _event_mean_ms(fn, n, stream):
+    """Mean device time of fn(i) over n calls, with events around each call
+    (the way the library's GEMM is timed)."""
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for i, (a, b) in enumerate(evs):
+        a.record(stream)
+        fn(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def _library_comparisons(ctx, d, stream, n, gemm_ms):
+    """torch bf16 addmm (cuBLAS), torch._int_mm and the pages' fake-INT8
+    forward on the same rotating inputs, each call timed with events around
+    it like the library's GEMM."""
+    shape = ctx["shape"]
+    M, K, N = shape.M, shape.K, shape.N
+    ops = 2.0 * M * N * K
+    R, sets = ctx["R"], ctx["sets"]
+    b, s_w = ctx["b_dev"], ctx["s_w"]
+    w_bf16 = d["w"].to(stream.device)
+    wts = [w_bf16.t()] + [w_bf16.clone().t() for _ in range(R - 1)]
+    ys = [torch.empty(M, N, dtype=torch.bfloat16, device=stream.device) for _ in range(R)]
+    out = {}
+    t = _event_mean_ms(lambda i: torch.addmm(b, sets[i % R]["x"], wts[i % R], out=ys[i % R]), n, stream)
+    out["torch_bf16_addmm"] = {"us": t * 1e3, "tflops": ops / (t * 1e-3) / 1e12,
+                               "int8_gemm_speedup": t / gemm_ms}
+    if M > 16:
+        wqt = [s_["w"].t() for s_ in sets]
+        t = _event_mean_ms(lambda i: torch._int_mm(sets[i % R]["aq"], wqt[i % R]), n, stream)
+        out["torch_int_mm"] = {"us": t * 1e3, "tops": ops / (t * 1e-3) / 1e12,
+                               "int8_gemm_speedup": t / gemm_ms, "output": "int32 only, no epilogue"}
+    s_w16 = s_w.to(torch.bfloat16)[:, None]
+
+    def fake(i):
+        r = sets[i % R]
+        a_deq = r["aq"].to(torch.bfloat16) * r["s_a"].to(torch.bfloat16)[:, None]
+        w_deq = r["w"].to(torch.bfloat16) * s_w16
+        torch.addmm(b, a_deq, w_deq.t(), out=ys[i % R])
+
+    t = _event_mean_ms(fake, n, stream)
+    out["fake_int8"] = {"us": t * 1e3, "tops": ops / (t * 1e-3) / 1e12, "int8_gemm_speedup": t / gemm_ms,
+                        "what": "dequantize A_q and W_q to bf16, then bf16 addmm (torch ops)"}
+    out["timing"] = "CUDA events around each call, inputs rotating like the library's"
+    del wts, ys
+    return out
+
+
+def _cosines(ctx, d, i8):
+    """The pages report cosine 1.0 and no NaN against the reference: the
+    library's output against the fake-INT8 forward and against the
+    unquantized bf16 product, on the headline inputs (informational)."""
+    t = ctx["sets"][0]
+    y = i8.linear(t["x"], t["w"], ctx["s_w"], ctx["b_dev"]).double()
+    w_bf16 = d["w"].to(t["x"].device)
+    b = ctx["b_dev"]
+    aq, s_a = i8.quant_act_pertoken(t["x"])
+    fake = torch.addmm(b, (aq.to(torch.bfloat16) * s_a.to(torch.bfloat16)[:, None]),
+                       (t["w"].to(torch.bfloat16) * ctx["s_w"].to(torch.bfloat16)[:, None]).t()).double()
+    ref = torch.addmm(b, t["x"], w_bf16.t()).double()
+
+    def cos(a, c):
+        return float((a * c).sum() / (a.norm() * c.norm()))
+
+    return {"vs_fake_int8": cos(y, fake), "vs_bf16_unquantized": cos(y, ref),
+            "nan_or_inf": int((~torch.isfinite(y)).sum().item()),
+            "what": "cosine of the fused W8A8 output (fp64) with each reference, all M x N elements"}
+
+
+def _int8_engine(stream):
+    """Rate of the int8 tensor instruction of this GPU (mma.sync m16n8k32
+    s8 -> s32, register-only loop), measured now."""
+    from w8a8_int8_quantized_i8_gb300 import build as _b
+    try:
+        lib = ctypes.CDLL(_b.PROBE_LIB)
+    except OSError as e:
+        return {"error": f"libi8probe.so not loaded: {e}"}
+    sink = torch.zeros(1, dtype=torch.int32, device=stream.device)
+    s8 = ctypes.c_double(0.0)
+    f16 = ctypes.c_double(0.0)
+    lib.i8probe_mma_rates.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                      ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                      ctypes.c_void_p]
+    rc = lib.i8probe_mma_rates(3, 256, ctypes.c_void_p(sink.data_ptr()), ctypes.byref(s8),
+                               ctypes.byref(f16), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        return {"error": f"probe returned {rc}"}
+    return {"mma_sync_s8_tops": s8.value, "mma_sync_f16_tflops": f16.value,
+            "how": "register-only loops of mma.sync m16n8k32 s8 (and m16n8k16 f16), 4 CTAs of "
+                   "256 threads per SM, best of 3 launches, measured in this run"}
+
+
+def _stack_config(i8, dev, steps):
+    """Linear-layer time per denoising step of the synthetic 28-block DiT
+    stack at 1024px, batch 2 (M = 8704): the sum over its 112 layers of each
+    layer's per-token quantizer + fused GEMM, timed with events around each
+    layer; the LayerNorm / GELU / V-slice glue runs in torch between the
+    timed layers and is excluded."""
+    from w8a8_int8_quantized_i8_gb300 import dit_stack
+    M = 8704
+    stack = dit_stack.build(blocks=28, seed=5, device=dev)
+    h = inputs.activations(M, dit_stack.WIDTH, torch.Generator().manual_seed(5)).to(dev)
+    events = []
+
+    def timer(begin):
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record()
+        events.append(ev)
+
+    dit_stack.forward(stack, h)   # warm-up
+    torch.cuda.synchronize(dev)
+    lin, tot = [], []
+    for _ in range(steps):
+        events.clear()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dit_stack.forward(stack, h, timer=timer)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        lin.append(sum(events[i].elapsed_time(events[i + 1]) for i in range(0, len(events), 2)))
+        tot.append(e0.elapsed_time(e1))
+    i8.sync_check(dev)
+    ops = 2.0 * M * 28 * sum(K * N for _, K, N in dit_stack.LAYERS)
+    lin_ms = statistics.median(lin)
+    del stack
+    torch.cuda.empty_cache()
+    return {"workload": "dit_linear_stack_1024px_b2_28blocks_M8704", "layers": 112,
+            "linear_ms_per_step": lin_ms, "linear_tops": ops / (lin_ms * 1e-3) / 1e12,
+            "step_ms_with_glue": statistics.median(tot), "steps": steps,
+            "how": "sum of the 112 layers' quant + GEMM times (events around each layer), median "
+                   "over steps; torch LayerNorm / GELU / V-slice glue excluded"}
+
+
+def _config_entry(i8, lib, shape, dev, stream, steps, warmup, tc_peak, hbm_peak, peak_kind, library):
+    d = inputs.linear_inputs(shape)
+    ctx = _setup_int8(i8, lib, shape, d, dev, stream)
+    t_ms, gemm_all, quant_ms = _time_int8(ctx, stream, dev, steps, warmup)
+    gemm_ms = statistics.mean(gemm_all)
+    ops = 2.0 * shape.M * shape.N * shape.K
+    e = {"M": shape.M, "K": shape.K, "N": shape.N, "value": ops / (t_ms * 1e-3) / 1e12, "unit": "TOPS",
+         "ms_per_step": t_ms, "gemm_us": gemm_ms * 1e3,
+         "gemm_us_p10_p50_p90": [gemm_all[int(q * (len(gemm_all) - 1))] * 1e3 for q in (0.1, 0.5, 0.9)],
+         "roofline": _gemm_roofline(shape, gemm_ms, tc_peak, hbm_peak, peak_kind),
+         "quant_roofline": _quant_roofline(shape, quant_ms, hbm_peak),
+         "plan": i8.plan_query(shape.M, shape.N, shape.K, "int8")["kernel"],
+         "l2": f"rotating {ctx['R']} buffer sets of {ctx['set_bytes'] / 1e6:.0f} MB"}
+    if library:
+        e["library"] = _library_comparisons(ctx, d, stream, max(10, min(steps, 50)), gemm_ms)
+    i8.sync_check(dev)
+    del ctx
+    torch.cuda.empty_cache()
+    return e
+
+
 def run_ours(args, shape, dist, rank, world, local):
     import w8a8_int8_quantized_i8_gb300 as i8
     from w8a8_int8_quantized_i8_gb300 import binding
@@ -319,88 +583,26 @@ def run_ours(args, shape, dist, rank, world, local):
 
     d = inputs.linear_inputs(shape)
     x_host = d["x"]
-    set_bytes = M * K * 2 + M * K + M * 4 + M * N * 2 + N * K * (2 if args.weights == "w16" else 1)
-    R = max(2, min(8, -(-ROTATE_MIN_BYTES // set_bytes)))
-    sets = []
-    w_dev = d["w"].to(dev)
-    b_dev = d["bias"].to(dev)
-    wq0, s_w = i8.quant_weight_perchannel(w_dev)
-    if args.weights == "w16":
-        wq0 = i8.widen_weight_codes(wq0)
-    ws_bytes = i8.workspace_bytes(M, N, K)
-    for r in range(R):
-        sets.append(dict(
-            x=x_host.to(dev), aq=torch.empty(M, K, dtype=torch.int8, device=dev),
-            s_a=torch.empty(M, dtype=torch.float32, device=dev),
-            w=wq0.clone(), y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
-            ws=torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)))
-    del wq0
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
-    gemm_fn = lib.i8_gemm_dequant_bias_bf16_w16 if args.weights == "w16" else lib.i8_gemm_dequant_bias_bf16
-    vp = ctypes.c_void_p
-    calls = []
-    for s in sets:
-        calls.append((
-            (vp(s["x"].data_ptr()), M, K, K, vp(s["aq"].data_ptr()), K, vp(s["s_a"].data_ptr()), sp),
-            (vp(s["aq"].data_ptr()), vp(s["s_a"].data_ptr()), vp(s["w"].data_ptr()),
-             vp(s_w.data_ptr()), vp(b_dev.data_ptr()), M, N, K, vp(s["y"].data_ptr()), N,
-             vp(s["ws"].data_ptr()), ws_bytes, sp)))
-    quant_fn = lib.i8_quant_act_pertoken
-
-    def step(i, evq=None, evg=None):
-        qa, ga = calls[i % R]
-        if evq is not None:
-            evq[0].record(stream)
-        st = quant_fn(*qa)
-        if evg is not None:
-            evg[0].record(stream)
-        st |= gemm_fn(*ga)
-        if evg is not None:
-            evg[1].record(stream)
-        if st:
-            raise RuntimeError(f"libi8 call failed with status {st}")
-
-    for i in range(args.warmup):
-        step(i)
+    ctx = _setup_int8(i8, lib, shape, d, dev, stream, args.weights)
+    R, ws_bytes, set_bytes = ctx["R"], ctx["ws_bytes"], ctx["set_bytes"]
+    sets, s_w, b_dev = ctx["sets"], ctx["s_w"], ctx["b_dev"]
     binding.sync_check(dev)
 
-    ev_q = [(torch.cuda.Event(enable_timing=True),) for _ in range(args.steps)]
-    ev_g = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    _barrier(dist)
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    _barrier(dist)
-    # Per-kernel durations: the same K steps again with an event before and
-    # after each kernel.  An event between two kernels keeps the second from
-    # being scheduled while the first drains, so the headline pass above
-    # records none.
-    for i in range(args.steps):
-        step(i, ev_q[i], ev_g[i])
-    torch.cuda.synchronize(dev)
+    t_ms, gemm_all, quant_ms = _time_int8(ctx, stream, dev, args.steps, args.warmup, dist)
     clk = clocks.stop()
     binding.sync_check(dev)
-    t_ms = e0.elapsed_time(e1) / args.steps
     t_ms = _max_over_ranks(dist, t_ms)
-    gemm_all = sorted(a.elapsed_time(b) for a, b in ev_g)
     gemm_ms = statistics.mean(gemm_all)
     pct = lambda q: gemm_all[min(len(gemm_all) - 1, int(q * len(gemm_all)))] * 1e3
-    quant_ms = statistics.mean(q[0].elapsed_time(g[0]) for q, g in zip(ev_q, ev_g))
     ops = 2.0 * M * N * K
     total_ops = _sum_over_ranks(dist, ops * args.steps)
     value = total_ops / (t_ms * 1e-3 * args.steps) / 1e12
     gemm_tops = ops / (gemm_ms * 1e-3) / 1e12
-    quant_bytes = 3.0 * M * K + 4.0 * M
     splits = 1 if ws_bytes == 0 else "split-K"
     launches_per_step = 2 + (1 if ws_bytes > 0 else 0)
 
@@ -451,18 +653,38 @@ def run_ours(args, shape, dist, rank, world, local):
     e2e_ms = _max_over_ranks(dist, (time.perf_counter() - t0) * 1e3 / e2e_steps)
     e2e_val = _sum_over_ranks(dist, ops) / (e2e_ms * 1e-3) / 1e12
 
-    # ---- the E4M3 (FP8) arm on the same workload: per-token E4M3 quant +
-    # the fused E4M3 GEMM, timed the same way (headline pass without events,
-    # then a pass with events around each GEMM), rotating the same number of
-    # buffer sets.  Reported beside the int8 line, against the FP8 peak.
-    e4m3 = None
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        # ---- same-run comparisons on the headline workload: library GEMMs,
+        # the pages' cosine, the int8 tensor instruction's rate
+        extras["library"] = _library_comparisons(ctx, d, stream, max(10, min(args.steps, 50)), gemm_ms)
+        extras["cosine"] = _cosines(ctx, d, i8)
+        extras["int8_engine"] = _int8_engine(stream)
+    del ctx, sets, slots
+    torch.cuda.empty_cache()
+
+    # ---- the E4M3 (FP8) arm and the exact path with fp16-held codes on the
+    # same workload, timed the same way, reported beside the int8 line
+    e4m3 = f16codes = None
     if not args.no_e4m3:
         e4m3 = _run_e4m3(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, local)
-    # ---- the same exact W8A8 product with the codes held as fp16 values
-    # (quantizer fp16-code output, weights widened offline), no on-chip widening
-    f16codes = None
-    if not args.no_e4m3:
         f16codes = _run_f16codes(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, local)
+
+    # ---- the other DiT configurations (rank 0): MLP pair at 1024px, one
+    # few-token shape, the 28-block stack
+    configs = None
+    if rank == 0 and not args.no_extras:
+        configs = {}
+        cclk = ClockSampler(local)
+        cclk.start()
+        for cs, lib_cmp in ((inputs.MLP_UP_1024, True), (inputs.MLP_DOWN_1024, True),
+                            (WORKLOADS["sweep_M1_K3072_N9216"], False)):
+            configs[cs.name] = _config_entry(i8, lib, cs, dev, stream, args.steps, args.warmup,
+                                             tc_peak, hbm_peak, peak_kind, lib_cmp)
+        st = _stack_config(i8, dev, max(3, min(args.steps, 5)))
+        configs[st.pop("workload")] = st
+        c = cclk.stop()
+        configs["clocks"] = {k: c[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")}
 
     # ---- oracle on the host cores (rank 0, N = 1 only)
     cpu = None
@@ -472,12 +694,9 @@ def run_ours(args, shape, dist, rank, world, local):
                "sample": (f"{o['rows']} of {M} token rows (all N={N} channels, K={K}): "
                           f"quant + int32 GEMM + epilogue in {o['seconds']:.2f} s")}
 
-    # algorithmic bytes of one GEMM launch: codes of A and W, bf16 Y, the
-    # scales and the bias
     wbytes = 2 if args.weights == "w16" else 1
-    alg_bytes = M * K + wbytes * N * K + 2 * M * N + 4 * M + 6 * N
-    rb, ra, rp, ru = _bound(ops, alg_bytes, gemm_ms * 1e-3, tc_peak, hbm_peak)
     if rank == 0:
+        eng = extras.get("int8_engine", {}).get("mma_sync_s8_tops")
         line = {
             "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
@@ -489,26 +708,20 @@ def run_ours(args, shape, dist, rank, world, local):
                        "l2": f"rotating {R} buffer sets of {set_bytes / 1e6:.0f} MB "
                              f"(inputs of a step last touched {R - 1} steps earlier)",
                        "k_split": splits, "replicas": world},
-            "roofline": {"bound": rb, "achieved": ra, "peak": rp, "unit": ru, "frac": ra / rp,
-                         "alg_bytes": alg_bytes,
-                         "traffic": (_profiled_traffic(shape.name, "int8")
-                                     if args.weights == "int8" else None),
-                         "traffic_unit": "bytes per launch (ncu dram read + write)",
-                         "kernel": "gemm_w8a8 (CTA-pair or single-CTA per the shape table)",
-                         "peak_note": f"{peak_kind} dense bf16 burst (same nominal rate as the "
-                                      "fp16 kind the int8 codes run through)"},
-            "quant_roofline": {"bound": "hbm", "achieved": quant_bytes / (quant_ms * 1e-3) / 1e9,
-                               "peak": hbm_peak, "unit": "GB/s",
-                               "frac": quant_bytes / (quant_ms * 1e-3) / 1e9 / hbm_peak,
-                               "kernel": "quant_rows_kernel", "us": quant_ms * 1e3},
+            "roofline": _gemm_roofline(shape, gemm_ms, tc_peak, hbm_peak, peak_kind, wbytes),
+            "quant_roofline": _quant_roofline(shape, quant_ms, hbm_peak),
             "gemm_us": gemm_ms * 1e3,
             "gemm_us_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
             "kernel_timing": "CUDA events around each kernel in a second pass of the same "
                              "steps (the headline pass has no events between kernels)",
-            "vs_int8_engine": {"int8_tops_measured": INT8_ENGINE_TOPS, "gemm_ratio": gemm_tops / INT8_ENGINE_TOPS,
-                               "source": "mma.sync m16n8k32 s8 rate on this GB300 (bench_engines.py)"},
+            "int8_engine": extras.get("int8_engine"),
+            "vs_int8_engine": ({"gemm_ratio": gemm_tops / eng, "int8_tops_measured": eng}
+                               if eng else None),
+            "library": extras.get("library"),
+            "cosine": extras.get("cosine"),
             "e4m3": e4m3,
             "f16codes": f16codes,
+            "configs": configs,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TOPS", "h2d_bytes_per_step": M * K * 2,
                     "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
@@ -684,6 +897,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e4m3", action="store_true",
                     help="skip the E4M3 (FP8) arm and the fp16-code variant")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other DiT configurations, the library comparisons, the "
+                         "cosines and the int8 engine rate")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

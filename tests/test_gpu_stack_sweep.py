@@ -34,7 +34,7 @@ def _oracle_rows(orc, x_bits_rows, w_bits, b_bits):
 
 
 @pytest.mark.parametrize("shape", inputs.sweep_shapes(), ids=lambda s: s.name)
-def test_sweep_shape_sampled_rows(orc, shape):
+def test_sweep_shape_every_m_tile(orc, shape):
     d = inputs.linear_inputs(shape)
     wq, s_w = i8.quant_weight_perchannel(d["w"].cuda())
     y = i8.linear(d["x"].cuda(), wq, s_w, d["bias"].cuda())

@@ -93,8 +93,8 @@ def test_roofline_side_follows_arithmetic_intensity():
 
 
 def test_profile_lookup_uses_the_summarys_source_set(tmp_path, monkeypatch):
-    """A summary quotes its DRAM traffic only while the kernel sources it names
-    still hash to the recorded value."""
+    """A capture's DRAM traffic (profiles/traffic.json) is quoted only while
+    the kernel sources of its source set still hash to the recorded value."""
     import bench
     prof = tmp_path / "profiles"
     prof.mkdir()
@@ -103,9 +103,11 @@ def test_profile_lookup_uses_the_summarys_source_set(tmp_path, monkeypatch):
         p = tmp_path / src
         p.parent.mkdir(parents=True, exist_ok=True)
         p.write_text("// " + src)
+    import json
     sha = bench.kernel_sources_sha256("int8_skinny")
-    (prof / "gemm_skinny_M1_K3072_N9216.md").write_text(
-        f"workload: sweep_M1_K3072_N9216\ntraffic_bytes_per_launch: 123\nkernel_sources_sha256: {sha}\n")
+    (prof / "traffic.json").write_text(json.dumps({"entries": [
+        {"arm": "int8", "workload": "sweep_M1_K3072_N9216", "source_set": "int8_skinny",
+         "traffic_bytes_per_launch": 123, "kernel_sources_sha256": sha}]}))
     assert bench._profiled_traffic("sweep_M1_K3072_N9216", "int8") == 123
     (tmp_path / bench.KERNEL_SOURCES["int8_skinny"][0]).write_text("// changed")
     assert bench._profiled_traffic("sweep_M1_K3072_N9216", "int8") is None
