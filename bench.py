@@ -343,7 +343,7 @@ def _setup_int8(i8, lib, shape, d, dev, stream, weights="int8"):
 def _time_int8(ctx, stream, dev, steps, warmup, dist=None):
     """Time `steps` steps (per-token quant + fused GEMM) back to back with no
     event between kernels, then the same steps again with events around each
-    kernel.  Returns (ms per step, sorted GEMM ms, mean quant ms)."""
+    kernel, then each kernel alone back to back."""
     calls, R = ctx["calls"], ctx["R"]
     qf, gf = ctx["quant_fn"], ctx["gemm_fn"]
 
@@ -382,10 +382,28 @@ def _time_int8(ctx, stream, dev, steps, warmup, dist=None):
     for i in range(steps):
         step(i, ev_q[i], ev_g[i])
     torch.cuda.synchronize(dev)
+    # Each kernel alone, `steps` launches back to back over the rotating sets
+    # with events only at the ends of the pass: its average launch duration
+    # when launches follow one another, as in a chain of layers.  (An event
+    # right before a launch adds the launch latency that a launch queued
+    # behind another kernel hides: 4-5 us on this GPU for an empty kernel.)
+    pass_ms = []
+    for which in (0, 1):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            st = (qf if which == 0 else gf)(*calls[i % R][which])
+            if st:
+                raise RuntimeError(f"libi8 call failed with status {st}")
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        pass_ms.append(a.elapsed_time(b) / steps)
     t_ms = e0.elapsed_time(e1) / steps
     gemm_all = sorted(a.elapsed_time(b) for a, b in ev_g)
     quant_ms = statistics.mean(q.elapsed_time(g[0]) for q, g in zip(ev_q, ev_g))
-    return t_ms, gemm_all, quant_ms
+    return dict(step_ms=t_ms, gemm_bracketed=gemm_all, quant_bracketed_ms=quant_ms,
+                quant_ms=pass_ms[0], gemm_ms=pass_ms[1])
 
 
 def _gemm_roofline(shape, gemm_ms, tc_peak, hbm_peak, peak_kind, wbytes=1, arm="int8"):
@@ -404,33 +422,44 @@ def _gemm_roofline(shape, gemm_ms, tc_peak, hbm_peak, peak_kind, wbytes=1, arm="
                           "int8 codes run through)" if rb == "tensor" else f"{peak_kind} HBM copy")}
 
 
-def _quant_roofline(shape, quant_ms, hbm_peak):
+def _quant_roofline(shape, tm, hbm_peak):
     qb = 3.0 * shape.M * shape.K + 4.0 * shape.M
-    gbs = qb / (quant_ms * 1e-3) / 1e9
+    gbs = qb / (tm["quant_ms"] * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-            "alg_bytes": qb, "kernel": "quant_rows_kernel", "us": quant_ms * 1e3}
+            "alg_bytes": qb, "kernel": "quant_rows_kernel", "us": tm["quant_ms"] * 1e3,
+            "us_event_bracketed": tm["quant_bracketed_ms"] * 1e3,
+            "timing": "average launch duration over a pass of back-to-back quantizer launches "
+                      "(rotating L2-cold inputs); us_event_bracketed: mean of single launches "
+                      "with an event right before and after each"}
 
 
-def _event_mean_ms(fn, n, stream):
-    """Mean device time of fn(i) over n calls, with events around each call
-    (the way the library's GEMM is timed)."""
+def _gemm_fields(tm):
+    g = tm["gemm_bracketed"]
+    return {"gemm_us": tm["gemm_ms"] * 1e3,
+            "gemm_us_event_bracketed": statistics.mean(g) * 1e3,
+            "gemm_us_event_bracketed_p10_p50_p90": [g[int(q * (len(g) - 1))] * 1e3 for q in (0.1, 0.5, 0.9)]}
+
+
+def _pass_ms(fn, n, stream):
+    """Average device time of fn(i) over n calls back to back, events only at
+    the ends of the pass (the way the library's kernels are timed)."""
     for i in range(3):
         fn(i)
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n)]
-    for i, (a, b) in enumerate(evs):
-        a.record(stream)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(n):
         fn(i)
-        b.record(stream)
+    b.record(stream)
     torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return a.elapsed_time(b) / n
 
 
 def _library_comparisons(ctx, d, stream, n, gemm_ms):
     """torch bf16 addmm (cuBLAS), torch._int_mm and the pages' fake-INT8
-    forward on the same rotating inputs, each call timed with events around
-    it like the library's GEMM."""
+    forward on the same rotating inputs, each timed like the library's GEMM
+    (a pass of back-to-back calls, events at its ends)."""
     shape = ctx["shape"]
     M, K, N = shape.M, shape.K, shape.N
     ops = 2.0 * M * N * K
@@ -440,12 +469,12 @@ def _library_comparisons(ctx, d, stream, n, gemm_ms):
     wts = [w_bf16.t()] + [w_bf16.clone().t() for _ in range(R - 1)]
     ys = [torch.empty(M, N, dtype=torch.bfloat16, device=stream.device) for _ in range(R)]
     out = {}
-    t = _event_mean_ms(lambda i: torch.addmm(b, sets[i % R]["x"], wts[i % R], out=ys[i % R]), n, stream)
+    t = _pass_ms(lambda i: torch.addmm(b, sets[i % R]["x"], wts[i % R], out=ys[i % R]), n, stream)
     out["torch_bf16_addmm"] = {"us": t * 1e3, "tflops": ops / (t * 1e-3) / 1e12,
                                "int8_gemm_speedup": t / gemm_ms}
     if M > 16:
         wqt = [s_["w"].t() for s_ in sets]
-        t = _event_mean_ms(lambda i: torch._int_mm(sets[i % R]["aq"], wqt[i % R]), n, stream)
+        t = _pass_ms(lambda i: torch._int_mm(sets[i % R]["aq"], wqt[i % R]), n, stream)
         out["torch_int_mm"] = {"us": t * 1e3, "tops": ops / (t * 1e-3) / 1e12,
                                "int8_gemm_speedup": t / gemm_ms, "output": "int32 only, no epilogue"}
     s_w16 = s_w.to(torch.bfloat16)[:, None]
@@ -456,10 +485,11 @@ def _library_comparisons(ctx, d, stream, n, gemm_ms):
         w_deq = r["w"].to(torch.bfloat16) * s_w16
         torch.addmm(b, a_deq, w_deq.t(), out=ys[i % R])
 
-    t = _event_mean_ms(fake, n, stream)
+    t = _pass_ms(fake, n, stream)
     out["fake_int8"] = {"us": t * 1e3, "tops": ops / (t * 1e-3) / 1e12, "int8_gemm_speedup": t / gemm_ms,
                         "what": "dequantize A_q and W_q to bf16, then bf16 addmm (torch ops)"}
-    out["timing"] = "CUDA events around each call, inputs rotating like the library's"
+    out["timing"] = ("a pass of back-to-back calls over the library's rotating inputs, events at "
+                     "its ends; int8_gemm_speedup = that time / the library GEMM's gemm_us")
     del wts, ys
     return out
 
@@ -553,14 +583,13 @@ def _stack_config(i8, dev, steps):
 def _config_entry(i8, lib, shape, dev, stream, steps, warmup, tc_peak, hbm_peak, peak_kind, library):
     d = inputs.linear_inputs(shape)
     ctx = _setup_int8(i8, lib, shape, d, dev, stream)
-    t_ms, gemm_all, quant_ms = _time_int8(ctx, stream, dev, steps, warmup)
-    gemm_ms = statistics.mean(gemm_all)
+    tm = _time_int8(ctx, stream, dev, steps, warmup)
+    t_ms, gemm_ms = tm["step_ms"], tm["gemm_ms"]
     ops = 2.0 * shape.M * shape.N * shape.K
     e = {"M": shape.M, "K": shape.K, "N": shape.N, "value": ops / (t_ms * 1e-3) / 1e12, "unit": "TOPS",
-         "ms_per_step": t_ms, "gemm_us": gemm_ms * 1e3,
-         "gemm_us_p10_p50_p90": [gemm_all[int(q * (len(gemm_all) - 1))] * 1e3 for q in (0.1, 0.5, 0.9)],
+         "ms_per_step": t_ms, **_gemm_fields(tm),
          "roofline": _gemm_roofline(shape, gemm_ms, tc_peak, hbm_peak, peak_kind),
-         "quant_roofline": _quant_roofline(shape, quant_ms, hbm_peak),
+         "quant_roofline": _quant_roofline(shape, tm, hbm_peak),
          "plan": i8.plan_query(shape.M, shape.N, shape.K, "int8")["kernel"],
          "l2": f"rotating {ctx['R']} buffer sets of {ctx['set_bytes'] / 1e6:.0f} MB"}
     if library:
@@ -593,12 +622,11 @@ def run_ours(args, shape, dist, rank, world, local):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    t_ms, gemm_all, quant_ms = _time_int8(ctx, stream, dev, args.steps, args.warmup, dist)
+    tm = _time_int8(ctx, stream, dev, args.steps, args.warmup, dist)
     clk = clocks.stop()
     binding.sync_check(dev)
-    t_ms = _max_over_ranks(dist, t_ms)
-    gemm_ms = statistics.mean(gemm_all)
-    pct = lambda q: gemm_all[min(len(gemm_all) - 1, int(q * len(gemm_all)))] * 1e3
+    t_ms = _max_over_ranks(dist, tm["step_ms"])
+    gemm_ms = tm["gemm_ms"]
     ops = 2.0 * M * N * K
     total_ops = _sum_over_ranks(dist, ops * args.steps)
     value = total_ops / (t_ms * 1e-3 * args.steps) / 1e12
@@ -709,11 +737,15 @@ def run_ours(args, shape, dist, rank, world, local):
                              f"(inputs of a step last touched {R - 1} steps earlier)",
                        "k_split": splits, "replicas": world},
             "roofline": _gemm_roofline(shape, gemm_ms, tc_peak, hbm_peak, peak_kind, wbytes),
-            "quant_roofline": _quant_roofline(shape, quant_ms, hbm_peak),
-            "gemm_us": gemm_ms * 1e3,
-            "gemm_us_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
-            "kernel_timing": "CUDA events around each kernel in a second pass of the same "
-                             "steps (the headline pass has no events between kernels)",
+            "quant_roofline": _quant_roofline(shape, tm, hbm_peak),
+            **_gemm_fields(tm),
+            "kernel_timing": ("value / ms_per_step: K steps (quant + GEMM) back to back, events "
+                              "only at the ends.  gemm_us (the roofline's time) and the quantizer's "
+                              "us: each kernel alone, K launches back to back over the same "
+                              "rotating sets, events only at the ends of the pass (average launch "
+                              "duration).  *_event_bracketed: a pass with an event right before "
+                              "and after every launch, which adds the launch latency that a "
+                              "launch queued behind other work hides"),
             "int8_engine": extras.get("int8_engine"),
             "vs_int8_engine": ({"gemm_ratio": gemm_tops / eng, "int8_tops_measured": eng}
                                if eng else None),
@@ -786,18 +818,20 @@ def _run_e4m3(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kind, l
     for i in range(steps):
         step(i, evg[i])
     torch.cuda.synchronize(dev)
+    # the GEMM alone, back to back over the rotating sets (average launch duration)
+    g_ms = _pass_ms(lambda i: gf(*calls[i % R][1]), steps, stream)
     clk = clocks.stop()
     binding.sync_check(dev)
     ops = 2.0 * M * N * K
     t_ms = e0.elapsed_time(e1) / steps
-    g_ms = statistics.mean(a.elapsed_time(b) for a, b in evg)
+    g_br = statistics.mean(a.elapsed_time(b) for a, b in evg)
     peak = tc_peak * FP8_OVER_BF16
     g_tflops = ops / (g_ms * 1e-3) / 1e12
     alg_bytes = M * K + N * K + 2 * M * N + 4 * M + 6 * N
     rb, ra, rp, ru = _bound(ops, alg_bytes, g_ms * 1e-3, peak, _peaks()[0])
     return {
         "value": ops / (t_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": t_ms, "steps": steps,
-        "dtype": "e4m3", "gemm_us": g_ms * 1e3,
+        "dtype": "e4m3", "gemm_us": g_ms * 1e3, "gemm_us_event_bracketed": g_br * 1e3,
         "roofline": {"bound": rb, "achieved": ra, "peak": rp, "unit": ru, "frac": ra / rp,
                      "alg_bytes": alg_bytes, "traffic": _profiled_traffic(shape.name, "e4m3"),
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
@@ -864,17 +898,20 @@ def _run_f16codes(args, i8, lib, shape, d, dev, stream, sp, R, tc_peak, peak_kin
     for i in range(steps):
         step(i, evg[i])
     torch.cuda.synchronize(dev)
+    # the GEMM alone, back to back over the rotating sets (average launch duration)
+    g_ms = _pass_ms(lambda i: gf(*calls[i % R][1]), steps, stream)
     clk = clocks.stop()
     binding.sync_check(dev)
     ops = 2.0 * M * N * K
     t_ms = e0.elapsed_time(e1) / steps
-    g_ms = statistics.mean(a.elapsed_time(b) for a, b in evg)
+    g_br = statistics.mean(a.elapsed_time(b) for a, b in evg)
     g_tops = ops / (g_ms * 1e-3) / 1e12
     alg_bytes = 2 * M * K + 2 * N * K + 2 * M * N + 4 * M + 6 * N
     rb, ra, rp, ru = _bound(ops, alg_bytes, g_ms * 1e-3, tc_peak, _peaks()[0])
     return {
         "value": ops / (t_ms * 1e-3) / 1e12, "unit": "TOPS", "ms_per_step": t_ms, "steps": steps,
         "dtype": "int8 codes held as fp16 (exact int32 accumulation)", "gemm_us": g_ms * 1e3,
+        "gemm_us_event_bracketed": g_br * 1e3,
         "bytes_note": "activation codes 2 B (written by the quantizer), weight codes 2 B (widened offline)",
         "roofline": {"bound": rb, "achieved": ra, "peak": rp, "unit": ru, "frac": ra / rp,
                      "alg_bytes": alg_bytes, "traffic": _profiled_traffic(shape.name, "f16codes"),
