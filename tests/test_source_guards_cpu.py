@@ -128,7 +128,7 @@ def test_tma_inner_coordinates_are_16_byte_multiples():
     and output column starts (64 bf16 or 32 int32 columns from a multiple of
     128)."""
     allowed_x = {"kb * Cfg::BK8", "k16", "kb * Cfg::BK", "kc * kSkinnyK + b * Cfg::BOX_K",
-                 "nb", "n0 + g * 32"}
+                 "nb", "n0 + g * 32", "n0 + g * 64"}
     calls = 0
     for name in GEMM_SOURCES:
         src = _code(name)
@@ -152,5 +152,10 @@ def test_tma_inner_coordinates_are_16_byte_multiples():
     # output column starts passed to the store helpers: multiples of 128
     for src, expr in ((gemm, "tc.nb * Cfg::BN + cg * 128"),
                       (direct, "const int n_base = t.nb * Cfg::PAIR_N + cg * 128;"),
-                      (pair, "const int n_loc = cg * 128;")):
+                      (pair, "const int n_loc = cg * 128;"),
+                      (pair, "const int n_sub = n_loc + 64 * h;")):
         assert expr in src, expr
+    # the staged-scale store starts its 64-column groups at the callers' n0:
+    # a tile column base plus n_loc or n_sub, multiples of 64 bf16 columns
+    assert "tc.nb * Cfg::PAIR_N + n_sub, sum, sa," in pair
+    assert "tc.nb * Cfg::PAIR_N + n_loc, acc, sa," in pair

@@ -311,6 +311,71 @@ __device__ __forceinline__ void store_warp_tile_bf16(const GemmParams& p, const 
   }
 }
 
+// The same store with the per-channel scales and the bias already staged in
+// shared memory (fp32 scales at sw, bf16 bias patterns at bias, both for
+// columns n0, n0 + 1, ...; zero past N) and the row's per-token scale sa
+// already loaded, so no global load sits between the accumulator and the
+// bulk store.  All lanes read the same scale words (one broadcast each).
+template <int COLS>
+__device__ __forceinline__ void store_warp_tile_bf16_staged(const CUtensorMap* tmY, uint32_t stage,
+                                                            int lane, int m_base, int n0,
+                                                            const int (&acc)[COLS], float sa,
+                                                            uint32_t sw, uint32_t bias) {
+  const uint32_t row = stage + static_cast<uint32_t>(lane) * 128u;
+  const uint32_t x = static_cast<uint32_t>(lane & 7);
+#pragma unroll
+  for (int g = 0; g < COLS / 64; ++g) {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int j = g * 64 + 8 * c;
+      const uint4 w0 = lds128(sw + 4u * static_cast<uint32_t>(j));
+      const uint4 w1 = lds128(sw + 4u * static_cast<uint32_t>(j) + 16u);
+      const uint4 bb = lds128(bias + 2u * static_cast<uint32_t>(j));
+      const uint32_t swb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // ((float(acc) * s_a) * s_w) + bias, each step rounded to fp32
+        // (scalar __fmul_rn / __fadd_rn: never contracted into an FMA)
+        const float lo = dequant_one(acc[j + 2 * i], sa, __uint_as_float(swb[2 * i]),
+                                     __uint_as_float(bw[i] << 16));
+        const float hi = dequant_one(acc[j + 2 * i + 1], sa, __uint_as_float(swb[2 * i + 1]),
+                                     __uint_as_float(bw[i] & 0xFFFF0000u));
+        o[i] = pack_bf16x2(lo, hi);
+      }
+      sts128(row + ((static_cast<uint32_t>(c) ^ x) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tmY, stage, n0 + g * 64, m_base, 0);
+      bulk_commit_group();
+    }
+  }
+}
+
+// Stages the per-channel scales and bias of columns [n0, n0 + 32 * nwarps)
+// in shared memory: lane `lane` of warp `w` loads column n0 + 32 w + lane
+// (zeros past N and for a missing bias).
+__device__ __forceinline__ void stage_channel_scales(const GemmParams& p, uint32_t sw, uint32_t bias,
+                                                     int n0, int w, int lane) {
+  const int c = 32 * w + lane;
+  const int n = n0 + c;
+  float s = 0.0f;
+  uint32_t b = 0;
+  if (n < p.N) {
+    s = p.s_w[n];
+    if (p.bias) b = p.bias[n];
+  }
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(sw + 4u * static_cast<uint32_t>(c)), "f"(s) : "memory");
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(bias + 2u * static_cast<uint32_t>(c)),
+               "h"(static_cast<unsigned short>(b))
+               : "memory");
+}
+
 // int32 values (results or partials) through the same staging buffer in
 // 32-column groups; z selects the plane of the 3-D map tm.
 template <int COLS>

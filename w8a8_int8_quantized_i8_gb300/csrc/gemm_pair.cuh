@@ -67,8 +67,8 @@ struct PairCfg {
   static constexpr int EPI_WARP0 = 8;
   static constexpr int NUM_WARPS = 16;
   static constexpr int THREADS = 512;
-  static constexpr int REG_LO = 88;
-  static constexpr int REG_HI = 168;
+  static constexpr int REG_LO = 80;
+  static constexpr int REG_HI = 176;
   static_assert(2 * 128 * REG_LO + 2 * 128 * REG_HI <= THREADS * (65536 / THREADS),
                 "register split exceeds the launch allocation");
   static constexpr int A_ITEMS = CONV_A ? BM * 4 : 0;
@@ -88,10 +88,14 @@ struct PairCfg {
   static constexpr int OFF_EPI = OFF_S16 + S16 * STAGE16;   // 4 KB store staging per epilogue warp
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 4096;
   // full8[S8] empty8[S8] full16[S16] tma16[S16] empty16[S16] pfull16[S16]
-  // accfull[2] accempty[2] paccempty[2] done skstored skdecided
-  static constexpr int NUM_BARS = 2 * S8 + 4 * S16 + 9;
+  // accfull[2] accempty[2] paccempty[2] done skstored skdecided sclfull sclfree
+  static constexpr int NUM_BARS = 2 * S8 + 4 * S16 + 11;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  // the current tile's per-channel scales (fp32) and bias (bf16), staged by
+  // the epilogue warps: PAIR_N columns
+  static constexpr int OFF_SCL = (OFF_MISC + 16 + 15) / 16 * 16;
+  static constexpr int OFF_SCL_BIAS = OFF_SCL + PAIR_N * 4;
+  static constexpr int SMEM_BYTES = OFF_SCL_BIAS + PAIR_N * 2 + 1024;
   static constexpr int TMEM_COLS = 2 * PAIR_N;
   static constexpr uint32_t TX8 = STAGE8;
   static constexpr uint32_t TX16 = (CONV_A ? 0 : A16_BYTES) + (CONV_B ? 0 : B16_BYTES);
@@ -117,6 +121,10 @@ struct PairBars {
   // whether this CTA finishes the tile is made
   __device__ uint32_t skstored() const { return base + 8u * (2 * S8 + 4 * S16 + 7); }
   __device__ uint32_t skdecided() const { return base + 8u * (2 * S8 + 4 * S16 + 8); }
+  // the staged per-channel scales: written (one arrive per epilogue warp) /
+  // read by every epilogue warp
+  __device__ uint32_t sclfull() const { return base + 8u * (2 * S8 + 4 * S16 + 9); }
+  __device__ uint32_t sclfree() const { return base + 8u * (2 * S8 + 4 * S16 + 10); }
 };
 
 struct PairTile {
@@ -208,12 +216,31 @@ __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CU
   const int cg = ew >> 2;
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
-  Ring racc;
+  const bool bf16_out = p.out_mode == kOutBf16;
+  const uint32_t scl_w = sbase + Cfg::OFF_SCL;
+  const uint32_t scl_b = sbase + Cfg::OFF_SCL_BIAS;
+  Ring racc, rscl;
   bool ok = true;
   PairTile tc;
   for (int it = 0; ok && pair_item(p, pair, npairs, it, tc); ++it) {
     const int nst = 2 * (tc.kb1 - tc.kb0) / Cfg::K64_PER_STAGE;
     const int chunk = p.chunk_stages / Cfg::K64_PER_STAGE;
+    const int m_loc = static_cast<int>(rank) * Cfg::BM + quarter * 32;  // rows within the tile
+    const int n_loc = cg * 128;
+    float sa = 0.0f;
+    if (bf16_out) {
+      // Stage this tile's per-channel scales and bias (once the previous
+      // tile's readers are done with them) and load this lane's per-token
+      // scale, while the tile's MMAs run: the loads' latency stays off the
+      // path from the last accumulator to the store.
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.sclfree(), rscl.ph ^ 1u, abort_flag));
+      if (!ok) break;
+      stage_channel_scales(p, scl_w, scl_b, tc.nb * Cfg::PAIR_N, ew, lane);
+      const int m = tc.mp * Cfg::PAIR_M + m_loc + lane;
+      if (m < p.M) sa = p.s_a[m];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.sclfull());
+    }
     int acc[128];
 #pragma unroll
     for (int i = 0; i < 128; ++i) acc[i] = 0;
@@ -237,9 +264,11 @@ __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CU
       racc.advance(2);
     }
     if (!ok) break;
+    if (bf16_out) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.sclfull(), rscl.ph, abort_flag));
+      if (!ok) break;
+    }
     const uint32_t stage = sbase + Cfg::OFF_EPI + static_cast<uint32_t>(ew) * 4096u;
-    const int m_loc = static_cast<int>(rank) * Cfg::BM + quarter * 32;  // rows within the tile
-    const int n_loc = cg * 128;
     if (tc.partial) {
       // Stream-K fix-up.  Publish this pair's int32 partial in its slot,
       // count the arrival, and let the last of the tile's pairs add the
@@ -286,49 +315,66 @@ __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CU
       }
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.skdecided(), sk_phase, abort_flag));
       if (!ok) break;
-      if (*sk_flag == 0) continue;
-      // Last to arrive: rebuild the tile from all the pairs' slots (this
-      // pair's own included, so acc is no longer needed), 64 columns at a
-      // time, and write it.
-      __threadfence();
-      const int q0 = first_pair();
-      const int q1 = last_pair();
+      if (*sk_flag != 0) {
+        // Last to arrive: rebuild the tile from all the pairs' slots (this
+        // pair's own included, so acc is no longer needed), 64 columns at a
+        // time, and write it.
+        __threadfence();
+        const int q0 = first_pair();
+        const int q1 = last_pair();
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        int sum[64];
+        for (int h = 0; h < 2; ++h) {
+          int sum[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) sum[i] = 0;
+          for (int i = 0; i < 64; ++i) sum[i] = 0;
 #pragma unroll 1
-        for (int q = q0; q <= q1; ++q) {
-          const int slot =
-              2 * q + (sk_first(p, q, npairs) / static_cast<uint32_t>(p.total_kb) ==
-                               static_cast<uint32_t>(tc.tile) ? 0 : 1);
-          const int4* src = reinterpret_cast<const int4*>(
-              p.sk_part + (static_cast<int64_t>(slot) * 256 + m_loc + lane) * 256 + n_loc + 64 * h);
-          // 8 loads in flight at a time (the compiler barrier keeps the next
-          // group's loads behind this group's adds)
+          for (int q = q0; q <= q1; ++q) {
+            const int slot =
+                2 * q + (sk_first(p, q, npairs) / static_cast<uint32_t>(p.total_kb) ==
+                                 static_cast<uint32_t>(tc.tile) ? 0 : 1);
+            const int4* src = reinterpret_cast<const int4*>(
+                p.sk_part + (static_cast<int64_t>(slot) * 256 + m_loc + lane) * 256 + n_loc + 64 * h);
+            // 8 loads in flight at a time (the compiler barrier keeps the next
+            // group's loads behind this group's adds)
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            int4 v[8];
+            for (int g = 0; g < 2; ++g) {
+              int4 v[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) v[c] = __ldcg(src + 8 * g + c);
+              for (int c = 0; c < 8; ++c) v[c] = __ldcg(src + 8 * g + c);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              sum[32 * g + 4 * c] += v[c].x;
-              sum[32 * g + 4 * c + 1] += v[c].y;
-              sum[32 * g + 4 * c + 2] += v[c].z;
-              sum[32 * g + 4 * c + 3] += v[c].w;
+              for (int c = 0; c < 8; ++c) {
+                sum[32 * g + 4 * c] += v[c].x;
+                sum[32 * g + 4 * c + 1] += v[c].y;
+                sum[32 * g + 4 * c + 2] += v[c].z;
+                sum[32 * g + 4 * c + 3] += v[c].w;
+              }
+              asm volatile("" ::: "memory");
             }
-            asm volatile("" ::: "memory");
           }
+          const int n_sub = n_loc + 64 * h;
+          if (bf16_out)
+            store_warp_tile_bf16_staged<64>(tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
+                                            tc.nb * Cfg::PAIR_N + n_sub, sum, sa,
+                                            scl_w + 4u * n_sub, scl_b + 2u * n_sub);
+          else
+            store_warp_tile<64>(p, tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
+                                tc.nb * Cfg::PAIR_N + n_sub, sum, tc.ks);
         }
-        store_warp_tile<64>(p, tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
-                            tc.nb * Cfg::PAIR_N + n_loc + 64 * h, sum, tc.ks);
       }
-      continue;
+    } else if (bf16_out) {
+      store_warp_tile_bf16_staged<128>(tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
+                                       tc.nb * Cfg::PAIR_N + n_loc, acc, sa, scl_w + 4u * n_loc,
+                                       scl_b + 2u * n_loc);
+    } else {
+      store_warp_tile<128>(p, tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
+                           tc.nb * Cfg::PAIR_N + n_loc, acc, tc.ks);
     }
-    store_warp_tile<128>(p, tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
-                         tc.nb * Cfg::PAIR_N + n_loc, acc, tc.ks);
+    if (bf16_out) {
+      // this warp's reads of the staged scales are done
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.sclfree());
+      rscl.advance(1);
+    }
   }
   if (lane == 0) bulk_wait_all();
   __syncwarp();
@@ -358,6 +404,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
   volatile int* sk_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 8);
 
+  if (warp >= 2 && lane == 0) {
+    // The first read of a launch parameter misses the constant cache (about
+    // 1 us on GB300) and would sit on every role's path to its first tile;
+    // touch the fields the roles decode first while warps 0 and 1 set up the
+    // barriers and the tensor memory.
+    const int t = p.num_tiles ^ p.splits ^ p.total_kb ^ p.kb_per_split ^ p.num_m_blk ^
+                  p.num_n_blk ^ p.n_fastest ^ p.stream_k ^ p.chunk_stages ^ p.out_mode ^ p.M ^
+                  p.N ^ static_cast<int>(reinterpret_cast<uintptr_t>(p.s_a)) ^
+                  static_cast<int>(reinterpret_cast<uintptr_t>(p.s_w)) ^
+                  static_cast<int>(reinterpret_cast<uintptr_t>(p.sk_arrive));
+    asm volatile("" ::"r"(t));
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::S8; ++s) {
       mbar_init(bars.full8(s), 1);
@@ -377,6 +435,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     mbar_init(bars.done(), 1);
     mbar_init(bars.skstored(), Cfg::EPI_WARPS);
     mbar_init(bars.skdecided(), 1);
+    mbar_init(bars.sclfull(), Cfg::EPI_WARPS);
+    mbar_init(bars.sclfree(), Cfg::EPI_WARPS);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
