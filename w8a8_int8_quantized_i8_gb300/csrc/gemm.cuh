@@ -316,7 +316,9 @@ __device__ __forceinline__ void store_warp_tile_bf16(const GemmParams& p, const 
 // columns n0, n0 + 1, ...; zero past N) and the row's per-token scale sa
 // already loaded, so no global load sits between the accumulator and the
 // bulk store.  All lanes read the same scale words (one broadcast each).
-template <int COLS>
+// F32_BITS: acc holds fp32 bit patterns (the E4M3 arm's accumulators)
+// instead of exact int32 sums.
+template <int COLS, bool F32_BITS = false>
 __device__ __forceinline__ void store_warp_tile_bf16_staged(const CUtensorMap* tmY, uint32_t stage,
                                                             int lane, int m_base, int n0,
                                                             const int (&acc)[COLS], float sa,
@@ -340,10 +342,18 @@ __device__ __forceinline__ void store_warp_tile_bf16_staged(const CUtensorMap* t
       for (int i = 0; i < 4; ++i) {
         // ((float(acc) * s_a) * s_w) + bias, each step rounded to fp32
         // (scalar __fmul_rn / __fadd_rn: never contracted into an FMA)
-        const float lo = dequant_one(acc[j + 2 * i], sa, __uint_as_float(swb[2 * i]),
-                                     __uint_as_float(bw[i] << 16));
-        const float hi = dequant_one(acc[j + 2 * i + 1], sa, __uint_as_float(swb[2 * i + 1]),
-                                     __uint_as_float(bw[i] & 0xFFFF0000u));
+        float lo, hi;
+        if constexpr (F32_BITS) {
+          lo = dequant_one(__int_as_float(acc[j + 2 * i]), sa, __uint_as_float(swb[2 * i]),
+                           __uint_as_float(bw[i] << 16));
+          hi = dequant_one(__int_as_float(acc[j + 2 * i + 1]), sa, __uint_as_float(swb[2 * i + 1]),
+                           __uint_as_float(bw[i] & 0xFFFF0000u));
+        } else {
+          lo = dequant_one(acc[j + 2 * i], sa, __uint_as_float(swb[2 * i]),
+                           __uint_as_float(bw[i] << 16));
+          hi = dequant_one(acc[j + 2 * i + 1], sa, __uint_as_float(swb[2 * i + 1]),
+                           __uint_as_float(bw[i] & 0xFFFF0000u));
+        }
         o[i] = pack_bf16x2(lo, hi);
       }
       sts128(row + ((static_cast<uint32_t>(c) ^ x) << 4), make_uint4(o[0], o[1], o[2], o[3]));

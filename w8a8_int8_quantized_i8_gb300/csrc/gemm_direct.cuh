@@ -36,7 +36,8 @@
 //     warps arrive on CTA 0's barrier), and write the tile through swizzled
 //     shared-memory staging with bulk tensor stores: dequant + bias -> bf16,
 //     or the raw accumulator (fp32 / int32) for the checking paths.
-// Warps: 0 producer, 1 TMEM allocation + MMA issuer, 2-3 idle, 4-11 epilogue.
+// Warps: 0 producer, 1 TMEM allocation + MMA issuer, 2-3 idle, 4-11 epilogue;
+// setmaxnreg moves registers from warpgroup 0 to the epilogue warpgroups.
 // With few tiles (small M or N) the K range is split: each (tile, split) item
 // writes a partial into a workspace plane, and a fix-up kernel adds the
 // planes in split order (fp32 for E4M3, exact int32 for F16 codes) and
@@ -63,13 +64,23 @@ struct DirectCfg {
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_WARP0 = 4;
   static constexpr int THREADS = 384;
+  // registers per thread after setmaxnreg: warpgroup 0 (producer, MMA
+  // issuer, two idle warps) hands registers to the two epilogue warpgroups
+  static constexpr int REG_LO = 136;
+  static constexpr int REG_HI = 176;
+  static_assert(128 * REG_LO + 256 * REG_HI <= THREADS * ((65536 / THREADS) & ~7),
+                "register split exceeds the launch allocation");
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_EPI = STAGES * STAGE_BYTES;          // 4 KB staging per epilogue warp
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 4096;
-  // full[S] empty[S] accfull[2] accempty[2] done
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  // full[S] empty[S] accfull[2] accempty[2] done sclfull sclfree
+  static constexpr int NUM_BARS = 2 * STAGES + 7;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  // the current tile's per-channel scales (fp32) and bias (bf16), staged by
+  // the epilogue warps: PAIR_N columns
+  static constexpr int OFF_SCL = (OFF_MISC + 16 + 15) / 16 * 16;
+  static constexpr int OFF_SCL_BIAS = OFF_SCL + PAIR_N * 4;
+  static constexpr int SMEM_BYTES = OFF_SCL_BIAS + PAIR_N * 2 + 1024;
   static constexpr int TMEM_COLS = 2 * PAIR_N;
   static constexpr uint32_t TX = 2 * STAGE_BYTES;               // both CTAs' loads of a stage
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -99,6 +110,8 @@ struct DirectBars {
   __device__ uint32_t accfull(int b) const { return base + 8u * (2 * STAGES + b); }
   __device__ uint32_t accempty(int b) const { return base + 8u * (2 * STAGES + 2 + b); }
   __device__ uint32_t done() const { return base + 8u * (2 * STAGES + 4); }
+  __device__ uint32_t sclfull() const { return base + 8u * (2 * STAGES + 5); }
+  __device__ uint32_t sclfree() const { return base + 8u * (2 * STAGES + 6); }
 };
 
 template <int KIND>
@@ -133,8 +146,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DirectCfg<KIND>::THR
       mbar_init(bars.accempty(b), 2 * Cfg::EPI_WARPS);  // CTA 0: both CTAs' epilogue warps
     }
     mbar_init(bars.done(), 1);
+    mbar_init(bars.sclfull(), Cfg::EPI_WARPS);
+    mbar_init(bars.sclfree(), Cfg::EPI_WARPS);
     *abort_flag = 0;
     fence_mbarrier_init();
+  }
+  if (warp >= 2 && lane == 0) {
+    // The first read of a launch parameter misses the constant cache (about
+    // 1 us on GB300) and would sit on every role's path to its first tile;
+    // touch the fields the roles decode first while warps 0 and 1 set up the
+    // barriers and the tensor memory.
+    const int t = p.num_tiles ^ p.splits ^ p.total_kb ^ p.kb_per_split ^ p.num_m_blk ^
+                  p.num_n_blk ^ p.n_fastest ^ p.chunk_stages ^ p.out_mode ^ p.M ^ p.N ^
+                  static_cast<int>(reinterpret_cast<uintptr_t>(p.s_a)) ^
+                  static_cast<int>(reinterpret_cast<uintptr_t>(p.s_w));
+    asm volatile("" ::"r"(t));
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -153,6 +179,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DirectCfg<KIND>::THR
   pdl_wait();  // operands and outputs may belong to the previous kernel
 
   if (warp == 0) {
+    regs_dec<Cfg::REG_LO>();
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint32_t full0 = mapa_shared(bars.full(0), 0);
@@ -174,6 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DirectCfg<KIND>::THR
       }
     }
   } else if (warp == 1) {
+    regs_dec<Cfg::REG_LO>();
     // ------------------------------------------------------------ MMA issuer (CTA 0)
     if (lane == 0 && rank == 0) {
       constexpr uint32_t idesc = KIND == kDirectF16 ? idesc_f16_f32(Cfg::PAIR_M, Cfg::PAIR_N)
@@ -214,18 +242,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DirectCfg<KIND>::THR
       mbar_wait_bounded(bars.done(), 0u, 100000000ull);
     }
   } else if (warp >= Cfg::EPI_WARP0) {
+    regs_inc<Cfg::REG_HI>();
     // ------------------------------------------------------------ epilogue
     const int ew = warp - Cfg::EPI_WARP0;
     const int quarter = warp & 3;
     const int cg = ew >> 2;
     const uint32_t stage_y = sbase + Cfg::OFF_EPI + static_cast<uint32_t>(ew) * 4096u;
     const uint32_t accempty0 = rank == 0 ? bars.accempty(0) : mapa_shared(bars.accempty(0), 0);
-    Ring racc;
+    const bool bf16_out = p.out_mode == kOutBf16;
+    const uint32_t scl_w = sbase + Cfg::OFF_SCL;
+    const uint32_t scl_b = sbase + Cfg::OFF_SCL_BIAS;
+    Ring racc, rscl;
     bool ok = true;
     const int items = p.num_tiles * p.splits;
     for (int item = pair; ok && item < items; item += npairs) {
       const DirectItem t = direct_item(p, item);
       const int chunk = KIND == kDirectF16 ? p.chunk_stages : t.kb1 - t.kb0;
+      const int m_base = t.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM + quarter * 32;
+      float sa = 0.0f;
+      if (bf16_out) {
+        // Stage this tile's per-channel scales and bias (once the previous
+        // tile's readers are done with them) and load this lane's per-token
+        // scale while the tile's MMAs run.
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.sclfree(), rscl.ph ^ 1u, abort_flag));
+        if (!ok) break;
+        stage_channel_scales(p, scl_w, scl_b, t.nb * Cfg::PAIR_N, ew, lane);
+        if (m_base + lane < p.M) sa = p.s_a[m_base + lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.sclfull());
+      }
       // F16: exact int32 sum of the chunks; E4M3: the fp32 bit patterns
       int acc[128];
 #pragma unroll
@@ -260,27 +305,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DirectCfg<KIND>::THR
         racc.advance(2);
       }
       if (!ok) break;
-      const int m_base = t.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM + quarter * 32;
       const int n_base = t.nb * Cfg::PAIR_N + cg * 128;
       const int z = p.out_mode == kOutPartial ? t.ks : 0;
-      if constexpr (KIND == kDirectF16) {
-        // int32 results, or a K split's exact int32 partial (plane ks)
-        if (p.out_mode == kOutBf16) store_warp_tile_bf16<128, int>(p, &tmY, stage_y, lane, m_base, n_base, acc);
-        else store_warp_tile_s32<128>(&tmY, stage_y, lane, m_base, n_base, acc, z);
+      if (bf16_out) {
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.sclfull(), rscl.ph, abort_flag));
+        if (!ok) break;
+        // F16 codes: exact int32 sums; E4M3: fp32 accumulator bit patterns
+        store_warp_tile_bf16_staged<128, KIND != kDirectF16>(&tmY, stage_y, lane, m_base, n_base,
+                                                             acc, sa, scl_w + 4u * (cg * 128),
+                                                             scl_b + 2u * (cg * 128));
+        // this warp's reads of the staged scales are done
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.sclfree());
+        rscl.advance(1);
       } else {
-        if (p.out_mode == kOutBf16) {
-          float f[128];
-#pragma unroll
-          for (int i = 0; i < 128; ++i) f[i] = __int_as_float(acc[i]);
-          store_warp_tile_bf16<128, float>(p, &tmY, stage_y, lane, m_base, n_base, f);
-        } else {
-          // fp32 accumulators (checking path) or a K split's fp32 partial
-          store_warp_tile_s32<128>(&tmY, stage_y, lane, m_base, n_base, acc, z);
-        }
+        // int32 (F16 codes) or fp32 (E4M3) accumulators for the checking
+        // paths, or a K split's partial in plane ks
+        store_warp_tile_s32<128>(&tmY, stage_y, lane, m_base, n_base, acc, z);
       }
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
+  } else {
+    regs_dec<Cfg::REG_LO>();   // warps 2-3: no role
   }
 
   __syncwarp();
