@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(256) zero_ws_kernel(uint4* __restrict__ ws, in
 
 constexpr int kSkinnyRows = 64;
 constexpr int kSkinnyK = 512;
+constexpr int kCh = 4;   // independent accumulator chains per n8 group
 
 template <bool W16>
 struct SkinnyCfg {
@@ -146,7 +147,17 @@ __global__ void __launch_bounds__(128) gemm_skinny_kernel(const __grid_constant_
     if (!ok) break;
     phase[stage] ^= 1u;
     const uint32_t tile = sbase + stage * Cfg::TILE_BYTES;
-    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // kCh independent accumulator chains per n8 group (16-blocks kb with the
+    // same kb % kCh share one), so consecutive MMAs do not wait for each
+    // other's results; each chain's fp32 partial is an exact integer below
+    // 127^2 * 512 < 2^24, and so is their sum.
+    float d[2][kCh][4];
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+      for (int c = 0; c < kCh; ++c)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[grp][c][i] = 0.0f;
 #pragma unroll
     for (int kb = 0; kb < kSkinnyK / 16; ++kb) {
       uint32_t a0, a1, a2, a3;
@@ -170,7 +181,7 @@ __global__ void __launch_bounds__(128) gemm_skinny_kernel(const __grid_constant_
           asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(addr));
           s8x4_to_f16x4(wb, b0, b1);
         }
-        mma_m16n8k16_f16(d[grp], a0, a1, a2, a3, b0, b1);
+        mma_m16n8k16_f16(d[grp][kb % kCh], a0, a1, a2, a3, b0, b1);
       }
     }
     // every thread is done reading this stage: refill it two chunks ahead
@@ -179,7 +190,12 @@ __global__ void __launch_bounds__(128) gemm_skinny_kernel(const __grid_constant_
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[grp][i] += f32_exact_int_to_s32(__float_as_uint(d[grp][i]));
+      for (int i = 0; i < 4; ++i) {
+        float t = d[grp][0][i];
+#pragma unroll
+        for (int c = 1; c < kCh; ++c) t = __fadd_rn(t, d[grp][c][i]);   // exact (integers < 2^24)
+        acc[grp][i] += f32_exact_int_to_s32(__float_as_uint(t));
+      }
   }
 
   pdl_trigger();
