@@ -69,10 +69,11 @@ def _check_plan(p, M, N, K, route, m):
     elif p["kernel"] == "pair_stream_k":
         tiles = p["num_m"] * p["num_n"]
         arrive = -(-tiles * 16 // 1024) * 1024
-        assert p["ws_bytes"] == arrive + p["grid"] * 256 * 256 * 4
+        assert p["ws_bytes"] == arrive + p["grid"] // 2 * 256 * 256 * 4   # one slot per pair
     else:
         assert p["ws_bytes"] == (s * M * (-(-N // 4) * 4) * 4 if s > 1 else 0)
-    assert p["n_fastest"] == (1 if M > N else 0)
+    # M blocks fastest under stream-K; otherwise N blocks fastest when M > N
+    assert p["n_fastest"] == (0 if p["kernel"] == "pair_stream_k" else 1 if M > N else 0)
     assert (p["model_us"] > 0) == (p["kernel"] == "direct")
 
 
@@ -196,14 +197,23 @@ def test_direct_splits_minimise_the_cost_model():
 
 
 def test_stream_k_rule():
-    # QKV-like K = 3072: never; K = 12288 with M-fastest tiles and a ragged
-    # last wave: stream-K; the same shape with M > N (N-fastest): split-K or whole tiles
-    assert i8.plan_query(2304, 3072, 3072, "int8", **GB300)["kernel"] == "pair"
+    # at least half a wave of tiles and a whole-tile wave efficiency below
+    # 0.93, at any K: stream-K, M blocks fastest even where M > N
+    for M, N, K in ((2304, 3072, 3072), (2304, 3072, 12288), (3328, 3072, 12288),
+                    (256, 12288, 3072), (1024, 3072, 3072), (8704, 3072, 12288)):
+        p = i8.plan_query(M, N, K, "int8", **GB300)
+        assert (p["kernel"], p["n_fastest"], p["splits"]) == ("pair_stream_k", 0, 1), (M, N, K)
     p = i8.plan_query(2304, 3072, 12288, "int8", **GB300)
-    assert p["kernel"] == "pair_stream_k" and p["grid"] == 2 * GB300["pairs"]
-    assert i8.plan_query(3328, 3072, 12288, "int8", **GB300)["kernel"] == "pair"
-    # a whole number of waves: no stream-K
+    assert p["grid"] == 2 * GB300["pairs"]
+    # high wave efficiency (QKV 2560 x 9216: 360 tiles on 76 pairs, 0.95),
+    # fewer than half a wave of tiles (split-K instead), a whole number of
+    # waves: no stream-K
+    assert i8.plan_query(2560, 9216, 3072, "int8", **GB300)["kernel"] == "pair"
     assert i8.plan_query(74 * 256, 256, 12288, "int8", **GB300)["kernel"] == "pair"
+    assert i8.plan_query(2 * GB300["pairs"] * 256, 256, 3072, "int8", **GB300)["kernel"] == "pair"
+    for M, N in ((256, 3072), (256, 9216)):
+        p = i8.plan_query(M, N, 3072, "int8", **GB300)
+        assert p["kernel"] == "pair" and p["splits"] > 1, (M, N)
     # the no-alloc entry's 16 MiB cannot hold the partial slots: falls back
     capped = i8.plan_query(2304, 3072, 12288, "int8", ws_cap=16 << 20, **GB300)
     assert capped["kernel"] == "pair"
@@ -239,7 +249,7 @@ def test_options_change_the_plan():
     i8.set_option("cta_pair", 1)
     assert i8.plan_query(4096, 3072, 3072, "int8", **GB300)["kernel"] == "tile"
     i8.set_option("cta_pair", 2)
-    assert i8.plan_query(4096, 3072, 3072, "w16", **GB300)["kernel"] == "pair"
+    assert i8.plan_query(4096, 9216, 3072, "w16", **GB300)["kernel"] == "pair"
     i8.set_option("cta_pair", 0)
     i8.set_option("tile_n", 128)
     assert i8.plan_query(4096, 3072, 3072, "w16", **GB300)["tile_n"] == 128
@@ -255,7 +265,7 @@ def test_bench_workloads():
     qkv = i8.plan_query(8704, 9216, 3072, "int8", **GB300)
     assert (qkv["kernel"], qkv["splits"], qkv["n_fastest"], qkv["ws_bytes"]) == ("pair", 1, 0, 0)
     down = i8.plan_query(8704, 3072, 12288, "int8", **GB300)
-    assert (down["kernel"], down["splits"], down["n_fastest"]) == ("pair", 1, 1)
+    assert (down["kernel"], down["splits"], down["n_fastest"]) == ("pair_stream_k", 1, 0)
     one = i8.plan_query(1, 9216, 3072, "int8", **GB300)
     assert (one["kernel"], one["splits"], one["grid"]) == ("skinny", 2, 288)
 

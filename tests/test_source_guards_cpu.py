@@ -126,13 +126,14 @@ def test_tma_inner_coordinates_are_16_byte_multiples():
     below, each a whole number of 128-byte rows: K-block starts (128 int8 /
     E4M3 codes, 64 fp16 codes, 512-code chunks of 128- or 64-element boxes)
     and output column starts (64 bf16 or 32 int32 columns from a multiple of
-    128)."""
+    128), and the stream-K partial reloads (32 int32 columns from a multiple
+    of 128)."""
     allowed_x = {"kb * Cfg::BK8", "k16", "kb * Cfg::BK", "kc * kSkinnyK + b * Cfg::BOX_K",
-                 "nb", "n0 + g * 32", "n0 + g * 64"}
+                 "nb", "n0 + g * 32", "n0 + g * 64", "n_loc + 32 * g"}
     calls = 0
     for name in GEMM_SOURCES:
         src = _code(name)
-        for m in re.finditer(r"\b(tma_load_2d(?:_pair)?|tma_store_3d)\(([^;]*)\);", src):
+        for m in re.finditer(r"\b(tma_load_[23]d(?:_pair)?|tma_store_3d)\(([^;]*)\);", src):
             args = [a.strip() for a in m.group(2).split(",")]
             x = args[3] if m.group(1).startswith("tma_load") else args[2]
             assert x in allowed_x, (name, m.group(0))
@@ -152,10 +153,9 @@ def test_tma_inner_coordinates_are_16_byte_multiples():
     # output column starts passed to the store helpers: multiples of 128
     for src, expr in ((gemm, "tc.nb * Cfg::BN + cg * 128"),
                       (direct, "const int n_base = t.nb * Cfg::PAIR_N + cg * 128;"),
-                      (pair, "const int n_loc = cg * 128;"),
-                      (pair, "const int n_sub = n_loc + 64 * h;")):
+                      (pair, "const int n_loc = cg * 128;")):
         assert expr in src, expr
     # the staged-scale store starts its 64-column groups at the callers' n0:
-    # a tile column base plus n_loc or n_sub, multiples of 64 bf16 columns
-    assert "tc.nb * Cfg::PAIR_N + n_sub, sum, sa," in pair
+    # a tile column base plus n_loc, a multiple of 128 bf16 columns
     assert "tc.nb * Cfg::PAIR_N + n_loc, acc, sa," in pair
+    assert "n_sub" not in pair

@@ -1,20 +1,26 @@
 """The stream-K schedule of the CTA-pair GEMM, modelled on the CPU.
 
 Stream-K splits the (tile, K-block) units of a GEMM evenly over the P CTA
-pairs of a persistent launch; tiles cut between pairs are finished by the
-last pair to arrive, from every participant's exact int32 partial.  The
-schedule is integer arithmetic only, so it can be checked here for many
-shapes.  The model restates the kernel's formulas:
+pairs of a persistent launch.  A tile cut between pairs is finished by the
+pair holding its first K blocks, from the accumulator it still holds plus the
+exact int32 partials the other participants published.  The schedule is
+integer arithmetic only, so it can be checked here for many shapes.  The
+model restates the kernel's formulas:
   units U = tiles * kb (tile-major), pair q owns [first(q), first(q + 1))
   with first(q) = U * q // P; its item `it` is tile first(q) // kb + it,
   cut to the pair's range; holder(u) = ((u + 1) * P - 1) // U;
   a split tile's participants are holder(first unit) .. holder(last unit);
-  a partial piece is stored in slot 2q + (it == 0 ? 0 : 1) and read back from
-  slot 2q + (first(q) // kb == tile ? 0 : 1); the fix-up barriers of a pair
-  are in phase (it > 0 and first(q) % kb != 0).
+  the piece starting at K block 0 finishes the tile, every other piece
+  publishes its partial in its pair's slot q, which the finisher reads back;
+  the finisher waits for the other participants' q1 - q0 arrivals; every
+  fix-up barrier is used in phase 0.
 and checks what correctness needs: every unit computed once, every tile's K
 blocks covered once, at most two split pieces per pair (its first and its
-last), consistent slots, arrival counts and barrier phases.  The host plans
+last), the finisher's piece the last item of its pair and every published
+piece the first item of its pair (so a pair publishes at most once, which
+one slot per pair needs, and finishes at most once, which phase 0 needs),
+and a finisher never
+waiting on a pair below it (the waits cannot form a cycle).  The host plans
 P = min(resident pairs, max(1, U // 4)), so every pair owns at least one unit
 (at least four whenever U >= 4).
 """
@@ -71,10 +77,13 @@ def test_stream_k_schedule(tiles):
                 # split pieces only at a pair's first and last item
                 assert all(it in (0, len(items) - 1) for it in partial_its)
                 assert len(partial_its) <= 2
-                for idx, it in enumerate(partial_its):
-                    # the fix-up barriers' phase: how many split pieces came before
-                    phase = 1 if (it > 0 and first(U, q, P) % kb != 0) else 0
-                    assert phase == idx % 2, (tiles, kb, P, q)
+                # a pair publishes at most one piece (its first) and finishes
+                # at most one (its last): each fix-up barrier is used once, in
+                # phase 0
+                publish = [it for it, _, k0, k1 in items if k0 > 0]
+                finish = [it for it, _, k0, k1 in items if k0 == 0 and k1 < kb]
+                assert publish in ([], [0]), (tiles, kb, P, q)
+                assert finish in ([], [len(items) - 1]), (tiles, kb, P, q)
                 for it, tile, k0, k1 in items:
                     assert 0 <= k0 < k1 <= kb
                     pieces.setdefault(tile, []).append((q, it, k0, k1))
@@ -92,14 +101,14 @@ def test_stream_k_schedule(tiles):
                 q0 = holder(U, tile * kb, P)
                 q1 = holder(U, (tile + 1) * kb - 1, P)
                 assert [q for q, *_ in ps] == list(range(q0, q1 + 1))
-                # each participant's partial is read from the slot it stored
-                for q, it, _, _ in ps:
-                    store = 2 * q + (0 if it == 0 else 1)
-                    read = 2 * q + (0 if first(U, q, P) // kb == tile else 1)
-                    assert store == read
-            # no slot is written twice
-            used = [2 * q + (0 if it == 0 else 1)
-                    for ps in pieces.values() if len(ps) > 1 for q, it, _, _ in ps]
+                # the finisher is the first participant; the others publish,
+                # so it waits for q1 - q0 arrivals from pairs above it
+                fin = [q for q, it, k0, _ in ps if k0 == 0]
+                assert fin == [q0]
+                pubs = [(q, it) for q, it, k0, _ in ps if k0 > 0]
+                assert len(pubs) == q1 - q0 and all(q > q0 for q, _ in pubs)
+            # no slot (one per pair) is written twice
+            used = [q for ps in pieces.values() if len(ps) > 1 for q, it, k0, _ in ps if k0 > 0]
             assert len(used) == len(set(used))
 
 
@@ -119,10 +128,13 @@ def test_model_restates_the_kernel_source():
         "if (u0 >= u1 || t0 >= u1) return false;",
         "t.kb0 = static_cast<int>((u0 > t0 ? u0 : t0) - t0);",
         "t.kb1 = static_cast<int>((u1 < t0 + kb ? u1 : t0 + kb) - t0);",
-        "2 * pair + (it == 0 ? 0 : 1)",
-        "2 * q + (sk_first(p, q, npairs) / static_cast<uint32_t>(p.total_kb) == "
-        "static_cast<uint32_t>(tc.tile) ? 0 : 1);",
-        "(it > 0 && sk_first(p, pair, npairs) % static_cast<uint32_t>(p.total_kb) != 0) ? 1u : 0u;",
-        "last_pair() - first_pair() + 1",
+        "store_warp_tile_s32<128>(tmP, stage, lane, m_loc, n_loc, acc, pair);",
+        "tma_load_3d(buf + 4096u * g, tmP, bars.skload(ew), n_loc + 32 * g, m_loc, q);",
+        "if (tc.kb0 != 0) {",
+        "sk_arrive(word, p.sk_epoch, q1 - q0 + 1, aok);",
+        "gmem_wait_eq(word, (p.sk_epoch << 16) | static_cast<unsigned long long>(q1 - q0),",
+        "mbar_wait(bars.skstored(), 0u, abort_flag)",
+        "mbar_wait(bars.skdecided(), 0u, abort_flag)",
+        "if (q == pair) continue;",
     ]:
         assert " ".join(text.split()) in src, text

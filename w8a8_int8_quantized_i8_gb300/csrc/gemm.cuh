@@ -62,7 +62,7 @@ struct GemmParams {
   // arrive at it.
   int stream_k;                        // 0: tile-strided schedule
   unsigned long long* sk_arrive;       // [num_tiles][2] arrival words: epoch << 16 | count
-  const int32_t* sk_part;              // [2 P][256][256] int32 partial slots
+  const int32_t* sk_part;              // [P][256][256] int32 partial slots
   unsigned long long sk_epoch;         // this launch's tag, in [1, 2^48)
   int n_fastest;                       // tile order: 0 M blocks fastest, 1 N blocks fastest
 };

@@ -89,7 +89,8 @@ struct PairCfg {
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 4096;
   // full8[S8] empty8[S8] full16[S16] tma16[S16] empty16[S16] pfull16[S16]
   // accfull[2] accempty[2] paccempty[2] done skstored skdecided sclfull sclfree
-  static constexpr int NUM_BARS = 2 * S8 + 4 * S16 + 11;
+  // skload[EPI_WARPS]
+  static constexpr int NUM_BARS = 2 * S8 + 4 * S16 + 11 + EPI_WARPS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   // the current tile's per-channel scales (fp32) and bias (bf16), staged by
   // the epilogue warps: PAIR_N columns
@@ -97,6 +98,9 @@ struct PairCfg {
   static constexpr int OFF_SCL_BIAS = OFF_SCL + PAIR_N * 4;
   static constexpr int SMEM_BYTES = OFF_SCL_BIAS + PAIR_N * 2 + 1024;
   static constexpr int TMEM_COLS = 2 * PAIR_N;
+  // a stream-K finisher loads the other pairs' partials into the pipeline
+  // buffers, 16 KB per epilogue warp
+  static_assert(OFF_EPI >= EPI_WARPS * 16384, "stream-K partial buffers overlap the staging");
   static constexpr uint32_t TX8 = STAGE8;
   static constexpr uint32_t TX16 = (CONV_A ? 0 : A16_BYTES) + (CONV_B ? 0 : B16_BYTES);
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -125,6 +129,8 @@ struct PairBars {
   // read by every epilogue warp
   __device__ uint32_t sclfull() const { return base + 8u * (2 * S8 + 4 * S16 + 9); }
   __device__ uint32_t sclfree() const { return base + 8u * (2 * S8 + 4 * S16 + 10); }
+  // stream-K: epilogue warp w's TMA loads of the other pairs' partials
+  __device__ uint32_t skload(int w) const { return base + 8u * (2 * S8 + 4 * S16 + 11 + w); }
 };
 
 struct PairTile {
@@ -188,8 +194,8 @@ __device__ __forceinline__ bool pair_item(const GemmParams& p, int pair, int npa
 }
 
 // Counts one arrival at a split tile's word and returns true for the n-th
-// (last) arrival of this launch.  A word left by an earlier launch carries
-// another epoch and counts as zero, so the array never needs clearing.  Each
+// arrival of this launch.  A word left by an earlier launch carries another
+// epoch and counts as zero, so the array never needs clearing.  Each
 // failed exchange means another participant arrived, so the loop ends within
 // n rounds; the bound only guards against a corrupted word.
 __device__ __forceinline__ bool sk_arrive(unsigned long long* word, unsigned long long epoch,
@@ -270,96 +276,100 @@ __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CU
     }
     const uint32_t stage = sbase + Cfg::OFF_EPI + static_cast<uint32_t>(ew) * 4096u;
     if (tc.partial) {
-      // Stream-K fix-up.  Publish this pair's int32 partial in its slot,
-      // count the arrival, and let the last of the tile's pairs add the
-      // others' partials and write the tile.  Nobody waits for another pair.
-      store_warp_tile_s32<128>(tmP, stage, lane, m_loc, n_loc, acc, 2 * pair + (it == 0 ? 0 : 1));
-      if (lane == 0) {
-        bulk_wait_all();             // the partial is in global memory
-        fence_proxy_async_global();
-        mbar_arrive(bars.skstored());
-      }
-      __syncwarp();
-      // A pair has at most two split items, its first and its last: the
-      // fix-up barriers' phase is 1 only for a last item after a split first.
-      const uint32_t sk_phase =
-          (it > 0 && sk_first(p, pair, npairs) % static_cast<uint32_t>(p.total_kb) != 0) ? 1u : 0u;
-      // the tile's pairs: [holder of its first unit, holder of its last unit]
-      auto first_pair = [&] {
-        return sk_holder(p, static_cast<uint32_t>(tc.tile) * static_cast<uint32_t>(p.total_kb),
-                         npairs);
-      };
-      auto last_pair = [&] {
-        return sk_holder(p, static_cast<uint32_t>(tc.tile + 1) * static_cast<uint32_t>(p.total_kb) - 1,
-                         npairs);
-      };
-      if (ew == 0 && lane == 0) {
-        // (a timed-out wait has raised the abort flag and the status word)
-        bool last = false;
-        if (mbar_wait(bars.skstored(), sk_phase, abort_flag)) {
-          bool aok = true;
-          __threadfence();
-          unsigned long long* word = p.sk_arrive + 2 * tc.tile + rank;
-          last = sk_arrive(word, p.sk_epoch, last_pair() - first_pair() + 1, aok);
-          // every participant has arrived: clear the word, so that a replay
-          // of this launch (same epoch, e.g. from a CUDA graph) starts at zero
-          if (last) atomicExch(word, 0ull);
-          __threadfence();
-          if (!aok) {
-            *abort_flag = 1;
-            atomicOr(&g_status, 1u << 5);  // I8_ERR_CUDA: corrupted arrival word
-          }
+      // Stream-K fix-up.  The pair holding the tile's first K blocks (always
+      // the last item of its range) finishes the tile; every other piece is
+      // the first item of its pair's range, done early.  Those pairs publish
+      // their int32 partials, each in its pair's slot (a pair publishes at
+      // most once), and count themselves in the tile's arrival word.  The finisher waits until the others have all
+      // arrived, loads their partials by TMA into its own pipeline buffers
+      // (idle once its last item's MMAs are done), adds them to the
+      // accumulator it still holds and writes the tile.
+      const int q0 = sk_holder(p, static_cast<uint32_t>(tc.tile) * static_cast<uint32_t>(p.total_kb),
+                               npairs);
+      const int q1 = sk_holder(p, static_cast<uint32_t>(tc.tile + 1) * static_cast<uint32_t>(p.total_kb) - 1,
+                               npairs);
+      unsigned long long* word = p.sk_arrive + 2 * tc.tile + rank;
+      if (tc.kb0 != 0) {
+        store_warp_tile_s32<128>(tmP, stage, lane, m_loc, n_loc, acc, pair);
+        if (lane == 0) {
+          bulk_wait_all();             // the partial is in global memory
+          fence_proxy_async_global();
+          mbar_arrive(bars.skstored());
         }
-        *sk_flag = last ? 1 : 0;
-        mbar_arrive(bars.skdecided());     // always, so no epilogue warp waits in vain
-      }
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.skdecided(), sk_phase, abort_flag));
-      if (!ok) break;
-      if (*sk_flag != 0) {
-        // Last to arrive: rebuild the tile from all the pairs' slots (this
-        // pair's own included, so acc is no longer needed), 64 columns at a
-        // time, and write it.
-        __threadfence();
-        const int q0 = first_pair();
-        const int q1 = last_pair();
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          int sum[64];
-#pragma unroll
-          for (int i = 0; i < 64; ++i) sum[i] = 0;
-#pragma unroll 1
-          for (int q = q0; q <= q1; ++q) {
-            const int slot =
-                2 * q + (sk_first(p, q, npairs) / static_cast<uint32_t>(p.total_kb) ==
-                                 static_cast<uint32_t>(tc.tile) ? 0 : 1);
-            const int4* src = reinterpret_cast<const int4*>(
-                p.sk_part + (static_cast<int64_t>(slot) * 256 + m_loc + lane) * 256 + n_loc + 64 * h);
-            // 8 loads in flight at a time (the compiler barrier keeps the next
-            // group's loads behind this group's adds)
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-              int4 v[8];
-#pragma unroll
-              for (int c = 0; c < 8; ++c) v[c] = __ldcg(src + 8 * g + c);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                sum[32 * g + 4 * c] += v[c].x;
-                sum[32 * g + 4 * c + 1] += v[c].y;
-                sum[32 * g + 4 * c + 2] += v[c].z;
-                sum[32 * g + 4 * c + 3] += v[c].w;
-              }
-              asm volatile("" ::: "memory");
+        __syncwarp();
+        if (ew == 0 && lane == 0) {
+          // (a timed-out wait has raised the abort flag and the status word;
+          // a pair publishes at most one partial, so the phase is 0)
+          if (mbar_wait(bars.skstored(), 0u, abort_flag)) {
+            bool aok = true;
+            __threadfence();
+            sk_arrive(word, p.sk_epoch, q1 - q0 + 1, aok);
+            if (!aok) {
+              *abort_flag = 1;
+              atomicOr(&g_status, 1u << 5);  // I8_ERR_CUDA: corrupted arrival word
             }
           }
-          const int n_sub = n_loc + 64 * h;
-          if (bf16_out)
-            store_warp_tile_bf16_staged<64>(tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
-                                            tc.nb * Cfg::PAIR_N + n_sub, sum, sa,
-                                            scl_w + 4u * n_sub, scl_b + 2u * n_sub);
-          else
-            store_warp_tile<64>(p, tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
-                                tc.nb * Cfg::PAIR_N + n_sub, sum, tc.ks);
         }
+      } else {
+        if (ew == 0 && lane == 0) {
+          // every other piece's partial is published (bounded wait); then
+          // clear the word, so that a replay of this launch (same epoch, e.g.
+          // from a CUDA graph) starts at zero
+          const bool fok = gmem_wait_eq(word, (p.sk_epoch << 16) | static_cast<unsigned long long>(q1 - q0),
+                                        abort_flag);
+          if (fok) {
+            atomicExch(word, 0ull);
+            __threadfence();
+            fence_proxy_async_global();
+          }
+          *sk_flag = fok ? 1 : 0;
+          mbar_arrive(bars.skdecided());   // always, so no epilogue warp waits in vain
+        }
+        // a pair finishes at most one tile, its last item: the phase is 0
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.skdecided(), 0u, abort_flag)) && *sk_flag != 0;
+        if (!ok) break;
+        // This warp's 32 rows x 128 columns of each other pair's slot: four
+        // 32 x 32 int32 boxes (16 KB, 128-byte swizzle, the layout the
+        // partial was stored with) into this warp's 16 KB of the buffers.
+        const uint32_t buf = sbase + Cfg::OFF_S8 + static_cast<uint32_t>(ew) * 16384u;
+        uint32_t lph = 0;
+#pragma unroll 1
+        for (int q = q0; ok && q <= q1; ++q) {
+          if (q == pair) continue;
+          if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bars.skload(ew), 16384u);
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              tma_load_3d(buf + 4096u * g, tmP, bars.skload(ew), n_loc + 32 * g, m_loc, q);
+          }
+          __syncwarp();
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.skload(ew), lph, abort_flag));
+          lph ^= 1u;
+          if (!ok) break;
+          const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
+          const uint32_t x = static_cast<uint32_t>(lane & 7);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 v = lds128(row + 4096u * g + ((static_cast<uint32_t>(c) ^ x) << 4));
+              acc[32 * g + 4 * c] += static_cast<int>(v.x);
+              acc[32 * g + 4 * c + 1] += static_cast<int>(v.y);
+              acc[32 * g + 4 * c + 2] += static_cast<int>(v.z);
+              acc[32 * g + 4 * c + 3] += static_cast<int>(v.w);
+            }
+          }
+          __syncwarp();   // every lane has read the boxes before the next load overwrites them
+        }
+        if (!ok) break;
+        if (bf16_out)
+          store_warp_tile_bf16_staged<128>(tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
+                                           tc.nb * Cfg::PAIR_N + n_loc, acc, sa, scl_w + 4u * n_loc,
+                                           scl_b + 2u * n_loc);
+        else
+          store_warp_tile<128>(p, tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
+                               tc.nb * Cfg::PAIR_N + n_loc, acc, tc.ks);
       }
     } else if (bf16_out) {
       store_warp_tile_bf16_staged<128>(tmY, stage, lane, tc.mp * Cfg::PAIR_M + m_loc,
@@ -437,6 +447,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     mbar_init(bars.skdecided(), 1);
     mbar_init(bars.sclfull(), Cfg::EPI_WARPS);
     mbar_init(bars.sclfree(), Cfg::EPI_WARPS);
+    for (int w = 0; w < Cfg::EPI_WARPS; ++w) mbar_init(bars.skload(w), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }

@@ -383,6 +383,7 @@ struct Plan {
   int num_tiles = 1;
   int grid = 1;
   int chunk_stages = 8;
+  int n_fastest = 0;       // tile order: 1 N blocks fastest, 0 M blocks
   int64_t ws_ld = 0;       // row stride of the split partials (elements)
   size_t ws_bytes = 0;
 };
@@ -427,10 +428,12 @@ int tile_order_n_fastest(int64_t M, int64_t N) {
 //     would leave SMs idle);
 //   * stream-K on CTA pairs by the rule below, else split-K (exact int32
 //     partials + a reduction) when the tiles cannot fill every worker;
-//   * the tile order from tile_order_n_fastest, applied by the caller.
+//   * the tile order from tile_order_n_fastest (M blocks fastest under
+//     stream-K unless the raster option sets it), applied by the caller.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
                bool b16 = false, size_t ws_cap = SIZE_MAX, int skinny_slots = 0) {
   Plan p;
+  p.n_fastest = tile_order_n_fastest(M, N);
   if (pair_clusters <= 0) pair_clusters = sms / 2;
   if (skinny_slots <= 0) skinny_slots = 2 * sms;
   p.total_kb = static_cast<int>((K + 127) / 128);
@@ -476,29 +479,33 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
     if (g_opt.max_ctas > 0) slots = std::max(1, std::min(slots, g_opt.max_ctas / 2));
     // Stream-K: every pair gets an equal share of the (tile, K-block)
     // units, at least 4 K-blocks each.  Workspace: one arrival word per
-    // (tile, CTA) and two 256 x 256 int32 partial slots per pair.  Each tile
-    // cut between pairs costs its pairs a fix-up of roughly 5-10 us (int32
-    // partial out, partials back in), so the table takes it only where a
-    // tile carries far more MMA time than that and whole tiles leave many
-    // pairs idle: K >= 8192, at least half a wave of tiles, whole-tile wave
-    // efficiency below 0.93, and only in the M-blocks-fastest tile order.
-    // Measured (GEMM, GB300): +4 to +7 % at K = 12288 with M-fastest tiles;
-    // -3 to -76 % at K = 3072; with N blocks fastest (M > N) the whole-tile
-    // schedule is faster (MLP down-projection 482 -> 461 us with the order
-    // change, stream-K under N-fastest 525 us).
+    // (tile, CTA) and one 256 x 256 int32 partial slot per pair.  A pair's
+    // schedule then holds one item more than its share of whole tiles, and
+    // the tile it finishes last waits for one or two partials to load: about
+    // 6-9 us per launch against whole tiles at K = 3072.  The table takes it
+    // where whole tiles leave more than that idle: at least half a wave of
+    // tiles and a whole-tile wave efficiency below 0.93.  Stream-K plans take
+    // the M-blocks-fastest tile order, which measured as fast or faster
+    // under stream-K at every shape with M > N.
+    // Measured (GEMM, GB300, 30 DiT sweep shapes): every shape the rule
+    // takes gains 1-12 % (e.g. 1024 x 3072 x 3072 32.8 -> 30.3 us,
+    // 4096 x 3072 x 12288 230 -> 212 us, 1024 x 3072 x 12288 103 -> 66 us)
+    // but one, 16384 x 3072 x 12288 (820.0 -> 821.6 us); at a wave
+    // efficiency of 0.95 and above stream-K loses up to 9 %, and with 12 or
+    // 36 tiles split-K is faster.
     const int64_t units = tiles * p.total_kb;
     const int64_t waves = (tiles + slots - 1) / slots;
     const double wave_eff = static_cast<double>(tiles) / static_cast<double>(waves * slots);
-    const bool sk_table = p.total_kb >= 64 && 2 * tiles >= slots && wave_eff < 0.93 &&
-                          !tile_order_n_fastest(M, N);
+    const bool sk_table = 2 * tiles >= slots && wave_eff < 0.93;
     if ((g_opt.stream_k == 2 || (g_opt.stream_k == 1 && sk_table)) && g_opt.force_splits == 0 &&
         tiles % slots != 0 &&
         units * slots < (int64_t(1) << 31)) {   // the kernel's unit arithmetic is 32-bit
       const int pairs = static_cast<int>(std::min<int64_t>(slots, std::max<int64_t>(1, units / 4)));
       const size_t arrive = (static_cast<size_t>(tiles) * 16 + 1023) / 1024 * 1024;
-      const size_t part = static_cast<size_t>(2 * pairs) * 256 * 256 * sizeof(int32_t);
+      const size_t part = static_cast<size_t>(pairs) * 256 * 256 * sizeof(int32_t);
       if (arrive + part <= ws_cap) {
         p.stream_k = true;
+        p.n_fastest = g_opt.raster != 0 ? (g_opt.raster == 2 ? 1 : 0) : 0;
         p.num_tiles = static_cast<int>(tiles);
         p.kb_per_split = p.total_kb;
         p.grid = 2 * pairs;
@@ -766,7 +773,7 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   gp.K = static_cast<int>(K);
   gp.num_m_blk = pl.num_m;
   gp.num_n_blk = pl.num_n;
-  gp.n_fastest = tile_order_n_fastest(M, N);
+  gp.n_fastest = pl.n_fastest;
   gp.splits = pl.splits;
   gp.kb_per_split = pl.kb_per_split;
   gp.total_kb = pl.total_kb;
@@ -791,14 +798,14 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
                   static_cast<uint64_t>(M), static_cast<uint64_t>(gp.ldo),
                   static_cast<uint64_t>(pl.splits)))
     return I8_ERR_CUDA;
-  // Stream-K partial slots: {256 columns, 256 rows, 2 per pair} int32.
+  // Stream-K partial slots: {256 columns, 256 rows, 1 per pair} int32.
   CUtensorMap mp = my;
   if (pl.stream_k) {
     gp.stream_k = 1;
     gp.sk_arrive = static_cast<unsigned long long*>(ws);
     gp.sk_part = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(ws) + pl.sk_arrive_bytes);
     gp.sk_epoch = next_sk_epoch();
-    if (!encode_out(&mp, false, gp.sk_part, 256, 256, 256, static_cast<uint64_t>(pl.grid)))
+    if (!encode_out(&mp, false, gp.sk_part, 256, 256, 256, static_cast<uint64_t>(pl.grid / 2)))
       return I8_ERR_CUDA;
   }
   i8_status e;
@@ -1380,6 +1387,7 @@ i8_status i8_plan_query(int64_t M, int64_t N, int64_t K, i8_route route, int sms
     r.splits = pl.splits;
     r.kb_per_split = pl.kb_per_split;
     r.ws_bytes = static_cast<int64_t>(pl.ws_bytes);
+    r.n_fastest = pl.n_fastest;
     if (pl.skinny) {
       r.kernel = I8_KERNEL_SKINNY;
       r.tile_m = static_cast<int>(M);

@@ -107,6 +107,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   return true;
 }
 
+// Bounded wait for a 64-bit word in global memory to equal `want` (read with
+// acquire semantics at GPU scope, so what the writer published before its
+// release is visible afterwards).  Returns false (and raises the CTA abort
+// flag and the device status word) if the time limit passes or another role
+// has already aborted.
+__device__ __forceinline__ bool gmem_wait_eq(const unsigned long long* word, unsigned long long want,
+                                             volatile int* abort_flag,
+                                             unsigned long long limit_ns = kWaitLimitNs) {
+  const unsigned long long t0 = globaltimer_ns();
+#pragma unroll 1
+  while (true) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(word) : "memory");
+    if (v == want) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicOr(&g_status, 1u << 6);  // I8_ERR_DEVICE_TIMEOUT
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(desc)) : "memory");
@@ -133,6 +157,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* desc,
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
       ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// 3-D tiled bulk tensor load into this CTA's shared memory (completion as
+// transaction bytes on `bar`).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* desc, uint32_t bar, int c0,
+                                            int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
 
