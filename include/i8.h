@@ -276,9 +276,8 @@ i8_status i8_gelu_quant_act_pertoken(const void* x_bf16, int64_t M, int64_t K,
  *   stream capture.  The call itself allocates nothing.
  *   All calls share the one array and it keeps the last call's contents.
  *   Split-K partials are written in full before they are read; the
- *   few-token kernel's accumulator and counters, the part that must start
- *   at zero, are cleared by the call on its stream; stream-K arrival words
- *   carry a per-launch tag, so old words count as zero.  Calls whose
+ *   few-token kernel needs no scratch; stream-K arrival words carry a
+ *   per-launch tag, so old words count as zero.  Calls whose
  *   kernels overlap on the GPU -- on different streams, or from different
  *   host threads -- race on the array; serialize them.                      */
 i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a,
@@ -312,7 +311,8 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *                       1024: partial sums stay below 127*127*1024 < 2^24).
  *   I8_OPT_FORCE_SPLITS K-splits to use for every shape, on every GEMM route
  *                       (int8, fp16-held and E4M3 codes; at most one split
- *                       per K block); 0 = the plan's own choice.
+ *                       per K block, and at most 8 on the few-token
+ *                       kernel); 0 = the plan's own choice.
  *   I8_OPT_MAX_CTAS     cap on the persistent grid (0 = one CTA per SM).
  *   I8_OPT_TILE_N       GEMM tile width, 128 or 256 (0 = the table).
  *   I8_OPT_CTA_PAIR     GEMM on CTA pairs (256 x 256 tiles per cluster of 2):
@@ -415,7 +415,7 @@ typedef struct {
   int32_t tile_m;        /* output rows of one work item (M for the skinny kernel) */
   int32_t tile_n;        /* output columns of one work item */
   int32_t num_m, num_n;  /* work items along M and along N */
-  int32_t block_k;       /* K per K block (skinny kernel: per 512-K chunk) */
+  int32_t block_k;       /* K per K block (skinny kernel: per 256-K stage) */
   int32_t total_kb;      /* K blocks */
   int32_t splits;        /* K splits (1 = none; stream-K reports 1) */
   int32_t kb_per_split;  /* K blocks per split (the last may hold fewer) */

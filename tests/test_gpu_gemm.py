@@ -219,8 +219,9 @@ def test_gemm_int32_both_kernels(orc, cta_pair_option, mode, M, N, K):
 @pytest.mark.parametrize("M,N,K", [(1, 200, 8192), (16, 520, 8192), (9, 64, 131072)])
 def test_skinny_kernel_adversarial_exact(orc, M, N, K):
     """Few tokens take the weight-streaming kernel (forced up to M = 16 here):
-    per-CTA partial sums over 512 K in fp32 (< 2^24 for +-127 operands) plus
-    int32 atomics."""
+    each warp's fp32 chains over 512 K of its half-stages (< 2^24 for +-127
+    operands) drained into int32, then integer adds across warps and K
+    splits."""
     a, w = _adversarial(max(M, 4), N, K, seed=M + N)
     a = a[:M].contiguous()
     i8.set_option("skinny_max_m", 16)
@@ -399,38 +400,48 @@ def test_stream_k_workspace_garbage_and_graph_replay(stream_k_option):
     i8.sync_check()
 
 
-@pytest.mark.parametrize("M,N,K", [(2, 9216, 3072), (16, 3072, 12288)])
-def test_skinny_split_k_workspace_garbage_and_graph_replay(orc, M, N, K):
-    """The skinny kernel's K splits: a workspace full of random bytes,
-    back-to-back calls and CUDA-graph replays (the call clears its
-    accumulator on the stream, so the clear is captured too) all give the
-    exact result."""
+@pytest.mark.parametrize("M,N,K,splits", [(2, 9216, 3072, 0), (5, 3072, 12288, 0), (1, 200, 8192, 8),
+                                           (7, 520, 3584, 7), (3, 64, 1280, 3), (16, 136, 2560, 5)])
+def test_skinny_cluster_splits_back_to_back_and_graph_replay(orc, M, N, K, splits):
+    """The few-token kernel's K splits meet in the distributed shared memory
+    of their cluster: no workspace, and back-to-back calls and CUDA-graph
+    replays give the exact result.  Forced split counts up to the cluster
+    limit of 8, odd ones (uneven shares of the outputs) and 16 tokens (two
+    token groups) included."""
     a = inputs.random_int8(M, K, seed=M + 11)
     w = inputs.random_int8(N, K, seed=N + 12)
     want = orc.gemm_s32(a.numpy(), w.numpy())
     a, w = a.cuda(), w.cuda()
-    nbytes = i8.workspace_bytes(M, N, K)
-    assert nbytes > 0
-    ws = torch.randint(-128, 128, (nbytes,), dtype=torch.int8, device="cuda").view(torch.uint8)
-    out = torch.empty(M, N, dtype=torch.int32, device="cuda")
-    for _ in range(2):
-        out.fill_(7)
-        i8.gemm_int32(a, w, out=out, workspace=ws)
+    i8.set_option("skinny_max_m", 16)
+    i8.set_option("force_splits", splits)
+    try:
+        plan = i8.plan_query(M, N, K, "int8")
+        assert plan["kernel"] == "skinny" and plan["ws_bytes"] == 0
+        if splits:
+            assert plan["splits"] == splits
+        assert i8.workspace_bytes(M, N, K) == 0
+        out = torch.empty(M, N, dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            out.fill_(7)
+            i8.gemm_int32(a, w, out=out)
+            i8.sync_check()
+            assert np.array_equal(out.cpu().numpy(), want)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                i8.gemm_int32(a, w, out=out)
+        torch.cuda.current_stream().wait_stream(side)
+        for _ in range(3):
+            out.fill_(7)
+            graph.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(out.cpu().numpy(), want)
         i8.sync_check()
-        assert np.array_equal(out.cpu().numpy(), want)
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(graph, stream=side):
-            i8.gemm_int32(a, w, out=out, workspace=ws)
-    torch.cuda.current_stream().wait_stream(side)
-    for _ in range(3):
-        out.fill_(7)
-        graph.replay()
-        torch.cuda.synchronize()
-        assert np.array_equal(out.cpu().numpy(), want)
-    i8.sync_check()
+    finally:
+        i8.set_option("skinny_max_m", SKINNY_DEFAULT)
+        i8.set_option("force_splits", 0)
 
 
 @pytest.fixture

@@ -124,18 +124,21 @@ def test_tma_inner_coordinates_are_16_byte_multiples():
     """A tiled TMA copy must start its innermost coordinate on a 16-byte
     boundary.  Every x argument in the kernels is one of the expressions
     below, each a whole number of 128-byte rows: K-block starts (128 int8 /
-    E4M3 codes, 64 fp16 codes, 512-code chunks of 128- or 64-element boxes)
+    E4M3 codes, 64 fp16 codes, 256-code stages of 128- or 64-element boxes)
     and output column starts (64 bf16 or 32 int32 columns from a multiple of
     128), and the stream-K partial reloads (32 int32 columns from a multiple
     of 128)."""
-    allowed_x = {"kb * Cfg::BK8", "k16", "kb * Cfg::BK", "kc * kSkinnyK + b * Cfg::BOX_K",
+    allowed_x = {"kb * Cfg::BK8", "k16", "kb * Cfg::BK", "k0 + b * Cfg::BOX_K", "k0 + b * 128",
+                 "(ks0 + i) * kSkinnyK + b * Cfg::BOX_K", "(ks0 + i + Cfg::STAGES) * kSkinnyK + b * Cfg::BOX_K",
                  "nb", "n0 + g * 32", "n0 + g * 64", "n_loc + 32 * g"}
     calls = 0
     for name in GEMM_SOURCES:
         src = _code(name)
-        for m in re.finditer(r"\b(tma_load_[23]d(?:_pair)?|tma_store_3d)\(([^;]*)\);", src):
+        for m in re.finditer(r"\b(tma_load_[23]d(?:_pair)?|tma_store_3d|tma_prefetch_l2_2d)\(([^;]*)\);",
+                             src):
             args = [a.strip() for a in m.group(2).split(",")]
-            x = args[3] if m.group(1).startswith("tma_load") else args[2]
+            x = (args[3] if m.group(1).startswith("tma_load")
+                 else args[1] if m.group(1).startswith("tma_prefetch") else args[2])
             assert x in allowed_x, (name, m.group(0))
             calls += 1
     assert calls >= 12
@@ -145,7 +148,8 @@ def test_tma_inner_coordinates_are_16_byte_multiples():
     assert "static constexpr int BK8 = 128;" in gemm and "static constexpr int BK16 = 64;" in gemm
     assert "static constexpr int BK8 = 128;" in pair and "static constexpr int BK16 = 64;" in pair
     assert "static constexpr int BK = KIND == kDirectF16 ? 64 : 128;" in direct
-    assert "constexpr int kSkinnyK = 512;" in skinny
+    assert "constexpr int kSkinnyK = 256;" in skinny
+    assert "const int k0 = (ks0 + i) * kSkinnyK;" in skinny
     assert "static constexpr int BOX_K = W16 ? 64 : 128;" in skinny
     assert "const int k16 = kb * Cfg::BK8 + h * Cfg::BK16;" in gemm
     assert "const int k16 = kb * Cfg::BK8 + (h + q) * Cfg::BK16;" in pair

@@ -98,11 +98,12 @@ def test_model_restates_the_kernel_sources():
         assert body in text(name), name
 
 
-def test_skinny_splits_partition_the_k_chunks():
-    """The weight-streaming kernel: CTA (x, y) streams 64 weight rows of
-    N-block x over K chunks [y * kc_per_cta, min((y + 1) * kc_per_cta,
-    num_kc)); with several splits the CTA whose arrival finds the block's
-    counter at splits - 1 is the last and applies the epilogue."""
+def test_skinny_splits_partition_the_k_stages():
+    """The weight-streaming kernel: CTA x streams 64 weight rows of N-block
+    x / S over the 256-K stages [r * ks_per_cta, min((r + 1) * ks_per_cta,
+    num_ks)) of split r = x % S, its rank in the N-block's cluster of S CTAs;
+    rank r owns outputs [cut(r), cut(r + 1)) of the block's E, cut(r) =
+    E r / S, and the other ranks add their partials of those into r's."""
     n = 0
     for M in (1, 2, 3, 8):
         for N in (16, 200, 768, 3072, 9216, 18432):
@@ -110,21 +111,37 @@ def test_skinny_splits_partition_the_k_chunks():
                 p = i8.plan_query(M, N, K, "int8", **GB300)
                 if p["kernel"] != "skinny":
                     continue
-                s, per, nkc = p["splits"], p["kb_per_split"], p["total_kb"]
-                assert nkc == -(-K // 512) and p["num_n"] == -(-N // 64)
-                ranges = [(y * per, min(y * per + per, nkc)) for y in range(s)]
+                s, per, nks = p["splits"], p["kb_per_split"], p["total_kb"]
+                assert nks == -(-K // 256) and p["num_n"] == -(-N // 64)
+                assert 1 <= s <= 8 and p["grid"] == p["num_n"] * s
+                ranges = [(r * per, min(r * per + per, nks)) for r in range(s)]
                 assert all(a < b for a, b in ranges)
-                assert ranges[0][0] == 0 and ranges[-1][1] == nkc
+                assert ranges[0][0] == 0 and ranges[-1][1] == nks
                 assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
-                # arrivals 0..s-1 at a block's counter: exactly one sees s - 1
-                assert sum(prev == s - 1 for prev in range(s)) == 1
+                # every CTA of the grid: one N-block, one split, each pair once
+                cover = {(x // s, x % s) for x in range(p["grid"])}
+                assert len(cover) == p["grid"] and {b for b, _ in cover} == set(range(p["num_n"]))
+                # the owned slices partition the block's outputs, none empty
+                E = min(M, 8) * 64
+                cut = [E * r // s for r in range(s + 1)]
+                assert cut[0] == 0 and cut[-1] == E
+                assert all(a < b for a, b in zip(cut, cut[1:]))
+                # the owner search finds the slice of every output
+                for e in range(E):
+                    r = max([0] + [rr for rr in range(1, s) if cut[rr] <= e])
+                    assert cut[r] <= e < cut[r + 1]
                 n += 1
     assert n > 50
     src_path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                             "w8a8_int8_quantized_i8_gb300", "csrc", "skinny.cuh")
     with open(src_path) as fh:
         src = " ".join(fh.read().split())
-    for text in ["const int kc0 = blockIdx.y * p.kc_per_cta;",
-                 "const int kc1 = min(kc0 + p.kc_per_cta, p.num_kc);",
-                 "last_cta = (prev == gridDim.y - 1) ? 1 : 0;"]:
+    for text in ["const int split = static_cast<int>(blockIdx.x) % p.splits;",
+                 "const int n0 = (static_cast<int>(blockIdx.x) / p.splits) * kSkinnyRows;",
+                 "const int ks0 = split * p.ks_per_cta;",
+                 "const int ks1 = min(ks0 + p.ks_per_cta, p.num_ks);",
+                 "auto cut = [&](int r) { return E * r / S; };",
+                 "const int own0 = cut(split);",
+                 "const int own1 = cut(split + 1);",
+                 "for (int rr = 1; rr < S; ++rr) if (cut(rr) <= e) r = rr;"]:
         assert text in src, text

@@ -8,12 +8,13 @@ different allocator, or a latency-critical loop where cudaMalloc/cudaFree
 workspace it uses a fixed 16 MiB scratch array inside the library, and caps
 its launch plan to that size.
 
-Every route through the array is covered: the few-token kernel's split-K
-accumulator, the tiled kernels' split-K partials, a shape whose regular plan
-needs more than 16 MiB (so the capped plan splits K fewer times), and the
-stream-K schedule, whose arrival words stay behind in the array between
-calls.  Each shape is called twice in a row and both results must equal the
-oracle's bit for bit.
+Every route through the array is covered: the tiled kernels' split-K
+partials, a shape whose regular plan needs more than 16 MiB (so the capped
+plan splits K fewer times), and the stream-K schedule, whose arrival words
+stay behind in the array between calls; and the few-token kernel, whose K
+splits meet in distributed shared memory and use none of it.  Each shape is
+called twice in a row and both results must equal the oracle's bit for
+bit.
 
 This file is named so that pytest collects it last; it also passes when run
 alone in a fresh process.
@@ -72,7 +73,7 @@ def _twice_against_oracle(orc, lib, M, N, K, seed, what):
 
 @pytest.mark.parametrize("M,N,K,seed,route", [
     (16, 3072, 12288, 21, "tiled split-K"),
-    (2, 9216, 3072, 22, "few-token split-K"),
+    (2, 3072, 12288, 22, "few-token cluster split-K"),
     (256, 3072, 3072, 24, "split-K capped to the array"),
     (256, 9216, 3072, 26, "split-K capped to none"),
 ])
@@ -81,13 +82,18 @@ def test_noalloc_matches_oracle_on_two_calls(orc, saved_options, M, N, K, seed, 
     i8.set_option("chunk_k", 1024)
     i8.set_option("force_splits", 0)
     p = i8.plan_query(M, N, K, "int8")
-    assert p["ws_bytes"] > 0                     # the regular plan needs scratch
     capped = i8.plan_query(M, N, K, "int8", ws_cap=STATIC_BYTES)
     assert capped["ws_bytes"] <= STATIC_BYTES
+    if route.startswith("few-token"):
+        # K splits, and no scratch at all
+        assert p["kernel"] == "skinny" and p["splits"] > 1 and p["ws_bytes"] == 0
+        assert capped == p
+    else:
+        assert p["ws_bytes"] > 0                 # the regular plan needs scratch
     if route.startswith("split-K capped"):
         # the regular plan's partials outgrow the array: fewer splits
         assert p["ws_bytes"] > STATIC_BYTES and capped["splits"] < p["splits"]
-    if route != "split-K capped to none":
+    if route in ("tiled split-K", "split-K capped to the array"):
         assert capped["ws_bytes"] > 0           # the array is used
     _twice_against_oracle(orc, lib, M, N, K, seed, route)
 

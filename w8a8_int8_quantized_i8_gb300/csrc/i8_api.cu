@@ -95,7 +95,7 @@ struct DeviceInfo {
   int sms = 0;
   int pair_clusters[4] = {};  // co-resident clusters per pair-kernel config
   int cc_major = 0, cc_minor = 0;
-  bool smem_set[8] = {};
+  bool smem_set[12] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -440,30 +440,33 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
   // Few tokens: the weight-streaming kernel, which measured faster than the
   // tiled kernels up to M = 8 (up to M = 2 for weights above 48 M codes).
   if (M <= g_opt.skinny_max_m && (M <= 2 || N * K <= (int64_t(48) << 20))) {
-    // K split so that the whole grid is resident at once (skinny_slots CTAs):
-    // a second wave would stream its weights only after the first finished.
-    // Each split owns whole 512-K chunks.  Workspace: an int32 [M, N]
-    // accumulator + one completion counter per 64-row N-block, zeroed by the
-    // call before the launch.
+    // K splits: the fewest that give every SM a CTA, as long as the grid
+    // stays within the resident CTA slots (skinny_slots; a second wave would
+    // stream its weights only after the first finished) and every split owns
+    // at least kSkinnyMinStages whole 256-K stages.  One N-block's splits
+    // form a cluster of at most kSkinnyMaxSplits CTAs.  No workspace: the
+    // splits add their partials over distributed shared memory.
+    // Measured (GB300, 1 token, back-to-back calls): 1 x 3072 x 3072 7.5 /
+    // 6.1 / 5.8 / 5.7 / 9.3 us with 1 / 2 / 3 / 4 / 6 splits; 1 x 3072 x
+    // 12288 24.8 / 15.3 / 15.0 / 12.6 / 16.6 us with 1 / 2 / 3 / 4 / 6 (with
+    // 3 the clusters pack two CTAs on some SMs and leave others idle); grids
+    // beyond the resident slots cost 40-60 %.
     p.skinny = true;
     p.num_n = static_cast<int>((N + kSkinnyRows - 1) / kSkinnyRows);
     p.num_m = 1;
-    const int chunks = static_cast<int>((K + kSkinnyK - 1) / kSkinnyK);
-    int splits = g_opt.force_splits > 0 ? g_opt.force_splits : skinny_slots / p.num_n;
-    splits = std::max(1, std::min(splits, chunks));
-    // a capped workspace too small for the accumulator: one split, none needed
-    if (g_opt.force_splits == 0 &&
-        (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 15) / 16 * 16 +
-                (static_cast<size_t>(p.num_n) * 4 + 15) / 16 * 16 > ws_cap)
-      splits = 1;
-    p.kb_per_split = (chunks + splits - 1) / splits;          // chunks per split
-    p.splits = (chunks + p.kb_per_split - 1) / p.kb_per_split;
-    p.total_kb = chunks;
-    p.ws_ld = N;
-    if (p.splits > 1) {
-      const size_t acc_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 15) / 16 * 16;
-      p.ws_bytes = acc_bytes + (static_cast<size_t>(p.num_n) * 4 + 15) / 16 * 16;
+    const int stages = static_cast<int>((K + kSkinnyK - 1) / kSkinnyK);
+    int splits;
+    if (g_opt.force_splits > 0) {
+      splits = g_opt.force_splits;
+    } else {
+      splits = std::min((sms + p.num_n - 1) / p.num_n, std::max(1, stages / kSkinnyMinStages));
+      while (splits > 1 && p.num_n * splits > skinny_slots) --splits;
     }
+    splits = std::max(1, std::min(std::min(splits, stages), kSkinnyMaxSplits));
+    p.kb_per_split = (stages + splits - 1) / splits;          // stages per split
+    p.splits = (stages + p.kb_per_split - 1) / p.kb_per_split;
+    p.total_kb = stages;
+    p.grid = p.num_n * p.splits;
     return p;
   }
   const bool pair_ok = M >= 256 && N >= 256;
@@ -625,32 +628,69 @@ i8_status launch_pair_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const CU
                                 my, mp, gp));
 }
 
-// CTAs of the skinny kernel resident at once on this device (its split
-// choice keeps the grid within one wave).
-int skinny_slots(DeviceInfo* d, bool b16) {
-  static int cached[kMaxDevices][2] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 2 * d->sms;
-  if (cached[dev][b16] > 0) return cached[dev][b16];
-  int n = 0;
-  cudaError_t e;
-  if (b16) {
-    e = cudaFuncSetAttribute(gemm_skinny_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SkinnyCfg<true>::SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_skinny_kernel<true>, 128,
-                                                        SkinnyCfg<true>::SMEM_BYTES);
-  } else {
-    e = cudaFuncSetAttribute(gemm_skinny_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SkinnyCfg<false>::SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_skinny_kernel<false>, 128,
-                                                        SkinnyCfg<false>::SMEM_BYTES);
+// The skinny kernel for fp16-code weights (W16) and MT groups of 8 tokens:
+// its shared-memory size is set once per device (slots 4..7 of smem_set).
+template <bool W16, int MT>
+bool skinny_prepare(DeviceInfo* d) {
+  const int slot = 4 + 2 * (W16 ? 1 : 0) + (MT - 1);
+  if (!d->smem_set[slot]) {
+    if (cudaFuncSetAttribute(gemm_skinny_kernel<W16, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SkinnyCfg<W16, MT>::SMEM_BYTES) != cudaSuccess)
+      return false;
+    d->smem_set[slot] = true;
   }
+  return true;
+}
+
+// CTAs of one skinny kernel variant resident at once on this device (its
+// split choice keeps the grid within one wave).
+template <bool W16, int MT>
+int skinny_slots_of(DeviceInfo* d) {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return d->sms;
+  if (cached[dev] > 0) return cached[dev];
+  int n = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (skinny_prepare<W16, MT>(d))
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_skinny_kernel<W16, MT>,
+                                                      SkinnyCfg<W16, MT>::THREADS,
+                                                      SkinnyCfg<W16, MT>::SMEM_BYTES);
   cudaGetLastError();
-  if (e != cudaSuccess || n <= 0) n = 2;
-  cached[dev][b16] = n * d->sms;
-  return cached[dev][b16];
+  if (e != cudaSuccess || n <= 0) n = 1;
+  cached[dev] = n * d->sms;
+  return cached[dev];
+}
+int skinny_slots(DeviceInfo* d, bool b16, int64_t M) {
+  if (M > 8) return b16 ? skinny_slots_of<true, 2>(d) : skinny_slots_of<false, 2>(d);
+  return b16 ? skinny_slots_of<true, 1>(d) : skinny_slots_of<false, 1>(d);
+}
+
+template <bool W16, int MT>
+cudaError_t launch_skinny(DeviceInfo* d, const CUtensorMap& mw, const CUtensorMap& ma,
+                          const SkinnyParams& sp, int grid, cudaStream_t st) {
+  using Cfg = SkinnyCfg<W16, MT>;
+  if (!skinny_prepare<W16, MT>(d)) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeClusterDimension;   // one N-block's K splits
+  attr[n].val.clusterDim.x = static_cast<unsigned>(sp.splits);
+  attr[n].val.clusterDim.y = 1;
+  attr[n].val.clusterDim.z = 1;
+  ++n;
+  if (g_opt.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = static_cast<unsigned>(n);
+  return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<W16, MT>, mw, ma, sp);
 }
 
 using PairConv = PairCfg<3, 3, true, true>;    // int8 weights, CTA pair, 64-K fp16 stages
@@ -697,21 +737,13 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   if (i8_status e = device_info(&d, nullptr)) return e;
   const int clusters = b16 ? wide_pair_clusters(d)
                            : conv_pair_clusters(d);
-  const Plan pl = make_plan(M, N, K, d->sms, clusters, b16, ws_cap, skinny_slots(d, b16));
+  const Plan pl = make_plan(M, N, K, d->sms, clusters, b16, ws_cap, skinny_slots(d, b16, M));
   if (pl.ws_bytes > 0) {
     if (!ws || ws_bytes < pl.ws_bytes) return I8_ERR_WORKSPACE;
     if (!aligned16(ws)) return I8_ERR_ALIGNMENT;
   }
   if (pl.skinny) {
-    const size_t acc_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 15) / 16 * 16;
-    if (pl.splits > 1) {   // ws_bytes is a multiple of 16 (the plan rounds both parts)
-      const int64_t n16 = static_cast<int64_t>(pl.ws_bytes / 16);
-      const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n16 + 255) / 256, 4 * d->sms));
-      if (cudaError_t e = launch_pdl(zero_ws_kernel, dim3(blocks), dim3(256), 0, st,
-                                     static_cast<uint4*>(ws), n16))
-        return cuda_status(e);
-    }
-    CUtensorMap mw;
+    CUtensorMap mw, ma;
     if (b16) {
       if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wb, K, N, 2 * K, 64, kSkinnyRows))
         return I8_ERR_CUDA;
@@ -719,43 +751,29 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
       if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, K, N, K, 128, kSkinnyRows))
         return I8_ERR_CUDA;
     }
+    const int mt = M > 8 ? 2 : 1;   // token groups of 8 (M <= 16)
+    if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M, K, 128, 8 * mt)) return I8_ERR_CUDA;
     SkinnyParams sp{};
     sp.M = static_cast<int>(M);
     sp.N = static_cast<int>(N);
     sp.K = static_cast<int>(K);
-    sp.num_kc = pl.total_kb;
-    sp.kc_per_cta = pl.kb_per_split;
+    sp.num_ks = pl.total_kb;
+    sp.ks_per_cta = pl.kb_per_split;
+    sp.splits = pl.splits;
     sp.out_mode = out_mode;
-    sp.aq = aq;
     sp.s_a = s_a;
     sp.s_w = s_w;
     sp.bias = static_cast<const uint16_t*>(bias);
     sp.out = out;
     sp.ldo = ldo;
-    sp.acc = static_cast<int32_t*>(ws);
-    sp.counters = ws ? reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + acc_bytes) : nullptr;
-    const dim3 grid(static_cast<unsigned>(pl.num_n), static_cast<unsigned>(pl.splits));
-    if (b16) {
-      auto kern = gemm_skinny_kernel<true>;
-      if (!d->smem_set[5]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SkinnyCfg<true>::SMEM_BYTES) != cudaSuccess)
-          return I8_ERR_CUDA;
-        d->smem_set[5] = true;
-      }
-      if (cudaError_t le = launch_pdl(kern, grid, dim3(128), SkinnyCfg<true>::SMEM_BYTES, st, mw, sp))
-        return cuda_status(le);
-    } else {
-      auto kern = gemm_skinny_kernel<false>;
-      if (!d->smem_set[4]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SkinnyCfg<false>::SMEM_BYTES) != cudaSuccess)
-          return I8_ERR_CUDA;
-        d->smem_set[4] = true;
-      }
-      if (cudaError_t le = launch_pdl(kern, grid, dim3(128), SkinnyCfg<false>::SMEM_BYTES, st, mw, sp))
-        return cuda_status(le);
-    }
+    cudaError_t le;
+    if (b16)
+      le = mt == 2 ? launch_skinny<true, 2>(d, mw, ma, sp, pl.grid, st)
+                   : launch_skinny<true, 1>(d, mw, ma, sp, pl.grid, st);
+    else
+      le = mt == 2 ? launch_skinny<false, 2>(d, mw, ma, sp, pl.grid, st)
+                   : launch_skinny<false, 1>(d, mw, ma, sp, pl.grid, st);
+    if (le != cudaSuccess) return cuda_status(le);
     return cuda_status(cudaGetLastError());
   }
   CUtensorMap ma, mb;
@@ -1183,9 +1201,9 @@ size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (device_info(&d, nullptr) != I8_OK) return 0;
   // the larger of the two weight formats' plans, so one query serves both
   const size_t a = make_plan(M, N, K, d->sms, conv_pair_clusters(d), false,
-                             SIZE_MAX, skinny_slots(d, false)).ws_bytes;
+                             SIZE_MAX, skinny_slots(d, false, M)).ws_bytes;
   const size_t b = make_plan(M, N, K, d->sms, wide_pair_clusters(d), true,
-                             SIZE_MAX, skinny_slots(d, true)).ws_bytes;
+                             SIZE_MAX, skinny_slots(d, true, M)).ws_bytes;
   return a > b ? a : b;
 }
 
@@ -1214,17 +1232,17 @@ i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a, 
   // scratch comes from the library's fixed device array, and the plan is
   // capped to its size (fewer K splits, or none).  What the array must hold
   // at the start of a call: the tiled kernels' split-K partials are written
-  // in full before the reduction reads them; the few-token kernel's int32
-  // accumulator and completion counters are zeroed on the stream before its
-  // launch; the stream-K arrival words carry a per-launch epoch tag, so words
-  // left by an earlier call count as zero.
+  // in full before the reduction reads them; the few-token kernel uses none
+  // of it (its K splits meet in distributed shared memory); the stream-K
+  // arrival words carry a per-launch epoch tag, so words left by an earlier
+  // call count as zero.
   void* ws = nullptr;
   if (M > 0 && N > 0 && K > 0 && K % 16 == 0 && K <= 131072 && M <= INT32_MAX &&
       N <= INT32_MAX) {
     DeviceInfo* d;
     if (i8_status e = device_info(&d, nullptr)) return e;
     if (make_plan(M, N, K, d->sms, conv_pair_clusters(d), false, kStaticWsBytes,
-                  skinny_slots(d, false))
+                  skinny_slots(d, false, M))
             .ws_bytes > kStaticWsBytes)
       return I8_ERR_WORKSPACE;
     if (i8_status e = static_ws_address(&ws)) return e;
@@ -1358,7 +1376,7 @@ i8_status i8_plan_query(int64_t M, int64_t N, int64_t K, i8_route route, int sms
             : route == I8_ROUTE_F16CODES ? direct_cluster_capacity<kDirectF16>(d)
             : b16                        ? wide_pair_clusters(d)
                                          : conv_pair_clusters(d);
-    skinny_slots_in = skinny_slots(d, b16);
+    skinny_slots_in = skinny_slots(d, b16, M);
   }
   if (pairs == 0) pairs = std::max(1, sms / 2);
   i8_plan_info r{};

@@ -136,6 +136,17 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(desc)) : "memory");
 }
 
+// Starts fetching a 2-D tile into L2 (nothing is written to shared memory
+// and no barrier is signalled).  L2 is the coherence point of global memory,
+// so a prefetch issued before griddepcontrol.wait cannot leave stale data:
+// writes of the previous kernel that reach L2 later update the line.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* desc, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(desc)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // 2-D tiled bulk tensor load into this CTA's shared memory; completion is
 // signalled as transaction bytes on `bar`.  c0 is the innermost coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* desc, uint32_t bar, int c0,
@@ -264,6 +275,18 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
       return false;
     }
   }
+}
+
+// Atomic add of v into a 32-bit word in the shared memory of a CTA of this
+// cluster (mapa_shared addresses), counted as 4 transaction bytes on that
+// CTA's mbarrier.  The value leaves from a register, so the adding CTA may
+// exit at once.
+__device__ __forceinline__ void red_async_add_s32(uint32_t cluster_addr, int v, uint32_t cluster_bar) {
+  asm volatile(
+      "red.async.relaxed.cluster.shared::cluster.mbarrier::complete_tx::bytes.add.s32 [%0], %1, [%2];" ::"r"(
+          cluster_addr),
+      "r"(v), "r"(cluster_bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
