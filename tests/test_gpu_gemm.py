@@ -165,10 +165,11 @@ def test_error_paths():
     with pytest.raises(i8.I8Error) as e:
         i8.gemm_int32(raw[1:1 + 64 * 128].view(64, 128), w)
     assert e.value.status == 2
-    # a split-K shape with a too-small workspace
-    a2 = torch.zeros(2, 3072, dtype=torch.int8, device="cuda")
-    w2 = torch.zeros(9216, 3072, dtype=torch.int8, device="cuda")
-    need = i8.workspace_bytes(2, 9216, 3072)
+    # a split-K shape with a too-small workspace (16 tokens, K = 12288: the
+    # tiled kernel with K splits)
+    a2 = torch.zeros(16, 12288, dtype=torch.int8, device="cuda")
+    w2 = torch.zeros(3072, 12288, dtype=torch.int8, device="cuda")
+    need = i8.workspace_bytes(16, 3072, 12288)
     assert need > 0
     with pytest.raises(i8.I8Error) as e:
         i8.gemm_int32(a2, w2, workspace=torch.empty(need - 16, dtype=torch.uint8, device="cuda"))
