@@ -425,6 +425,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                   static_cast<int>(reinterpret_cast<uintptr_t>(p.s_w)) ^
                   static_cast<int>(reinterpret_cast<uintptr_t>(p.sk_arrive));
     asm volatile("" ::"r"(t));
+    if constexpr (Cfg::ANY_CONV) {
+      // The first int8 stages of this CTA's first item on their way into L2
+      // while the previous kernel of the stream drains (prefetches cannot
+      // leave stale data; the loads still wait for it).
+      PairTile t0;
+      if (warp == 2 && pair_item(p, pair, npairs, 0, t0)) {
+        const int m0 = t0.mp * Cfg::PAIR_M + static_cast<int>(rank) * Cfg::BM;
+        const int n0 = t0.nb * Cfg::PAIR_N + static_cast<int>(rank) * Cfg::BN;
+        for (int kb = t0.kb0; kb < t0.kb1 && kb < t0.kb0 + Cfg::S8; ++kb) {
+          if constexpr (Cfg::CONV_A) tma_prefetch_l2_2d(&tmA, kb * Cfg::BK8, m0);
+          if constexpr (Cfg::CONV_B) tma_prefetch_l2_2d(&tmB, kb * Cfg::BK8, n0);
+        }
+      }
+    }
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::S8; ++s) {

@@ -82,9 +82,12 @@ __global__ void __launch_bounds__(256) producer_quant_kernel(
   const int lane = threadIdx.x & 31;
   const int64_t row = blockIdx.x;
   const int slice0 = warp * (32 * 8 * V);
+  const uint16_t* xr = x + row * ldx;
+  // this warp's slice on its way into L2 while the previous kernel drains
+  if (lane == 0 && slice0 < K)
+    bulk_prefetch_l2(xr + slice0, static_cast<uint32_t>(min(32 * 8 * V, K - slice0)) * 2u);
 
   pdl_wait();  // X may be the previous kernel's output
-  const uint16_t* xr = x + row * ldx;
   uint4 v[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) {

@@ -147,6 +147,15 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* desc, int c0, int
                : "memory");
 }
 
+// Starts fetching `bytes` (a multiple of 16, from a 16-byte-aligned address)
+// of global memory into L2; the same coherence argument as for
+// tma_prefetch_l2_2d makes it safe before griddepcontrol.wait.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 // 2-D tiled bulk tensor load into this CTA's shared memory; completion is
 // signalled as transaction bytes on `bar`.  c0 is the innermost coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* desc, uint32_t bar, int c0,

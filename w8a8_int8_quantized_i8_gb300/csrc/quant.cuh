@@ -197,9 +197,14 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   const int wig = warp % G;
   const bool valid_row = (warp / G) < rows_per_cta && row < rows;
   const int slice0 = wig * (32 * 8 * V);  // first element of this warp's slice
+  const uint16_t* xr = x + (valid_row ? row : 0) * ldx;
+  // Start this warp's slice on its way into L2 while the previous kernel of
+  // the stream drains (a prefetch cannot leave stale data; the loads below
+  // still wait for it).
+  if (valid_row && lane == 0 && slice0 < K)
+    bulk_prefetch_l2(xr + slice0, static_cast<uint32_t>(min(32 * 8 * V, K - slice0)) * 2u);
 
   pdl_wait();  // X may be the previous kernel's output
-  const uint16_t* xr = x + (valid_row ? row : 0) * ldx;
   uint4 v[V];
   uint32_t amax2 = 0;  // bf16x2 running max of |x| (sign bits meaningless)
 #pragma unroll
