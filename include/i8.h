@@ -319,11 +319,10 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *                       0 = the table (default: pairs for int8 weights when
  *                       the 256 x 256 tiles fill every pair of SMs), 1 = never,
  *                       2 = whenever M, N >= 256.
- *   I8_OPT_SKINNY_MAX_M token counts M up to this value (0..16, default 8)
- *                       use the weight-streaming kernel for few tokens;
- *                       above M = 2 only while the weights are at most
- *                       48 M codes (beyond, the tiled kernels measured
- *                       faster).
+ *   I8_OPT_SKINNY_MAX_M token counts M up to this value (0..16, default 16)
+ *                       use the weight-streaming kernel for few tokens
+ *                       (measured faster than the tiled kernels at every
+ *                       M <= 16 of the DiT shapes).
  *   I8_OPT_QUANT_VPL    quantizer: most 16-byte vectors one lane holds
  *                       (1..16, default 6); more warps share a row above.
  *   I8_OPT_PDL          1 (default): launch the kernels with programmatic

@@ -16,7 +16,7 @@ from tests._util import assert_bf16_exact, gpu_bf16_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
-SKINNY_DEFAULT = 8     # the library's default weight-streaming threshold
+SKINNY_DEFAULT = 16    # the library's default weight-streaming threshold
 
 INT_SHAPES = [
     (64, 128, 256),
@@ -26,7 +26,8 @@ INT_SHAPES = [
     (256, 384, 1024),
     (300, 200, 1040),
     (2, 9216, 3072),       # skinny: split-K
-    (16, 3072, 12288),     # few tokens, deep: split-K
+    (16, 3072, 12288),     # few tokens, deep: cluster split-K
+    (32, 3072, 12288),     # tiled, split-K
     (1024, 1024, 4096),
 ]
 
@@ -165,11 +166,11 @@ def test_error_paths():
     with pytest.raises(i8.I8Error) as e:
         i8.gemm_int32(raw[1:1 + 64 * 128].view(64, 128), w)
     assert e.value.status == 2
-    # a split-K shape with a too-small workspace (16 tokens, K = 12288: the
+    # a split-K shape with a too-small workspace (32 tokens, K = 12288: the
     # tiled kernel with K splits)
-    a2 = torch.zeros(16, 12288, dtype=torch.int8, device="cuda")
+    a2 = torch.zeros(32, 12288, dtype=torch.int8, device="cuda")
     w2 = torch.zeros(3072, 12288, dtype=torch.int8, device="cuda")
-    need = i8.workspace_bytes(16, 3072, 12288)
+    need = i8.workspace_bytes(32, 3072, 12288)
     assert need > 0
     with pytest.raises(i8.I8Error) as e:
         i8.gemm_int32(a2, w2, workspace=torch.empty(need - 16, dtype=torch.uint8, device="cuda"))

@@ -95,7 +95,7 @@ def test_kernel_choice_table():
     for M in MS:
         for N in NS:
             for K in KS:
-                few = M <= 8 and (M <= 2 or N * K <= 48 << 20)
+                few = M <= 16
                 k8 = i8.plan_query(M, N, K, "int8", **GB300)["kernel"]
                 k16 = i8.plan_query(M, N, K, "w16", **GB300)["kernel"]
                 if few:
@@ -244,9 +244,10 @@ def test_options_change_the_plan():
     i8.set_option("raster", 0)
     i8.set_option("skinny_max_m", 0)
     assert i8.plan_query(1, 3072, 3072, "int8", **GB300)["kernel"] == "tile"
+    i8.set_option("skinny_max_m", 8)
+    assert i8.plan_query(16, 3072, 3072, "int8", **GB300)["kernel"] == "tile"
     i8.set_option("skinny_max_m", 16)
     assert i8.plan_query(16, 3072, 3072, "int8", **GB300)["kernel"] == "skinny"
-    i8.set_option("skinny_max_m", 8)
     i8.set_option("cta_pair", 1)
     assert i8.plan_query(4096, 3072, 3072, "int8", **GB300)["kernel"] == "tile"
     i8.set_option("cta_pair", 2)

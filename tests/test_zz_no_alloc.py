@@ -72,7 +72,7 @@ def _twice_against_oracle(orc, lib, M, N, K, seed, what):
 
 
 @pytest.mark.parametrize("M,N,K,seed,route", [
-    (16, 3072, 12288, 21, "tiled split-K"),
+    (32, 3072, 12288, 21, "tiled split-K"),
     (2, 3072, 12288, 22, "few-token cluster split-K"),
     (256, 3072, 3072, 24, "split-K capped to the array"),
     (256, 9216, 3072, 26, "split-K capped to none"),

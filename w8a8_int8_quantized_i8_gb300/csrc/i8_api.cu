@@ -68,7 +68,7 @@ struct Options {
   int force_bn = 0;        // 0 = table, else 128 or 256
   int quant_vpl = 6;       // max 16-byte vectors per lane in the quantizer
   int cta_pair = 0;        // 0 = table, 1 = never, 2 = whenever the shape allows
-  int skinny_max_m = 8;    // token counts up to this use the weight-streaming kernel (0 = off)
+  int skinny_max_m = 16;   // token counts up to this use the weight-streaming kernel (0 = off)
   int pdl = 1;             // launch with programmatic stream serialization
   int quant_rows = 0;      // quantizer rows per CTA (0 = by shape)
   int stream_k = 1;        // CTA-pair stream-K: 0 never, 1 by the table, 2 whenever pairs idle
@@ -420,7 +420,7 @@ int tile_order_n_fastest(int64_t M, int64_t N) {
 }
 
 // Shape -> configuration (replaces per-shape autotuning).
-//   * few tokens (M <= 8 by default): the weight-streaming kernel;
+//   * few tokens (M <= 16 by default): the weight-streaming kernel;
 //   * CTA pairs (one 256 x 256 tile per cluster of two SMs, each SM staging
 //     and widening half of B) for int8 weights whenever M, N >= 256; with
 //     pre-widened weights the single-CTA kernel measured slightly faster;
@@ -437,9 +437,11 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
   if (pair_clusters <= 0) pair_clusters = sms / 2;
   if (skinny_slots <= 0) skinny_slots = 2 * sms;
   p.total_kb = static_cast<int>((K + 127) / 128);
-  // Few tokens: the weight-streaming kernel, which measured faster than the
-  // tiled kernels up to M = 8 (up to M = 2 for weights above 48 M codes).
-  if (M <= g_opt.skinny_max_m && (M <= 2 || N * K <= (int64_t(48) << 20))) {
+  // Few tokens: the weight-streaming kernel, which measured 1.4-2.2x faster
+  // than the tiled kernels with K splits at every M <= 16 of the DiT sweep
+  // (e.g. 16 x 3072 x 9216: 10.4 against 20.1 us; 8 x 3072 x 18432: 13.2
+  // against 27.6 us).
+  if (M <= g_opt.skinny_max_m) {
     // K splits: the fewest that give every SM a CTA, as long as the grid
     // stays within the resident CTA slots (skinny_slots; a second wave would
     // stream its weights only after the first finished) and every split owns

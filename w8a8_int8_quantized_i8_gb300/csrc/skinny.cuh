@@ -10,7 +10,7 @@
 //     cluster; grid = N-blocks x S, cluster rank = K split.
 //   * One producer warp streams the CTA's weight rows and the token codes of
 //     every stage through a ring of STAGES stages by TMA (128-byte swizzle);
-//     two CTAs fit on an SM.
+//     two CTAs fit on an SM (int8 weights).
 //     The parts of a box outside the tensors (rows past N, tokens past M, K
 //     past its end) arrive as zeros and add nothing.  The weights of the
 //     first fill are prefetched into L2 before the wait for the previous
@@ -71,7 +71,7 @@ struct SkinnyCfg {
   static constexpr int A_ROWS = 8 * MT;                         // token rows per box
   static constexpr int A_BOX_BYTES = A_ROWS * 128;
   static constexpr int STAGE_BYTES = W_BOXES * W_BOX_BYTES + A_BOXES * A_BOX_BYTES;
-  static constexpr int STAGES = W16 ? 4 : 6;
+  static constexpr int STAGES = W16 ? 4 : (MT == 1 ? 6 : 5);
   static constexpr int COMPUTE_WARPS = 8;
   static constexpr int THREADS = 32 * (COMPUTE_WARPS + 1);    // + the producer warp
   static constexpr int OFF_PART = STAGES * STAGE_BYTES;        // int32 [A_ROWS][64], token-major
@@ -84,7 +84,7 @@ struct SkinnyCfg {
   static constexpr int OFF_REDBAR = (OFF_SCL + (2 * kSkinnyRows + A_ROWS) * 4 + 7) / 8 * 8;
   static constexpr int SMEM_BYTES = OFF_REDBAR + 8 + 1024;   // + 1 KB alignment room
   // two CTAs per SM: 228 KB per SM, 1 KB of it reserved per CTA
-  static_assert(W16 || MT > 1 || 2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs must fit on an SM");
+  static_assert(W16 || 2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs must fit on an SM");
   static_assert(SMEM_BYTES <= 227 * 1024, "more shared memory than a CTA may hold");
   static_assert(STAGE_BYTES % 1024 == 0 && W_BOX_BYTES % 1024 == 0 && A_BOX_BYTES % 1024 == 0,
                 "128-byte-swizzled boxes must start on 1 KB boundaries");
