@@ -423,6 +423,8 @@ typedef struct {
   int64_t ws_bytes;      /* workspace the call needs (0 = none) */
   double model_us;       /* direct kernels: the split cost model's time (us,
                             up to a constant) for this plan; else 0 */
+  int32_t sk_waves;      /* stream-K: whole waves of tiles before the split ones */
+  int32_t sk_pairs;      /* stream-K: CTA pairs sharing the split tiles' units */
 } i8_plan_info;
 
 i8_status i8_plan_query(int64_t M, int64_t N, int64_t K, i8_route route, int sms,

@@ -321,9 +321,12 @@ def stream_k_option():
 
 # Shapes on CTA pairs whose whole tiles leave pairs idle, so the stream-K
 # schedule splits tiles between pairs: 2 x 3 tiles spread over many pairs
-# (each tile shared by several), a ragged one, and a multi-wave one with a
-# partial last wave.
-STREAM_K_SHAPES = [(512, 768, 4096), (300, 520, 1040), (1280, 2816, 2048)]
+# (each tile shared by several), a ragged one, a multi-wave one with a
+# partial last wave, and two with K >= 64 blocks, whose schedule runs one
+# whole wave of 76 (or 74) tiles first and splits only the 5 (or 7) left
+# over (ragged M, N and K in the second).
+STREAM_K_SHAPES = [(512, 768, 4096), (300, 520, 1040), (1280, 2816, 2048), (2304, 2304, 8192),
+                   (2200, 2104, 8208)]
 
 
 @pytest.mark.parametrize("M,N,K", STREAM_K_SHAPES)

@@ -70,11 +70,18 @@ def _check_plan(p, M, N, K, route, m):
     elif p["kernel"] == "pair_stream_k":
         tiles = p["num_m"] * p["num_n"]
         arrive = -(-tiles * 16 // 1024) * 1024
-        assert p["ws_bytes"] == arrive + p["grid"] // 2 * 256 * 256 * 4   # one slot per pair
+        assert p["ws_bytes"] == arrive + p["sk_pairs"] * 256 * 256 * 4   # one slot per sharing pair
+        # long K: whole waves on every resident pair first, when there is one
+        assert 1 <= p["sk_pairs"] <= p["grid"] // 2
+        assert p["sk_waves"] == (tiles // pairs if p["total_kb"] >= 64 else 0)
+        if p["sk_waves"] > 0:
+            assert p["grid"] == 2 * pairs
     else:
         assert p["ws_bytes"] == (s * M * (-(-N // 4) * 4) * 4 if s > 1 else 0)
-    # M blocks fastest under stream-K; otherwise N blocks fastest when M > N
-    assert p["n_fastest"] == (0 if p["kernel"] == "pair_stream_k" else 1 if M > N else 0)
+    # M blocks fastest when stream-K splits every tile; otherwise N blocks
+    # fastest when M > N
+    every_tile_split = p["kernel"] == "pair_stream_k" and p["sk_waves"] == 0
+    assert p["n_fastest"] == (0 if every_tile_split else 1 if M > N else 0)
     assert (p["model_us"] > 0) == (p["kernel"] == "direct")
 
 
@@ -199,11 +206,15 @@ def test_direct_splits_minimise_the_cost_model():
 
 def test_stream_k_rule():
     # at least half a wave of tiles and a whole-tile wave efficiency below
-    # 0.93, at any K: stream-K, M blocks fastest even where M > N
-    for M, N, K in ((2304, 3072, 3072), (2304, 3072, 12288), (3328, 3072, 12288),
-                    (256, 12288, 3072), (1024, 3072, 3072), (8704, 3072, 12288)):
+    # 0.93, at any K: stream-K.  Short K: every tile split, M blocks fastest
+    # even where M > N.  Long K: whole waves first, the table's tile order.
+    for M, N, K, waves, nf in ((2304, 3072, 3072, 0, 0), (2304, 3072, 12288, 1, 0),
+                               (3328, 3072, 12288, 2, 1), (256, 12288, 3072, 0, 0),
+                               (1024, 3072, 3072, 0, 0), (8704, 3072, 12288, 5, 1),
+                               (1024, 3072, 12288, 0, 0)):
         p = i8.plan_query(M, N, K, "int8", **GB300)
-        assert (p["kernel"], p["n_fastest"], p["splits"]) == ("pair_stream_k", 0, 1), (M, N, K)
+        assert (p["kernel"], p["n_fastest"], p["splits"], p["sk_waves"]) == \
+            ("pair_stream_k", nf, 1, waves), (M, N, K)
     p = i8.plan_query(2304, 3072, 12288, "int8", **GB300)
     assert p["grid"] == 2 * GB300["pairs"]
     # high wave efficiency (QKV 2560 x 9216: 360 tiles on 76 pairs, 0.95),
@@ -267,7 +278,7 @@ def test_bench_workloads():
     qkv = i8.plan_query(8704, 9216, 3072, "int8", **GB300)
     assert (qkv["kernel"], qkv["splits"], qkv["n_fastest"], qkv["ws_bytes"]) == ("pair", 1, 0, 0)
     down = i8.plan_query(8704, 3072, 12288, "int8", **GB300)
-    assert (down["kernel"], down["splits"], down["n_fastest"]) == ("pair_stream_k", 1, 0)
+    assert (down["kernel"], down["splits"], down["n_fastest"], down["sk_waves"]) == ("pair_stream_k", 1, 1, 5)
     one = i8.plan_query(1, 9216, 3072, "int8", **GB300)
     assert (one["kernel"], one["splits"], one["grid"]) == ("skinny", 2, 288)
 

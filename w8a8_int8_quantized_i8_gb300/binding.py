@@ -41,7 +41,8 @@ class PlanInfo(ctypes.Structure):
                 ("total_kb", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("kb_per_split", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("n_fastest", ctypes.c_int32), ("ws_bytes", ctypes.c_int64),
-                ("model_us", ctypes.c_double)]
+                ("model_us", ctypes.c_double), ("sk_waves", ctypes.c_int32),
+                ("sk_pairs", ctypes.c_int32)]
 
 
 class I8Error(RuntimeError):

@@ -55,12 +55,16 @@ struct GemmParams {
   void* out;                           // y (bf16), c (int32) or workspace (int32)
   int64_t ldo;                         // elements
   int64_t split_stride;                // elements between split partials (kOutPartial)
-  // Stream-K schedule (CTA-pair kernel only): pair p of P takes the units
-  // [p*U/P, (p+1)*U/P) of the U = num_tiles * total_kb (tile, K-block) units,
-  // so every pair does the same work whatever the tile count.  A tile cut
-  // between pairs is finished from exact int32 partials by the last pair to
-  // arrive at it.
+  // Stream-K schedule (CTA-pair kernel only): first sk_waves whole waves of
+  // tiles (tile = pair + wave * P), then pair q < Q = sk_pairs takes the
+  // units [q*U/Q, (q+1)*U/Q) of the U = (num_tiles - sk_waves * P) *
+  // total_kb (tile, K-block) units of the remaining tiles, so every pair
+  // does about the same work whatever the tile count.  A tile cut between
+  // pairs is finished from exact int32 partials by the pair holding its first
+  // K blocks.
   int stream_k;                        // 0: tile-strided schedule
+  int sk_waves;                        // whole waves before the split tiles
+  int sk_pairs;                        // Q: pairs sharing the split tiles' units
   unsigned long long* sk_arrive;       // [num_tiles][2] arrival words: epoch << 16 | count
   const int32_t* sk_part;              // [P][256][256] int32 partial slots
   unsigned long long sk_epoch;         // this launch's tag, in [1, 2^48)

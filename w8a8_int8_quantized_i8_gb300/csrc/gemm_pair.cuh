@@ -150,27 +150,33 @@ __device__ __forceinline__ PairTile decode_pair_tile(const GemmParams& p, int ti
   return t;
 }
 
-// Stream-K units are (tile, K-block) pairs in tile-major order; pair q of P
-// owns units [sk_first(q), sk_first(q + 1)).  The host plans stream-K only
-// when units * P < 2^31, so 32-bit arithmetic is exact here.
-__device__ __forceinline__ uint32_t sk_units(const GemmParams& p) {
-  return static_cast<uint32_t>(p.num_tiles) * static_cast<uint32_t>(p.total_kb);
+// Stream-K: after sk_waves whole waves of tiles, the units of the remaining
+// tiles are (tile, K-block) pairs in tile-major order, numbered from the
+// first of those tiles; pair q of the Q = sk_pairs that share them owns
+// units [sk_first(q), sk_first(q + 1)).  The host plans stream-K only when
+// units * Q < 2^31, so 32-bit arithmetic is exact here.
+__device__ __forceinline__ int sk_tile0(const GemmParams& p, int npairs) {
+  return p.sk_waves * npairs;   // the first split-region tile
+}
+__device__ __forceinline__ uint32_t sk_units(const GemmParams& p, int npairs) {
+  return static_cast<uint32_t>(p.num_tiles - sk_tile0(p, npairs)) * static_cast<uint32_t>(p.total_kb);
 }
 __device__ __forceinline__ uint32_t sk_first(const GemmParams& p, int q, int npairs) {
-  return sk_units(p) * static_cast<uint32_t>(q) / static_cast<uint32_t>(npairs);
+  return sk_units(p, npairs) * static_cast<uint32_t>(q) / static_cast<uint32_t>(p.sk_pairs);
 }
 // The pair whose range holds unit u: the largest q with sk_first(q) <= u.
 __device__ __forceinline__ int sk_holder(const GemmParams& p, uint32_t u, int npairs) {
-  return static_cast<int>(((u + 1) * static_cast<uint32_t>(npairs) - 1) / sk_units(p));
+  return static_cast<int>(((u + 1) * static_cast<uint32_t>(p.sk_pairs) - 1) / sk_units(p, npairs));
 }
 
 // Item `it` of this pair's schedule; false once the pair has no more work.
-// Without stream-K the items are the tiles pair, pair + P, ...; with it they
-// are the pieces of the pair's unit range cut at tile boundaries (only the
-// first and the last piece can be part of a tile).
+// Without stream-K the items are the tiles pair, pair + P, ...; with it the
+// first sk_waves items are those, and the rest the pieces of the pair's unit
+// range cut at tile boundaries (only the first and the last piece can be
+// part of a tile).
 __device__ __forceinline__ bool pair_item(const GemmParams& p, int pair, int npairs, int it,
                                           PairTile& t) {
-  if (!p.stream_k) {
+  if (!p.stream_k || it < p.sk_waves) {
     const int tile = pair + it * npairs;
     if (tile >= p.num_tiles) return false;
     t = decode_pair_tile(p, tile);
@@ -178,13 +184,14 @@ __device__ __forceinline__ bool pair_item(const GemmParams& p, int pair, int npa
     t.partial = false;
     return true;
   }
+  if (pair >= p.sk_pairs) return false;
   const uint32_t kb = static_cast<uint32_t>(p.total_kb);
   const uint32_t u0 = sk_first(p, pair, npairs);
   const uint32_t u1 = sk_first(p, pair + 1, npairs);
-  const uint32_t tile = u0 / kb + static_cast<uint32_t>(it);
-  const uint32_t t0 = tile * kb;
+  const uint32_t rel = u0 / kb + static_cast<uint32_t>(it - p.sk_waves);   // tile within the region
+  const uint32_t t0 = rel * kb;
   if (u0 >= u1 || t0 >= u1) return false;
-  t.tile = static_cast<int>(tile);
+  t.tile = sk_tile0(p, npairs) + static_cast<int>(rel);
   t.ks = 0;
   tile_coords(p, t.tile, t.mp, t.nb);
   t.kb0 = static_cast<int>((u0 > t0 ? u0 : t0) - t0);
@@ -284,10 +291,9 @@ __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CU
       // arrived, loads their partials by TMA into its own pipeline buffers
       // (idle once its last item's MMAs are done), adds them to the
       // accumulator it still holds and writes the tile.
-      const int q0 = sk_holder(p, static_cast<uint32_t>(tc.tile) * static_cast<uint32_t>(p.total_kb),
-                               npairs);
-      const int q1 = sk_holder(p, static_cast<uint32_t>(tc.tile + 1) * static_cast<uint32_t>(p.total_kb) - 1,
-                               npairs);
+      const uint32_t rel = static_cast<uint32_t>(tc.tile - sk_tile0(p, npairs));   // tile within the region
+      const int q0 = sk_holder(p, rel * static_cast<uint32_t>(p.total_kb), npairs);
+      const int q1 = sk_holder(p, (rel + 1) * static_cast<uint32_t>(p.total_kb) - 1, npairs);
       unsigned long long* word = p.sk_arrive + 2 * tc.tile + rank;
       if (tc.kb0 != 0) {
         store_warp_tile_s32<128>(tmP, stage, lane, m_loc, n_loc, acc, pair);
@@ -420,7 +426,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     // touch the fields the roles decode first while warps 0 and 1 set up the
     // barriers and the tensor memory.
     const int t = p.num_tiles ^ p.splits ^ p.total_kb ^ p.kb_per_split ^ p.num_m_blk ^
-                  p.num_n_blk ^ p.n_fastest ^ p.stream_k ^ p.chunk_stages ^ p.out_mode ^ p.M ^
+                  p.num_n_blk ^ p.n_fastest ^ p.stream_k ^ p.sk_waves ^ p.sk_pairs ^ p.chunk_stages ^
+                  p.out_mode ^ p.M ^
                   p.N ^ static_cast<int>(reinterpret_cast<uintptr_t>(p.s_a)) ^
                   static_cast<int>(reinterpret_cast<uintptr_t>(p.s_w)) ^
                   static_cast<int>(reinterpret_cast<uintptr_t>(p.sk_arrive));

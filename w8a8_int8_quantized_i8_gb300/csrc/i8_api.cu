@@ -374,6 +374,8 @@ struct Plan {
   bool skinny = false;     // few tokens: weight-streaming kernel
   bool pair = false;       // CTA-pair kernel (256 x 256 tiles per cluster of 2)
   bool stream_k = false;   // pair kernel with the stream-K schedule
+  int sk_waves = 0;        // stream-K: whole waves of tiles before the split ones
+  int sk_pairs = 0;        // stream-K: pairs sharing the split tiles' units
   size_t sk_arrive_bytes = 0;  // stream-K: arrival words at the start of ws
   int bn = 128;
   int splits = 1;
@@ -489,9 +491,11 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
     // the tile it finishes last waits for one or two partials to load: about
     // 6-9 us per launch against whole tiles at K = 3072.  The table takes it
     // where whole tiles leave more than that idle: at least half a wave of
-    // tiles and a whole-tile wave efficiency below 0.93.  Stream-K plans take
-    // the M-blocks-fastest tile order, which measured as fast or faster
-    // under stream-K at every shape with M > N.
+    // tiles and a whole-tile wave efficiency below 0.93.  Plans that split
+    // every tile take the M-blocks-fastest tile order, which measured as
+    // fast or faster there at every shape with M > N; plans with whole waves
+    // first take the table's order (N-blocks fastest when M > N: MLP
+    // down-projection 431.2 against 442.4 us).
     // Measured (GEMM, GB300, 30 DiT sweep shapes): every shape the rule
     // takes gains 1-12 % (e.g. 1024 x 3072 x 3072 32.8 -> 30.3 us,
     // 4096 x 3072 x 12288 230 -> 212 us, 1024 x 3072 x 12288 103 -> 66 us)
@@ -505,12 +509,27 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
     if ((g_opt.stream_k == 2 || (g_opt.stream_k == 1 && sk_table)) && g_opt.force_splits == 0 &&
         tiles % slots != 0 &&
         units * slots < (int64_t(1) << 31)) {   // the kernel's unit arithmetic is 32-bit
-      const int pairs = static_cast<int>(std::min<int64_t>(slots, std::max<int64_t>(1, units / 4)));
+      // Long K (>= 64 K-blocks): whole waves of tiles first (tile = pair +
+      // wave * pairs, neighbours in flight together), then only the
+      // remaining tiles' units split evenly.  Shorter K: every tile's units
+      // split evenly.  At least 4 K-blocks per pair either way.
+      // Measured (GEMM, GB300, both schedules forced, one process): whole
+      // waves first gained 2-14 % at K = 12288 (MLP down-projection 445.2 ->
+      // 431.2 us, 16384 x 3072 x 12288 857 -> 804 us, with the table's tile
+      // order) and lost 1-7 % at K = 3072 (QKV 106.7 -> 109.9 us).
+      const int64_t dp_waves = p.total_kb >= 64 ? tiles / slots : 0;
+      const int pairs = dp_waves > 0 ? slots
+                                     : static_cast<int>(std::min<int64_t>(slots, std::max<int64_t>(1, units / 4)));
+      const int64_t sk_units = (tiles - dp_waves * pairs) * p.total_kb;
+      const int sk_pairs = static_cast<int>(std::min<int64_t>(pairs, std::max<int64_t>(1, sk_units / 4)));
       const size_t arrive = (static_cast<size_t>(tiles) * 16 + 1023) / 1024 * 1024;
-      const size_t part = static_cast<size_t>(pairs) * 256 * 256 * sizeof(int32_t);
+      const size_t part = static_cast<size_t>(sk_pairs) * 256 * 256 * sizeof(int32_t);
       if (arrive + part <= ws_cap) {
         p.stream_k = true;
-        p.n_fastest = g_opt.raster != 0 ? (g_opt.raster == 2 ? 1 : 0) : 0;
+        p.sk_waves = static_cast<int>(dp_waves);
+        p.sk_pairs = sk_pairs;
+        p.n_fastest = g_opt.raster != 0 ? (g_opt.raster == 2 ? 1 : 0)
+                                        : (dp_waves > 0 ? tile_order_n_fastest(M, N) : 0);
         p.num_tiles = static_cast<int>(tiles);
         p.kb_per_split = p.total_kb;
         p.grid = 2 * pairs;
@@ -818,14 +837,16 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
                   static_cast<uint64_t>(M), static_cast<uint64_t>(gp.ldo),
                   static_cast<uint64_t>(pl.splits)))
     return I8_ERR_CUDA;
-  // Stream-K partial slots: {256 columns, 256 rows, 1 per pair} int32.
+  // Stream-K partial slots: {256 columns, 256 rows, 1 per sharing pair} int32.
   CUtensorMap mp = my;
   if (pl.stream_k) {
     gp.stream_k = 1;
+    gp.sk_waves = pl.sk_waves;
+    gp.sk_pairs = pl.sk_pairs;
     gp.sk_arrive = static_cast<unsigned long long*>(ws);
     gp.sk_part = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(ws) + pl.sk_arrive_bytes);
     gp.sk_epoch = next_sk_epoch();
-    if (!encode_out(&mp, false, gp.sk_part, 256, 256, 256, static_cast<uint64_t>(pl.grid / 2)))
+    if (!encode_out(&mp, false, gp.sk_part, 256, 256, 256, static_cast<uint64_t>(pl.sk_pairs)))
       return I8_ERR_CUDA;
   }
   i8_status e;
@@ -1408,6 +1429,8 @@ i8_status i8_plan_query(int64_t M, int64_t N, int64_t K, i8_route route, int sms
     r.kb_per_split = pl.kb_per_split;
     r.ws_bytes = static_cast<int64_t>(pl.ws_bytes);
     r.n_fastest = pl.n_fastest;
+    r.sk_waves = pl.sk_waves;
+    r.sk_pairs = pl.sk_pairs;
     if (pl.skinny) {
       r.kernel = I8_KERNEL_SKINNY;
       r.tile_m = static_cast<int>(M);
