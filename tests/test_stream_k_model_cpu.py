@@ -164,7 +164,8 @@ def test_model_restates_the_kernel_source():
         "const int q1 = sk_holder(p, (rel + 1) * static_cast<uint32_t>(p.total_kb) - 1, npairs);",
         "if (tc.kb0 != 0) {",
         "sk_arrive(word, p.sk_epoch, q1 - q0 + 1, aok);",
-        "gmem_wait_eq(word, (p.sk_epoch << 16) | static_cast<unsigned long long>(q1 - q0),",
+        "const unsigned long long want = (p.sk_epoch << 16) | static_cast<unsigned long long>(q1 - q0);",
+        "fok = gmem_wait_eq(word, want, abort_flag);",
         "mbar_wait(bars.skstored(), 0u, abort_flag)",
         "mbar_wait(bars.skdecided(), 0u, abort_flag)",
         "if (q == pair) continue;",

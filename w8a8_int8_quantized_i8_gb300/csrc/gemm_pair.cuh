@@ -254,9 +254,43 @@ __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CU
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.sclfull());
     }
+    // Stream-K finisher (below): one thread checks, without waiting, at the
+    // start of the piece whether every other piece's partial is already
+    // published (the usual case: those pieces open their pairs' ranges), so
+    // that the check's memory latency overlaps the MMAs; otherwise it waits
+    // after the drains.  A drain is never held back by it.
+    const bool sk_finisher = tc.partial && tc.kb0 == 0 && ew == 0 && lane == 0;
+    bool sk_decided = false;
+    auto sk_decide = [&](bool wait) {
+      const uint32_t rel = static_cast<uint32_t>(tc.tile - sk_tile0(p, npairs));
+      const int q0 = sk_holder(p, rel * static_cast<uint32_t>(p.total_kb), npairs);
+      const int q1 = sk_holder(p, (rel + 1) * static_cast<uint32_t>(p.total_kb) - 1, npairs);
+      unsigned long long* word = p.sk_arrive + 2 * tc.tile + rank;
+      const unsigned long long want = (p.sk_epoch << 16) | static_cast<unsigned long long>(q1 - q0);
+      bool fok;
+      if (wait) {
+        fok = gmem_wait_eq(word, want, abort_flag);   // bounded
+      } else {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(word) : "memory");
+        if (v != want) return;
+        fok = true;
+      }
+      // the word is complete: clear it, which nothing else does in this
+      // launch, so that a replay of the launch with the same epoch (a CUDA
+      // graph) starts at zero
+      if (fok) {
+        *reinterpret_cast<volatile unsigned long long*>(word) = 0ull;
+        fence_proxy_async_global();   // the partials are read by TMA below
+      }
+      *sk_flag = fok ? 1 : 0;
+      mbar_arrive(bars.skdecided());   // always, so no epilogue warp waits in vain
+      sk_decided = true;
+    };
     int acc[128];
 #pragma unroll
     for (int i = 0; i < 128; ++i) acc[i] = 0;
+    if (sk_finisher) sk_decide(false);
     for (int st0 = 0; st0 < nst; st0 += chunk) {
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.accfull(racc.s), racc.ph, abort_flag));
       if (!ok) break;
@@ -287,8 +321,9 @@ __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CU
       // the last item of its range) finishes the tile; every other piece is
       // the first item of its pair's range, done early.  Those pairs publish
       // their int32 partials, each in its pair's slot (a pair publishes at
-      // most once), and count themselves in the tile's arrival word.  The finisher waits until the others have all
-      // arrived, loads their partials by TMA into its own pipeline buffers
+      // most once), and count themselves in the tile's arrival word.  The
+      // finisher waits until the others have all arrived (above, while its
+      // MMAs run), loads their partials by TMA into its own pipeline buffers
       // (idle once its last item's MMAs are done), adds them to the
       // accumulator it still holds and writes the tile.
       const uint32_t rel = static_cast<uint32_t>(tc.tile - sk_tile0(p, npairs));   // tile within the region
@@ -317,20 +352,7 @@ __device__ __forceinline__ void pair_epilogue_role(const GemmParams& p, const CU
           }
         }
       } else {
-        if (ew == 0 && lane == 0) {
-          // every other piece's partial is published (bounded wait); then
-          // clear the word, so that a replay of this launch (same epoch, e.g.
-          // from a CUDA graph) starts at zero
-          const bool fok = gmem_wait_eq(word, (p.sk_epoch << 16) | static_cast<unsigned long long>(q1 - q0),
-                                        abort_flag);
-          if (fok) {
-            atomicExch(word, 0ull);
-            __threadfence();
-            fence_proxy_async_global();
-          }
-          *sk_flag = fok ? 1 : 0;
-          mbar_arrive(bars.skdecided());   // always, so no epilogue warp waits in vain
-        }
+        if (sk_finisher && !sk_decided) sk_decide(true);
         // a pair finishes at most one tile, its last item: the phase is 0
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(bars.skdecided(), 0u, abort_flag)) && *sk_flag != 0;
         if (!ok) break;
