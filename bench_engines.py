@@ -154,8 +154,13 @@ def shape_row(shape, iters, full=True):
     b = d["bias"].to(dev)
     wq, s_w = i8.quant_weight_perchannel(w)
     w16 = i8.widen_weight_codes(wq)
-    per_set = M * K * 2 + M * K + M * N * 2
-    R = max(2, min(16, -(-3 * 129 * 2**20 // max(per_set, 1))))
+    # Every set holds its own copy of the weights too: with few tokens the
+    # weights are most of the bytes, and one shared copy would stay in L2.
+    # The bytes of one call (int8 weights, the smallest) times R exceed 3 x L2.
+    per_set = M * K + N * K + M * N * 2
+    R = max(2, min(64, -(-3 * 129 * 2**20 // max(per_set, 1))))
+    wqs = [wq] + [wq.clone() for _ in range(R - 1)]
+    w16s = [w16] + [w16.clone() for _ in range(R - 1)]
     xs = [d["x"].to(dev) for _ in range(R)]
     aqs = [torch.empty(M, K, dtype=torch.int8, device=dev) for _ in range(R)]
     sas = [torch.empty(M, dtype=torch.float32, device=dev) for _ in range(R)]
@@ -167,21 +172,21 @@ def shape_row(shape, iters, full=True):
     res = {"shape": shape.name, "M": M, "K": K, "N": N, "l2_sets": R,
            "k_splits": "yes" if i8.workspace_bytes(M, N, K) else "no"}
 
-    def step(wmat):
+    def step(wmats):
         def f(i):
             r = i % R
             i8.quant_act_pertoken(xs[r], aqs[r], sas[r])
-            i8.gemm_dequant_bias_bf16(aqs[r], sas[r], wmat, s_w, b, out=ys[r], workspace=ws)
+            i8.gemm_dequant_bias_bf16(aqs[r], sas[r], wmats[r], s_w, b, out=ys[r], workspace=ws)
         return f
 
-    def gemm(wmat):
+    def gemm(wmats):
         def f(i):
             r = i % R
-            i8.gemm_dequant_bias_bf16(aqs[r], sas[r], wmat, s_w, b, out=ys[r], workspace=ws)
+            i8.gemm_dequant_bias_bf16(aqs[r], sas[r], wmats[r], s_w, b, out=ys[r], workspace=ws)
         return f
 
-    for key, fn in (("step_int8_us", step(wq)), ("gemm_int8_us", gemm(wq)),
-                    ("step_w16_us", step(w16)), ("gemm_w16_us", gemm(w16))):
+    for key, fn in (("step_int8_us", step(wqs)), ("gemm_int8_us", gemm(wqs)),
+                    ("step_w16_us", step(w16s)), ("gemm_w16_us", gemm(w16s))):
         res[key] = _time(fn, iters) * 1e6
     i8.sync_check()
     res["gemm_int8_tops"] = ops / (res["gemm_int8_us"] * 1e-6) / 1e12
@@ -189,6 +194,7 @@ def shape_row(shape, iters, full=True):
     res["step_int8_tops"] = ops / (res["step_int8_us"] * 1e-6) / 1e12
     # the E4M3 arm on the same inputs
     wq8, s_w8 = i8.quant_weight_perchannel_e4m3(w)
+    wq8s = [wq8] + [wq8.clone() for _ in range(R - 1)]
     aq8 = [torch.empty(M, K, dtype=torch.float8_e4m3fn, device=dev) for _ in range(R)]
     sa8 = [torch.empty(M, dtype=torch.float32, device=dev) for _ in range(R)]
     for r in range(R):
@@ -198,11 +204,11 @@ def shape_row(shape, iters, full=True):
     def step8(i):
         r = i % R
         i8.quant_act_pertoken_e4m3(xs[r], aq8[r], sa8[r])
-        i8.gemm_e4m3_dequant_bias_bf16(aq8[r], sa8[r], wq8, s_w8, b, out=ys[r], workspace=ws8)
+        i8.gemm_e4m3_dequant_bias_bf16(aq8[r], sa8[r], wq8s[r], s_w8, b, out=ys[r], workspace=ws8)
 
     def gemm8(i):
         r = i % R
-        i8.gemm_e4m3_dequant_bias_bf16(aq8[r], sa8[r], wq8, s_w8, b, out=ys[r], workspace=ws8)
+        i8.gemm_e4m3_dequant_bias_bf16(aq8[r], sa8[r], wq8s[r], s_w8, b, out=ys[r], workspace=ws8)
 
     res["step_e4m3_us"] = _time(step8, iters) * 1e6
     res["gemm_e4m3_us"] = _time(gemm8, iters) * 1e6
@@ -215,11 +221,11 @@ def shape_row(shape, iters, full=True):
     def step16(i):
         r = i % R
         i8.quant_act_pertoken_f16codes(xs[r], a16[r], sas[r])
-        i8.gemm_dequant_bias_bf16_f16codes(a16[r], sas[r], w16, s_w, b, out=ys[r], workspace=ws16)
+        i8.gemm_dequant_bias_bf16_f16codes(a16[r], sas[r], w16s[r], s_w, b, out=ys[r], workspace=ws16)
 
     def gemm16(i):
         r = i % R
-        i8.gemm_dequant_bias_bf16_f16codes(a16[r], sas[r], w16, s_w, b, out=ys[r], workspace=ws16)
+        i8.gemm_dequant_bias_bf16_f16codes(a16[r], sas[r], w16s[r], s_w, b, out=ys[r], workspace=ws16)
 
     res["step_f16codes_us"] = _time(step16, iters) * 1e6
     res["gemm_f16codes_us"] = _time(gemm16, iters) * 1e6
@@ -228,15 +234,16 @@ def shape_row(shape, iters, full=True):
     res["gemm_e4m3_tflops"] = ops / (res["gemm_e4m3_us"] * 1e-6) / 1e12
     res["e4m3_k_splits"] = "yes" if i8.e4m3_workspace_bytes(M, N, K) else "no"
     if full:
-        wt = w.t()
-        res["torch_bf16_us"] = _time(lambda i: torch.addmm(b, xs[i % R], wt, out=ys[i % R]), iters) * 1e6
+        wts = [w.t()] + [w.clone().t() for _ in range(R - 1)]
+        res["torch_bf16_us"] = _time(lambda i: torch.addmm(b, xs[i % R], wts[i % R], out=ys[i % R]),
+                                     iters) * 1e6
+        del wts
         if M > 16:
-            wqt = wq.t()
-            res["torch_int_mm_us"] = _time(lambda i: torch._int_mm(aqs[i % R], wqt), iters) * 1e6
+            res["torch_int_mm_us"] = _time(lambda i: torch._int_mm(aqs[i % R], wqs[i % R].t()), iters) * 1e6
         def fake(i):
             r = i % R
             a_deq = aqs[r].to(torch.bfloat16) * sas[r].to(torch.bfloat16)[:, None]
-            w_deq = wq.to(torch.bfloat16) * s_w.to(torch.bfloat16)[:, None]
+            w_deq = wqs[r].to(torch.bfloat16) * s_w.to(torch.bfloat16)[:, None]
             torch.addmm(b, a_deq, w_deq.t(), out=ys[r])
         res["fake_int8_us"] = _time(fake, iters) * 1e6
         res["torch_bf16_tflops"] = ops / (res["torch_bf16_us"] * 1e-6) / 1e12

@@ -385,8 +385,10 @@ i8_status i8_get_option(i8_option opt, int64_t* value);
  *   sms     > 0: describe the machine by hand, and the call needs no GPU:
  *           `pairs` = CTA pairs of the route's pair kernel resident at once
  *           (0 = sms / 2), `skinny_slots` = weight-streaming CTAs resident
- *           at once (0 = 2 * sms).  0: use the current device's own figures
- *           (needs the device; pairs and skinny_slots are then ignored).
+ *           at once (0 = 2 * sms; clusters of K splits are assumed to pack
+ *           those slots fully).  0: use the current device's own figures,
+ *           including how many clusters of each size fit at once (needs the
+ *           device; pairs and skinny_slots are then ignored).
  *   ws_cap  workspace bytes the plan may use (0 = unbounded; the no-alloc
  *           entry point plans with its fixed 16 MiB).
  *   out     host pointer, filled on I8_OK.

@@ -141,9 +141,12 @@ def test_quant_e4m3_every_bf16_input(orc, amax):
 # ----------------------------------------------------------------- GEMM
 GEMM_SHAPES = [(64, 128, 256), (1, 8, 16), (7, 24, 48), (129, 136, 272), (300, 520, 1040),
                (256, 256, 3072), (200, 304, 12288), (513, 264, 400),
-               # few tiles: the plan's cost model splits K (fp32 partials + ordered
-               # fix-up) for the first and third, not for the others
-               (16, 3072, 3072), (256, 9216, 3072), (1, 3072, 12288), (2, 18432, 3072)]
+               # few tokens (the weight-streaming kernel: E4M3 m16n8k32 MMAs,
+               # cluster K splits summed in a fixed order) and few tiles (the
+               # cost model splits K for the last one: fp32 partials + ordered
+               # fix-up)
+               (16, 3072, 3072), (256, 9216, 3072), (1, 3072, 12288), (2, 18432, 3072),
+               (32, 3072, 3072)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -157,7 +160,7 @@ def test_gemm_e4m3_f32_within_bound(orc, M, N, K):
     _check_acc(orc, aq, wq, c, f"{M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 3072, 3072), (1, 3072, 12288)])
+@pytest.mark.parametrize("M,N,K", [(32, 3072, 3072), (64, 3072, 12288)])
 def test_gemm_e4m3_split_k_is_deterministic(M, N, K):
     assert i8.e4m3_workspace_bytes(M, N, K) > 0          # these shapes split K
     a = torch.randint(0, 0x7E, (M, K), dtype=torch.uint8, device="cuda")
@@ -170,6 +173,36 @@ def test_gemm_e4m3_split_k_is_deterministic(M, N, K):
     with pytest.raises(i8.I8Error) as e:
         i8.gemm_e4m3_f32(a, w, workspace=ws[:-16])
     assert e.value.status == 4
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(1, 3072, 12288, 0), (5, 520, 3584, 7), (16, 136, 2560, 5),
+                                           (3, 200, 8192, 8)])
+def test_gemm_e4m3_few_tokens(orc, M, N, K, splits):
+    """Few tokens take the weight-streaming kernel: no workspace, the
+    accumulators within the bound, the same bits on every call (the K splits
+    of a cluster are summed in a fixed order), and bf16 outputs equal to the
+    oracle's epilogue of those accumulators."""
+    shape = inputs.LinearShape("t", M, K, N, seed=M + K, outliers=True)
+    d = inputs.linear_inputs(shape)
+    aq, s_a = i8.quant_act_pertoken_e4m3(to_dev(d["x"]))
+    wq, s_w = i8.quant_weight_perchannel_e4m3(to_dev(d["w"]))
+    i8.set_option("force_splits", splits)
+    try:
+        p = i8.plan_query(M, N, K, "e4m3")
+        assert p["kernel"] == "skinny" and p["ws_bytes"] == 0
+        if splits:
+            assert p["splits"] == splits
+        assert i8.e4m3_workspace_bytes(M, N, K) == 0
+        c = i8.gemm_e4m3_f32(aq, wq)
+        c2 = i8.gemm_e4m3_f32(aq, wq)
+        y = i8.gemm_e4m3_dequant_bias_bf16(aq, s_a, wq, s_w, to_dev(d["bias"]))
+        i8.sync_check()
+    finally:
+        i8.set_option("force_splits", 0)
+    assert torch.equal(c.view(torch.int32), c2.view(torch.int32))
+    exact, P, got = _check_acc(orc, aq, wq, c, f"{M}x{N}x{K} splits {splits}")
+    _check_bf16(orc, gpu_bf16_bits(y), exact, P, got, s_a.cpu().numpy(), s_w.cpu().numpy(),
+                inputs.bits(d["bias"]), K, f"{M}x{N}x{K} splits {splits}")
 
 
 def test_gemm_e4m3_closed_forms(orc):

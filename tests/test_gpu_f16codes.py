@@ -37,8 +37,10 @@ def test_quant_f16codes_are_the_int8_codes(orc, M, K):
 
 SHAPES = [(64, 128, 256), (1, 8, 16), (7, 24, 48), (129, 136, 272), (256, 384, 1024),
           (300, 200, 1040), (1024, 1024, 4096), (513, 264, 400),
-          # few tiles: the plan splits K (exact int32 partials)
-          (2, 9216, 3072), (16, 3072, 12288), (256, 3072, 3072)]
+          # few tokens: the weight-streaming kernel with fp16-held codes on
+          # both sides (cluster K splits); few tiles: the plan splits K
+          # (exact int32 partials)
+          (2, 9216, 3072), (16, 3072, 12288), (256, 3072, 3072), (32, 9216, 3072)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -94,9 +96,9 @@ def test_linear_f16codes_matches_oracle_and_int8_path(orc, M, N, K, bias):
 
 
 def test_f16codes_workspace_errors():
-    a = torch.zeros(2, 3072, dtype=torch.float16, device="cuda")
+    a = torch.zeros(32, 3072, dtype=torch.float16, device="cuda")
     w = torch.zeros(9216, 3072, dtype=torch.float16, device="cuda")
-    need = i8.f16codes_workspace_bytes(2, 9216, 3072)
+    need = i8.f16codes_workspace_bytes(32, 9216, 3072)
     assert need > 0
     with pytest.raises(i8.I8Error) as e:
         i8.gemm_int32_f16codes(a, w, workspace=torch.empty(need - 16, dtype=torch.uint8, device="cuda"))
@@ -125,3 +127,21 @@ def test_f16codes_forced_splits_exact(orc, splits):
     assert np.array_equal(c.cpu().numpy(), orc.gemm_s32(a.numpy(), w.numpy()))
     want = orc.linear(inputs.bits(d["x"]), inputs.bits(d["w"]), inputs.bits(d["bias"]))["y"]
     assert_bf16_exact(gpu_bf16_bits(y), want, f"splits {splits}")
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(1, 200, 8192, 8), (7, 520, 3584, 7), (16, 136, 2560, 5)])
+def test_f16codes_few_tokens_exact(orc, M, N, K, splits):
+    """Few tokens with fp16-held codes on both sides take the weight-streaming
+    kernel (forced cluster splits included): the oracle's int32 sums, no
+    workspace."""
+    a = inputs.random_int8(M, K, seed=M + 7)
+    w = inputs.random_int8(N, K, seed=N + 9)
+    i8.set_option("force_splits", splits)
+    try:
+        p = i8.plan_query(M, N, K, "f16codes")
+        assert (p["kernel"], p["splits"], p["ws_bytes"]) == ("skinny", splits, 0)
+        c = i8.gemm_int32_f16codes(to_dev(a).half(), to_dev(w).half())
+        i8.sync_check()
+    finally:
+        i8.set_option("force_splits", 0)
+    assert np.array_equal(c.cpu().numpy(), orc.gemm_s32(a.numpy(), w.numpy()))

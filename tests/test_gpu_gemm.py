@@ -218,20 +218,27 @@ def test_gemm_int32_both_kernels(orc, cta_pair_option, mode, M, N, K):
     assert bad.size == 0, f"mode {mode}: {len(bad)} mismatches, first {bad[:4].tolist()}"
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 200, 8192), (16, 520, 8192), (9, 64, 131072)])
-def test_skinny_kernel_adversarial_exact(orc, M, N, K):
+@pytest.mark.parametrize("M,N,K,splits", [(1, 200, 8192, 0), (16, 520, 8192, 0), (9, 64, 131072, 0),
+                                           (1, 200, 8192, 1), (16, 520, 8192, 1), (3, 64, 6144, 1)])
+def test_skinny_kernel_adversarial_exact(orc, M, N, K, splits):
     """Few tokens take the weight-streaming kernel (forced up to M = 16 here):
-    each warp's fp32 chains over 512 K of its half-stages (< 2^24 for +-127
-    operands) drained into int32, then integer adds across warps and K
-    splits."""
+    each warp's fp32 accumulators gather 16-K MMA partials over 8 stages (16
+    partials of at most 16 * 127^2 for +-127 operands, < 2^22) and drain into
+    int32, then integer adds across warps and K splits.  One split: whole
+    drain windows in one CTA (8192 K: four; 6144 K: two and a short one)."""
     a, w = _adversarial(max(M, 4), N, K, seed=M + N)
     a = a[:M].contiguous()
     i8.set_option("skinny_max_m", 16)
+    i8.set_option("force_splits", splits)
     try:
+        assert i8.plan_query(M, N, K, "int8")["kernel"] == "skinny"
+        if splits:
+            assert i8.plan_query(M, N, K, "int8")["splits"] == splits
         c = i8.gemm_int32(to_dev(a), to_dev(w))
         i8.sync_check()
     finally:
         i8.set_option("skinny_max_m", SKINNY_DEFAULT)
+        i8.set_option("force_splits", 0)
     got = c.cpu().numpy()
     want = orc.gemm_s32(a.numpy(), w.numpy())
     bad = np.argwhere(got != want)
@@ -405,7 +412,7 @@ def test_stream_k_workspace_garbage_and_graph_replay(stream_k_option):
     i8.sync_check()
 
 
-@pytest.mark.parametrize("M,N,K,splits", [(2, 9216, 3072, 0), (5, 3072, 12288, 0), (1, 200, 8192, 8),
+@pytest.mark.parametrize("M,N,K,splits", [(2, 3072, 3072, 0), (5, 3072, 12288, 0), (1, 200, 8192, 8),
                                            (7, 520, 3584, 7), (3, 64, 1280, 3), (16, 136, 2560, 5)])
 def test_skinny_cluster_splits_back_to_back_and_graph_replay(orc, M, N, K, splits):
     """The few-token kernel's K splits meet in the distributed shared memory

@@ -187,9 +187,14 @@ def test_capped_workspace_plans_fit_the_cap():
 def test_direct_splits_minimise_the_cost_model():
     """Direct plans: no split while the 256 x 256 tiles fill every pair;
     otherwise the chosen split count has the lowest modelled time among the
-    counts with at least 4 K blocks per split."""
+    counts with at least 4 K blocks per split.  (Up to 16 tokens both routes
+    take the weight-streaming kernel instead.)"""
     for route in ("f16codes", "e4m3"):
-        for M in (1, 8, 64, 256, 512, 1024, 4096):
+        for M in (1, 8):
+            for N in (768, 3072, 9216):
+                p = i8.plan_query(M, N, 3072, route, **GB300)
+                assert p["kernel"] == "skinny" and p["ws_bytes"] == 0 and p["block_k"] == 256
+        for M in (17, 64, 256, 512, 1024, 4096):
             for N in (768, 3072, 9216):
                 for K in (512, 3072, 12288):
                     i8.set_option("force_splits", 0)
@@ -280,7 +285,7 @@ def test_bench_workloads():
     down = i8.plan_query(8704, 3072, 12288, "int8", **GB300)
     assert (down["kernel"], down["splits"], down["n_fastest"], down["sk_waves"]) == ("pair_stream_k", 1, 1, 5)
     one = i8.plan_query(1, 9216, 3072, "int8", **GB300)
-    assert (one["kernel"], one["splits"], one["grid"]) == ("skinny", 2, 288)
+    assert (one["kernel"], one["splits"], one["grid"]) == ("skinny", 1, 144)
 
 
 def test_plan_query_errors():
@@ -306,3 +311,33 @@ def test_plan_query_errors():
         i8.plan_query(64, 64, 100, "int8", sms=152)
     with pytest.raises(KeyError):
         i8.plan_query(64, 64, 64, "int4", sms=152)
+
+
+def test_skinny_split_rule():
+    """Few tokens: no K split while the N-blocks of 64 weight rows occupy at
+    least 90 % of the SMs; otherwise the fewest splits that give every SM a
+    CTA, at most 8 and with at least 4 stages (1024 K) each, lowered until
+    the grid fits the resident CTA slots (a machine described by hand: its
+    clusters assumed to pack those slots fully)."""
+    n = 0
+    for m in (GB300, dict(sms=152, pairs=74, skinny_slots=152), dict(sms=20, pairs=9, skinny_slots=40)):
+        sms, slots = m["sms"], m["skinny_slots"]
+        for route in ("int8", "w16", "f16codes", "e4m3"):
+            for M in (1, 16):
+                for N in (64, 768, 3072, 6144, 8704, 9216, 18432):
+                    for K in (256, 1024, 3072, 12288):
+                        p = i8.plan_query(M, N, K, route, **m)
+                        assert p["kernel"] == "skinny"
+                        B, st = -(-N // 64), -(-K // 256)
+                        want = 1
+                        if 10 * B < 9 * sms:
+                            want = min(-(-sms // B), max(1, st // 4), 8)
+                            while want > 1 and B * want > slots:
+                                want -= 1
+                        per = -(-st // want)
+                        assert (p["splits"], p["kb_per_split"]) == (-(-st // per), per), (m, M, N, K)
+                        n += 1
+    assert n == 3 * 4 * 2 * 7 * 4
+    # the measured cases on GB300 figures (two CTAs per SM)
+    assert i8.plan_query(1, 3072, 12288, "int8", **GB300)["splits"] == 4
+    assert i8.plan_query(1, 9216, 3072, "int8", **GB300)["splits"] == 1

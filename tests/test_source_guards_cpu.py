@@ -128,7 +128,7 @@ def test_tma_inner_coordinates_are_16_byte_multiples():
     and output column starts (64 bf16 or 32 int32 columns from a multiple of
     128), and the stream-K partial reloads (32 int32 columns from a multiple
     of 128)."""
-    allowed_x = {"kb * Cfg::BK8", "k16", "kb * Cfg::BK", "k0 + b * Cfg::BOX_K", "k0 + b * 128",
+    allowed_x = {"kb * Cfg::BK8", "k16", "kb * Cfg::BK", "k0 + b * Cfg::BOX_K", "k0 + b * Cfg::A_BOX_K",
                  "(ks0 + i) * kSkinnyK + b * Cfg::BOX_K", "(ks0 + i + Cfg::STAGES) * kSkinnyK + b * Cfg::BOX_K",
                  "nb", "n0 + g * 32", "n0 + g * 64", "n_loc + 32 * g"}
     calls = 0
@@ -150,7 +150,8 @@ def test_tma_inner_coordinates_are_16_byte_multiples():
     assert "static constexpr int BK = KIND == kDirectF16 ? 64 : 128;" in direct
     assert "constexpr int kSkinnyK = 256;" in skinny
     assert "const int k0 = (ks0 + i) * kSkinnyK;" in skinny
-    assert "static constexpr int BOX_K = W16 ? 64 : 128;" in skinny
+    assert "static constexpr int BOX_K = W_F16 ? 64 : 128;" in skinny
+    assert "static constexpr int A_BOX_K = A_F16 ? 64 : 128;" in skinny
     assert "const int k16 = kb * Cfg::BK8 + h * Cfg::BK16;" in gemm
     assert "const int k16 = kb * Cfg::BK8 + (h + q) * Cfg::BK16;" in pair
     assert "const int nb = n0 + g * 64;" in gemm

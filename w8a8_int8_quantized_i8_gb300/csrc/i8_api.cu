@@ -421,6 +421,61 @@ int tile_order_n_fastest(int64_t M, int64_t N) {
   return M > N ? 1 : 0;
 }
 
+// Few tokens: the weight-streaming kernel (any code format), which measured
+// 1.4-2.2x faster than the tiled kernels with K splits at every M <= 16 of
+// the DiT sweep (e.g. 16 x 3072 x 9216: 10.4 against 20.1 us; 8 x 3072 x
+// 18432: 13.2 against 27.6 us).
+// What one few-token kernel variant can hold on the device at once: its
+// resident CTA slots, and for each cluster size s the clusters of s CTAs
+// resident together (0 where unknown: slots / s).  A cluster sits within one
+// GPC, so with one CTA per SM fewer fit than slots / s (GB300, 152 SMs, one
+// CTA per SM: 46 clusters of 3, 36 of 4, 15 of 8).
+struct SkinnyFit {
+  int slots = 0;
+  int clusters[kSkinnyMaxSplits + 1] = {};
+  int cap(int s) const { return clusters[s] > 0 ? clusters[s] : slots / s; }
+};
+
+void plan_skinny(Plan& p, int64_t M, int64_t N, int64_t K, int sms, const SkinnyFit& fit) {
+  (void)M;
+  // K splits, when the N-blocks leave more than a tenth of the SMs idle:
+  // the fewest that give every SM a CTA, as long as all CTAs are resident
+  // at once (within the CTA slots, and the N-blocks' clusters within the
+  // clusters that fit; a second wave would stream its weights only after
+  // the first finished) and every split owns at least kSkinnyMinStages
+  // whole 256-K stages.  One N-block's splits form a cluster of at most
+  // kSkinnyMaxSplits CTAs.  No workspace: the splits add their partials
+  // over distributed shared memory.
+  // Measured (GB300, graph replay, weights rotating past L2; M x K x N):
+  //   * 1 x 12288 x 3072 int8 codes: 23.2 / 13.1 / 13.2 / 11.1 / 10.6 /
+  //     14.3 / 14.8 us with 1 / 2 / 3 / 4 / 5 / 6 / 8 splits (6 and 8: the
+  //     48 clusters no longer fit at once; 3: one CTA per SM, and one CTA
+  //     alone streams no faster than about 25 GB/s);
+  //   * 16 x 12288 x 3072 fp16-held codes (one CTA per SM): 29.6 / 18.8 /
+  //     27.2 / 22.8 us with 1 / 2 / 3 / 4 splits (46 clusters of 3 fit);
+  //   * 144 N-blocks (1 x 3072 x 9216): 8.1 / 8.3 us (int8), 7.2 / 8.2 us
+  //     (E4M3) with 1 / 2 splits.
+  p.skinny = true;
+  p.num_n = static_cast<int>((N + kSkinnyRows - 1) / kSkinnyRows);
+  p.num_m = 1;
+  const int stages = static_cast<int>((K + kSkinnyK - 1) / kSkinnyK);
+  int splits = 1;
+  if (g_opt.force_splits > 0) {
+    splits = g_opt.force_splits;
+  } else if (10LL * p.num_n < 9LL * sms) {
+    splits = std::min((sms + p.num_n - 1) / p.num_n, std::max(1, stages / kSkinnyMinStages));
+    splits = std::min(splits, kSkinnyMaxSplits);
+    while (splits > 1 &&
+           (static_cast<int64_t>(p.num_n) * splits > fit.slots || p.num_n > fit.cap(splits)))
+      --splits;
+  }
+  splits = std::max(1, std::min(std::min(splits, stages), kSkinnyMaxSplits));
+  p.kb_per_split = (stages + splits - 1) / splits;          // stages per split
+  p.splits = (stages + p.kb_per_split - 1) / p.kb_per_split;
+  p.total_kb = stages;
+  p.grid = p.num_n * p.splits;
+}
+
 // Shape -> configuration (replaces per-shape autotuning).
 //   * few tokens (M <= 16 by default): the weight-streaming kernel;
 //   * CTA pairs (one 256 x 256 tile per cluster of two SMs, each SM staging
@@ -433,44 +488,14 @@ int tile_order_n_fastest(int64_t M, int64_t N) {
 //   * the tile order from tile_order_n_fastest (M blocks fastest under
 //     stream-K unless the raster option sets it), applied by the caller.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters = 0,
-               bool b16 = false, size_t ws_cap = SIZE_MAX, int skinny_slots = 0) {
+               bool b16 = false, size_t ws_cap = SIZE_MAX, SkinnyFit fit = SkinnyFit()) {
   Plan p;
   p.n_fastest = tile_order_n_fastest(M, N);
   if (pair_clusters <= 0) pair_clusters = sms / 2;
-  if (skinny_slots <= 0) skinny_slots = 2 * sms;
+  if (fit.slots <= 0) fit.slots = 2 * sms;
   p.total_kb = static_cast<int>((K + 127) / 128);
-  // Few tokens: the weight-streaming kernel, which measured 1.4-2.2x faster
-  // than the tiled kernels with K splits at every M <= 16 of the DiT sweep
-  // (e.g. 16 x 3072 x 9216: 10.4 against 20.1 us; 8 x 3072 x 18432: 13.2
-  // against 27.6 us).
   if (M <= g_opt.skinny_max_m) {
-    // K splits: the fewest that give every SM a CTA, as long as the grid
-    // stays within the resident CTA slots (skinny_slots; a second wave would
-    // stream its weights only after the first finished) and every split owns
-    // at least kSkinnyMinStages whole 256-K stages.  One N-block's splits
-    // form a cluster of at most kSkinnyMaxSplits CTAs.  No workspace: the
-    // splits add their partials over distributed shared memory.
-    // Measured (GB300, 1 token, back-to-back calls): 1 x 3072 x 3072 7.5 /
-    // 6.1 / 5.8 / 5.7 / 9.3 us with 1 / 2 / 3 / 4 / 6 splits; 1 x 3072 x
-    // 12288 24.8 / 15.3 / 15.0 / 12.6 / 16.6 us with 1 / 2 / 3 / 4 / 6 (with
-    // 3 the clusters pack two CTAs on some SMs and leave others idle); grids
-    // beyond the resident slots cost 40-60 %.
-    p.skinny = true;
-    p.num_n = static_cast<int>((N + kSkinnyRows - 1) / kSkinnyRows);
-    p.num_m = 1;
-    const int stages = static_cast<int>((K + kSkinnyK - 1) / kSkinnyK);
-    int splits;
-    if (g_opt.force_splits > 0) {
-      splits = g_opt.force_splits;
-    } else {
-      splits = std::min((sms + p.num_n - 1) / p.num_n, std::max(1, stages / kSkinnyMinStages));
-      while (splits > 1 && p.num_n * splits > skinny_slots) --splits;
-    }
-    splits = std::max(1, std::min(std::min(splits, stages), kSkinnyMaxSplits));
-    p.kb_per_split = (stages + splits - 1) / splits;          // stages per split
-    p.splits = (stages + p.kb_per_split - 1) / p.kb_per_split;
-    p.total_kb = stages;
-    p.grid = p.num_n * p.splits;
+    plan_skinny(p, M, N, K, sms, fit);
     return p;
   }
   const bool pair_ok = M >= 256 && N >= 256;
@@ -649,49 +674,82 @@ i8_status launch_pair_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const CU
                                 my, mp, gp));
 }
 
-// The skinny kernel for fp16-code weights (W16) and MT groups of 8 tokens:
-// its shared-memory size is set once per device (slots 4..7 of smem_set).
-template <bool W16, int MT>
+// The skinny kernel for the code formats KIND (SkinnyKind) and MT groups of
+// 8 tokens: its shared-memory size is set once per device (slots 4..11 of
+// smem_set).
+template <int KIND, int MT>
 bool skinny_prepare(DeviceInfo* d) {
-  const int slot = 4 + 2 * (W16 ? 1 : 0) + (MT - 1);
+  const int slot = 4 + 2 * KIND + (MT - 1);
   if (!d->smem_set[slot]) {
-    if (cudaFuncSetAttribute(gemm_skinny_kernel<W16, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SkinnyCfg<W16, MT>::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_skinny_kernel<KIND, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SkinnyCfg<KIND, MT>::SMEM_BYTES) != cudaSuccess)
       return false;
     d->smem_set[slot] = true;
   }
   return true;
 }
 
-// CTAs of one skinny kernel variant resident at once on this device (its
-// split choice keeps the grid within one wave).
-template <bool W16, int MT>
-int skinny_slots_of(DeviceInfo* d) {
-  static int cached[kMaxDevices] = {};
+// CTA slots and cluster capacities of one skinny kernel variant on this
+// device (its split choice keeps the grid within one wave), queried once.
+template <int KIND, int MT>
+SkinnyFit skinny_fit_of(DeviceInfo* d) {
+  static SkinnyFit cached[kMaxDevices];
+  static std::atomic<int> ready[kMaxDevices];
+  static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return d->sms;
-  if (cached[dev] > 0) return cached[dev];
-  int n = 0;
-  cudaError_t e = cudaErrorInvalidValue;
-  if (skinny_prepare<W16, MT>(d))
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_skinny_kernel<W16, MT>,
-                                                      SkinnyCfg<W16, MT>::THREADS,
-                                                      SkinnyCfg<W16, MT>::SMEM_BYTES);
-  cudaGetLastError();
-  if (e != cudaSuccess || n <= 0) n = 1;
-  cached[dev] = n * d->sms;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    SkinnyFit f;
+    f.slots = d->sms;
+    return f;
+  }
+  if (ready[dev].load(std::memory_order_acquire)) return cached[dev];
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ready[dev].load(std::memory_order_relaxed)) {
+    SkinnyFit f;
+    int n = 0;
+    if (skinny_prepare<KIND, MT>(d)) {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_skinny_kernel<KIND, MT>,
+                                                        SkinnyCfg<KIND, MT>::THREADS,
+                                                        SkinnyCfg<KIND, MT>::SMEM_BYTES) != cudaSuccess)
+        n = 0;
+      for (int s = 1; s <= kSkinnyMaxSplits; ++s) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(s, 1, 1);
+        cfg.blockDim = dim3(SkinnyCfg<KIND, MT>::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = SkinnyCfg<KIND, MT>::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = s;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, gemm_skinny_kernel<KIND, MT>, &cfg) != cudaSuccess) c = 0;
+        f.clusters[s] = c;
+      }
+    }
+    cudaGetLastError();
+    f.slots = (n > 0 ? n : 1) * d->sms;
+    cached[dev] = f;
+    ready[dev].store(1, std::memory_order_release);
+  }
   return cached[dev];
 }
-int skinny_slots(DeviceInfo* d, bool b16, int64_t M) {
-  if (M > 8) return b16 ? skinny_slots_of<true, 2>(d) : skinny_slots_of<false, 2>(d);
-  return b16 ? skinny_slots_of<true, 1>(d) : skinny_slots_of<false, 1>(d);
+template <int KIND>
+SkinnyFit skinny_fit_k(DeviceInfo* d, int64_t M) {
+  return M > 8 ? skinny_fit_of<KIND, 2>(d) : skinny_fit_of<KIND, 1>(d);
+}
+SkinnyFit skinny_fit(DeviceInfo* d, bool b16, int64_t M) {
+  return b16 ? skinny_fit_k<kSkW16>(d, M) : skinny_fit_k<kSkI8>(d, M);
 }
 
-template <bool W16, int MT>
+template <int KIND, int MT>
 cudaError_t launch_skinny(DeviceInfo* d, const CUtensorMap& mw, const CUtensorMap& ma,
                           const SkinnyParams& sp, int grid, cudaStream_t st) {
-  using Cfg = SkinnyCfg<W16, MT>;
-  if (!skinny_prepare<W16, MT>(d)) return cudaErrorInvalidValue;
+  using Cfg = SkinnyCfg<KIND, MT>;
+  if (!skinny_prepare<KIND, MT>(d)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(Cfg::THREADS);
@@ -711,7 +769,43 @@ cudaError_t launch_skinny(DeviceInfo* d, const CUtensorMap& mw, const CUtensorMa
   }
   cfg.attrs = attr;
   cfg.numAttrs = static_cast<unsigned>(n);
-  return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<W16, MT>, mw, ma, sp);
+  return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<KIND, MT>, mw, ma, sp);
+}
+
+// The few-token route for any code format: tensor maps of the weights and
+// the token codes, then one launch (the plan from plan_skinny).  out_mode
+// kOutInt32 writes the raw accumulator: int32, or fp32 for E4M3.
+template <int KIND>
+i8_status skinny_route(DeviceInfo* d, const Plan& pl, const void* aq, const void* wb, int64_t M,
+                       int64_t N, int64_t K, int out_mode, void* out, int64_t ldo,
+                       const float* s_a, const float* s_w, const void* bias, cudaStream_t st) {
+  constexpr bool W_F16 = SkinnyCfg<KIND, 1>::W_F16;
+  constexpr bool A_F16 = SkinnyCfg<KIND, 1>::A_F16;
+  CUtensorMap mw, ma;
+  if (!encode_2d(&mw, W_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, K, N,
+                 W_F16 ? 2 * K : K, W_F16 ? 64 : 128, kSkinnyRows))
+    return I8_ERR_CUDA;
+  const int mt = M > 8 ? 2 : 1;   // token groups of 8 (M <= 16)
+  if (!encode_2d(&ma, A_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M,
+                 A_F16 ? 2 * K : K, A_F16 ? 64 : 128, 8 * mt))
+    return I8_ERR_CUDA;
+  SkinnyParams sp{};
+  sp.M = static_cast<int>(M);
+  sp.N = static_cast<int>(N);
+  sp.K = static_cast<int>(K);
+  sp.num_ks = pl.total_kb;
+  sp.ks_per_cta = pl.kb_per_split;
+  sp.splits = pl.splits;
+  sp.out_mode = out_mode;
+  sp.s_a = s_a;
+  sp.s_w = s_w;
+  sp.bias = static_cast<const uint16_t*>(bias);
+  sp.out = out;
+  sp.ldo = ldo;
+  const cudaError_t le = mt == 2 ? launch_skinny<KIND, 2>(d, mw, ma, sp, pl.grid, st)
+                                 : launch_skinny<KIND, 1>(d, mw, ma, sp, pl.grid, st);
+  if (le != cudaSuccess) return cuda_status(le);
+  return cuda_status(cudaGetLastError());
 }
 
 using PairConv = PairCfg<3, 3, true, true>;    // int8 weights, CTA pair, 64-K fp16 stages
@@ -758,45 +852,14 @@ i8_status gemm_common(const int8_t* aq, const void* wb, bool b16, int64_t M, int
   if (i8_status e = device_info(&d, nullptr)) return e;
   const int clusters = b16 ? wide_pair_clusters(d)
                            : conv_pair_clusters(d);
-  const Plan pl = make_plan(M, N, K, d->sms, clusters, b16, ws_cap, skinny_slots(d, b16, M));
+  const Plan pl = make_plan(M, N, K, d->sms, clusters, b16, ws_cap, skinny_fit(d, b16, M));
   if (pl.ws_bytes > 0) {
     if (!ws || ws_bytes < pl.ws_bytes) return I8_ERR_WORKSPACE;
     if (!aligned16(ws)) return I8_ERR_ALIGNMENT;
   }
-  if (pl.skinny) {
-    CUtensorMap mw, ma;
-    if (b16) {
-      if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wb, K, N, 2 * K, 64, kSkinnyRows))
-        return I8_ERR_CUDA;
-    } else {
-      if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, K, N, K, 128, kSkinnyRows))
-        return I8_ERR_CUDA;
-    }
-    const int mt = M > 8 ? 2 : 1;   // token groups of 8 (M <= 16)
-    if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M, K, 128, 8 * mt)) return I8_ERR_CUDA;
-    SkinnyParams sp{};
-    sp.M = static_cast<int>(M);
-    sp.N = static_cast<int>(N);
-    sp.K = static_cast<int>(K);
-    sp.num_ks = pl.total_kb;
-    sp.ks_per_cta = pl.kb_per_split;
-    sp.splits = pl.splits;
-    sp.out_mode = out_mode;
-    sp.s_a = s_a;
-    sp.s_w = s_w;
-    sp.bias = static_cast<const uint16_t*>(bias);
-    sp.out = out;
-    sp.ldo = ldo;
-    cudaError_t le;
-    if (b16)
-      le = mt == 2 ? launch_skinny<true, 2>(d, mw, ma, sp, pl.grid, st)
-                   : launch_skinny<true, 1>(d, mw, ma, sp, pl.grid, st);
-    else
-      le = mt == 2 ? launch_skinny<false, 2>(d, mw, ma, sp, pl.grid, st)
-                   : launch_skinny<false, 1>(d, mw, ma, sp, pl.grid, st);
-    if (le != cudaSuccess) return cuda_status(le);
-    return cuda_status(cudaGetLastError());
-  }
+  if (pl.skinny)
+    return b16 ? skinny_route<kSkW16>(d, pl, aq, wb, M, N, K, out_mode, out, ldo, s_a, s_w, bias, st)
+               : skinny_route<kSkI8>(d, pl, aq, wb, M, N, K, out_mode, out, ldo, s_a, s_w, bias, st);
   CUtensorMap ma, mb;
   const uint32_t bn = pl.pair ? 128u : static_cast<uint32_t>(pl.bn);
   if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, K, M, K, 128, 128)) return I8_ERR_CUDA;
@@ -995,6 +1058,13 @@ i8_status gemm_direct_common(const void* aq, const void* wq, int64_t M, int64_t 
   if (out_mode != kOutBf16 && ldo % 4 != 0) return I8_ERR_ALIGNMENT;
   DeviceInfo* d;
   if (i8_status e = device_info(&d, nullptr)) return e;
+  if (M <= g_opt.skinny_max_m) {
+    // few tokens: the weight-streaming kernel, no workspace
+    constexpr int SK = KIND == kDirectF16 ? kSkF16 : kSkE4M3;
+    Plan sp;
+    plan_skinny(sp, M, N, K, d->sms, skinny_fit_k<SK>(d, M));
+    return skinny_route<SK>(d, sp, aq, wq, M, N, K, out_mode, out, ldo, s_a, s_w, bias, st);
+  }
   const int clusters = direct_cluster_capacity<KIND>(d);
   const DirectPlan pl = plan_direct(M, N, K, clusters, Cfg::BK);
   if (pl.tiles * pl.splits > INT32_MAX) return I8_ERR_UNSUPPORTED;
@@ -1140,6 +1210,7 @@ size_t i8_gemm_e4m3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   I8_NVTX();
   if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX)
     return 0;
+  if (M <= g_opt.skinny_max_m) return 0;   // the weight-streaming kernel needs none
   DeviceInfo* d;
   if (device_info(&d, nullptr) != I8_OK) return 0;
   return plan_direct(M, N, K, direct_cluster_capacity<kDirectE4M3>(d),
@@ -1176,6 +1247,7 @@ size_t i8_gemm_f16codes_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   I8_NVTX();
   if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX)
     return 0;
+  if (M <= g_opt.skinny_max_m) return 0;   // the weight-streaming kernel needs none
   DeviceInfo* d;
   if (device_info(&d, nullptr) != I8_OK) return 0;
   return plan_direct(M, N, K, direct_cluster_capacity<kDirectF16>(d),
@@ -1224,9 +1296,9 @@ size_t i8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (device_info(&d, nullptr) != I8_OK) return 0;
   // the larger of the two weight formats' plans, so one query serves both
   const size_t a = make_plan(M, N, K, d->sms, conv_pair_clusters(d), false,
-                             SIZE_MAX, skinny_slots(d, false, M)).ws_bytes;
+                             SIZE_MAX, skinny_fit(d, false, M)).ws_bytes;
   const size_t b = make_plan(M, N, K, d->sms, wide_pair_clusters(d), true,
-                             SIZE_MAX, skinny_slots(d, true, M)).ws_bytes;
+                             SIZE_MAX, skinny_fit(d, true, M)).ws_bytes;
   return a > b ? a : b;
 }
 
@@ -1265,7 +1337,7 @@ i8_status i8_gemm_dequant_bias_bf16_noalloc(const int8_t* aq, const float* s_a, 
     DeviceInfo* d;
     if (i8_status e = device_info(&d, nullptr)) return e;
     if (make_plan(M, N, K, d->sms, conv_pair_clusters(d), false, kStaticWsBytes,
-                  skinny_slots(d, false, M))
+                  skinny_fit(d, false, M))
             .ws_bytes > kStaticWsBytes)
       return I8_ERR_WORKSPACE;
     if (i8_status e = static_ws_address(&ws)) return e;
@@ -1391,6 +1463,9 @@ i8_status i8_plan_query(int64_t M, int64_t N, int64_t K, i8_route route, int sms
     return I8_ERR_INVALID_ARG;
   if (K % 16 != 0 || K > 131072 || M > INT32_MAX || N > INT32_MAX) return I8_ERR_UNSUPPORTED;
   const bool b16 = route == I8_ROUTE_W16;
+  // a machine described by hand: clusters assumed to pack the slots fully
+  SkinnyFit fit;
+  fit.slots = skinny_slots_in;
   if (sms == 0) {
     DeviceInfo* d;
     if (i8_status e = device_info(&d, nullptr)) return e;
@@ -1399,12 +1474,31 @@ i8_status i8_plan_query(int64_t M, int64_t N, int64_t K, i8_route route, int sms
             : route == I8_ROUTE_F16CODES ? direct_cluster_capacity<kDirectF16>(d)
             : b16                        ? wide_pair_clusters(d)
                                          : conv_pair_clusters(d);
-    skinny_slots_in = skinny_slots(d, b16, M);
+    fit = route == I8_ROUTE_E4M3       ? skinny_fit_k<kSkE4M3>(d, M)
+          : route == I8_ROUTE_F16CODES ? skinny_fit_k<kSkF16>(d, M)
+                                       : skinny_fit(d, b16, M);
   }
+  if (fit.slots <= 0) fit.slots = 2 * sms;
   if (pairs == 0) pairs = std::max(1, sms / 2);
   i8_plan_info r{};
   r.n_fastest = tile_order_n_fastest(M, N);
-  if (route == I8_ROUTE_F16CODES || route == I8_ROUTE_E4M3) {
+  const bool direct_route = route == I8_ROUTE_F16CODES || route == I8_ROUTE_E4M3;
+  if (direct_route && M <= g_opt.skinny_max_m) {
+    // few tokens: the weight-streaming kernel, as on the int8 routes
+    Plan pl;
+    plan_skinny(pl, M, N, K, sms, fit);
+    r.kernel = I8_KERNEL_SKINNY;
+    r.tile_m = static_cast<int>(M);
+    r.tile_n = kSkinnyRows;
+    r.num_m = 1;
+    r.num_n = pl.num_n;
+    r.block_k = kSkinnyK;
+    r.total_kb = pl.total_kb;
+    r.splits = pl.splits;
+    r.kb_per_split = pl.kb_per_split;
+    r.grid = pl.grid;
+    r.ws_bytes = 0;
+  } else if (direct_route) {
     const int bk = route == I8_ROUTE_E4M3 ? DirectCfg<kDirectE4M3>::BK : DirectCfg<kDirectF16>::BK;
     const DirectPlan pl = plan_direct(M, N, K, pairs, bk);
     if (pl.tiles * pl.splits > INT32_MAX) return I8_ERR_UNSUPPORTED;
@@ -1421,7 +1515,7 @@ i8_status i8_plan_query(int64_t M, int64_t N, int64_t K, i8_route route, int sms
     r.model_us = direct_plan_us(pl.tiles, pairs, pl.total_kb, pl.splits, M, N);
   } else {
     const Plan pl = make_plan(M, N, K, sms, pairs, b16, ws_cap ? ws_cap : SIZE_MAX,
-                              skinny_slots_in);
+                              fit);
     r.num_m = pl.num_m;
     r.num_n = pl.num_n;
     r.total_kb = pl.total_kb;

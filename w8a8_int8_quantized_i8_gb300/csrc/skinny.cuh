@@ -3,7 +3,10 @@
 // Same operation as gemm.cuh (Fused INT8 GEMM Kernel for Ideogram 4.0, arXiv
 // 2606.14598, abstract: int8 x int8 -> int32, per-token x per-channel dequant
 // + bias -> bf16), for the skinny shapes where the weights dominate the bytes
-// and the 128-row tensor-core tiles would be almost empty.
+// and the 128-row tensor-core tiles would be almost empty.  KIND selects the
+// code formats: int8 weights and tokens; fp16-held weight codes with int8
+// tokens; fp16-held codes on both sides (all three exact, int32); or E4M3 on
+// both sides (the FP8 arm, fp32 accumulation, m16n8k32 E4M3 MMAs).
 //
 //   * A CTA owns 64 weight rows (an N-block) and a range of whole 256-K
 //     stages.  The S <= 8 CTAs that split one N-block's K form a thread-block
@@ -15,17 +18,20 @@
 //     past its end) arrive as zeros and add nothing.  The weights of the
 //     first fill are prefetched into L2 before the wait for the previous
 //     kernel, so their DRAM latency overlaps its tail.
-//   * Eight compute warps: warp w takes weight rows 16 (w % 4) .. + 16 and
-//     K-half w / 4 of every stage, and runs mma.sync m16n8k16 (fp16 in, fp32
-//     out) with the 16 weight rows as the A operand and the tokens (8, or 16
-//     in two groups) as B.  Both operands take the same permutation of K
-//     inside each 16-wide block (lane q of a quad reads the 4 consecutive
-//     codes 4q..4q+3 as one word), which leaves every dot product unchanged.
-//   * Four independent fp32 accumulator chains per token group, so
-//     consecutive MMAs do not wait for each other; every 4 stages they are
-//     summed and drained into int32 registers.  A warp's MMA covers 16 K, so
-//     |partial| <= 16 * 127^2 = 258064; a chain gathers at most 8 of them and
-//     the four chains' sum stays below 32 * 258064 < 2^24: exact in fp32.
+//   * Eight compute warps: warp w takes the K slice [32 w, 32 w + 32) of
+//     every stage for all 64 weight rows, and runs mma.sync m16n8k16 (fp16
+//     in, fp32 out) with each 16-row tile of weights as the A operand and
+//     the tokens (8, or 16 in two groups) as B.  So every token code is read
+//     and widened by one warp only.  Both operands take the same
+//     permutation of K inside each 16-wide block (lane q of a quad reads the
+//     4 consecutive codes 4q..4q+3 as one word), which leaves every dot
+//     product unchanged.
+//   * One fp32 accumulator per (row tile, token group): the four row tiles
+//     give consecutive MMAs independent accumulators.  Every 8 stages they
+//     are drained into int32 registers.  An MMA covers 16 K, so |partial| <=
+//     16 * 127^2 = 258064, and an accumulator gathers at most 16 of them,
+//     below 2^22: exact in fp32.  (E4M3: m16n8k32 E4M3 MMAs, fp32 over the
+//     whole range.)
 //   * The warps' int32 partials meet in shared memory (integer adds).  With
 //     one split the CTA applies the epilogue.  With S, cluster rank r owns a
 //     slice of about 1/S of the outputs: every other CTA of the cluster adds
@@ -33,6 +39,11 @@
 //     mbarrier), and r applies the epilogue once they are all in.  No global
 //     workspace, no atomics in global memory, nothing to clear between
 //     calls, and no CTA waits for another except for the partials it owns.
+//     E4M3 keeps its sums deterministic instead: each warp writes its fp32
+//     partials to its own slab of the idle stage ring, the CTA adds the
+//     eight slabs in a fixed order, and the owner adds the cluster's ranks
+//     in a fixed order, reading the other CTAs' shared memory between two
+//     cluster barriers.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -59,23 +70,36 @@ constexpr int kSkinnyRows = 64;       // weight rows per CTA
 constexpr int kSkinnyK = 256;         // K per stage
 constexpr int kSkinnyMaxSplits = 8;   // portable cluster size
 constexpr int kSkinnyMinStages = 4;   // least stages per K split (1024 K)
-constexpr int kCh = 4;                // independent accumulator chains per token group
-constexpr int kDrainStages = 4;       // stages between drains into int32
+constexpr int kDrainStages = 8;       // stages between drains into int32
 
-template <bool W16, int MT>
+// Code formats (weights, tokens).
+enum SkinnyKind : int {
+  kSkI8 = 0,     // int8, int8
+  kSkW16 = 1,    // fp16-held int8 codes, int8
+  kSkF16 = 2,    // fp16-held int8 codes, fp16-held int8 codes
+  kSkE4M3 = 3    // E4M3, E4M3 (fp32 accumulation)
+};
+
+template <int KIND, int MT>
 struct SkinnyCfg {
-  static constexpr int BOX_K = W16 ? 64 : 128;                  // weight codes per 128-byte row
-  static constexpr int W_BOXES = kSkinnyK / BOX_K;              // 2 (int8) or 4 (fp16 codes)
+  static constexpr bool W_F16 = KIND == kSkW16 || KIND == kSkF16;
+  static constexpr bool A_F16 = KIND == kSkF16;
+  static constexpr bool FP8 = KIND == kSkE4M3;
+  static constexpr int BOX_K = W_F16 ? 64 : 128;                // weight codes per 128-byte row
+  static constexpr int W_BOXES = kSkinnyK / BOX_K;              // 2 (1-byte codes) or 4 (fp16)
   static constexpr int W_BOX_BYTES = kSkinnyRows * 128;         // 8 KB
-  static constexpr int A_BOXES = kSkinnyK / 128;                // token codes are int8
+  static constexpr int A_BOX_K = A_F16 ? 64 : 128;              // token codes per 128-byte row
+  static constexpr int A_BOXES = kSkinnyK / A_BOX_K;
   static constexpr int A_ROWS = 8 * MT;                         // token rows per box
   static constexpr int A_BOX_BYTES = A_ROWS * 128;
   static constexpr int STAGE_BYTES = W_BOXES * W_BOX_BYTES + A_BOXES * A_BOX_BYTES;
-  static constexpr int STAGES = W16 ? 4 : (MT == 1 ? 6 : 5);
+  static constexpr int STAGES = W_F16 ? 4 : (MT == 1 && !FP8 ? 6 : 5);
   static constexpr int COMPUTE_WARPS = 8;
   static constexpr int THREADS = 32 * (COMPUTE_WARPS + 1);    // + the producer warp
-  static constexpr int OFF_PART = STAGES * STAGE_BYTES;        // int32 [A_ROWS][64], token-major
-  static constexpr int OFF_BAR = OFF_PART + A_ROWS * kSkinnyRows * 4;   // full[STAGES] empty[STAGES]
+  // partials, token-major: int32 [A_ROWS][64] (E4M3: fp32)
+  static constexpr int OFF_PART = STAGES * STAGE_BYTES;
+  static constexpr int PART_BYTES = A_ROWS * kSkinnyRows * 4;
+  static constexpr int OFF_BAR = OFF_PART + PART_BYTES;         // full[STAGES] empty[STAGES]
   static constexpr int OFF_FLAG = OFF_BAR + 2 * STAGES * 8;
   // the epilogue's constants: channel scales and bias (as fp32) of the 64
   // rows, token scales of the A_ROWS tokens
@@ -84,18 +108,30 @@ struct SkinnyCfg {
   static constexpr int OFF_REDBAR = (OFF_SCL + (2 * kSkinnyRows + A_ROWS) * 4 + 7) / 8 * 8;
   static constexpr int SMEM_BYTES = OFF_REDBAR + 8 + 1024;   // + 1 KB alignment room
   // two CTAs per SM: 228 KB per SM, 1 KB of it reserved per CTA
-  static_assert(W16 || 2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs must fit on an SM");
+  static_assert(W_F16 || 2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs must fit on an SM");
   static_assert(SMEM_BYTES <= 227 * 1024, "more shared memory than a CTA may hold");
+  static_assert(!FP8 || COMPUTE_WARPS * A_ROWS * kSkinnyRows * 4 <= OFF_PART,
+                "the E4M3 warps' slabs fit in the stage ring");
   static_assert(STAGE_BYTES % 1024 == 0 && W_BOX_BYTES % 1024 == 0 && A_BOX_BYTES % 1024 == 0,
                 "128-byte-swizzled boxes must start on 1 KB boundaries");
-  static_assert((kDrainStages * kSkinnyK / 2 / 16) / kCh * 16 * 127 * 127 * kCh < (1 << 24),
-                "fp32 chains must stay exact between drains");
+  // an accumulator gathers two 16-K MMAs per stage between drains
+  static_assert(2 * kDrainStages * 16 * 127 * 127 < (1 << 24),
+                "fp32 accumulators must stay exact between drains");
 };
 
 __device__ __forceinline__ void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uint32_t a1,
                                                  uint32_t a2, uint32_t a3, uint32_t b0,
                                                  uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_m16n8k32_e4m3(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                  uint32_t a2, uint32_t a3, uint32_t b0,
+                                                  uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -112,11 +148,11 @@ __device__ __forceinline__ uint2 lds64(uint32_t a) {
   return v;
 }
 
-template <bool W16, int MT>
-__global__ void __launch_bounds__(SkinnyCfg<W16, MT>::THREADS)
+template <int KIND, int MT>
+__global__ void __launch_bounds__(SkinnyCfg<KIND, MT>::THREADS)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                        const SkinnyParams p) {
-  using Cfg = SkinnyCfg<W16, MT>;
+  using Cfg = SkinnyCfg<KIND, MT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -125,6 +161,8 @@ __global__ void __launch_bounds__(SkinnyCfg<W16, MT>::THREADS)
   const uint32_t empty0 = full0 + 8u * Cfg::STAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_FLAG);
   int* part = reinterpret_cast<int*>(smem + Cfg::OFF_PART);
+  float* partf = reinterpret_cast<float*>(smem + Cfg::OFF_PART);   // E4M3
+  float* slab = reinterpret_cast<float*>(smem);   // E4M3, after the last stage: [warp][token][row]
   float* scl_w = reinterpret_cast<float*>(smem + Cfg::OFF_SCL);   // [64]
   float* scl_b = scl_w + kSkinnyRows;                              // [64]
   float* scl_a = scl_b + kSkinnyRows;                              // [A_ROWS]
@@ -145,7 +183,7 @@ __global__ void __launch_bounds__(SkinnyCfg<W16, MT>::THREADS)
   const int own0 = cut(split);
   const int own1 = cut(split + 1);
 
-  for (int i = threadIdx.x; i < Cfg::A_ROWS * kSkinnyRows; i += Cfg::THREADS) part[i] = 0;
+  for (int i = threadIdx.x; i < Cfg::PART_BYTES / 4; i += Cfg::THREADS) part[i] = 0;
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -155,7 +193,7 @@ __global__ void __launch_bounds__(SkinnyCfg<W16, MT>::THREADS)
     mbar_init(redbar, 1);
     fence_mbarrier_init();
     // the bytes the other CTAs will add into this CTA's slice
-    if (S > 1) mbar_arrive_expect_tx(redbar, static_cast<uint32_t>((S - 1) * (own1 - own0) * 4));
+    if (S > 1 && !Cfg::FP8) mbar_arrive_expect_tx(redbar, static_cast<uint32_t>((S - 1) * (own1 - own0) * 4));
   }
   if (warp == Cfg::COMPUTE_WARPS && lane == 0) {
     // Start the DRAM reads of the ring's first fill while the previous
@@ -192,7 +230,7 @@ __global__ void __launch_bounds__(SkinnyCfg<W16, MT>::THREADS)
 #pragma unroll
         for (int b = 0; b < Cfg::A_BOXES; ++b)
           tma_load_2d(st + Cfg::W_BOXES * Cfg::W_BOX_BYTES + b * Cfg::A_BOX_BYTES, &tmA, bar,
-                      k0 + b * 128, 0);
+                      k0 + b * Cfg::A_BOX_K, 0);
         issued = i + 1;
         // keep a second ring's worth of weights on its way into L2 (no
         // shared memory needed), doubling the bytes in flight
@@ -211,21 +249,23 @@ __global__ void __launch_bounds__(SkinnyCfg<W16, MT>::THREADS)
       }
     }
   } else {
-    // ---- compute warps
+    // ---- compute warps: warp w takes the K slice [32 w, 32 w + 32) of
+    // every stage for all 64 weight rows (four row tiles of 16), so every
+    // token code is read and widened by one warp only
     const int g = lane >> 2;         // weight row (and token) within an 8-group
     const int q = lane & 3;          // quad lane: codes 4q..4q+3 of each 16-block
-    const int rw = (warp & 3) * 16;  // the warp's first weight row
-    const int h = warp >> 2;         // the warp's K-half of every stage
-    float d[MT][kCh][4];
-    int acc[MT][4];
+    const int w = warp;
+    float d[4][MT][4];               // [row tile][token group][fragment]
+    int acc[4][MT][4];
 #pragma unroll
-    for (int t = 0; t < MT; ++t)
+    for (int rt = 0; rt < 4; ++rt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc[t][e] = 0;
+      for (int t = 0; t < MT; ++t)
 #pragma unroll
-        for (int c = 0; c < kCh; ++c) d[t][c][e] = 0.0f;
-      }
+        for (int e = 0; e < 4; ++e) {
+          acc[rt][t][e] = 0;
+          d[rt][t][e] = 0.0f;
+        }
     if (warp == Cfg::COMPUTE_WARPS - 1 && p.out_mode == kOutBf16) {
       // the epilogue's constants, fetched while the first stage streams in
       for (int r = lane; r < kSkinnyRows; r += 32) {
@@ -243,84 +283,180 @@ __global__ void __launch_bounds__(SkinnyCfg<W16, MT>::THREADS)
                                              static_cast<uint32_t>((i / Cfg::STAGES) & 1), abort_flag));
       if (!ok) break;
       const uint32_t st = sbase + static_cast<uint32_t>(s * Cfg::STAGE_BYTES);
-      const uint32_t abox = st + Cfg::W_BOXES * Cfg::W_BOX_BYTES + h * Cfg::A_BOX_BYTES;
-      // all of this half-stage's operand words first (8 K-blocks of 16), then
-      // the conversions and MMAs
-      uint32_t wlo[8][2], whi[8][2], x[8][MT];
+      const uint32_t abase = st + Cfg::W_BOXES * Cfg::W_BOX_BYTES;
+      if constexpr (Cfg::FP8) {
+        // E4M3: K-block w of 32 is in box w / 4, 16-byte chunks 2 (w % 4)
+        // and 2 (w % 4) + 1.  Lane q of a quad reads codes 8q..8q+7 of its
+        // rows: the first four fill the fragment's K slots 4q..4q+3, the
+        // last four slots 16+4q..16+4q+3, for the weights and the tokens
+        // alike.
+        const uint32_t off = ((static_cast<uint32_t>(2 * (w & 3) + (q >> 1)) ^ g) << 4) + 8u * (q & 1);
+        const uint32_t wbox = st + static_cast<uint32_t>((w >> 2) * Cfg::W_BOX_BYTES);
+        const uint32_t abox = abase + static_cast<uint32_t>((w >> 2) * Cfg::A_BOX_BYTES);
+        uint2 wl[4], wh[4], x[MT];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if constexpr (W16) {
-          // fp16 codes: K-block j of half h is in box 2h + j / 4, 16-byte
-          // chunk 2 (j % 4) + q / 2, bytes 8 (q % 2) .. + 8
-          const uint32_t wbox = st + static_cast<uint32_t>((2 * h + (j >> 2)) * Cfg::W_BOX_BYTES);
-          const uint32_t off = ((static_cast<uint32_t>(2 * (j & 3) + (q >> 1)) ^ g) << 4) + 8u * (q & 1);
-          const uint2 lo = lds64(wbox + (rw + g) * 128u + off);
-          const uint2 hi = lds64(wbox + (rw + g + 8) * 128u + off);
-          wlo[j][0] = lo.x;
-          wlo[j][1] = lo.y;
-          whi[j][0] = hi.x;
-          whi[j][1] = hi.y;
-        } else {
-          // int8 codes: K-block j of half h is 16-byte chunk j of box h
-          const uint32_t wbox = st + static_cast<uint32_t>(h * Cfg::W_BOX_BYTES);
-          const uint32_t off = ((static_cast<uint32_t>(j) ^ g) << 4) + 4u * q;
-          wlo[j][0] = lds32(wbox + (rw + g) * 128u + off);
-          whi[j][0] = lds32(wbox + (rw + g + 8) * 128u + off);
+        for (int rt = 0; rt < 4; ++rt) {
+          wl[rt] = lds64(wbox + (16 * rt + g) * 128u + off);
+          wh[rt] = lds64(wbox + (16 * rt + g + 8) * 128u + off);
         }
 #pragma unroll
-        for (int t = 0; t < MT; ++t)
-          x[j][t] = lds32(abox + (8 * t + g) * 128u + ((static_cast<uint32_t>(j) ^ g) << 4) + 4u * q);
+        for (int t = 0; t < MT; ++t) x[t] = lds64(abox + (8 * t + g) * 128u + off);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8u * s);   // the words are in registers: free the stage
+#pragma unroll
+        for (int rt = 0; rt < 4; ++rt)
+#pragma unroll
+          for (int t = 0; t < MT; ++t)
+            mma_m16n8k32_e4m3(d[rt][t], wl[rt].x, wh[rt].x, wl[rt].y, wh[rt].y, x[t].x, x[t].y);
+      } else {
+        // the slice's two 16-blocks kb = 2w, 2w + 1: all operand words
+        // first, then the conversions and MMAs
+        uint32_t wlo[2][4][2], whi[2][4][2], x[2][MT][2];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          // fp16 codes: 16-block kb is in box kb / 4, 16-byte chunk
+          // 2 (kb % 4) + q / 2, bytes 8 (q % 2) .. + 8; 1-byte codes: in box
+          // kb / 8, chunk kb % 8, bytes 4q .. + 4
+          const int kb = 2 * w + jj;
+          const uint32_t off16 = ((static_cast<uint32_t>(2 * (kb & 3) + (q >> 1)) ^ g) << 4) + 8u * (q & 1);
+          const uint32_t off8 = ((static_cast<uint32_t>(kb & 7) ^ g) << 4) + 4u * q;
+#pragma unroll
+          for (int rt = 0; rt < 4; ++rt) {
+            if constexpr (Cfg::W_F16) {
+              const uint32_t wbox = st + static_cast<uint32_t>((kb >> 2) * Cfg::W_BOX_BYTES);
+              const uint2 lo = lds64(wbox + (16 * rt + g) * 128u + off16);
+              const uint2 hi = lds64(wbox + (16 * rt + g + 8) * 128u + off16);
+              wlo[jj][rt][0] = lo.x;
+              wlo[jj][rt][1] = lo.y;
+              whi[jj][rt][0] = hi.x;
+              whi[jj][rt][1] = hi.y;
+            } else {
+              const uint32_t wbox = st + static_cast<uint32_t>((kb >> 3) * Cfg::W_BOX_BYTES);
+              wlo[jj][rt][0] = lds32(wbox + (16 * rt + g) * 128u + off8);
+              whi[jj][rt][0] = lds32(wbox + (16 * rt + g + 8) * 128u + off8);
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            if constexpr (Cfg::A_F16) {
+              const uint32_t abox = abase + static_cast<uint32_t>((kb >> 2) * Cfg::A_BOX_BYTES);
+              const uint2 v = lds64(abox + (8 * t + g) * 128u + off16);
+              x[jj][t][0] = v.x;
+              x[jj][t][1] = v.y;
+            } else {
+              const uint32_t abox = abase + static_cast<uint32_t>((kb >> 3) * Cfg::A_BOX_BYTES);
+              x[jj][t][0] = lds32(abox + (8 * t + g) * 128u + off8);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8u * s);   // the words are in registers: free the stage
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          uint32_t b[MT][2];
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            if constexpr (Cfg::A_F16) {
+              b[t][0] = x[jj][t][0];
+              b[t][1] = x[jj][t][1];
+            } else {
+              s8x4_to_f16x4(x[jj][t][0], b[t][0], b[t][1]);
+            }
+          }
+#pragma unroll
+          for (int rt = 0; rt < 4; ++rt) {
+            uint32_t a0, a1, a2, a3;
+            if constexpr (Cfg::W_F16) {
+              a0 = wlo[jj][rt][0];
+              a2 = wlo[jj][rt][1];
+              a1 = whi[jj][rt][0];
+              a3 = whi[jj][rt][1];
+            } else {
+              s8x4_to_f16x4(wlo[jj][rt][0], a0, a2);
+              s8x4_to_f16x4(whi[jj][rt][0], a1, a3);
+            }
+#pragma unroll
+            for (int t = 0; t < MT; ++t) mma_m16n8k16_f16(d[rt][t], a0, a1, a2, a3, b[t][0], b[t][1]);
+          }
+        }
+        if (i % kDrainStages == kDrainStages - 1 || i == nst - 1) {
+#pragma unroll
+          for (int rt = 0; rt < 4; ++rt)
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                acc[rt][t][e] += f32_exact_int_to_s32(__float_as_uint(d[rt][t][e]));
+                d[rt][t][e] = 0.0f;
+              }
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8u * s);   // the words are in registers: free the stage
+    }
+    // E4M3 reuses the ring for its slabs once every compute warp has read
+    // its last stage (the producer issues nothing after the last stage)
+    if constexpr (Cfg::FP8) named_bar_sync(1, 32 * Cfg::COMPUTE_WARPS);
+    // D fragment: e = 0, 1 -> weight row 16 rt + g, tokens 2q, 2q + 1 of
+    // group t; e = 2, 3 -> weight row 16 rt + g + 8.  Token-major: [token][row].
+    if (ok) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t a0, a1, a2, a3;
-        if constexpr (W16) {
-          a0 = wlo[j][0];
-          a2 = wlo[j][1];
-          a1 = whi[j][0];
-          a3 = whi[j][1];
-        } else {
-          s8x4_to_f16x4(wlo[j][0], a0, a2);
-          s8x4_to_f16x4(whi[j][0], a1, a3);
-        }
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          uint32_t b0, b1;
-          s8x4_to_f16x4(x[j][t], b0, b1);
-          mma_m16n8k16_f16(d[t][j % kCh], a0, a1, a2, a3, b0, b1);
-        }
-      }
-      if (i % kDrainStages == kDrainStages - 1 || i == nst - 1) {
+      for (int rt = 0; rt < 4; ++rt)
 #pragma unroll
         for (int t = 0; t < MT; ++t)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float v = d[t][0][e];
-#pragma unroll
-            for (int c = 1; c < kCh; ++c) v = __fadd_rn(v, d[t][c][e]);   // exact (integers < 2^24)
-            acc[t][e] += f32_exact_int_to_s32(__float_as_uint(v));
-#pragma unroll
-            for (int c = 0; c < kCh; ++c) d[t][c][e] = 0.0f;
+            const int token = 8 * t + 2 * q + (e & 1);
+            const int row = 16 * rt + g + (e >= 2 ? 8 : 0);
+            if constexpr (Cfg::FP8) {
+              // into this warp's own slab of the (now idle) stage ring
+              slab[(w * Cfg::A_ROWS + token) * kSkinnyRows + row] = d[rt][t][e];
+            } else {
+              if (acc[rt][t][e] != 0) atomicAdd(part + token * kSkinnyRows + row, acc[rt][t][e]);
+            }
           }
-      }
-    }
-    // D fragment: e = 0, 1 -> weight row g, tokens 2q, 2q + 1 of group t;
-    // e = 2, 3 -> weight row g + 8.  part is token-major: [token][row].
-    if (ok) {
-#pragma unroll
-      for (int t = 0; t < MT; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int token = 8 * t + 2 * q + (e & 1);
-          const int row = rw + g + (e >= 2 ? 8 : 0);
-          if (acc[t][e] != 0) atomicAdd(part + token * kSkinnyRows + row, acc[t][e]);
-        }
     }
   }
   pdl_trigger();
   __syncthreads();
+  if constexpr (Cfg::FP8) {
+    // E4M3: this CTA's partials, the eight warps' slabs added in a fixed
+    // order; then this CTA's share of the outputs, summed over the
+    // cluster's ranks in a fixed order (distributed shared memory, between
+    // two cluster barriers).  With one split a thread reads back only the
+    // values it wrote.
+    for (int e = static_cast<int>(threadIdx.x); e < E; e += Cfg::THREADS) {
+      float v = slab[e];
+#pragma unroll
+      for (int ww = 1; ww < Cfg::COMPUTE_WARPS; ++ww) v = __fadd_rn(v, slab[ww * Cfg::A_ROWS * kSkinnyRows + e]);
+      partf[e] = v;
+    }
+    if (S > 1) cluster_sync_all();   // every CTA's partials are complete and visible
+    const bool write = *abort_flag == 0;
+    for (int e = own0 + static_cast<int>(threadIdx.x); e < own1; e += Cfg::THREADS) {
+      const int m = e / kSkinnyRows;
+      const int r = e % kSkinnyRows;
+      const int n = n0 + r;
+      if (n >= p.N) continue;
+      float v;
+      if (S > 1) {
+        v = 0.0f;
+#pragma unroll 1
+        for (int rk = 0; rk < S; ++rk)
+          v = __fadd_rn(v, ld_shared_cluster_f32(mapa_shared(smem_u32(partf + e), static_cast<uint32_t>(rk))));
+      } else {
+        v = partf[e];
+      }
+      if (!write) continue;
+      if (p.out_mode == kOutBf16) {
+        const __nv_bfloat16 y = __float2bfloat16_rn(dequant_one(v, scl_a[m], scl_w[r], scl_b[r]));
+        static_cast<uint16_t*>(p.out)[static_cast<int64_t>(m) * p.ldo + n] =
+            *reinterpret_cast<const uint16_t*>(&y);
+      } else {
+        static_cast<float*>(p.out)[static_cast<int64_t>(m) * p.ldo + n] = v;
+      }
+    }
+    if (S > 1) cluster_sync_all();   // no CTA leaves while another still reads its partials
+    return;
+  }
   if (S > 1) {
     // Add this CTA's partials of the other owners' slices into theirs
     // (always, so that no owner waits in vain), then wait for the other
