@@ -286,14 +286,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
-// 32-bit load from shared memory anywhere in the cluster (a mapa_shared
-// address).
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-  return v;
-}
-
 // Atomic add of v into a 32-bit word in the shared memory of a CTA of this
 // cluster (mapa_shared addresses), counted as 4 transaction bytes on that
 // CTA's mbarrier.  The value leaves from a register, so the adding CTA may
