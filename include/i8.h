@@ -334,10 +334,12 @@ i8_status i8_gemm_dequant_bias_bf16_w16(const int8_t* aq, const float* s_a,
  *   I8_OPT_STREAM_K     stream-K schedule for the CTA-pair kernel (equal
  *                       (tile, K-block) shares per pair, tiles cut between
  *                       pairs finished from exact int32 partials; it needs
- *                       workspace): 1 (default) where the table predicts a
- *                       gain (K >= 8192, whole tiles leave many pairs idle
- *                       and the tiles run M blocks fastest), 2 whenever
- *                       whole tiles leave pairs idle, 0 never.
+ *                       workspace; with 64 or more K blocks, whole waves of
+ *                       tiles first and only the rest shared): 1 (default)
+ *                       where the table predicts a gain (at least half a
+ *                       wave of tiles and whole tiles filling under 93 % of
+ *                       the last wave), 2 whenever whole tiles leave pairs
+ *                       idle, 0 never.
  *   I8_OPT_NVTX         1: every call of this header opens an NVTX range
  *                       named after the call (visible in Nsight timelines;
  *                       free when no tool is attached); 0 (default): none.
