@@ -22,7 +22,10 @@
 //     every stage for all 64 weight rows, and runs mma.sync m16n8k16 (fp16
 //     in, fp32 out) with each 16-row tile of weights as the A operand and
 //     the tokens (8, or 16 in two groups) as B.  So every token code is read
-//     and widened by one warp only.  Both operands take the same
+//     and widened by one warp only.  Int8 codes for up to 8 tokens skip the
+//     widening: the integer m16n8k32 MMA (s8 in, s32 out) takes the codes
+//     as they are, exact, at a rate that still outpaces the weight stream
+//     for one token group (not for two).  Both operands take the same
 //     permutation of K inside each 16-wide block (lane q of a quad reads the
 //     4 consecutive codes 4q..4q+3 as one word), which leaves every dot
 //     product unchanged.
@@ -85,6 +88,11 @@ struct SkinnyCfg {
   static constexpr bool W_F16 = KIND == kSkW16 || KIND == kSkF16;
   static constexpr bool A_F16 = KIND == kSkF16;
   static constexpr bool FP8 = KIND == kSkE4M3;
+  // int8 codes for up to 8 tokens: the integer m16n8k32 MMA straight from
+  // the codes (exact int32, nothing to widen); 16 tokens would make its
+  // lower rate the limit, so they take the fp16 MMA on widened codes
+  static constexpr bool S8MMA = KIND == kSkI8 && MT == 1;
+  static constexpr bool K32 = FP8 || S8MMA;                     // m16n8k32 MMAs on 1-byte codes
   static constexpr int BOX_K = W_F16 ? 64 : 128;                // weight codes per 128-byte row
   static constexpr int W_BOXES = kSkinnyK / BOX_K;              // 2 (1-byte codes) or 4 (fp16)
   static constexpr int W_BOX_BYTES = kSkinnyRows * 128;         // 8 KB
@@ -134,6 +142,14 @@ __device__ __forceinline__ void mma_m16n8k32_e4m3(float (&d)[4], uint32_t a0, ui
   asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_m16n8k32_s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
@@ -292,9 +308,10 @@ __global__ void __launch_bounds__(SkinnyCfg<KIND, MT>::THREADS)
       if (!ok) break;
       const uint32_t st = sbase + static_cast<uint32_t>(s * Cfg::STAGE_BYTES);
       const uint32_t abase = st + Cfg::W_BOXES * Cfg::W_BOX_BYTES;
-      if constexpr (Cfg::FP8) {
-        // E4M3: K-block w of 32 is in box w / 4, 16-byte chunks 2 (w % 4)
-        // and 2 (w % 4) + 1.  Lane q of a quad reads codes 8q..8q+7 of its
+      if constexpr (Cfg::K32) {
+        // 1-byte codes, 32-K MMAs (E4M3, or int8 for up to 8 tokens):
+        // K-block w of 32 is in box w / 4, 16-byte chunks 2 (w % 4) and
+        // 2 (w % 4) + 1.  Lane q of a quad reads codes 8q..8q+7 of its
         // rows: the first four fill the fragment's K slots 4q..4q+3, the
         // last four slots 16+4q..16+4q+3, for the weights and the tokens
         // alike.
@@ -314,8 +331,12 @@ __global__ void __launch_bounds__(SkinnyCfg<KIND, MT>::THREADS)
 #pragma unroll
         for (int rt = 0; rt < 4; ++rt)
 #pragma unroll
-          for (int t = 0; t < MT; ++t)
-            mma_m16n8k32_e4m3(d[rt][t], wl[rt].x, wh[rt].x, wl[rt].y, wh[rt].y, x[t].x, x[t].y);
+          for (int t = 0; t < MT; ++t) {
+            if constexpr (Cfg::FP8)
+              mma_m16n8k32_e4m3(d[rt][t], wl[rt].x, wh[rt].x, wl[rt].y, wh[rt].y, x[t].x, x[t].y);
+            else   // exact: |sum| <= 127^2 * K < 2^31
+              mma_m16n8k32_s8(acc[rt][t], wl[rt].x, wh[rt].x, wl[rt].y, wh[rt].y, x[t].x, x[t].y);
+          }
       } else {
         // the slice's two 16-blocks kb = 2w, 2w + 1: all operand words
         // first, then the conversions and MMAs
