@@ -315,10 +315,11 @@ def test_plan_query_errors():
 
 def test_skinny_split_rule():
     """Few tokens: no K split while the N-blocks of 64 weight rows occupy at
-    least 90 % of the SMs; otherwise the fewest splits that give every SM a
-    CTA, at most 8 and with at least 4 stages (1024 K) each, lowered until
-    the grid fits the resident CTA slots (a machine described by hand: its
-    clusters assumed to pack those slots fully)."""
+    least 90 % of the SMs.  Otherwise the fewest splits that give 5/8 of the
+    SMs a CTA, or, when a CTA would then carry more than 12 stages (3072 K),
+    the fewest that give every SM a CTA; at most 8, at least 2 stages (512
+    K) each, lowered until the grid fits the resident CTA slots (a machine
+    described by hand: its clusters assumed to pack those slots fully)."""
     n = 0
     for m in (GB300, dict(sms=152, pairs=74, skinny_slots=152), dict(sms=20, pairs=9, skinny_slots=40)):
         sms, slots = m["sms"], m["skinny_slots"]
@@ -331,13 +332,19 @@ def test_skinny_split_rule():
                         B, st = -(-N // 64), -(-K // 256)
                         want = 1
                         if 10 * B < 9 * sms:
-                            want = min(-(-sms // B), max(1, st // 4), 8)
+                            want = -(-max(1, 5 * sms // 8) // B)
+                            if -(-st // want) > 12:
+                                want = -(-sms // B)
+                            want = min(want, max(1, st // 2), 8)
                             while want > 1 and B * want > slots:
                                 want -= 1
                         per = -(-st // want)
                         assert (p["splits"], p["kb_per_split"]) == (-(-st // per), per), (m, M, N, K)
                         n += 1
     assert n == 3 * 4 * 2 * 7 * 4
-    # the measured cases on GB300 figures (two CTAs per SM)
+    # the measured cases on GB300 figures (two CTAs per SM); M, N, K
     assert i8.plan_query(1, 3072, 12288, "int8", **GB300)["splits"] == 4
     assert i8.plan_query(1, 9216, 3072, "int8", **GB300)["splits"] == 1
+    assert i8.plan_query(16, 3072, 3072, "int8", **GB300)["splits"] == 2
+    assert i8.plan_query(1, 768, 3072, "int8", **GB300)["splits"] == 6
+    assert i8.plan_query(1, 6144, 2048, "int8", **GB300)["splits"] == 1

@@ -436,25 +436,34 @@ struct SkinnyFit {
   int cap(int s) const { return clusters[s] > 0 ? clusters[s] : slots / s; }
 };
 
+// Few-token split planning: least 256-K stages per K split (512 K), and the
+// stages per CTA above which K counts as long.
+constexpr int kSkinnySplitMinStages = 2;
+constexpr int kSkinnyLongStages = 12;
+
 void plan_skinny(Plan& p, int64_t M, int64_t N, int64_t K, int sms, const SkinnyFit& fit) {
   (void)M;
-  // K splits, when the N-blocks leave more than a tenth of the SMs idle:
-  // the fewest that give every SM a CTA, as long as all CTAs are resident
-  // at once (within the CTA slots, and the N-blocks' clusters within the
-  // clusters that fit; a second wave would stream its weights only after
-  // the first finished) and every split owns at least kSkinnyMinStages
-  // whole 256-K stages.  One N-block's splits form a cluster of at most
-  // kSkinnyMaxSplits CTAs.  No workspace: the splits add their partials
-  // over distributed shared memory.
-  // Measured (GB300, graph replay, weights rotating past L2; M x K x N):
-  //   * 1 x 12288 x 3072 int8 codes: 23.2 / 13.1 / 13.2 / 11.1 / 10.6 /
-  //     14.3 / 14.8 us with 1 / 2 / 3 / 4 / 5 / 6 / 8 splits (6 and 8: the
-  //     48 clusters no longer fit at once; 3: one CTA per SM, and one CTA
-  //     alone streams no faster than about 25 GB/s);
-  //   * 16 x 12288 x 3072 fp16-held codes (one CTA per SM): 29.6 / 18.8 /
-  //     27.2 / 22.8 us with 1 / 2 / 3 / 4 splits (46 clusters of 3 fit);
-  //   * 144 N-blocks (1 x 3072 x 9216): 8.1 / 8.3 us (int8), 7.2 / 8.2 us
-  //     (E4M3) with 1 / 2 splits.
+  // K splits, when the N-blocks leave more than a tenth of the SMs idle.
+  // Short K: the fewest that give about 5/8 of the SMs a CTA; every CTA
+  // carries a fixed cost (start, epilogue, its share of the cluster's
+  // reduction) that more, shorter CTAs would not repay.  Long K (more than
+  // kSkinnyLongStages stages per CTA that way): the fewest that give every
+  // SM a CTA, since one CTA alone streams no faster than about 25-50 GB/s.
+  // Then at most kSkinnyMaxSplits, at least kSkinnySplitMinStages whole
+  // 256-K stages per split, and lowered until all CTAs are resident at once
+  // (within the CTA slots, and the N-blocks' clusters within the clusters
+  // that fit; a second wave would stream its weights only after the first
+  // finished).  One N-block's splits form a cluster.  No workspace: the
+  // splits add their partials over distributed shared memory.
+  // Measured (GB300, graph replay, weights rotating past L2; M x K x N,
+  // int8 codes, us with 1 / 2 / 3 / 4 / 6 splits):
+  //   * 16 x 3072 x 3072: 8.5 / 5.9 / 6.7 / 6.9 / 11.6 (48 N-blocks);
+  //   * 1 x 3072 x 768: 6.1 / 4.1 / 3.6 / 3.2 / 2.9 (12 N-blocks);
+  //   * 1 x 2048 x 6144: 4.8 / 5.2 / 5.6 / 7.1 (96 N-blocks);
+  //   * 1 x 12288 x 3072: 23.2 / 13.1 / 13.2 / 11.1 / 14.3 (long K; with 6
+  //     the 48 clusters no longer fit at once);
+  //   * 16 x 12288 x 3072, fp16-held codes (one CTA per SM): 29.6 / 18.8 /
+  //     27.2 / 22.8 with 1 / 2 / 3 / 4 (46 clusters of 3 fit, not 48).
   p.skinny = true;
   p.num_n = static_cast<int>((N + kSkinnyRows - 1) / kSkinnyRows);
   p.num_m = 1;
@@ -463,7 +472,10 @@ void plan_skinny(Plan& p, int64_t M, int64_t N, int64_t K, int sms, const Skinny
   if (g_opt.force_splits > 0) {
     splits = g_opt.force_splits;
   } else if (10LL * p.num_n < 9LL * sms) {
-    splits = std::min((sms + p.num_n - 1) / p.num_n, std::max(1, stages / kSkinnyMinStages));
+    const int short_ctas = std::max(1, 5 * sms / 8);
+    splits = (short_ctas + p.num_n - 1) / p.num_n;
+    if ((stages + splits - 1) / splits > kSkinnyLongStages) splits = (sms + p.num_n - 1) / p.num_n;
+    splits = std::min(splits, std::max(1, stages / kSkinnySplitMinStages));
     splits = std::min(splits, kSkinnyMaxSplits);
     while (splits > 1 &&
            (static_cast<int64_t>(p.num_n) * splits > fit.slots || p.num_n > fit.cap(splits)))

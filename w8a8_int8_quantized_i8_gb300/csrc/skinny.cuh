@@ -72,7 +72,6 @@ struct SkinnyParams {
 constexpr int kSkinnyRows = 64;       // weight rows per CTA
 constexpr int kSkinnyK = 256;         // K per stage
 constexpr int kSkinnyMaxSplits = 8;   // portable cluster size
-constexpr int kSkinnyMinStages = 4;   // least stages per K split (1024 K)
 constexpr int kDrainStages = 8;       // stages between drains into int32
 
 // Code formats (weights, tokens).
